@@ -1,0 +1,558 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8-KV decode hot path on GB300.
+
+One step = one decode layer of the batch-16, 8192-token workload (16 query /
+2 KV heads, head_dim 128, e4m3 K and V with per-(token, head) fp32 scales):
+  1. fp8kv_append of the step's new token for every sequence (position 8191),
+  2. fp8kv_decode_split (flash-decoding split kernel, fp32 partials),
+  3. fp8kv_decode_merge (second kernel, bf16 output).
+Each step reads a different one of L distinct layer caches (L * 69 MB well
+above the 126 MB L2), so every step streams its cache from HBM.  Steps are
+replayed from CUDA graphs; timing uses CUDA events on the launching stream.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the oracle (plain
+fp64 C on the host cores) on the same metric instead.
+"""
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp8_quantized_kv_gb300 import synth  # noqa: E402
+
+WORKLOAD = "decode_b16_ctx8192"
+METRIC = "decode attn KV-read GB/s (% of HBM peak) and µs/layer at B16 ctx8192, 1 GB300"
+PAGE_NUMBER_GBS = 550.0   # the pages' figure for this workload (RTX 5070 Ti, Triton, codes only)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="fp8kv", choices=["fp8kv", "reference"])
+    ap.add_argument("--dtype", default="k8v8", choices=["k8v8", "k16v8", "k16v16"])
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--chunk", type=int, default=200)
+    ap.add_argument("--no-controls", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- bytes --
+
+def step_bytes(spec, dtype, T):
+    """Algorithmic bytes of one step: KV codes (or bf16) + scales read, Q read,
+    O written (bf16), plus the appended token's rows (bf16 in, cache out)."""
+    B, Hq, Hkv, D = spec.batch, spec.q_heads, spec.kv_heads, spec.head_dim
+    k8, v8 = dtype == "k8v8", dtype != "k16v16"
+    row_bytes = D * ((1 if k8 else 2) + (1 if v8 else 2)) + 4 * (int(k8) + int(v8))
+    kv = B * Hkv * T * row_bytes
+    qo = 2 * B * Hq * D * 2
+    append = B * Hkv * (2 * D * 2 + row_bytes)
+    split = kv + B * Hq * D * 2
+    return {"step": kv + qo + append, "kv": kv, "split_kernel": split, "qo": qo, "append": append}
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [s for t, s in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not inside:
+            near = min(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))
+            inside = [near[1]]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+        mx = [num(s[2]) for s in inside if num(s[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in inside for n, v in zip(names, s[5:9]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ----------------------------------------------------------------- peaks --
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_gb_s", "hbm"):
+            if key in d:
+                v = d[key]
+                v = v.get("value", v.get("gbs")) if isinstance(v, dict) else v
+                return float(v), "measured"
+        for k, v in d.items():
+            if "hbm" in k.lower() and isinstance(v, (int, float)):
+                return float(v), "measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return 6800.0, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_quantized_kv_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(kernel_key, sha):
+    """dram bytes per launch from a committed ncu summary, only if it was taken
+    on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(kernel_key)
+        if ent and ent.get("source_sha") == sha:
+            return float(ent["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError, TypeError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- oracle --
+
+def oracle_sample(inp, n_seqs, tokens):
+    """Oracle work for `n_seqs` sequences over `tokens` cached tokens: e4m3
+    dequantisation of their K/V and fp64 decode attention.  Returns seconds
+    and the algorithmic KV bytes this sample stands for."""
+    import numpy as np
+    import oracle
+    spec = inp.spec
+    D, Hkv = spec.head_dim, spec.kv_heads
+    q = oracle.bf16_to_double(synth.bf16_bits(inp.q[:n_seqs]))
+    kb, vb = [], []
+    for b in range(n_seqs):
+        s = int(inp.cu_seqlens[b])
+        kb.append(synth.bf16_bits(inp.k[s:s + tokens]).transpose(1, 0, 2))
+        vb.append(synth.bf16_bits(inp.v[s:s + tokens]).transpose(1, 0, 2))
+    kc, ks = oracle.quantize(np.stack(kb))
+    vc, vs = oracle.quantize(np.stack(vb))
+    lens = np.full(n_seqs, tokens, np.int32)
+    t0 = time.perf_counter()
+    k = oracle.dequantize(kc, ks)
+    v = oracle.dequantize(vc, vs)
+    oracle.decode_attention(q, k, v, lens, 1.0 / math.sqrt(D))
+    dt = time.perf_counter() - t0
+    nbytes = n_seqs * Hkv * tokens * (2 * D + 8) + 2 * n_seqs * spec.q_heads * D * 2
+    return dt, nbytes
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    spec = synth.WORKLOADS[WORKLOAD]
+    T = spec.seq_lens[0]
+    inp = synth.decode_inputs(spec, device="cpu", seq_lens=[T] * 2)
+    # size each step so the whole run stays within about two minutes
+    dt1, _ = oracle_sample(inp, 1, 512)
+    per_token = dt1 / 512
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    tokens = int(max(16, min(T, budget / per_token)))
+    tokens -= tokens % 16 or 0
+    tokens = max(16, tokens)
+    for _ in range(args.warmup):
+        oracle_sample(inp, 1, tokens)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = oracle_sample(inp, 1, tokens)
+        tot_t += dt
+        tot_b += nb
+    gbs = tot_b / tot_t / 1e9
+    ms_per_layer = tot_t / args.steps * 1e3 * (spec.batch * T) / tokens
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_layer,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": spec.batch, "q_heads": spec.q_heads,
+                   "kv_heads": spec.kv_heads, "head_dim": spec.head_dim, "ctx": T, "cache": "k8v8"},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: 1 sequence x {tokens} tokens of the workload "
+                                   "(e4m3 dequantise + fp64 decode attention), single thread; "
+                                   "ms_per_step scaled to the full 16 x 8192 layer"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU arm --
+
+class Layer:
+    """One layer: its own cache plus pre-built C-ABI argument tuples."""
+
+    def __init__(self, cache, q, lens, ws_tensor, out, knew, vnew, sidx, pos, Hq, sm_scale):
+        from fp8_quantized_kv_gb300._lib import get_lib
+        self.lib = get_lib()
+        self.cache = cache
+        self.keep = (q, lens, ws_tensor, out, knew, vnew, sidx, pos)
+        P = lambda t: ctypes.c_void_p(t.data_ptr())
+        self.a_append = (cache.struct_ref, P(knew), P(vnew), P(sidx), P(pos), knew.shape[0])
+        wsb = ws_tensor.numel()
+        self.a_split = (P(q), cache.struct_ref, P(lens), Hq, ctypes.c_float(sm_scale), 0, P(ws_tensor), wsb)
+        self.a_merge = (cache.struct_ref, Hq, 0, P(ws_tensor), wsb, P(out), 0)
+
+    def append(self, s):
+        r = self.lib.fp8kv_append(*self.a_append, s)
+        if r:
+            raise RuntimeError(f"fp8kv_append status {r}")
+
+    def split(self, s):
+        r = self.lib.fp8kv_decode_split(*self.a_split, s)
+        if r:
+            raise RuntimeError(f"fp8kv_decode_split status {r}")
+
+    def merge(self, s):
+        r = self.lib.fp8kv_decode_merge(*self.a_merge, s)
+        if r:
+            raise RuntimeError(f"fp8kv_decode_merge status {r}")
+
+
+def build_layers(spec, dtype, L, inp):
+    import fp8_quantized_kv_gb300 as fk
+    B, Hq, Hkv, D = spec.batch, spec.q_heads, spec.kv_heads, spec.head_dim
+    T = spec.seq_lens[0]
+    cap = T
+    base = fk.Fp8KVCache.contiguous(B, Hkv, D, cap, dtype)
+    # tokens 0..T-2 are the cached context; token T-1 is appended by each step
+    lens_prev = torch.full((B,), T - 1, dtype=torch.int64)
+    keep = torch.ones(B * T, dtype=torch.bool)
+    keep[T - 1::T] = False
+    sidx = torch.repeat_interleave(torch.arange(B), lens_prev).to(torch.int32).cuda()
+    pos = torch.cat([torch.arange(T - 1)] * B).to(torch.int32).cuda()
+    fk.fp8kv_append(base, inp.k[keep.cuda()].contiguous(), inp.v[keep.cuda()].contiguous(), sidx, pos)
+    knew = inp.k[T - 1::T].contiguous()          # [B, Hkv, D]: token T-1 of each sequence
+    vnew = inp.v[T - 1::T].contiguous()
+    new_sidx = torch.arange(B, dtype=torch.int32, device="cuda")
+    new_pos = torch.full((B,), T - 1, dtype=torch.int32, device="cuda")
+    lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    q = inp.q.contiguous()
+    layers = []
+    for li in range(L):
+        if li == 0:
+            c = base
+        else:
+            clone = lambda t: None if t is None else t.clone()
+            c = fk.Fp8KVCache(dtype=dtype, layout=0, batch=B, kv_heads=Hkv, head_dim=D,
+                              k=clone(base.k), v=clone(base.v), k_scale=clone(base.k_scale),
+                              v_scale=clone(base.v_scale), max_tokens=cap)
+        wsb = fk.fp8kv_decode_workspace_bytes(c, Hq, 0)
+        ws_t = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+        layers.append(Layer(c, q, lens, ws_t, out, knew, vnew, new_sidx, new_pos, Hq, 1.0 / math.sqrt(D)))
+    torch.cuda.synchronize()
+    return layers, (q, knew, vnew, new_sidx, new_pos, lens)
+
+
+def capture(layers, n_steps, with_events):
+    """CUDA graph of n_steps steps cycling over the layers; optionally with
+    timing events around each kernel (event-record nodes)."""
+    g = torch.cuda.CUDAGraph()
+    evs = []
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            sp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            for i in range(n_steps):
+                L = layers[i % len(layers)]
+                if with_events:
+                    e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+                    e[0].record()
+                L.append(sp)
+                if with_events:
+                    e[1].record()
+                L.split(sp)
+                if with_events:
+                    e[2].record()
+                L.merge(sp)
+                if with_events:
+                    e[3].record()
+                    evs.append(e)
+    torch.cuda.current_stream().wait_stream(s)
+    return g, evs
+
+
+def time_graph_steps(layers, K, chunk, ws):
+    """Time exactly K steps (graph replays); returns (ms total, per-kernel ms)."""
+    chunk = max(1, min(chunk, K))
+    try:                                         # event-record graph nodes need `external`
+        torch.cuda.Event(enable_timing=True, external=True)
+        ext = True
+    except TypeError:
+        ext = False
+    g, evs = capture(layers, chunk, ext)
+    rem = K % chunk
+    g_rem = capture(layers, rem, False)[0] if rem else None
+    reps = K // chunk
+    g.replay()                                  # one untimed replay: instantiate, warm
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    start.record()
+    for _ in range(reps):
+        g.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    end.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(ws)
+    total_ms = start.elapsed_time(end)
+    per = None
+    if evs:
+        a = [e[0].elapsed_time(e[1]) for e in evs]
+        sp = [e[1].elapsed_time(e[2]) for e in evs]
+        m = [e[2].elapsed_time(e[3]) for e in evs]
+        per = {"append_ms": statistics.mean(a), "split_ms": statistics.mean(sp), "merge_ms": statistics.mean(m)}
+    return total_ms, per, (t_wall0, t_wall1)
+
+
+def e2e_run(layers, host, K, W):
+    """Through the public Python API: pinned host inputs copied in each step,
+    the output copied back each step."""
+    import fp8_quantized_kv_gb300 as fk
+    q, knew, vnew, sidx, pos, lens = host["dev"]
+    hq, hk, hv, hs, hp, hl = host["pinned"]
+    out_h = host["out"]
+    outs = [torch.empty_like(out_h, device="cuda") for _ in layers]
+    wss = [torch.empty(fk.fp8kv_decode_workspace_bytes(L.cache, q.shape[1], 0), dtype=torch.uint8,
+                       device="cuda") for L in layers]
+
+    def step(i):
+        L = layers[i % len(layers)]
+        q.copy_(hq, non_blocking=True)
+        knew.copy_(hk, non_blocking=True)
+        vnew.copy_(hv, non_blocking=True)
+        sidx.copy_(hs, non_blocking=True)
+        pos.copy_(hp, non_blocking=True)
+        lens.copy_(hl, non_blocking=True)
+        fk.fp8kv_append(L.cache, knew, vnew, sidx, pos)
+        fk.fp8kv_decode_attention(q, L.cache, lens, out=outs[i % len(layers)],
+                                  workspace=wss[i % len(layers)])
+        out_h.copy_(outs[i % len(layers)], non_blocking=True)
+
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    st = torch.cuda.Event(enable_timing=True)
+    en = torch.cuda.Event(enable_timing=True)
+    st.record()
+    for i in range(K):
+        step(i)
+    en.record()
+    torch.cuda.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hp, hl))
+    d2h = out_h.numel() * out_h.element_size()
+    return st.elapsed_time(en), h2d, d2h
+
+
+def measure_variant(spec, dtype, args, ws, inp):
+    layers, dev = build_layers(spec, dtype, args.layers, inp)
+    for i in range(max(3, args.warmup)):                      # eager warm-up steps
+        L = layers[i % len(layers)]
+        sp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        L.append(sp); L.split(sp); L.merge(sp)
+    torch.cuda.synchronize()
+    total_ms, per, wall = time_graph_steps(layers, args.steps, args.chunk, ws)
+    return layers, dev, total_ms, per, wall
+
+
+def run_gpu(args, ws, rank):
+    spec = synth.WORKLOADS[WORKLOAD]
+    T = spec.seq_lens[0]
+    inp = synth.decode_inputs(spec, device="cuda")
+    dev_index = torch.cuda.current_device()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = int(vis.split(",")[dev_index]) if vis and vis.split(",")[dev_index].isdigit() else dev_index
+    sampler = ClockSampler(smi_index)
+    sampler.start()
+    time.sleep(0.3)
+
+    layers, dev, total_ms, per, wall = measure_variant(spec, args.dtype, args, ws, inp)
+    t_max = max_over_ranks(total_ms, ws)
+    nb = step_bytes(spec, args.dtype, T)
+    ms_per_step = t_max / args.steps
+    value = ws * nb["step"] * args.steps / (t_max * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    clocks = sampler.summary(*wall)
+
+    # e2e through the public API with host buffers
+    q, knew, vnew, sidx, pos, lens = dev
+    pinned = tuple(t.cpu().pin_memory() for t in dev)
+    out_h = torch.empty((spec.batch, spec.q_heads, spec.head_dim), dtype=torch.bfloat16).pin_memory()
+    e2e_ms, h2d, d2h = e2e_run(layers, {"dev": dev, "pinned": pinned, "out": out_h}, args.steps, args.warmup)
+    e2e_ms = max_over_ranks(e2e_ms, ws)
+    e2e_val = ws * nb["step"] * args.steps / (e2e_ms * 1e-3) / 1e9
+    sampler.stop()
+
+    roof = None
+    if per is not None:
+        achieved = nb["split_kernel"] / (per["split_ms"] * 1e-3) / 1e9
+        sha = kernel_source_sha()
+        roof = {"bound": "hbm", "kernel": "decode_split", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} (HBM copy)",
+                "traffic": traffic_from_profile("decode_split_k8v8_b16_ctx8192", sha)
+                if args.dtype == "k8v8" else None,
+                "algorithmic_bytes_per_launch": nb["split_kernel"],
+                "avg_launch_us": per["split_ms"] * 1e3, "source_sha": sha}
+
+    controls = {}
+    del layers
+    torch.cuda.empty_cache()
+    if not args.no_controls:
+        for other in ("k8v8", "k16v8", "k16v16"):
+            if other == args.dtype:
+                continue
+            ls, _, tms, pr, _ = measure_variant(spec, other, args, ws, inp)
+            tms = max_over_ranks(tms, ws)
+            ob = step_bytes(spec, other, T)
+            controls[other] = {"us_per_layer": tms / args.steps * 1e3,
+                               "GBps": ob["step"] * args.steps / (tms * 1e-3) / 1e9,
+                               "split_us": None if pr is None else pr["split_ms"] * 1e3}
+            del ls
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        host_inp = synth.decode_inputs(spec, device="cpu", seq_lens=[T] * 8)
+        dt, nbytes = oracle_sample(host_inp, 8, T)
+        cpu = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"8 of 16 sequences x {T} tokens (e4m3 dequantise + fp64 decode attention), "
+                         f"single thread, {dt:.2f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
+            "pct_of_hbm_peak": 100.0 * value / peak, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": value / PAGE_NUMBER_GBS,
+            "vs_baseline_note": "the pages' ~550 GB/s of codes for this workload, RTX 5070 Ti Triton: context only",
+            "dtype": "fp32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": spec.batch, "q_heads": spec.q_heads,
+                       "kv_heads": spec.kv_heads, "head_dim": spec.head_dim, "ctx": T,
+                       "cache": args.dtype, "layout": "contiguous", "parallelism": f"replicas x{ws}",
+                       "step": "append 1 token/seq + decode split + merge",
+                       "l2": f"{args.layers} distinct layer caches rotated (inputs larger than L2)"},
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "kernels_us": None if per is None else {k.replace("_ms", "_us"): v * 1e3 for k, v in per.items()},
+            "clocks": clocks, "controls": controls,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU (the FP8-KV kernels have no CPU path)")
+        from fp8_quantized_kv_gb300._lib import get_lib
+        get_lib()
+        run_gpu(args, ws, rank)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,306 @@
+// api.cu -- the extern "C" boundary: argument checks, launch configuration,
+// status codes.  Every entry point validates on the host, launches on the
+// caller's stream and returns; nothing here allocates device memory.
+#include <cmath>
+#include <cstring>
+
+#include "params.cuh"
+
+namespace fp8kv {
+
+// Device error word (one per device that loads the library).  Kernels get
+// its address as an argument.
+__device__ unsigned int g_device_error;
+
+static unsigned int* device_error_ptr() {
+  constexpr int kMaxDev = 64;
+  static unsigned int* ptrs[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { (void)cudaGetLastError(); return nullptr; }
+  if (dev < 0 || dev >= kMaxDev) return nullptr;
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) { (void)cudaGetLastError(); return nullptr; }
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  return ptrs[dev];
+}
+
+static int sm_count() {
+  constexpr int kMaxDev = 64;
+  static int counts[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { (void)cudaGetLastError(); return 148; }
+  if (dev < 0 || dev >= kMaxDev) return 148;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = 148;
+    }
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+static fp8kv_status check_cache(const fp8kv_cache* c, CacheView* view) {
+  if (c == nullptr) return FP8KV_ERR_INVALID_ARG;
+  if (c->dtype < FP8KV_K8V8 || c->dtype > FP8KV_K16V16) return FP8KV_ERR_INVALID_ARG;
+  if (c->layout != FP8KV_LAYOUT_CONTIGUOUS && c->layout != FP8KV_LAYOUT_PAGED) return FP8KV_ERR_INVALID_ARG;
+  if (c->batch < 0 || c->kv_heads <= 0 || c->head_dim <= 0) return FP8KV_ERR_INVALID_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128) return FP8KV_ERR_UNSUPPORTED;
+  if (c->k == nullptr || c->v == nullptr) return FP8KV_ERR_INVALID_ARG;
+  const bool k8 = c->dtype == FP8KV_K8V8;
+  const bool v8 = c->dtype != FP8KV_K16V16;
+  if (k8 != (c->k_scale != nullptr) || v8 != (c->v_scale != nullptr)) return FP8KV_ERR_INVALID_ARG;
+  // 16-byte vector copies read the cache: every base pointer must be aligned
+  const uintptr_t align = (uintptr_t)c->k | (uintptr_t)c->v | (uintptr_t)c->k_scale |
+                          (uintptr_t)c->v_scale | (uintptr_t)c->page_table;
+  if (align & 15) return FP8KV_ERR_INVALID_ARG;
+  std::memset(view, 0, sizeof(*view));
+  if (c->layout == FP8KV_LAYOUT_CONTIGUOUS) {
+    if (c->max_tokens < 0) return FP8KV_ERR_INVALID_ARG;
+    if (c->max_tokens % 16 != 0) return FP8KV_ERR_UNSUPPORTED;
+  } else {
+    if (c->page_table == nullptr || c->num_pages <= 0 || c->max_pages_per_seq <= 0)
+      return FP8KV_ERR_INVALID_ARG;
+    if (!is_pow2(c->page_size) || c->page_size < 16 || c->page_size > 64) return FP8KV_ERR_UNSUPPORTED;
+    view->page_size = c->page_size;
+    int sh = 0;
+    while ((1 << sh) < c->page_size) ++sh;
+    view->page_shift = sh;
+    view->num_pages = c->num_pages;
+    view->max_pages_per_seq = c->max_pages_per_seq;
+    view->page_table = c->page_table;
+    view->paged = 1;
+  }
+  view->k = static_cast<const uint8_t*>(c->k);
+  view->v = static_cast<const uint8_t*>(c->v);
+  view->k_scale = c->k_scale;
+  view->v_scale = c->v_scale;
+  view->batch = c->batch;
+  view->kv_heads = c->kv_heads;
+  view->head_dim = c->head_dim;
+  view->max_tokens = c->layout == FP8KV_LAYOUT_CONTIGUOUS ? c->max_tokens : 0;
+  return FP8KV_OK;
+}
+
+static int capacity_of(const fp8kv_cache* c) {
+  return c->layout == FP8KV_LAYOUT_PAGED ? c->max_pages_per_seq * c->page_size : c->max_tokens;
+}
+
+// Split plan: split boundaries are multiples of 64-token tiles anchored at
+// token 0.  Automatic: enough CTAs for about `kCtasPerSm` per SM over the
+// (sequence, KV head) units, each split at least kMinSplitTiles tiles.
+constexpr int kCtasPerSm = 4;
+constexpr int kMinSplitTiles = 2;
+
+struct SplitPlan { int splits, chunk_tiles; };
+
+static SplitPlan plan_splits(const fp8kv_cache* c, int requested) {
+  const int max_tiles = (capacity_of(c) + kTileTokens - 1) / kTileTokens;
+  if (max_tiles <= 0) return {1, 1};
+  int want = requested;
+  if (want <= 0) {
+    const long units = (long)c->batch * c->kv_heads;
+    const long target = (long)kCtasPerSm * sm_count();
+    want = units > 0 ? (int)((target + units - 1) / units) : 1;
+    const int cap_by_min = (max_tiles + kMinSplitTiles - 1) / kMinSplitTiles;
+    if (want > cap_by_min) want = cap_by_min;
+  }
+  if (want < 1) want = 1;
+  if (want > max_tiles) want = max_tiles;
+  const int chunk = (max_tiles + want - 1) / want;
+  const int splits = (max_tiles + chunk - 1) / chunk;
+  return {splits, chunk};
+}
+
+}  // namespace fp8kv
+
+using namespace fp8kv;
+
+static fp8kv_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FP8KV_OK;
+  (void)cudaGetLastError();
+  return FP8KV_ERR_CUDA;
+}
+
+extern "C" {
+
+const char* fp8kv_status_string(fp8kv_status s) {
+  switch (s) {
+    case FP8KV_OK: return "ok";
+    case FP8KV_ERR_INVALID_ARG: return "invalid argument";
+    case FP8KV_ERR_UNSUPPORTED: return "unsupported shape or layout";
+    case FP8KV_ERR_WORKSPACE: return "workspace missing or too small";
+    case FP8KV_ERR_CUDA: return "CUDA runtime error";
+    case FP8KV_ERR_TIMEOUT: return "bounded device wait ran out";
+    case FP8KV_ERR_DEVICE_CHECK: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+fp8kv_status fp8kv_quantize(const void* x, int64_t rows, int32_t head_dim, uint8_t* codes, float* scales,
+                            fp8kv_stream_t stream) {
+  if (rows < 0) return FP8KV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return FP8KV_ERR_UNSUPPORTED;
+  if (rows > 0 && (x == nullptr || codes == nullptr || scales == nullptr)) return FP8KV_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize(x, rows, head_dim, codes, scales, (cudaStream_t)stream));
+}
+
+fp8kv_status fp8kv_append(const fp8kv_cache* cache, const void* k_new, const void* v_new,
+                          const int32_t* seq_idx, const int32_t* pos, int64_t n_tokens,
+                          fp8kv_stream_t stream) {
+  CacheView view;
+  fp8kv_status st = check_cache(cache, &view);
+  if (st != FP8KV_OK) return st;
+  if (n_tokens < 0) return FP8KV_ERR_INVALID_ARG;
+  if (n_tokens == 0) return FP8KV_OK;
+  if (!k_new || !v_new || !seq_idx || !pos) return FP8KV_ERR_INVALID_ARG;
+  unsigned int* err = device_error_ptr();
+  if (!err) return FP8KV_ERR_CUDA;
+  return cuda_status(launch_append(view, cache->dtype, k_new, v_new, seq_idx, pos, n_tokens, err,
+                                   (cudaStream_t)stream));
+}
+
+int32_t fp8kv_decode_num_splits(const fp8kv_cache* cache, int32_t q_heads, int32_t num_splits) {
+  CacheView view;
+  if (check_cache(cache, &view) != FP8KV_OK) return 0;
+  if (q_heads <= 0 || q_heads % cache->kv_heads != 0 || num_splits < 0) return 0;
+  return plan_splits(cache, num_splits).splits;
+}
+
+size_t fp8kv_decode_workspace_bytes(const fp8kv_cache* cache, int32_t q_heads, int32_t num_splits) {
+  const int S = fp8kv_decode_num_splits(cache, q_heads, num_splits);
+  if (S <= 0) return 0;
+  const size_t rows = (size_t)cache->batch * q_heads * S;
+  return rows * ((size_t)cache->head_dim + 2) * sizeof(float);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the decode calls; fills the parameter block and the plan.
+fp8kv_status prepare_decode(const void* q, const fp8kv_cache* cache, const int32_t* seq_lens,
+                            int32_t q_heads, float sm_scale, int32_t num_splits, const void* workspace,
+                            size_t workspace_bytes, bool need_q, DecodeParams* p) {
+  CacheView view;
+  fp8kv_status st = check_cache(cache, &view);
+  if (st != FP8KV_OK) return st;
+  if (q_heads <= 0 || q_heads % cache->kv_heads != 0 || num_splits < 0) return FP8KV_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return FP8KV_ERR_INVALID_ARG;
+  const int G = q_heads / cache->kv_heads;
+  if (G > 8) return FP8KV_ERR_UNSUPPORTED;
+  if (need_q && cache->batch > 0 && (!q || !seq_lens)) return FP8KV_ERR_INVALID_ARG;
+  const SplitPlan plan = plan_splits(cache, num_splits);
+  const size_t need = fp8kv_decode_workspace_bytes(cache, q_heads, num_splits);
+  if (cache->batch > 0 && (workspace == nullptr || workspace_bytes < need)) return FP8KV_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 15) != 0) return FP8KV_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)cache->batch * q_heads;
+  p->c = view;
+  p->q = static_cast<const __nv_bfloat16*>(q);
+  p->seq_lens = seq_lens;
+  p->part_o = static_cast<float*>(const_cast<void*>(workspace));
+  p->part_m = p->part_o + rows * plan.splits * cache->head_dim;
+  p->part_l = p->part_m + rows * plan.splits;
+  p->err = nullptr;
+  p->q_heads = q_heads;
+  p->group = G;
+  p->num_splits = plan.splits;
+  p->chunk_tiles = plan.chunk_tiles;
+  p->scale_log2 = sm_scale * kLog2e;
+  return FP8KV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8kv_status fp8kv_decode_split(const void* q, const fp8kv_cache* cache, const int32_t* seq_lens,
+                                int32_t q_heads, float sm_scale, int32_t num_splits, void* workspace,
+                                size_t workspace_bytes, fp8kv_stream_t stream) {
+  DecodeParams p;
+  fp8kv_status st = prepare_decode(q, cache, seq_lens, q_heads, sm_scale, num_splits, workspace,
+                                   workspace_bytes, true, &p);
+  if (st != FP8KV_OK || cache->batch == 0) return st;
+  p.err = device_error_ptr();
+  if (!p.err) return FP8KV_ERR_CUDA;
+  return cuda_status(launch_decode_fma(p, cache->dtype, cache->batch, (cudaStream_t)stream));
+}
+
+fp8kv_status fp8kv_decode_merge(const fp8kv_cache* cache, int32_t q_heads, int32_t num_splits,
+                                const void* workspace, size_t workspace_bytes, void* out,
+                                int32_t out_dtype, fp8kv_stream_t stream) {
+  if (out_dtype != FP8KV_OUT_BF16 && out_dtype != FP8KV_OUT_F32) return FP8KV_ERR_INVALID_ARG;
+  DecodeParams p;
+  fp8kv_status st = prepare_decode(nullptr, cache, nullptr, q_heads, 1.0f, num_splits, workspace,
+                                   workspace_bytes, false, &p);
+  if (st != FP8KV_OK || cache->batch == 0) return st;
+  if (!out) return FP8KV_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)cache->batch * q_heads;
+  return cuda_status(launch_decode_merge(p.part_o, p.part_m, p.part_l, p.num_splits, rows,
+                                         cache->head_dim, out, out_dtype == FP8KV_OUT_F32,
+                                         (cudaStream_t)stream));
+}
+
+fp8kv_status fp8kv_decode_attention(const void* q, const fp8kv_cache* cache, const int32_t* seq_lens,
+                                    int32_t q_heads, float sm_scale, int32_t num_splits, void* workspace,
+                                    size_t workspace_bytes, void* out, int32_t out_dtype,
+                                    fp8kv_stream_t stream) {
+  if (out_dtype != FP8KV_OUT_BF16 && out_dtype != FP8KV_OUT_F32) return FP8KV_ERR_INVALID_ARG;
+  if (cache != nullptr && cache->batch > 0 && out == nullptr) return FP8KV_ERR_INVALID_ARG;
+  fp8kv_status st = fp8kv_decode_split(q, cache, seq_lens, q_heads, sm_scale, num_splits, workspace,
+                                       workspace_bytes, stream);
+  if (st != FP8KV_OK) return st;
+  return fp8kv_decode_merge(cache, q_heads, num_splits, workspace, workspace_bytes, out, out_dtype,
+                            stream);
+}
+
+fp8kv_status fp8kv_prefill_attention(const void* q, const fp8kv_cache* cache, const int32_t* q_pos0,
+                                     int32_t n_q, int32_t q_heads, float sm_scale, void* out,
+                                     int32_t out_dtype, fp8kv_stream_t stream) {
+  CacheView view;
+  fp8kv_status st = check_cache(cache, &view);
+  if (st != FP8KV_OK) return st;
+  if (n_q < 0 || q_heads <= 0 || q_heads % cache->kv_heads != 0) return FP8KV_ERR_INVALID_ARG;
+  if (out_dtype != FP8KV_OUT_BF16 && out_dtype != FP8KV_OUT_F32) return FP8KV_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return FP8KV_ERR_INVALID_ARG;
+  if (q_heads / cache->kv_heads > 16) return FP8KV_ERR_UNSUPPORTED;
+  if (cache->batch == 0 || n_q == 0) return FP8KV_OK;
+  if (!q || !q_pos0 || !out) return FP8KV_ERR_INVALID_ARG;
+  if (n_q > capacity_of(cache)) return FP8KV_ERR_INVALID_ARG;
+  unsigned int* err = device_error_ptr();
+  if (!err) return FP8KV_ERR_CUDA;
+  PrefillParams p;
+  p.c = view;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.q_pos0 = q_pos0;
+  p.out = out;
+  p.err = err;
+  p.n_q = n_q;
+  p.q_heads = q_heads;
+  p.group = q_heads / cache->kv_heads;
+  p.out_f32 = out_dtype == FP8KV_OUT_F32;
+  p.scale_log2 = sm_scale * kLog2e;
+  return cuda_status(launch_prefill_fma(p, cache->dtype, cache->batch, (cudaStream_t)stream));
+}
+
+fp8kv_status fp8kv_get_device_error(uint32_t* bits, int32_t clear) {
+  if (bits == nullptr) return FP8KV_ERR_INVALID_ARG;
+  unsigned int v = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+  if (e == cudaSuccess && clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+  }
+  if (e != cudaSuccess) return cuda_status(e);
+  *bits = v;
+  if (v & FP8KV_DEVERR_TIMEOUT) return FP8KV_ERR_TIMEOUT;
+  return v ? FP8KV_ERR_DEVICE_CHECK : FP8KV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,133 @@
+// common.cuh -- device helpers shared by the FP8-KV kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp8kv.h"
+
+namespace fp8kv {
+
+constexpr int kTileTokens = 64;       // KV tile (tokens) of every attention kernel
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kTwoPow120 = 1.329227995784916e36f;   // 2^120, exact in fp32
+
+// Cache element kinds, resolved at compile time per kernel instance.
+enum : int { ELEM_E4M3 = 0, ELEM_BF16 = 1 };
+
+// Plain-data view of a cache, passed by value to kernels.
+struct CacheView {
+  const uint8_t* k;
+  const uint8_t* v;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* page_table;
+  int batch, kv_heads, head_dim;
+  int max_tokens;                  // contiguous capacity
+  int page_size, page_shift, num_pages, max_pages_per_seq;
+  int paged;
+};
+
+__device__ __forceinline__ void raise_error(unsigned int* err, unsigned int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// ---------------------------------------------------------------- e4m3 ----
+// E4M3 -> fp32 by moving bits: sign to bit 31, the 7 exponent+mantissa bits
+// to bits 20..26.  The result is the code's value times 2^-120 (fp32 bias 127
+// vs E4M3 bias 7), exact for every finite code, subnormals included (they
+// land on fp32 subnormals, which the FMA pipe keeps since nothing here is
+// compiled with flush-to-zero).  Callers multiply the 2^120 back in once per
+// dot product or output row.  Byte i of the word is element i.
+__device__ __forceinline__ void e4m3x4_to_f32_scaled(uint32_t w, float (&f)[4]) {
+  f[0] = __int_as_float(((int)(w << 24) >> 4) & 0x87F00000);
+  f[1] = __int_as_float(((int)(w << 16) >> 4) & 0x87F00000);
+  f[2] = __int_as_float(((int)(w << 8) >> 4) & 0x87F00000);
+  f[3] = __int_as_float(((int)w >> 4) & 0x87F00000);
+}
+
+// bf16 pair (one 32-bit word, element 0 in the low half) -> two exact fp32.
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float (&f)[2]) {
+  f[0] = __uint_as_float(w << 16);
+  f[1] = __uint_as_float(w & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// ------------------------------------------------------------ cp.async ----
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  uint32_t s = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem_src));
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::);
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ------------------------------------------------------------- swizzle ----
+// 16-byte chunk permutation inside a shared-memory row of `cpr` chunks, so
+// that threads reading the same logical chunk of consecutive rows hit
+// different bank groups.  Rows of >= 8 chunks XOR the low 3 bits with the row
+// index; 4-chunk rows (two per 128-byte bank line) XOR with row/2.
+__device__ __forceinline__ int swz_chunk(int chunk, int row, int cpr) {
+  return cpr >= 8 ? (chunk ^ (row & 7)) : (chunk ^ ((row >> 1) & 3));
+}
+
+// ----------------------------------------------------------- reductions ---
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Location of cache row (sequence b, KV head h, token t) in elements of
+// head_dim; returns -1 (and raises an error bit) for an invalid page.
+__device__ __forceinline__ int64_t cache_row(const CacheView& c, int b, int h, int t,
+                                             unsigned int* err) {
+  if (c.paged) {
+    int pi = t >> c.page_shift;
+    if (pi >= c.max_pages_per_seq) { raise_error(err, FP8KV_DEVERR_SEQ_TOO_LONG); return -1; }
+    int page = c.page_table[(int64_t)b * c.max_pages_per_seq + pi];
+    if (page < 0 || page >= c.num_pages) { raise_error(err, FP8KV_DEVERR_BAD_PAGE); return -1; }
+    return ((int64_t)page * c.kv_heads + h) * c.page_size + (t & (c.page_size - 1));
+  }
+  if (t >= c.max_tokens) { raise_error(err, FP8KV_DEVERR_SEQ_TOO_LONG); return -1; }
+  return ((int64_t)b * c.kv_heads + h) * c.max_tokens + t;
+}
+
+__device__ __forceinline__ int cache_capacity(const CacheView& c) {
+  return c.paged ? c.max_pages_per_seq * c.page_size : c.max_tokens;
+}
+
+// Opt a kernel into `bytes` of dynamic shared memory, once per (kernel,
+// device).  A failure is read and cleared before it is returned, so that it
+// does not stay pending on the stream.
+inline cudaError_t ensure_smem_optin(const void* func, int bytes) {
+  constexpr int kMaxDev = 64, kMaxFn = 128;
+  static const void* done_fn[kMaxDev][kMaxFn];
+  static int done_n[kMaxDev];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { (void)cudaGetLastError(); return e; }
+  if (dev < 0 || dev >= kMaxDev) dev = 0;
+  for (int i = 0; i < done_n[dev]; ++i)
+    if (done_fn[dev][i] == func) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) { (void)cudaGetLastError(); return e; }
+  if (done_n[dev] < kMaxFn) done_fn[dev][done_n[dev]++] = func;
+  return cudaSuccess;
+}
+
+}  // namespace fp8kv

@@ -1,0 +1,41 @@
+// params.cuh -- kernel parameter blocks and launcher declarations shared by
+// the C-ABI layer (api.cu) and the kernel translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace fp8kv {
+
+struct DecodeParams {
+  CacheView c;
+  const __nv_bfloat16* q;    // [B][Hq][D]
+  const int32_t* seq_lens;   // [B]
+  float* part_o;             // [B][Hq][S][D]  unnormalised O of each split
+  float* part_m;             // [B][Hq][S]     running max, log2 domain
+  float* part_l;             // [B][Hq][S]     running sum
+  unsigned int* err;         // device error word
+  int q_heads, group, num_splits, chunk_tiles;
+  float scale_log2;          // sm_scale * log2(e)
+};
+
+struct PrefillParams {
+  CacheView c;
+  const __nv_bfloat16* q;    // [B][n_q][Hq][D]
+  const int32_t* q_pos0;     // [B]
+  void* out;                 // [B][n_q][Hq][D]
+  unsigned int* err;
+  int n_q, q_heads, group, out_f32;
+  float scale_log2;
+};
+
+cudaError_t launch_quantize(const void* x, int64_t rows, int head_dim, uint8_t* codes, float* scales,
+                            cudaStream_t s);
+cudaError_t launch_append(const CacheView& c, int dtype, const void* k_new, const void* v_new,
+                          const int32_t* seq_idx, const int32_t* pos, int64_t n_tokens,
+                          unsigned int* err, cudaStream_t s);
+cudaError_t launch_decode_fma(const DecodeParams& p, int dtype, int batch, cudaStream_t st);
+cudaError_t launch_decode_merge(const float* part_o, const float* part_m, const float* part_l, int S,
+                                int64_t rows, int head_dim, void* out, int out_f32, cudaStream_t st);
+cudaError_t launch_prefill_fma(const PrefillParams& p, int dtype, int batch, cudaStream_t st);
+
+}  // namespace fp8kv

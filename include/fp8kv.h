@@ -1,0 +1,205 @@
+/*
+ * fp8kv.h -- C ABI of the GB300 (sm_103a) FP8-KV attention library.
+ *
+ * Fused attention over a quantised KV cache.  K and V live in HBM as FP8 E4M3
+ * codes with one fp32 scale per (token, KV head), scale = amax(|row|)/448 over
+ * the head dimension, written once when the token is appended ("FP8 KV cache
+ * (fp8_kv, opt-in)", bullet "Storage").  K may instead be kept in bf16
+ * ("K16/V8", "Fused KV-cache quantization", section "FlashInfer K16/V8"), and a
+ * bf16/bf16 cache is provided as the control ("FP8 KV attention: hardware
+ * paths and tile preparation", section "Collect the profiler evidence", the
+ * four dtype controls).  Attention folds the K scale into the scores and the V
+ * scale into P, with P rounded to bf16 before P.V ("FP8 KV cache", bullet
+ * "Math"), and advances an online softmax tile by tile ("03 · 8n — FA-style
+ * tiled prefill attention", section 2.1).
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no memory.  Scratch space for decode is sized by
+ *    fp8kv_decode_workspace_bytes() and passed in.
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream) and returns a status; no C++ exception crosses the ABI.
+ *  - A CUDA launch error is read and cleared (cudaGetLastError) before
+ *    FP8KV_ERR_CUDA is returned, so it does not poison later work on the
+ *    stream ("03 · 8n", section 3.3, the shared-memory opt-in pitfall).
+ *  - Data-dependent faults found on the device (a sequence longer than the
+ *    cache, a page id out of range, a bounded wait that ran out) never fault
+ *    the GPU: the kernel skips the access and raises a bit in a device error
+ *    word, read with fp8kv_get_device_error().
+ *  - bf16 means IEEE binary32 truncated to its upper 16 bits (torch.bfloat16);
+ *    codes are OCP E4M3 bytes (torch.float8_e4m3fn).
+ *  - Supported shapes: head_dim 64 or 128; q_heads a multiple of kv_heads with
+ *    group size q_heads/kv_heads from 1 to 8 for decode and from 1 to 16 for
+ *    prefill; page_size 16, 32 or 64; contiguous capacity max_tokens a
+ *    multiple of 16.  Anything else returns FP8KV_ERR_UNSUPPORTED.
+ */
+#ifndef FP8KV_H
+#define FP8KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define FP8KV_API __attribute__((visibility("default")))
+#else
+#define FP8KV_API
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA. */
+typedef struct CUstream_st *fp8kv_stream_t;
+
+typedef enum {
+  FP8KV_OK = 0,
+  FP8KV_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad enum */
+  FP8KV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, group, page size */
+  FP8KV_ERR_WORKSPACE = 3,     /* workspace pointer null or too small */
+  FP8KV_ERR_CUDA = 4,          /* a CUDA runtime call failed (error cleared) */
+  FP8KV_ERR_TIMEOUT = 5,       /* a bounded device wait ran out */
+  FP8KV_ERR_DEVICE_CHECK = 6   /* the device error word is non-zero */
+} fp8kv_status;
+
+/* Cache element types: which of K and V are E4M3 codes and which are bf16. */
+typedef enum {
+  FP8KV_K8V8 = 0,    /* K codes, V codes (symmetric FP8)            */
+  FP8KV_K16V8 = 1,   /* K bf16, V codes (no K transform)           */
+  FP8KV_K16V16 = 2   /* K bf16, V bf16 (the bf16-cache control)     */
+} fp8kv_kv_dtype;
+
+typedef enum {
+  FP8KV_LAYOUT_CONTIGUOUS = 0,  /* k, v: [batch][kv_heads][max_tokens][head_dim]
+                                   scales: [batch][kv_heads][max_tokens]       */
+  FP8KV_LAYOUT_PAGED = 1        /* k, v: [num_pages][kv_heads][page_size][head_dim]
+                                   scales: [num_pages][kv_heads][page_size]
+                                   token t of sequence b sits in page
+                                   page_table[b][t / page_size], slot t % page_size */
+} fp8kv_layout;
+
+typedef enum { FP8KV_OUT_BF16 = 0, FP8KV_OUT_F32 = 1 } fp8kv_out_dtype;
+
+/* Device error word bits (fp8kv_get_device_error). */
+#define FP8KV_DEVERR_SEQ_TOO_LONG 0x1u   /* a length/position exceeds the cache */
+#define FP8KV_DEVERR_BAD_PAGE 0x2u       /* a page id outside [0, num_pages)    */
+#define FP8KV_DEVERR_TIMEOUT 0x4u        /* a bounded mbarrier wait ran out    */
+
+/* A KV cache.  The struct is read on the host at every call (pass it by
+ * pointer; it may live on the stack).  All pointers are device pointers owned
+ * by the caller and 16-byte aligned.  For a bf16 side the scale pointer must
+ * be NULL. */
+typedef struct {
+  int32_t dtype;              /* fp8kv_kv_dtype                                */
+  int32_t layout;             /* fp8kv_layout                                  */
+  int32_t batch;              /* sequences (rows of page_table)                */
+  int32_t kv_heads;
+  int32_t head_dim;           /* 64 or 128                                     */
+  int32_t max_tokens;         /* contiguous: capacity per sequence (mult. of 16) */
+  int32_t page_size;          /* paged: tokens per page (16, 32 or 64)         */
+  int32_t num_pages;          /* paged: pages in the pool                      */
+  int32_t max_pages_per_seq;  /* paged: columns of page_table                  */
+  int32_t reserved;
+  void *k;                    /* e4m3 codes (uint8) or bf16, layout above      */
+  void *v;
+  float *k_scale;             /* fp32 per (token, KV head); NULL if K is bf16  */
+  float *v_scale;             /* NULL if V is bf16                             */
+  const int32_t *page_table;  /* paged: [batch][max_pages_per_seq]; else NULL  */
+} fp8kv_cache;
+
+/* Quantise `rows` rows of `head_dim` bf16 values into E4M3 codes and one fp32
+ * scale per row ("FP8 KV cache (fp8_kv, opt-in)", bullet "Storage",
+ * quantize_fp8_kv): scale = amax(|row|)/448 (IEEE fp32 division), code =
+ * round-to-nearest-even, saturating encode of the IEEE fp32 quotient x/scale;
+ * an all-zero row gets scale 0 and codes 0x00.
+ *   x:      [rows][head_dim] bf16      codes: [rows][head_dim] uint8
+ *   scales: [rows] fp32 */
+FP8KV_API fp8kv_status fp8kv_quantize(const void *x, int64_t rows, int32_t head_dim,
+                            uint8_t *codes, float *scales,
+                            fp8kv_stream_t stream);
+
+/* Append new tokens to the cache: each (token, KV head) row of K and of V is
+ * quantised as in fp8kv_quantize (or copied, for a bf16 side) and written
+ * once into its slot ("FP8 KV cache", bullet "Storage", Fp8KVCache.append).
+ *   k_new, v_new: [n_tokens][kv_heads][head_dim] bf16
+ *   seq_idx, pos: [n_tokens] int32 device arrays; token i goes to sequence
+ *                 seq_idx[i] at position pos[i].
+ * Rows whose position is outside the cache, or whose page id is out of range,
+ * are skipped and raise a device error bit. */
+FP8KV_API fp8kv_status fp8kv_append(const fp8kv_cache *cache, const void *k_new,
+                          const void *v_new, const int32_t *seq_idx,
+                          const int32_t *pos, int64_t n_tokens,
+                          fp8kv_stream_t stream);
+
+/* The flash-decoding split count a decode call will use for `num_splits`
+ * (0 = automatic: about four CTAs per SM, "FP8 KV cache", bullet "Speed").
+ * Returns 0 on invalid arguments. */
+FP8KV_API int32_t fp8kv_decode_num_splits(const fp8kv_cache *cache, int32_t q_heads,
+                                int32_t num_splits);
+
+/* Bytes of workspace fp8kv_decode_attention needs for these arguments: the
+ * fp32 partials (O, m, l) of every (sequence, query head, split). */
+FP8KV_API size_t fp8kv_decode_workspace_bytes(const fp8kv_cache *cache, int32_t q_heads,
+                                    int32_t num_splits);
+
+/* Decode attention: one query token per sequence, grouped-query heads, per-
+ * sequence lengths ("FP8 KV cache", bullet "Math", fp8_kv_attention).  Kernel
+ * 1 splits each sequence's cache over CTAs (flash-decoding, bullet "Speed")
+ * and writes fp32 partials; kernel 2 merges them.
+ *   q:        [batch][q_heads][head_dim] bf16; query head h reads KV head
+ *             h / (q_heads / kv_heads)
+ *   seq_lens: [batch] int32 device array; sequence b attends its tokens
+ *             0..seq_lens[b]-1; a length of 0 gives a zero output row
+ *   sm_scale: softmax scale (1/sqrt(head_dim) in the usual case)
+ *   out:      [batch][q_heads][head_dim], bf16 or fp32 per out_dtype
+ * Split boundaries are multiples of 64 tokens, so results for different
+ * num_splits differ only by fp32 re-association. */
+FP8KV_API fp8kv_status fp8kv_decode_attention(const void *q, const fp8kv_cache *cache,
+                                    const int32_t *seq_lens, int32_t q_heads,
+                                    float sm_scale, int32_t num_splits,
+                                    void *workspace, size_t workspace_bytes,
+                                    void *out, int32_t out_dtype,
+                                    fp8kv_stream_t stream);
+
+/* The two kernels of fp8kv_decode_attention as separate calls (same
+ * arguments, same results).  fp8kv_decode_split runs the flash-decoding split
+ * kernel and leaves the fp32 partials in `workspace`; fp8kv_decode_merge
+ * reduces them into `out`.  Both must be given the same cache, q_heads and
+ * num_splits, and the merge must follow the split on the same stream (or be
+ * ordered after it). */
+FP8KV_API fp8kv_status fp8kv_decode_split(const void *q, const fp8kv_cache *cache,
+                                          const int32_t *seq_lens, int32_t q_heads,
+                                          float sm_scale, int32_t num_splits,
+                                          void *workspace, size_t workspace_bytes,
+                                          fp8kv_stream_t stream);
+FP8KV_API fp8kv_status fp8kv_decode_merge(const fp8kv_cache *cache, int32_t q_heads,
+                                          int32_t num_splits, const void *workspace,
+                                          size_t workspace_bytes, void *out,
+                                          int32_t out_dtype, fp8kv_stream_t stream);
+
+/* Causal prefill attention over the cache ("03 · 8n — FA-style tiled prefill
+ * attention", sections 2-3): 64-token query tiles, online softmax over
+ * 64-token KV tiles.  Query i of sequence b sits at absolute position
+ * q_pos0[b] + i and attends cache tokens 0..q_pos0[b]+i (the cache must
+ * already hold them: append first).
+ *   q:      [batch][n_q][q_heads][head_dim] bf16
+ *   q_pos0: [batch] int32 device array
+ *   out:    [batch][n_q][q_heads][head_dim], bf16 or fp32 per out_dtype */
+FP8KV_API fp8kv_status fp8kv_prefill_attention(const void *q, const fp8kv_cache *cache,
+                                     const int32_t *q_pos0, int32_t n_q,
+                                     int32_t q_heads, float sm_scale, void *out,
+                                     int32_t out_dtype, fp8kv_stream_t stream);
+
+/* Read (and, if `clear` is non-zero, reset) the device error word of the
+ * current device.  Synchronous: waits for all work on the device. */
+FP8KV_API fp8kv_status fp8kv_get_device_error(uint32_t *bits, int32_t clear);
+
+/* Human-readable name of a status. */
+FP8KV_API const char *fp8kv_status_string(fp8kv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8KV_H */

@@ -1,0 +1,84 @@
+"""Test helpers: fill GPU caches through the C ABI from seeded synthetic
+inputs, and compute oracle references from the same bf16 bits.
+
+Nothing here does method arithmetic of its own: the GPU side calls the
+library, the reference side calls the oracle."""
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from fp8_quantized_kv_gb300 import synth
+import fp8_quantized_kv_gb300 as fk
+
+
+def fill_cache(inp: synth.DecodeInputs, dtype: str, device="cuda", capacity=None):
+    """Append every token of a decode workload into a new cache (contiguous or
+    paged per the workload) through fp8kv_append.  Returns the cache."""
+    spec = inp.spec
+    B = inp.seq_lens.numel()
+    if spec.page_size is None:
+        cap = capacity or max(16, ((inp.max_len + 63) // 64) * 64)
+        cache = fk.Fp8KVCache.contiguous(B, spec.kv_heads, spec.head_dim, cap, dtype, device)
+    else:
+        cache = fk.Fp8KVCache.paged(inp.page_table, inp.num_pages, spec.kv_heads, spec.head_dim,
+                                    spec.page_size, dtype, device)
+    lens = inp.seq_lens.to(torch.int64)
+    seq_idx = torch.repeat_interleave(torch.arange(B), lens).to(torch.int32)
+    pos = torch.cat([torch.arange(int(n)) for n in lens]).to(torch.int32) if B else torch.zeros(0, dtype=torch.int32)
+    fk.fp8kv_append(cache, inp.k.to(device).contiguous(), inp.v.to(device).contiguous(),
+                    seq_idx.to(device), pos.to(device))
+    return cache
+
+
+def seq_bits(inp: synth.DecodeInputs, which: str, b: int):
+    """bf16 bits of sequence b's K or V rows, as [Hkv, T_b, D]."""
+    t = inp.k if which == "k" else inp.v
+    s, e = int(inp.cu_seqlens[b]), int(inp.cu_seqlens[b + 1])
+    return synth.bf16_bits(t[s:e]).transpose(1, 0, 2)
+
+
+def oracle_kv(inp: synth.DecodeInputs, dtype: str, b: int):
+    """fp64 K and V of sequence b as the cache holds them: e4m3 round trip
+    for an FP8 side, the bf16 value for a bf16 side.  [Hkv, T_b, D]."""
+    out = []
+    for which, fp8 in (("k", dtype == "k8v8"), ("v", dtype != "k16v16")):
+        bits = seq_bits(inp, which, b)
+        if fp8:
+            c, s = oracle.quantize(bits)
+            out.append(oracle.dequantize(c, s))
+        else:
+            out.append(oracle.bf16_to_double(bits))
+    return out
+
+
+def oracle_decode(inp: synth.DecodeInputs, dtype: str, batch_ids, sm_scale=None):
+    """Oracle decode outputs [len(batch_ids), Hq, D] for the listed sequences."""
+    spec = inp.spec
+    D = spec.head_dim
+    sm = 1.0 / math.sqrt(D) if sm_scale is None else sm_scale
+    q_all = oracle.bf16_to_double(synth.bf16_bits(inp.q))
+    res = []
+    for b in batch_ids:
+        T = int(inp.seq_lens[b])
+        k, v = oracle_kv(inp, dtype, b)
+        Tc = max(T, 1)
+        kk = np.zeros((1, spec.kv_heads, Tc, D))
+        vv = np.zeros((1, spec.kv_heads, Tc, D))
+        kk[0, :, :T] = k
+        vv[0, :, :T] = v
+        res.append(oracle.decode_attention(q_all[b:b + 1], kk, vv, np.array([T], np.int32), sm)[0])
+    return np.stack(res) if res else np.zeros((0, spec.q_heads, D))
+
+
+def gpu_decode(inp, cache, num_splits=0, out_dtype=torch.float32):
+    q = inp.q.to("cuda").contiguous()
+    lens = inp.seq_lens.to("cuda")
+    return fk.fp8kv_decode_attention(q, cache, lens, num_splits=num_splits, out_dtype=out_dtype)
+
+
+def assert_gate(out, ref, what, rel_l2=1e-2, max_abs=2e-2):
+    ok, rel, mab = oracle.attention_gate(out, ref, rel_l2, max_abs)
+    assert ok, f"{what}: worst rel-L2 {rel:.3e}, worst max-abs {mab:.3e}"
+    return rel, mab

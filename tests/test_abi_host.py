@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI and of the workload generator.  No GPU: the
+library is loaded and its argument checks are exercised, but no kernel runs."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+from fp8_quantized_kv_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8kv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_quantized_kv_gb300 import build as kbuild
+    from fp8_quantized_kv_gb300._lib import get_lib
+    kbuild.build()
+    return get_lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return re.findall(r"FP8KV_API\s+[\w\s\*]+?\b(fp8kv_\w+)\s*\(", text)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    from fp8_quantized_kv_gb300._lib import EXPORTS
+    assert set(EXPORTS) == set(names)
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.fp8kv_status_string(s)
+    assert lib.fp8kv_status_string(99) == b"unknown status"
+
+
+def _cache(**kw):
+    from fp8_quantized_kv_gb300._lib import CacheStruct
+    base = dict(dtype=0, layout=0, batch=16, kv_heads=2, head_dim=128, max_tokens=8192,
+                k=0x1000, v=0x2000, k_scale=0x3000, v_scale=0x4000)
+    base.update(kw)
+    return CacheStruct(**base)
+
+
+def test_argument_checks_return_before_any_launch(lib):
+    # every case below is rejected on the host, before any CUDA call
+    c = _cache()
+    r = ctypes.byref
+    assert lib.fp8kv_quantize(None, -1, 128, None, None, None) == 1
+    assert lib.fp8kv_quantize(None, 10, 96, None, None, None) == 2
+    assert lib.fp8kv_quantize(None, 10, 128, None, None, None) == 1
+    assert lib.fp8kv_decode_attention(None, None, None, 16, 0.1, 0, None, 0, None, 0, None) == 1
+    bad_dim = _cache(head_dim=96)
+    out = 0x6000        # never dereferenced: each call is rejected first
+    assert lib.fp8kv_decode_attention(None, r(bad_dim), None, 16, 0.1, 0, None, 0, out, 0, None) == 2
+    assert lib.fp8kv_decode_attention(None, r(c), None, 15, 0.1, 0, None, 0, out, 0, None) == 1
+    assert lib.fp8kv_decode_attention(None, r(c), None, 16, 0.1, 0, None, 0, out, 7, None) == 1
+    assert lib.fp8kv_decode_attention(0x7000, r(c), 0x8000, 16, 0.1, 0, None, 0, out, 0, None) == 3
+    no_scale = _cache(k_scale=None)
+    assert lib.fp8kv_decode_attention(None, r(no_scale), None, 16, 0.1, 0, None, 0, out, 0, None) == 1
+    odd_cap = _cache(max_tokens=100)
+    assert lib.fp8kv_append(r(odd_cap), None, None, None, None, 1, None) == 2
+    paged_bad = _cache(layout=1, page_size=8, num_pages=4, max_pages_per_seq=2, page_table=0x5000)
+    assert lib.fp8kv_append(r(paged_bad), None, None, None, None, 1, None) == 2
+    paged_nopt = _cache(layout=1, page_size=16, num_pages=4, max_pages_per_seq=2)
+    assert lib.fp8kv_decode_num_splits(r(paged_nopt), 16, 0) == 0
+    big_group = _cache(kv_heads=1)
+    assert lib.fp8kv_decode_split(None, r(big_group), None, 16, 0.1, 0, None, 0, None) == 2
+
+
+def test_split_plan_and_workspace(lib):
+    c = _cache()
+    r = ctypes.byref
+    # explicit split counts: chunks are whole 64-token tiles anchored at 0
+    assert lib.fp8kv_decode_num_splits(r(c), 16, 1) == 1
+    assert lib.fp8kv_decode_num_splits(r(c), 16, 7) == 7           # 128 tiles -> 19 per split
+    assert lib.fp8kv_decode_num_splits(r(c), 16, 10 ** 6) == 128    # at most one tile each
+    S = lib.fp8kv_decode_num_splits(r(c), 16, 0)
+    assert 1 <= S <= 128
+    ws = lib.fp8kv_decode_workspace_bytes(r(c), 16, 0)
+    assert ws == 16 * 16 * S * (128 + 2) * 4
+
+
+def test_workloads_match_their_description():
+    spec = synth.WORKLOADS["paged_b64_hostile"]
+    # the lengths of the full paged workload, drawn as decode_inputs draws them
+    cpu = torch.Generator().manual_seed(spec.seed)
+    lens = torch.randint(1024, 16385, (64,), generator=cpu)
+    assert lens.min() >= 1024 and lens.max() <= 16384
+    small = synth.DecodeWorkload("s", 5, 8, 2, 64, seed=3, len_range=(1, 100), page_size=16,
+                                 hostile_keys=True)
+    inp = synth.decode_inputs(small)
+    P = 16
+    used = inp.page_table[inp.page_table >= 0]
+    assert sorted(used.tolist()) == list(range(inp.num_pages))      # a permutation of the pool
+    for b in range(5):
+        n = (int(inp.seq_lens[b]) + P - 1) // P
+        assert (inp.page_table[b, :n] >= 0).all() and (inp.page_table[b, n:] == -1).all()
+    # hostile keys: the four biased channels sit near +20
+    k = inp.k.float()
+    for c in synth.HOSTILE_CHANNELS:
+        if c < 64:
+            assert abs(k[..., c].mean().item() - 20) < 1.0
+    assert abs(inp.v.float().mean().item()) < 0.2
+    # determinism
+    again = synth.decode_inputs(small)
+    assert torch.equal(again.k, inp.k) and torch.equal(again.page_table, inp.page_table)
