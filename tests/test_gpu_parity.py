@@ -84,6 +84,8 @@ def test_append_bit_exact(dtype, paged):
         T = int(inp.seq_lens[b])
         for which, fp8 in (("k", dtype == "k8v8"), ("v", dtype != "k16v16")):
             store = cache.k if which == "k" else cache.v
+            if store.dtype == torch.bfloat16:
+                store = store.view(torch.int16)
             sc = cache.k_scale if which == "k" else cache.v_scale
             if paged:
                 got = oracle.gather_paged(store.cpu().numpy(), inp.page_table.numpy(), b, T)
