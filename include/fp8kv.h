@@ -178,6 +178,33 @@ FP8KV_API fp8kv_status fp8kv_decode_merge(const fp8kv_cache *cache, int32_t q_he
                                           size_t workspace_bytes, void *out,
                                           int32_t out_dtype, fp8kv_stream_t stream);
 
+/* Decode attention that allocates nothing (the paper has no counterpart:
+ * this is a convenience of the library).  Same arguments and results as
+ * fp8kv_decode_attention without the workspace: the fp32 partials go to a
+ * fixed array of fp8kv_decode_static_scratch_bytes() bytes (16 MiB) compiled
+ * into the library, which every GPU that loads the library keeps until the
+ * process exits.  It is for callers that cannot call cudaMalloc -- for
+ * example a runtime whose memory pool owns the device and forbids
+ * allocation on its serving path, or a plugin given only its input and
+ * output tensors.  The call makes no cudaMalloc, cudaFree or allocating
+ * library call.
+ *  - A call whose partials would not fit (fp8kv_decode_workspace_bytes above
+ *    the array size) returns FP8KV_ERR_WORKSPACE and launches nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array and it keeps the last call's
+ *    contents; nothing in it needs to start at zero.  Calls that overlap on
+ *    the GPU (other streams, or other host threads) race on it: order them. */
+FP8KV_API fp8kv_status fp8kv_decode_attention_static(const void *q, const fp8kv_cache *cache,
+                                                     const int32_t *seq_lens, int32_t q_heads,
+                                                     float sm_scale, int32_t num_splits,
+                                                     void *out, int32_t out_dtype,
+                                                     fp8kv_stream_t stream);
+
+/* Size in bytes of the fixed array used by fp8kv_decode_attention_static. */
+FP8KV_API size_t fp8kv_decode_static_scratch_bytes(void);
+
 /* Causal prefill attention over the cache ("03 · 8n — FA-style tiled prefill
  * attention", sections 2-3): 64-token query tiles, online softmax over
  * 64-token KV tiles.  Query i of sequence b sits at absolute position

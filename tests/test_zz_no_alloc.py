@@ -1,0 +1,66 @@
+"""The allocation-free decode entry point, fp8kv_decode_attention_static.
+
+It serves callers that cannot call cudaMalloc (a runtime whose pool owns the
+device memory, a plugin handed only its tensors): the partials live in a fixed
+array inside the library instead of a caller-allocated workspace.  Checked
+through the C ABI against fp8kv_decode_attention on the same inputs, on two
+calls in a row (the array keeps the previous call's contents).  This file is
+collected last on purpose."""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from fp8_quantized_kv_gb300 import synth
+import fp8_quantized_kv_gb300 as fk
+from fp8_quantized_kv_gb300._lib import get_lib
+from kvhelpers import fill_cache
+
+pytestmark = pytest.mark.gpu
+
+
+def _static_call(lib, q, cache, lens, out):
+    st = lib.fp8kv_decode_attention_static(
+        ctypes.c_void_p(q.data_ptr()), cache.struct_ref, ctypes.c_void_p(lens.data_ptr()),
+        q.shape[1], ctypes.c_float(1.0 / math.sqrt(q.shape[2])), 0,
+        ctypes.c_void_p(out.data_ptr()), 1, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, fk.fp8kv_status_string(st)
+
+
+def test_static_scratch_decode_matches_workspace_decode():
+    lib = get_lib()
+    assert lib.fp8kv_decode_static_scratch_bytes() == 16 << 20
+    cases = [synth.WORKLOADS["decode_b16_ctx8192"], synth.WORKLOADS["tiny_decode"]]
+    for spec in cases:                        # two different calls in a row
+        inp = synth.decode_inputs(spec, device="cuda")
+        cache = fill_cache(inp, "k8v8")
+        q = inp.q.contiguous()
+        lens = inp.seq_lens.cuda()
+        ref = fk.fp8kv_decode_attention(q, cache, lens, out_dtype=torch.float32)
+        for _ in range(2):
+            out = torch.full_like(ref, float("nan"))
+            _static_call(lib, q, cache, lens, out)
+            torch.cuda.synchronize()
+            o, r = out.double().cpu().numpy(), ref.double().cpu().numpy()
+            rel = np.linalg.norm(o - r, axis=-1) / np.linalg.norm(r, axis=-1)
+            assert np.all(np.isfinite(o))
+            assert rel.max() <= 1e-5 and np.abs(o - r).max() <= 2e-2
+
+
+def test_static_scratch_rejects_oversized_calls():
+    lib = get_lib()
+    # batch 16 x 16 query heads x 128 splits of (128 + 2) fp32 partials is
+    # 17,039,360 bytes: just above the 16 MiB array, so the call is refused
+    cache = fk.Fp8KVCache.contiguous(16, 2, 128, 8192, "k8v8")
+    q = torch.zeros(16, 16, 128, dtype=torch.bfloat16, device="cuda")
+    lens = torch.full((16,), 8192, dtype=torch.int32, device="cuda")
+    out = torch.empty(16, 16, 128, dtype=torch.float32, device="cuda")
+    assert fk.fp8kv_decode_workspace_bytes(cache, 16, 128) == 17039360
+    st = lib.fp8kv_decode_attention_static(
+        ctypes.c_void_p(q.data_ptr()), cache.struct_ref, ctypes.c_void_p(lens.data_ptr()), 16,
+        ctypes.c_float(0.1), 128, ctypes.c_void_p(out.data_ptr()), 1, None)
+    assert st == 3
+    # one split fewer fits
+    assert fk.fp8kv_decode_workspace_bytes(cache, 16, 120) <= lib.fp8kv_decode_static_scratch_bytes()
