@@ -34,6 +34,7 @@ from fp8_quantized_kv_gb300 import synth  # noqa: E402
 
 WORKLOAD = "decode_b16_ctx8192"
 METRIC = "decode attn KV-read GB/s (% of HBM peak) and µs/layer at B16 ctx8192, 1 GB300"
+KERNEL_IDS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
 PAGE_NUMBER_GBS = 550.0   # the pages' figure for this workload (RTX 5070 Ti, Triton, codes only)
 
 
@@ -46,6 +47,7 @@ def parse():
     ap.add_argument("--dtype", default="k8v8", choices=["k8v8", "k16v8", "k16v16"])
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--chunk", type=int, default=200)
+    ap.add_argument("--kernel", default="auto", choices=["auto", "cuda_cores", "tensor_cores"])
     ap.add_argument("--no-controls", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -273,7 +275,7 @@ def run_reference(args, ws, rank):
 class Layer:
     """One layer: its own cache plus pre-built C-ABI argument tuples."""
 
-    def __init__(self, cache, q, lens, ws_tensor, out, knew, vnew, sidx, pos, Hq, sm_scale):
+    def __init__(self, cache, q, lens, ws_tensor, out, knew, vnew, sidx, pos, Hq, sm_scale, kernel):
         from fp8_quantized_kv_gb300._lib import get_lib
         self.lib = get_lib()
         self.cache = cache
@@ -281,8 +283,9 @@ class Layer:
         P = lambda t: ctypes.c_void_p(t.data_ptr())
         self.a_append = (cache.struct_ref, P(knew), P(vnew), P(sidx), P(pos), knew.shape[0])
         wsb = ws_tensor.numel()
-        self.a_split = (P(q), cache.struct_ref, P(lens), Hq, ctypes.c_float(sm_scale), 0, P(ws_tensor), wsb)
-        self.a_merge = (cache.struct_ref, Hq, 0, P(ws_tensor), wsb, P(out), 0)
+        self.a_split = (P(q), cache.struct_ref, P(lens), Hq, ctypes.c_float(sm_scale), 0, kernel,
+                        P(ws_tensor), wsb)
+        self.a_merge = (cache.struct_ref, Hq, 0, kernel, P(ws_tensor), wsb, P(out), 0)
 
     def append(self, s):
         r = self.lib.fp8kv_append(*self.a_append, s)
@@ -300,7 +303,7 @@ class Layer:
             raise RuntimeError(f"fp8kv_decode_merge status {r}")
 
 
-def build_layers(spec, dtype, L, inp):
+def build_layers(spec, dtype, L, inp, kernel):
     import fp8_quantized_kv_gb300 as fk
     B, Hq, Hkv, D = spec.batch, spec.q_heads, spec.kv_heads, spec.head_dim
     T = spec.seq_lens[0]
@@ -328,10 +331,11 @@ def build_layers(spec, dtype, L, inp):
             c = fk.Fp8KVCache(dtype=dtype, layout=0, batch=B, kv_heads=Hkv, head_dim=D,
                               k=clone(base.k), v=clone(base.v), k_scale=clone(base.k_scale),
                               v_scale=clone(base.v_scale), max_tokens=cap)
-        wsb = fk.fp8kv_decode_workspace_bytes(c, Hq, 0)
+        wsb = fk.fp8kv_decode_workspace_bytes(c, Hq, 0, kernel)
         ws_t = torch.empty(wsb, dtype=torch.uint8, device="cuda")
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
-        layers.append(Layer(c, q, lens, ws_t, out, knew, vnew, new_sidx, new_pos, Hq, 1.0 / math.sqrt(D)))
+        layers.append(Layer(c, q, lens, ws_t, out, knew, vnew, new_sidx, new_pos, Hq, 1.0 / math.sqrt(D),
+                            kernel))
     torch.cuda.synchronize()
     return layers, (q, knew, vnew, new_sidx, new_pos, lens)
 
@@ -403,7 +407,7 @@ def time_graph_steps(layers, K, chunk, ws):
     return total_ms, per, (t_wall0, t_wall1)
 
 
-def e2e_run(layers, host, K, W):
+def e2e_run(layers, host, K, W, kernel):
     """Through the public Python API: pinned host inputs copied in each step,
     the output copied back each step."""
     import fp8_quantized_kv_gb300 as fk
@@ -411,7 +415,7 @@ def e2e_run(layers, host, K, W):
     hq, hk, hv, hs, hp, hl = host["pinned"]
     out_h = host["out"]
     outs = [torch.empty_like(out_h, device="cuda") for _ in layers]
-    wss = [torch.empty(fk.fp8kv_decode_workspace_bytes(L.cache, q.shape[1], 0), dtype=torch.uint8,
+    wss = [torch.empty(fk.fp8kv_decode_workspace_bytes(L.cache, q.shape[1], 0, kernel), dtype=torch.uint8,
                        device="cuda") for L in layers]
 
     def step(i):
@@ -424,7 +428,7 @@ def e2e_run(layers, host, K, W):
         lens.copy_(hl, non_blocking=True)
         fk.fp8kv_append(L.cache, knew, vnew, sidx, pos)
         fk.fp8kv_decode_attention(q, L.cache, lens, out=outs[i % len(layers)],
-                                  workspace=wss[i % len(layers)])
+                                  workspace=wss[i % len(layers)], kernel=kernel)
         out_h.copy_(outs[i % len(layers)], non_blocking=True)
 
     for i in range(W):
@@ -443,7 +447,7 @@ def e2e_run(layers, host, K, W):
 
 
 def measure_variant(spec, dtype, args, ws, inp):
-    layers, dev = build_layers(spec, dtype, args.layers, inp)
+    layers, dev = build_layers(spec, dtype, args.layers, inp, KERNEL_IDS[args.kernel])
     for i in range(max(3, args.warmup)):                      # eager warm-up steps
         L = layers[i % len(layers)]
         sp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -476,7 +480,8 @@ def run_gpu(args, ws, rank):
     q, knew, vnew, sidx, pos, lens = dev
     pinned = tuple(t.cpu().pin_memory() for t in dev)
     out_h = torch.empty((spec.batch, spec.q_heads, spec.head_dim), dtype=torch.bfloat16).pin_memory()
-    e2e_ms, h2d, d2h = e2e_run(layers, {"dev": dev, "pinned": pinned, "out": out_h}, args.steps, args.warmup)
+    e2e_ms, h2d, d2h = e2e_run(layers, {"dev": dev, "pinned": pinned, "out": out_h}, args.steps, args.warmup,
+                               KERNEL_IDS[args.kernel])
     e2e_ms = max_over_ranks(e2e_ms, ws)
     e2e_val = ws * nb["step"] * args.steps / (e2e_ms * 1e-3) / 1e9
     sampler.stop()
@@ -527,6 +532,7 @@ def run_gpu(args, ws, rank):
             "config": {"workload": WORKLOAD, "batch": spec.batch, "q_heads": spec.q_heads,
                        "kv_heads": spec.kv_heads, "head_dim": spec.head_dim, "ctx": T,
                        "cache": args.dtype, "layout": "contiguous", "parallelism": f"replicas x{ws}",
+                       "kernel": args.kernel,
                        "step": "append 1 token/seq + decode split + merge",
                        "l2": f"{args.layers} distinct layer caches rotated (inputs larger than L2)"},
             "roofline": roof, "cpu_baseline": cpu,

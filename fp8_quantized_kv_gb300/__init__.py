@@ -26,6 +26,8 @@ LAYOUT_CONTIGUOUS, LAYOUT_PAGED = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
 
 DEVERR_SEQ_TOO_LONG, DEVERR_BAD_PAGE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+KERNEL_AUTO, KERNEL_CUDA_CORES, KERNEL_TENSOR_CORES = 0, 1, 2
+KERNELS = {"auto": KERNEL_AUTO, "cuda_cores": KERNEL_CUDA_CORES, "tensor_cores": KERNEL_TENSOR_CORES}
 
 STATUS_NAMES = {0: "FP8KV_OK", 1: "FP8KV_ERR_INVALID_ARG", 2: "FP8KV_ERR_UNSUPPORTED",
                 3: "FP8KV_ERR_WORKSPACE", 4: "FP8KV_ERR_CUDA", 5: "FP8KV_ERR_TIMEOUT",
@@ -148,19 +150,25 @@ def fp8kv_append(cache: Fp8KVCache, k_new: torch.Tensor, v_new: torch.Tensor,
                                   _ptr(pos), n, _stream(stream)), "fp8kv_append")
 
 
-def fp8kv_decode_num_splits(cache: Fp8KVCache, q_heads: int, num_splits: int = 0) -> int:
-    return int(get_lib().fp8kv_decode_num_splits(cache.struct_ref, q_heads, num_splits))
+def _kernel(kernel) -> int:
+    return KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
 
 
-def fp8kv_decode_workspace_bytes(cache: Fp8KVCache, q_heads: int, num_splits: int = 0) -> int:
-    return int(get_lib().fp8kv_decode_workspace_bytes(cache.struct_ref, q_heads, num_splits))
+def fp8kv_decode_num_splits(cache: Fp8KVCache, q_heads: int, num_splits: int = 0, kernel=0) -> int:
+    return int(get_lib().fp8kv_decode_num_splits(cache.struct_ref, q_heads, num_splits, _kernel(kernel)))
+
+
+def fp8kv_decode_workspace_bytes(cache: Fp8KVCache, q_heads: int, num_splits: int = 0, kernel=0) -> int:
+    return int(get_lib().fp8kv_decode_workspace_bytes(cache.struct_ref, q_heads, num_splits,
+                                                      _kernel(kernel)))
 
 
 def fp8kv_decode_attention(q: torch.Tensor, cache: Fp8KVCache, seq_lens: torch.Tensor,
                            sm_scale: Optional[float] = None, num_splits: int = 0,
                            out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
-                           workspace: Optional[torch.Tensor] = None, stream=None):
-    """q [B, Hq, D] bf16, seq_lens [B] int32 -> out [B, Hq, D] (bf16 or fp32)."""
+                           workspace: Optional[torch.Tensor] = None, kernel=0, stream=None):
+    """q [B, Hq, D] bf16, seq_lens [B] int32 -> out [B, Hq, D] (bf16 or fp32).
+    kernel: "auto" / "cuda_cores" / "tensor_cores" (or 0 / 1 / 2)."""
     _need(q, torch.bfloat16, "q")
     _need(seq_lens, torch.int32, "seq_lens")
     B, Hq, D = q.shape
@@ -169,11 +177,12 @@ def fp8kv_decode_attention(q: torch.Tensor, cache: Fp8KVCache, seq_lens: torch.T
     if out is None:
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
     odt = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
-    need = fp8kv_decode_workspace_bytes(cache, Hq, num_splits)
+    k = _kernel(kernel)
+    need = fp8kv_decode_workspace_bytes(cache, Hq, num_splits, k)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _check(get_lib().fp8kv_decode_attention(
-        _ptr(q), cache.struct_ref, _ptr(seq_lens), Hq, float(sm_scale), num_splits,
+        _ptr(q), cache.struct_ref, _ptr(seq_lens), Hq, float(sm_scale), num_splits, k,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), odt,
         _stream(stream)), "fp8kv_decode_attention")
     return out
@@ -181,7 +190,7 @@ def fp8kv_decode_attention(q: torch.Tensor, cache: Fp8KVCache, seq_lens: torch.T
 
 def fp8kv_decode_split(q: torch.Tensor, cache: Fp8KVCache, seq_lens: torch.Tensor,
                        workspace: torch.Tensor, sm_scale: Optional[float] = None,
-                       num_splits: int = 0, stream=None):
+                       num_splits: int = 0, kernel=0, stream=None):
     """Kernel 1 of decode: fp32 partials of every split into `workspace`."""
     _need(q, torch.bfloat16, "q")
     _need(seq_lens, torch.int32, "seq_lens")
@@ -189,17 +198,17 @@ def fp8kv_decode_split(q: torch.Tensor, cache: Fp8KVCache, seq_lens: torch.Tenso
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     _check(get_lib().fp8kv_decode_split(
-        _ptr(q), cache.struct_ref, _ptr(seq_lens), Hq, float(sm_scale), num_splits,
+        _ptr(q), cache.struct_ref, _ptr(seq_lens), Hq, float(sm_scale), num_splits, _kernel(kernel),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
         "fp8kv_decode_split")
 
 
 def fp8kv_decode_merge(cache: Fp8KVCache, q_heads: int, workspace: torch.Tensor,
-                       out: torch.Tensor, num_splits: int = 0, stream=None):
+                       out: torch.Tensor, num_splits: int = 0, kernel=0, stream=None):
     """Kernel 2 of decode: merge the partials in `workspace` into `out`."""
     odt = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _check(get_lib().fp8kv_decode_merge(
-        cache.struct_ref, q_heads, num_splits, _ptr(workspace),
+        cache.struct_ref, q_heads, num_splits, _kernel(kernel), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), odt, _stream(stream)),
         "fp8kv_decode_merge")
     return out

@@ -64,11 +64,11 @@ def get_lib() -> ctypes.CDLL:
     sig = {
         "fp8kv_quantize": (i32, [vp, i64, i32, vp, vp, vp]),
         "fp8kv_append": (i32, [cp, vp, vp, vp, vp, i64, vp]),
-        "fp8kv_decode_num_splits": (i32, [cp, i32, i32]),
-        "fp8kv_decode_workspace_bytes": (sz, [cp, i32, i32]),
-        "fp8kv_decode_split": (i32, [vp, cp, vp, i32, f32, i32, vp, sz, vp]),
-        "fp8kv_decode_merge": (i32, [cp, i32, i32, vp, sz, vp, i32, vp]),
-        "fp8kv_decode_attention": (i32, [vp, cp, vp, i32, f32, i32, vp, sz, vp, i32, vp]),
+        "fp8kv_decode_num_splits": (i32, [cp, i32, i32, i32]),
+        "fp8kv_decode_workspace_bytes": (sz, [cp, i32, i32, i32]),
+        "fp8kv_decode_split": (i32, [vp, cp, vp, i32, f32, i32, i32, vp, sz, vp]),
+        "fp8kv_decode_merge": (i32, [cp, i32, i32, i32, vp, sz, vp, i32, vp]),
+        "fp8kv_decode_attention": (i32, [vp, cp, vp, i32, f32, i32, i32, vp, sz, vp, i32, vp]),
         "fp8kv_decode_attention_static": (i32, [vp, cp, vp, i32, f32, i32, vp, i32, vp]),
         "fp8kv_decode_static_scratch_bytes": (sz, []),
         "fp8kv_prefill_attention": (i32, [vp, cp, vp, i32, i32, f32, vp, i32, vp]),

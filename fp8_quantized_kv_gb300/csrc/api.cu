@@ -91,21 +91,33 @@ static int capacity_of(const fp8kv_cache* c) {
   return c->layout == FP8KV_LAYOUT_PAGED ? c->max_pages_per_seq * c->page_size : c->max_tokens;
 }
 
-// Split plan: split boundaries are multiples of 64-token tiles anchored at
-// token 0.  Automatic: enough CTAs for about `kCtasPerSm` per SM over the
+// Split plan: split boundaries are multiples of the kernel's tile anchored
+// at token 0.  Automatic: enough CTAs for about `ctas_per_sm` per SM over the
 // (sequence, KV head) units, each split at least kMinSplitTiles tiles.
-constexpr int kCtasPerSm = 4;
 constexpr int kMinSplitTiles = 2;
 
-struct SplitPlan { int splits, chunk_tiles; };
+struct SplitPlan { int splits, chunk_tiles, tile, kernel; };
 
-static SplitPlan plan_splits(const fp8kv_cache* c, int requested) {
-  const int max_tiles = (capacity_of(c) + kTileTokens - 1) / kTileTokens;
-  if (max_tiles <= 0) return {1, 1};
+// The kernel a decode call runs (FP8KV_KERNEL_CUDA_CORES or _TENSOR_CORES),
+// or 0 if the requested kernel does not support the shape.
+static int resolve_kernel(const fp8kv_cache* c, int q_heads, int requested) {
+  const int G = q_heads / c->kv_heads;
+  const bool mma_ok = c->head_dim == 128 && G >= 1 && G <= 8;
+  if (requested == FP8KV_KERNEL_TENSOR_CORES) return mma_ok ? FP8KV_KERNEL_TENSOR_CORES : 0;
+  if (requested == FP8KV_KERNEL_CUDA_CORES) return FP8KV_KERNEL_CUDA_CORES;
+  if (requested != FP8KV_KERNEL_AUTO) return 0;
+  return (mma_ok && G >= 5) ? FP8KV_KERNEL_TENSOR_CORES : FP8KV_KERNEL_CUDA_CORES;
+}
+
+static SplitPlan plan_splits(const fp8kv_cache* c, int requested, int kernel) {
+  const int tile = kernel == FP8KV_KERNEL_TENSOR_CORES ? 128 : kTileTokens;
+  const int ctas_per_sm = kernel == FP8KV_KERNEL_TENSOR_CORES ? 2 : 4;
+  const int max_tiles = (capacity_of(c) + tile - 1) / tile;
+  if (max_tiles <= 0) return {1, 1, tile, kernel};
   int want = requested;
   if (want <= 0) {
     const long units = (long)c->batch * c->kv_heads;
-    const long target = (long)kCtasPerSm * sm_count();
+    const long target = (long)ctas_per_sm * sm_count();
     want = units > 0 ? (int)((target + units - 1) / units) : 1;
     const int cap_by_min = (max_tiles + kMinSplitTiles - 1) / kMinSplitTiles;
     if (want > cap_by_min) want = cap_by_min;
@@ -114,7 +126,7 @@ static SplitPlan plan_splits(const fp8kv_cache* c, int requested) {
   if (want > max_tiles) want = max_tiles;
   const int chunk = (max_tiles + want - 1) / want;
   const int splits = (max_tiles + chunk - 1) / chunk;
-  return {splits, chunk};
+  return {splits, chunk, tile, kernel};
 }
 
 }  // namespace fp8kv
@@ -165,15 +177,19 @@ fp8kv_status fp8kv_append(const fp8kv_cache* cache, const void* k_new, const voi
                                    (cudaStream_t)stream));
 }
 
-int32_t fp8kv_decode_num_splits(const fp8kv_cache* cache, int32_t q_heads, int32_t num_splits) {
+int32_t fp8kv_decode_num_splits(const fp8kv_cache* cache, int32_t q_heads, int32_t num_splits,
+                                int32_t kernel) {
   CacheView view;
   if (check_cache(cache, &view) != FP8KV_OK) return 0;
   if (q_heads <= 0 || q_heads % cache->kv_heads != 0 || num_splits < 0) return 0;
-  return plan_splits(cache, num_splits).splits;
+  const int k = resolve_kernel(cache, q_heads, kernel);
+  if (k == 0) return 0;
+  return plan_splits(cache, num_splits, k).splits;
 }
 
-size_t fp8kv_decode_workspace_bytes(const fp8kv_cache* cache, int32_t q_heads, int32_t num_splits) {
-  const int S = fp8kv_decode_num_splits(cache, q_heads, num_splits);
+size_t fp8kv_decode_workspace_bytes(const fp8kv_cache* cache, int32_t q_heads, int32_t num_splits,
+                                    int32_t kernel) {
+  const int S = fp8kv_decode_num_splits(cache, q_heads, num_splits, kernel);
   if (S <= 0) return 0;
   const size_t rows = (size_t)cache->batch * q_heads * S;
   return rows * ((size_t)cache->head_dim + 2) * sizeof(float);
@@ -185,18 +201,22 @@ namespace {
 
 // Checks shared by the decode calls; fills the parameter block and the plan.
 fp8kv_status prepare_decode(const void* q, const fp8kv_cache* cache, const int32_t* seq_lens,
-                            int32_t q_heads, float sm_scale, int32_t num_splits, const void* workspace,
-                            size_t workspace_bytes, bool need_q, DecodeParams* p) {
+                            int32_t q_heads, float sm_scale, int32_t num_splits, int32_t kernel,
+                            const void* workspace, size_t workspace_bytes, bool need_q, DecodeParams* p,
+                            int* resolved) {
   CacheView view;
   fp8kv_status st = check_cache(cache, &view);
   if (st != FP8KV_OK) return st;
   if (q_heads <= 0 || q_heads % cache->kv_heads != 0 || num_splits < 0) return FP8KV_ERR_INVALID_ARG;
+  if (kernel < FP8KV_KERNEL_AUTO || kernel > FP8KV_KERNEL_TENSOR_CORES) return FP8KV_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return FP8KV_ERR_INVALID_ARG;
   const int G = q_heads / cache->kv_heads;
   if (G > 8) return FP8KV_ERR_UNSUPPORTED;
+  const int k = resolve_kernel(cache, q_heads, kernel);
+  if (k == 0) return FP8KV_ERR_UNSUPPORTED;
   if (need_q && cache->batch > 0 && (!q || !seq_lens)) return FP8KV_ERR_INVALID_ARG;
-  const SplitPlan plan = plan_splits(cache, num_splits);
-  const size_t need = fp8kv_decode_workspace_bytes(cache, q_heads, num_splits);
+  const SplitPlan plan = plan_splits(cache, num_splits, k);
+  const size_t need = fp8kv_decode_workspace_bytes(cache, q_heads, num_splits, kernel);
   if (cache->batch > 0 && (workspace == nullptr || workspace_bytes < need)) return FP8KV_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 15) != 0) return FP8KV_ERR_INVALID_ARG;
   const int64_t rows = (int64_t)cache->batch * q_heads;
@@ -212,6 +232,7 @@ fp8kv_status prepare_decode(const void* q, const fp8kv_cache* cache, const int32
   p->num_splits = plan.splits;
   p->chunk_tiles = plan.chunk_tiles;
   p->scale_log2 = sm_scale * kLog2e;
+  *resolved = k;
   return FP8KV_OK;
 }
 
@@ -220,24 +241,28 @@ fp8kv_status prepare_decode(const void* q, const fp8kv_cache* cache, const int32
 extern "C" {
 
 fp8kv_status fp8kv_decode_split(const void* q, const fp8kv_cache* cache, const int32_t* seq_lens,
-                                int32_t q_heads, float sm_scale, int32_t num_splits, void* workspace,
-                                size_t workspace_bytes, fp8kv_stream_t stream) {
+                                int32_t q_heads, float sm_scale, int32_t num_splits, int32_t kernel,
+                                void* workspace, size_t workspace_bytes, fp8kv_stream_t stream) {
   DecodeParams p;
-  fp8kv_status st = prepare_decode(q, cache, seq_lens, q_heads, sm_scale, num_splits, workspace,
-                                   workspace_bytes, true, &p);
+  int k = 0;
+  fp8kv_status st = prepare_decode(q, cache, seq_lens, q_heads, sm_scale, num_splits, kernel, workspace,
+                                   workspace_bytes, true, &p, &k);
   if (st != FP8KV_OK || cache->batch == 0) return st;
   p.err = device_error_ptr();
   if (!p.err) return FP8KV_ERR_CUDA;
-  return cuda_status(launch_decode_fma(p, cache->dtype, cache->batch, (cudaStream_t)stream));
+  cudaStream_t s = (cudaStream_t)stream;
+  return cuda_status(k == FP8KV_KERNEL_TENSOR_CORES ? launch_decode_mma(p, cache->dtype, cache->batch, s)
+                                                    : launch_decode_fma(p, cache->dtype, cache->batch, s));
 }
 
 fp8kv_status fp8kv_decode_merge(const fp8kv_cache* cache, int32_t q_heads, int32_t num_splits,
-                                const void* workspace, size_t workspace_bytes, void* out,
+                                int32_t kernel, const void* workspace, size_t workspace_bytes, void* out,
                                 int32_t out_dtype, fp8kv_stream_t stream) {
   if (out_dtype != FP8KV_OUT_BF16 && out_dtype != FP8KV_OUT_F32) return FP8KV_ERR_INVALID_ARG;
   DecodeParams p;
-  fp8kv_status st = prepare_decode(nullptr, cache, nullptr, q_heads, 1.0f, num_splits, workspace,
-                                   workspace_bytes, false, &p);
+  int k = 0;
+  fp8kv_status st = prepare_decode(nullptr, cache, nullptr, q_heads, 1.0f, num_splits, kernel, workspace,
+                                   workspace_bytes, false, &p, &k);
   if (st != FP8KV_OK || cache->batch == 0) return st;
   if (!out) return FP8KV_ERR_INVALID_ARG;
   const int64_t rows = (int64_t)cache->batch * q_heads;
@@ -247,16 +272,16 @@ fp8kv_status fp8kv_decode_merge(const fp8kv_cache* cache, int32_t q_heads, int32
 }
 
 fp8kv_status fp8kv_decode_attention(const void* q, const fp8kv_cache* cache, const int32_t* seq_lens,
-                                    int32_t q_heads, float sm_scale, int32_t num_splits, void* workspace,
-                                    size_t workspace_bytes, void* out, int32_t out_dtype,
+                                    int32_t q_heads, float sm_scale, int32_t num_splits, int32_t kernel,
+                                    void* workspace, size_t workspace_bytes, void* out, int32_t out_dtype,
                                     fp8kv_stream_t stream) {
   if (out_dtype != FP8KV_OUT_BF16 && out_dtype != FP8KV_OUT_F32) return FP8KV_ERR_INVALID_ARG;
   if (cache != nullptr && cache->batch > 0 && out == nullptr) return FP8KV_ERR_INVALID_ARG;
-  fp8kv_status st = fp8kv_decode_split(q, cache, seq_lens, q_heads, sm_scale, num_splits, workspace,
-                                       workspace_bytes, stream);
+  fp8kv_status st = fp8kv_decode_split(q, cache, seq_lens, q_heads, sm_scale, num_splits, kernel,
+                                       workspace, workspace_bytes, stream);
   if (st != FP8KV_OK) return st;
-  return fp8kv_decode_merge(cache, q_heads, num_splits, workspace, workspace_bytes, out, out_dtype,
-                            stream);
+  return fp8kv_decode_merge(cache, q_heads, num_splits, kernel, workspace, workspace_bytes, out,
+                            out_dtype, stream);
 }
 
 fp8kv_status fp8kv_prefill_attention(const void* q, const fp8kv_cache* cache, const int32_t* q_pos0,

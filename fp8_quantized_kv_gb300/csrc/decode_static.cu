@@ -51,14 +51,14 @@ fp8kv_status fp8kv_decode_attention_static(const void* q, const fp8kv_cache* cac
                                            fp8kv_stream_t stream) {
   // Invalid arguments give need == 0 here and are reported by the checks of
   // fp8kv_decode_attention below.
-  const size_t need = fp8kv_decode_workspace_bytes(cache, q_heads, num_splits);
+  const size_t need = fp8kv_decode_workspace_bytes(cache, q_heads, num_splits, FP8KV_KERNEL_AUTO);
   if (need > fp8kv::kStaticScratchBytes) return FP8KV_ERR_WORKSPACE;
   cudaError_t e = cudaSuccess;
   void* scratch = fp8kv::static_scratch_ptr(&e);
   if (scratch == nullptr) return FP8KV_ERR_CUDA;
   // Every split writes all of its partials (empty splits write m = -inf,
   // l = 0, O = 0) before the merge reads them, so nothing needs clearing.
-  return fp8kv_decode_attention(q, cache, seq_lens, q_heads, sm_scale, num_splits, scratch,
+  return fp8kv_decode_attention(q, cache, seq_lens, q_heads, sm_scale, num_splits, FP8KV_KERNEL_AUTO, scratch,
                                 fp8kv::kStaticScratchBytes, out, out_dtype, stream);
 }
 

@@ -34,6 +34,7 @@ cudaError_t launch_append(const CacheView& c, int dtype, const void* k_new, cons
                           const int32_t* seq_idx, const int32_t* pos, int64_t n_tokens,
                           unsigned int* err, cudaStream_t s);
 cudaError_t launch_decode_fma(const DecodeParams& p, int dtype, int batch, cudaStream_t st);
+cudaError_t launch_decode_mma(const DecodeParams& p, int dtype, int batch, cudaStream_t st);
 cudaError_t launch_decode_merge(const float* part_o, const float* part_m, const float* part_l, int S,
                                 int64_t rows, int head_dim, void* out, int out_f32, cudaStream_t st);
 cudaError_t launch_prefill_fma(const PrefillParams& p, int dtype, int batch, cudaStream_t st);

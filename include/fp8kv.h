@@ -81,6 +81,16 @@ typedef enum {
 
 typedef enum { FP8KV_OUT_BF16 = 0, FP8KV_OUT_F32 = 1 } fp8kv_out_dtype;
 
+/* Which split kernel a decode call runs.  AUTO picks per shape: the tensor
+ * cores for head_dim 128 with 5 to 8 query heads per KV head, the CUDA cores
+ * otherwise.  The tensor-core kernel (tcgen05) walks 128-token tiles and
+ * needs head_dim 128; the CUDA-core kernel walks 64-token tiles. */
+typedef enum {
+  FP8KV_KERNEL_AUTO = 0,
+  FP8KV_KERNEL_CUDA_CORES = 1,
+  FP8KV_KERNEL_TENSOR_CORES = 2
+} fp8kv_decode_kernel;
+
 /* Device error word bits (fp8kv_get_device_error). */
 #define FP8KV_DEVERR_SEQ_TOO_LONG 0x1u   /* a length/position exceeds the cache */
 #define FP8KV_DEVERR_BAD_PAGE 0x2u       /* a page id outside [0, num_pages)    */
@@ -136,12 +146,12 @@ FP8KV_API fp8kv_status fp8kv_append(const fp8kv_cache *cache, const void *k_new,
  * (0 = automatic: about four CTAs per SM, "FP8 KV cache", bullet "Speed").
  * Returns 0 on invalid arguments. */
 FP8KV_API int32_t fp8kv_decode_num_splits(const fp8kv_cache *cache, int32_t q_heads,
-                                int32_t num_splits);
+                                int32_t num_splits, int32_t kernel);
 
 /* Bytes of workspace fp8kv_decode_attention needs for these arguments: the
  * fp32 partials (O, m, l) of every (sequence, query head, split). */
 FP8KV_API size_t fp8kv_decode_workspace_bytes(const fp8kv_cache *cache, int32_t q_heads,
-                                    int32_t num_splits);
+                                    int32_t num_splits, int32_t kernel);
 
 /* Decode attention: one query token per sequence, grouped-query heads, per-
  * sequence lengths ("FP8 KV cache", bullet "Math", fp8_kv_attention).  Kernel
@@ -152,12 +162,13 @@ FP8KV_API size_t fp8kv_decode_workspace_bytes(const fp8kv_cache *cache, int32_t 
  *   seq_lens: [batch] int32 device array; sequence b attends its tokens
  *             0..seq_lens[b]-1; a length of 0 gives a zero output row
  *   sm_scale: softmax scale (1/sqrt(head_dim) in the usual case)
+ *   kernel:   fp8kv_decode_kernel
  *   out:      [batch][q_heads][head_dim], bf16 or fp32 per out_dtype
- * Split boundaries are multiples of 64 tokens, so results for different
- * num_splits differ only by fp32 re-association. */
+ * Split boundaries are multiples of the kernel's tile (64 or 128 tokens), so
+ * results for different num_splits differ only by fp32 re-association. */
 FP8KV_API fp8kv_status fp8kv_decode_attention(const void *q, const fp8kv_cache *cache,
                                     const int32_t *seq_lens, int32_t q_heads,
-                                    float sm_scale, int32_t num_splits,
+                                    float sm_scale, int32_t num_splits, int32_t kernel,
                                     void *workspace, size_t workspace_bytes,
                                     void *out, int32_t out_dtype,
                                     fp8kv_stream_t stream);
@@ -165,16 +176,17 @@ FP8KV_API fp8kv_status fp8kv_decode_attention(const void *q, const fp8kv_cache *
 /* The two kernels of fp8kv_decode_attention as separate calls (same
  * arguments, same results).  fp8kv_decode_split runs the flash-decoding split
  * kernel and leaves the fp32 partials in `workspace`; fp8kv_decode_merge
- * reduces them into `out`.  Both must be given the same cache, q_heads and
- * num_splits, and the merge must follow the split on the same stream (or be
- * ordered after it). */
+ * reduces them into `out`.  Both must be given the same cache, q_heads,
+ * num_splits and kernel, and the merge must follow the split on the same
+ * stream (or be ordered after it). */
 FP8KV_API fp8kv_status fp8kv_decode_split(const void *q, const fp8kv_cache *cache,
                                           const int32_t *seq_lens, int32_t q_heads,
-                                          float sm_scale, int32_t num_splits,
+                                          float sm_scale, int32_t num_splits, int32_t kernel,
                                           void *workspace, size_t workspace_bytes,
                                           fp8kv_stream_t stream);
 FP8KV_API fp8kv_status fp8kv_decode_merge(const fp8kv_cache *cache, int32_t q_heads,
-                                          int32_t num_splits, const void *workspace,
+                                          int32_t num_splits, int32_t kernel,
+                                          const void *workspace,
                                           size_t workspace_bytes, void *out,
                                           int32_t out_dtype, fp8kv_stream_t stream);
 
@@ -183,7 +195,8 @@ FP8KV_API fp8kv_status fp8kv_decode_merge(const fp8kv_cache *cache, int32_t q_he
  * fp8kv_decode_attention without the workspace: the fp32 partials go to a
  * fixed array of fp8kv_decode_static_scratch_bytes() bytes (16 MiB) compiled
  * into the library, which every GPU that loads the library keeps until the
- * process exits.  It is for callers that cannot call cudaMalloc -- for
+ * process exits.  The kernel is chosen as with FP8KV_KERNEL_AUTO.  It is
+ * for callers that cannot call cudaMalloc -- for
  * example a runtime whose memory pool owns the device and forbids
  * allocation on its serving path, or a plugin given only its input and
  * output tensors.  The call makes no cudaMalloc, cudaFree or allocating

@@ -72,10 +72,11 @@ def oracle_decode(inp: synth.DecodeInputs, dtype: str, batch_ids, sm_scale=None)
     return np.stack(res) if res else np.zeros((0, spec.q_heads, D))
 
 
-def gpu_decode(inp, cache, num_splits=0, out_dtype=torch.float32):
+def gpu_decode(inp, cache, num_splits=0, out_dtype=torch.float32, kernel="auto"):
     q = inp.q.to("cuda").contiguous()
     lens = inp.seq_lens.to("cuda")
-    return fk.fp8kv_decode_attention(q, cache, lens, num_splits=num_splits, out_dtype=out_dtype)
+    return fk.fp8kv_decode_attention(q, cache, lens, num_splits=num_splits, out_dtype=out_dtype,
+                                     kernel=kernel)
 
 
 def assert_gate(out, ref, what, rel_l2=1e-2, max_abs=2e-2):

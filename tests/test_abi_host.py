@@ -57,36 +57,45 @@ def test_argument_checks_return_before_any_launch(lib):
     assert lib.fp8kv_quantize(None, -1, 128, None, None, None) == 1
     assert lib.fp8kv_quantize(None, 10, 96, None, None, None) == 2
     assert lib.fp8kv_quantize(None, 10, 128, None, None, None) == 1
-    assert lib.fp8kv_decode_attention(None, None, None, 16, 0.1, 0, None, 0, None, 0, None) == 1
+    assert lib.fp8kv_decode_attention(None, None, None, 16, 0.1, 0, 0, None, 0, None, 0, None) == 1
     bad_dim = _cache(head_dim=96)
     out = 0x6000        # never dereferenced: each call is rejected first
-    assert lib.fp8kv_decode_attention(None, r(bad_dim), None, 16, 0.1, 0, None, 0, out, 0, None) == 2
-    assert lib.fp8kv_decode_attention(None, r(c), None, 15, 0.1, 0, None, 0, out, 0, None) == 1
-    assert lib.fp8kv_decode_attention(None, r(c), None, 16, 0.1, 0, None, 0, out, 7, None) == 1
-    assert lib.fp8kv_decode_attention(0x7000, r(c), 0x8000, 16, 0.1, 0, None, 0, out, 0, None) == 3
+    assert lib.fp8kv_decode_attention(None, r(bad_dim), None, 16, 0.1, 0, 0, None, 0, out, 0, None) == 2
+    assert lib.fp8kv_decode_attention(None, r(c), None, 15, 0.1, 0, 0, None, 0, out, 0, None) == 1
+    assert lib.fp8kv_decode_attention(None, r(c), None, 16, 0.1, 0, 0, None, 0, out, 7, None) == 1
+    assert lib.fp8kv_decode_attention(0x7000, r(c), 0x8000, 16, 0.1, 0, 0, None, 0, out, 0, None) == 3
     no_scale = _cache(k_scale=None)
-    assert lib.fp8kv_decode_attention(None, r(no_scale), None, 16, 0.1, 0, None, 0, out, 0, None) == 1
+    assert lib.fp8kv_decode_attention(None, r(no_scale), None, 16, 0.1, 0, 0, None, 0, out, 0, None) == 1
     odd_cap = _cache(max_tokens=100)
     assert lib.fp8kv_append(r(odd_cap), None, None, None, None, 1, None) == 2
     paged_bad = _cache(layout=1, page_size=8, num_pages=4, max_pages_per_seq=2, page_table=0x5000)
     assert lib.fp8kv_append(r(paged_bad), None, None, None, None, 1, None) == 2
     paged_nopt = _cache(layout=1, page_size=16, num_pages=4, max_pages_per_seq=2)
-    assert lib.fp8kv_decode_num_splits(r(paged_nopt), 16, 0) == 0
+    assert lib.fp8kv_decode_num_splits(r(paged_nopt), 16, 0, 0) == 0
     big_group = _cache(kv_heads=1)
-    assert lib.fp8kv_decode_split(None, r(big_group), None, 16, 0.1, 0, None, 0, None) == 2
+    assert lib.fp8kv_decode_split(None, r(big_group), None, 16, 0.1, 0, 0, None, 0, None) == 2
+    # the tensor-core kernel needs head_dim 128
+    d64 = _cache(head_dim=64)
+    assert lib.fp8kv_decode_split(None, r(d64), None, 16, 0.1, 0, 2, None, 0, None) == 2
+    assert lib.fp8kv_decode_split(None, r(c), None, 16, 0.1, 0, 3, None, 0, None) == 1
 
 
 def test_split_plan_and_workspace(lib):
     c = _cache()
     r = ctypes.byref
-    # explicit split counts: chunks are whole 64-token tiles anchored at 0
-    assert lib.fp8kv_decode_num_splits(r(c), 16, 1) == 1
-    assert lib.fp8kv_decode_num_splits(r(c), 16, 7) == 7           # 128 tiles -> 19 per split
-    assert lib.fp8kv_decode_num_splits(r(c), 16, 10 ** 6) == 128    # at most one tile each
-    S = lib.fp8kv_decode_num_splits(r(c), 16, 0)
-    assert 1 <= S <= 128
-    ws = lib.fp8kv_decode_workspace_bytes(r(c), 16, 0)
-    assert ws == 16 * 16 * S * (128 + 2) * 4
+    # explicit split counts: chunks are whole tiles anchored at 0; the CUDA-core
+    # kernel walks 64-token tiles, the tensor-core kernel 128-token tiles
+    for kern, tile in ((1, 64), (2, 128)):
+        n_tiles = 8192 // tile
+        assert lib.fp8kv_decode_num_splits(r(c), 16, 1, kern) == 1
+        assert lib.fp8kv_decode_num_splits(r(c), 16, 7, kern) == 7
+        assert lib.fp8kv_decode_num_splits(r(c), 16, 10 ** 6, kern) == n_tiles
+        S = lib.fp8kv_decode_num_splits(r(c), 16, 0, kern)
+        assert 1 <= S <= n_tiles
+        ws = lib.fp8kv_decode_workspace_bytes(r(c), 16, 0, kern)
+        assert ws == 16 * 16 * S * (128 + 2) * 4
+    # automatic choice: group 8 at head_dim 128 runs on the tensor cores
+    assert lib.fp8kv_decode_num_splits(r(c), 16, 10 ** 6, 0) == 64
 
 
 def test_workloads_match_their_description():

@@ -18,6 +18,7 @@ from kvhelpers import (assert_gate, fill_cache, gpu_decode, oracle_decode, oracl
 
 pytestmark = pytest.mark.gpu
 DTYPES = ["k8v8", "k16v8", "k16v16"]
+KERNELS = ["cuda_cores", "tensor_cores"]
 
 
 @pytest.fixture(autouse=True)
@@ -115,37 +116,40 @@ def test_decode_tiny(dtype):
     assert fk.fp8kv_get_device_error() == 0
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_decode_ctx512(dtype):
+def test_decode_ctx512(dtype, kernel):
     inp = synth.decode_inputs(synth.WORKLOADS["decode_b16_ctx512"], device="cuda")
     cache = fill_cache(inp, dtype)
-    out = gpu_decode(inp, cache).cpu().numpy()
+    out = gpu_decode(inp, cache, kernel=kernel).cpu().numpy()
     ref = oracle_decode(inp, dtype, range(16))
-    assert_gate(out, ref, f"ctx512 {dtype}")
+    assert_gate(out, ref, f"ctx512 {dtype} {kernel}")
 
 
+@pytest.mark.parametrize("kernel", ["auto"] + KERNELS)
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_decode_ctx8192_full(dtype):
+def test_decode_ctx8192_full(dtype, kernel):
     """The benchmark workload at full size, in the benchmark's launch
     configuration (automatic splits, bf16 output)."""
     inp = synth.decode_inputs(synth.WORKLOADS["decode_b16_ctx8192"], device="cuda")
     cache = fill_cache(inp, dtype)
-    out = gpu_decode(inp, cache, out_dtype=torch.bfloat16).float().cpu().numpy()
+    out = gpu_decode(inp, cache, out_dtype=torch.bfloat16, kernel=kernel).float().cpu().numpy()
     ref = oracle_decode(inp, dtype, range(16))
-    assert_gate(out, ref, f"ctx8192 {dtype}")
+    assert_gate(out, ref, f"ctx8192 {dtype} {kernel}")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_decode_ragged_and_edge_lengths(dtype):
+def test_decode_ragged_and_edge_lengths(dtype, kernel):
     lens = (0, 1, 2, 63, 64, 65, 127, 128, 129, 300, 1000, 17)
     spec = synth.DecodeWorkload("ragged", len(lens), 8, 1, 128, seed=5, seq_lens=lens)
     inp = synth.decode_inputs(spec, device="cuda")
     cache = fill_cache(inp, dtype, capacity=1024)
     for ns in (0, 1, 3):
-        out = gpu_decode(inp, cache, num_splits=ns).cpu().numpy()
+        out = gpu_decode(inp, cache, num_splits=ns, kernel=kernel).cpu().numpy()
         ref = oracle_decode(inp, dtype, range(len(lens)))
         assert np.all(out[0] == 0), "zero-length sequence must give a zero row"
-        assert_gate(out[1:], ref[1:], f"ragged {dtype} splits={ns}")
+        assert_gate(out[1:], ref[1:], f"ragged {dtype} {kernel} splits={ns}")
 
 
 @pytest.mark.parametrize("G", [1, 2, 3, 5, 8])
@@ -157,40 +161,83 @@ def test_decode_group_sizes(G):
     assert_gate(out, oracle_decode(inp, "k8v8", range(3)), f"G={G}")
 
 
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 8])
+def test_decode_group_sizes_tensor_cores(G):
+    spec = synth.DecodeWorkload("groups128", 3, 2 * G, 2, 128, seed=16, seq_lens=(100, 257, 128))
+    inp = synth.decode_inputs(spec, device="cuda")
+    for dtype in DTYPES:
+        cache = fill_cache(inp, dtype)
+        out = gpu_decode(inp, cache, kernel="tensor_cores").cpu().numpy()
+        assert_gate(out, oracle_decode(inp, dtype, range(3)), f"G={G} {dtype}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_decode_paged_small(dtype):
+def test_decode_paged_small(dtype, kernel):
     spec = synth.DecodeWorkload("paged_small", 6, 16, 4, 128, seed=7, len_range=(1, 700),
                                 page_size=16, hostile_keys=True)
     inp = synth.decode_inputs(spec, device="cuda")
     cache = fill_cache(inp, dtype)
-    out = gpu_decode(inp, cache).cpu().numpy()
-    assert_gate(out, oracle_decode(inp, dtype, range(6)), f"paged small {dtype}")
+    out = gpu_decode(inp, cache, kernel=kernel).cpu().numpy()
+    assert_gate(out, oracle_decode(inp, dtype, range(6)), f"paged small {dtype} {kernel}")
 
 
+@pytest.mark.parametrize("kernel", ["auto"] + KERNELS)
 @pytest.mark.parametrize("dtype", ["k8v8", "k16v8"])
-def test_decode_paged_b64_full_sampled(dtype):
+def test_decode_paged_b64_full_sampled(dtype, kernel):
     """The paged serving workload at full size (64 sequences up to 16384
     tokens, hostile keys); the oracle checks a sample of sequences."""
     inp = synth.decode_inputs(synth.WORKLOADS["paged_b64_hostile"], device="cuda")
     cache = fill_cache(inp, dtype)
-    out = gpu_decode(inp, cache, out_dtype=torch.bfloat16).float().cpu().numpy()
+    out = gpu_decode(inp, cache, out_dtype=torch.bfloat16, kernel=kernel).float().cpu().numpy()
     lens = inp.seq_lens.numpy()
     sample = sorted({int(lens.argmin()), int(lens.argmax()), 7, 33})
     ref = oracle_decode(inp, dtype, sample)
-    assert_gate(out[sample], ref, f"paged b64 {dtype}")
+    assert_gate(out[sample], ref, f"paged b64 {dtype} {kernel}")
     assert fk.fp8kv_get_device_error() == 0
 
 
-def test_split_invariance_ctx8192():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_split_invariance_ctx8192(kernel):
     """Split-KV merge versus unsplit: fp32 outputs within 1e-5 relative."""
     inp = synth.decode_inputs(synth.WORKLOADS["decode_b16_ctx8192"], device="cuda")
     for dtype in DTYPES:
         cache = fill_cache(inp, dtype)
-        one = gpu_decode(inp, cache, num_splits=1).double()
-        for ns in (0, 7, 128):
-            many = gpu_decode(inp, cache, num_splits=ns).double()
+        one = gpu_decode(inp, cache, num_splits=1, kernel=kernel).double()
+        for ns in (0, 7, 64):
+            many = gpu_decode(inp, cache, num_splits=ns, kernel=kernel).double()
             rel = ((many - one).norm(dim=-1) / one.norm(dim=-1)).max().item()
-            assert rel <= 1e-5, f"{dtype} splits={ns}: rel {rel:.3e}"
+            assert rel <= 1e-5, f"{dtype} {kernel} splits={ns}: rel {rel:.3e}"
+
+
+def test_tensor_core_path_subnormal_codes_and_tiny_queries():
+    """Rows whose amax is far above the rest put most codes in the E4M3
+    subnormal range; queries with components spanning many binades exercise
+    the two-term e4m3 split of Q and P.  Checked against the oracle."""
+    g = torch.Generator(device="cuda").manual_seed(17)
+    B, Hq, Hkv, D, T = 2, 8, 1, 128, 300
+    # amax 2 per row: every other element (|x| < 2 * 2^-6 / 448) gets a
+    # subnormal E4M3 code; outputs stay O(1), where the max-abs bar applies
+    k = torch.randn(B * T, Hkv, D, generator=g, device="cuda") * 3e-5
+    k[:, :, 5] = 2.0
+    v = torch.randn(B * T, Hkv, D, generator=g, device="cuda") * 3e-5
+    v[:, :, 9] = -2.0
+    q = torch.randn(B, Hq, D, generator=g, device="cuda") * torch.exp(
+        torch.randn(B, Hq, D, generator=g, device="cuda") * 3)
+    q[:, :, 5] = 1e-3                                      # keep the huge channel from dominating
+    spec = synth.DecodeWorkload("subnormal", B, Hq, Hkv, D, seed=0, seq_lens=(T, T))
+    inp = synth.DecodeInputs(spec, q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16),
+                             torch.tensor([T, T], dtype=torch.int32),
+                             torch.tensor([0, T, 2 * T], dtype=torch.int64))
+    for dtype in DTYPES:
+        cache = fill_cache(inp, dtype)
+        if dtype == "k8v8":
+            codes = cache.k[:, :, :T].cpu().numpy()
+            assert np.mean((codes & 0x78) == 0) > 0.5          # most K codes subnormal
+        ref = oracle_decode(inp, dtype, range(B))
+        for kernel in KERNELS:
+            out = gpu_decode(inp, cache, kernel=kernel).cpu().numpy()
+            assert_gate(out, ref, f"subnormal {dtype} {kernel}")
 
 
 def test_gpu_output_fails_gate_against_broken_oracle_scales():
@@ -219,14 +266,15 @@ def test_gpu_output_fails_gate_against_broken_oracle_scales():
     assert not oracle.attention_gate(out, bad_k)[0]
 
 
-def test_decode_repeat_is_bitwise_stable():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_decode_repeat_is_bitwise_stable(kernel):
     """Standalone repeat harness ("03 · 8n", section 4): many launches on the
     same inputs give bitwise-identical outputs."""
     inp = synth.decode_inputs(synth.WORKLOADS["decode_b16_ctx512"], device="cuda")
     cache = fill_cache(inp, "k8v8")
-    first = gpu_decode(inp, cache)
+    first = gpu_decode(inp, cache, kernel=kernel)
     for _ in range(200):
-        assert torch.equal(gpu_decode(inp, cache), first)
+        assert torch.equal(gpu_decode(inp, cache, kernel=kernel), first)
 
 
 # ---------------------------------------------------------------- prefill --

@@ -51,16 +51,17 @@ def test_static_scratch_decode_matches_workspace_decode():
 
 def test_static_scratch_rejects_oversized_calls():
     lib = get_lib()
-    # batch 16 x 16 query heads x 128 splits of (128 + 2) fp32 partials is
-    # 17,039,360 bytes: just above the 16 MiB array, so the call is refused
-    cache = fk.Fp8KVCache.contiguous(16, 2, 128, 8192, "k8v8")
-    q = torch.zeros(16, 16, 128, dtype=torch.bfloat16, device="cuda")
-    lens = torch.full((16,), 8192, dtype=torch.int32, device="cuda")
-    out = torch.empty(16, 16, 128, dtype=torch.float32, device="cuda")
-    assert fk.fp8kv_decode_workspace_bytes(cache, 16, 128) == 17039360
+    # batch 32 x 16 query heads x 64 splits (128-token tiles over 8192 tokens)
+    # of (128 + 2) fp32 partials is 17,039,360 bytes: just above the 16 MiB
+    # array, so the call is refused before anything is launched
+    cache = fk.Fp8KVCache.contiguous(32, 2, 128, 8192, "k8v8")
+    q = torch.zeros(32, 16, 128, dtype=torch.bfloat16, device="cuda")
+    lens = torch.full((32,), 8192, dtype=torch.int32, device="cuda")
+    out = torch.empty(32, 16, 128, dtype=torch.float32, device="cuda")
+    assert fk.fp8kv_decode_workspace_bytes(cache, 16, 64) == 17039360
     st = lib.fp8kv_decode_attention_static(
         ctypes.c_void_p(q.data_ptr()), cache.struct_ref, ctypes.c_void_p(lens.data_ptr()), 16,
-        ctypes.c_float(0.1), 128, ctypes.c_void_p(out.data_ptr()), 1, None)
+        ctypes.c_float(0.1), 64, ctypes.c_void_p(out.data_ptr()), 1, None)
     assert st == 3
-    # one split fewer fits
-    assert fk.fp8kv_decode_workspace_bytes(cache, 16, 120) <= lib.fp8kv_decode_static_scratch_bytes()
+    # a few splits fewer fit
+    assert fk.fp8kv_decode_workspace_bytes(cache, 16, 60) <= lib.fp8kv_decode_static_scratch_bytes()
