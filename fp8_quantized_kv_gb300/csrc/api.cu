@@ -110,15 +110,18 @@ static int resolve_kernel(const fp8kv_cache* c, int q_heads, int requested) {
 }
 
 static SplitPlan plan_splits(const fp8kv_cache* c, int requested, int kernel) {
-  const int tile = kernel == FP8KV_KERNEL_TENSOR_CORES ? 128 : kTileTokens;
-  const int ctas_per_sm = kernel == FP8KV_KERNEL_TENSOR_CORES ? 2 : 4;
+  const bool tc = kernel == FP8KV_KERNEL_TENSOR_CORES;
+  const int tile = tc ? 128 : kTileTokens;
   const int max_tiles = (capacity_of(c) + tile - 1) / tile;
   if (max_tiles <= 0) return {1, 1, tile, kernel};
   int want = requested;
   if (want <= 0) {
     const long units = (long)c->batch * c->kv_heads;
-    const long target = (long)ctas_per_sm * sm_count();
-    want = units > 0 ? (int)((target + units - 1) / units) : 1;
+    // tensor cores: one CTA per SM, and no partial second wave; CUDA cores:
+    // about four CTAs per SM
+    const long target = (long)(tc ? 1 : 4) * sm_count();
+    if (units <= 0) want = 1;
+    else want = tc ? (int)(target / units) : (int)((target + units - 1) / units);
     const int cap_by_min = (max_tiles + kMinSplitTiles - 1) / kMinSplitTiles;
     if (want > cap_by_min) want = cap_by_min;
   }

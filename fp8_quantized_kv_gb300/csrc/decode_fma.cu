@@ -332,29 +332,58 @@ __global__ void __launch_bounds__(128) decode_split_fma(DecodeParams p) {
 
 // ------------------------------------------------------------------ merge --
 // out[b,h] = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, M = max_s m_s;
-// a row with no valid split (length 0) is written as zeros.
+// a row with no valid split (length 0) is written as zeros.  One CTA per
+// (sequence, query head): warp 0 turns the split maxima into weights in
+// shared memory, then every thread sums its dim over the splits with
+// independent loads.
+constexpr int kMergeMaxS = 1024;
+
 template <int D>
 __global__ void __launch_bounds__(D) decode_merge(const float* __restrict__ part_o,
                                                   const float* __restrict__ part_m,
                                                   const float* __restrict__ part_l, int S, void* out,
                                                   int out_f32) {
+  __shared__ float wsh[kMergeMaxS];
+  __shared__ float inv_sh;
   const int64_t bh = blockIdx.x;
   const int d = threadIdx.x;
   const float* pm = part_m + bh * S;
   const float* pl = part_l + bh * S;
-  float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, pm[s]);
-  float L = 0.f, o = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
+  const int Sw = min(S, kMergeMaxS);
+  if (d < 32) {
+    float M = -INFINITY;
+    for (int s = d; s < S; s += 32) M = fmaxf(M, pm[s]);
+    M = warp_max(M);
+    float L = 0.f;
+    for (int s = d; s < S; s += 32) {
       const float ms = pm[s];
-      if (ms == -INFINITY) continue;
-      const float w = exp2f(ms - M);
+      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      if (s < Sw) wsh[s] = w;
       L = fmaf(w, pl[s], L);
-      o = fmaf(w, part_o[(bh * S + s) * D + d], o);
+    }
+    L = warp_sum(L);
+    if (d == 0) inv_sh = L > 0.f ? 1.0f / L : 0.f;
+  }
+  __syncthreads();
+  const float* po = part_o + bh * S * D + d;
+  float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+  int s = 0;
+  for (; s + 4 <= Sw; s += 4) {
+    o0 = fmaf(wsh[s], po[(int64_t)s * D], o0);
+    o1 = fmaf(wsh[s + 1], po[(int64_t)(s + 1) * D], o1);
+    o2 = fmaf(wsh[s + 2], po[(int64_t)(s + 2) * D], o2);
+    o3 = fmaf(wsh[s + 3], po[(int64_t)(s + 3) * D], o3);
+  }
+  for (; s < Sw; ++s) o0 = fmaf(wsh[s], po[(int64_t)s * D], o0);
+  if (S > kMergeMaxS) {      // rare: more splits than the weight table holds
+    float M = -INFINITY;
+    for (int k = 0; k < S; ++k) M = fmaxf(M, pm[k]);
+    for (int k = kMergeMaxS; k < S; ++k) {
+      const float ms = pm[k];
+      if (ms != -INFINITY) o1 = fmaf(exp2f(ms - M), po[(int64_t)k * D], o1);
     }
   }
-  const float r = L > 0.f ? o / L : 0.f;
+  const float r = ((o0 + o1) + (o2 + o3)) * inv_sh;
   if (out_f32)
     reinterpret_cast<float*>(out)[bh * D + d] = r;
   else

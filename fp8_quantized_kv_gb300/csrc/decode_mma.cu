@@ -56,11 +56,13 @@ struct TcCfg {
   static constexpr int K_TILE = kMmaTile * D * KB;
   static constexpr int V_TILE = kMmaTile * D * VB;
   static constexpr int STAGE = ((K_TILE + V_TILE + 2 * kMmaTile * 4) + 1023) / 1024 * 1024;
-  static constexpr int NST = (KE == ELEM_E4M3 && VE == ELEM_E4M3) ? 3 : 2;
+  static constexpr int NST = (KE == ELEM_E4M3 && VE == ELEM_E4M3) ? 6 : (VE == ELEM_E4M3 ? 4 : 3);
   static constexpr int QOP = KE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;
   static constexpr int POP = VE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;
-  static constexpr int MISC = 1024;
-  static constexpr int BYTES = NST * STAGE + QOP + 2 * POP + MISC + 1024;
+  static constexpr int XO = 8 * 128 * 4;    // group 1's O handed to group 0
+  static constexpr int MISC = 2048;
+  static constexpr int BYTES = NST * STAGE + QOP + 4 * POP + XO + MISC + 1024;
+  static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
 // Byte offset of (row r, byte column c) in a `rows`-row operand stored in the
@@ -72,11 +74,14 @@ __device__ __forceinline__ int sw128_off(int r, int byte_col, int rows) {
   return blk * rows * 128 + r * 128 + ((((within >> 4) ^ (r & 7))) << 4) + (within & 15);
 }
 
-__device__ __forceinline__ uint8_t e4m3_rn(float x) {
+// Two fp32 -> two E4M3 codes (round to nearest even, saturating); element 0
+// in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_rn(float x0, float x1) {
   uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(0.f), "f"(x));
-  return (uint8_t)(r & 0xFF);
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(x1), "f"(x0));
+  return r;
 }
+__device__ __forceinline__ uint8_t e4m3_rn(float x) { return (uint8_t)(e4m3x2_rn(x, 0.f) & 0xFF); }
 __device__ __forceinline__ float e4m3_val(uint8_t c) {
   float f[4];
   e4m3x4_to_f32_scaled((uint32_t)c, f);
@@ -88,6 +93,11 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
+}
+__device__ __forceinline__ float warp_max_redux(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(x));
+  return r;
 }
 // Exponent e with amax * 2^-e <= 448 (e = 0 for amax = 0).
 __device__ __forceinline__ int e4m3_row_exp(float amax) {
@@ -112,19 +122,21 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
-__device__ __forceinline__ bool softmax_group_any(bool pred) {
+// OR of `pred` over the 128 threads of softmax warpgroup `wg` (named barrier
+// 1 + wg), and a plain barrier over the same threads.
+__device__ __forceinline__ bool group_any(int wg, bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "bar.red.or.pred q, %2, 128, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}\n"
       : "=r"(r)
-      : "r"((uint32_t)pred)
+      : "r"((uint32_t)pred), "r"(1 + wg)
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void softmax_group_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+__device__ __forceinline__ void group_sync(int wg) { asm volatile("bar.sync %0, 128;\n" ::"r"(1 + wg) : "memory"); }
 
 struct DecodeTmaParams {
   CUtensorMap tmk;
@@ -132,28 +144,31 @@ struct DecodeTmaParams {
   DecodeParams p;
 };
 
+// Per-warpgroup barrier set (S, P and O double buffers).
+struct WgBars {
+  uint64_t s_full[2], s_empty[2], p_full[2], o_full[2], o_empty[2];
+};
+
 template <int KE, int VE>
-__global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant__ DecodeTmaParams tp) {
+__global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant__ DecodeTmaParams tp) {
   using C = TcCfg<KE, VE>;
   constexpr int D = 128;
   const DecodeParams& p = tp.p;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qop = smem + C::NST * C::STAGE;
-  uint8_t* pop0 = qop + C::QOP;
-  uint8_t* misc = pop0 + 2 * C::POP;
-  uint64_t* full = reinterpret_cast<uint64_t*>(misc);     // [4]
-  uint64_t* empty = full + 4;                              // [4]
-  uint64_t* s_full = empty + 4;                            // [2]
-  uint64_t* s_empty = s_full + 2;                          // [2]
-  uint64_t* p_full = s_empty + 2;                          // [2]
-  uint64_t* o_full = p_full + 2;                           // [2]
-  uint64_t* o_empty = o_full + 2;                          // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(o_empty + 2);
+  uint8_t* pop0 = qop + C::QOP;                            // [wg][buffer] P operands
+  float* xo = reinterpret_cast<float*>(pop0 + 4 * C::POP);   // [8][128]
+  uint8_t* misc = pop0 + 4 * C::POP + C::XO;
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc);     // [8]
+  uint64_t* empty = full + 8;                              // [8]
+  WgBars* wb = reinterpret_cast<WgBars*>(empty + 8);       // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(wb + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
-  float* qscale = reinterpret_cast<float*>(misc + 256);    // [8]
-  float* red = qscale + 8;                                 // [2][4][9]
-  float* lred = red + 72;                                  // [4][8]
+  float* qscale = reinterpret_cast<float*>(misc + 512);    // [8]
+  float* red = qscale + 8;                                 // [wg][2][4][9]
+  float* lred = red + 144;                                 // [wg][4][8]
+  float* xml = lred + 64;                                  // [16]: m and l of warpgroup 1
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -182,24 +197,25 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
   const int n_tiles = t_end - t_begin;
 
   // ---------------------------------------------------------------- setup
-  for (int i = tid; i < (C::QOP + 2 * C::POP) / 16; i += blockDim.x)
+  for (int i = tid; i < (C::QOP + 4 * C::POP) / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(qop)[i] = make_uint4(0, 0, 0, 0);
   if (warp == 1) {
-    umma::tmem_alloc(tslot, 64);
+    umma::tmem_alloc(tslot, 128);
     umma::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < C::NST; ++i) {
       umma::mbar_init(&full[i], 1);
-      umma::mbar_init(&empty[i], 1 + 4);     // PV commit + the four softmax warps
+      umma::mbar_init(&empty[i], 1 + 4);     // PV commit + the four warps of the owning group
     }
-    for (int i = 0; i < 2; ++i) {
-      umma::mbar_init(&s_full[i], 1);
-      umma::mbar_init(&s_empty[i], 4);
-      umma::mbar_init(&p_full[i], 4);
-      umma::mbar_init(&o_full[i], 1);
-      umma::mbar_init(&o_empty[i], 4);
-    }
+    for (int w = 0; w < 2; ++w)
+      for (int i = 0; i < 2; ++i) {
+        umma::mbar_init(&wb[w].s_full[i], 1);
+        umma::mbar_init(&wb[w].s_empty[i], 4);
+        umma::mbar_init(&wb[w].p_full[i], 4);
+        umma::mbar_init(&wb[w].o_full[i], 1);
+        umma::mbar_init(&wb[w].o_empty[i], 4);
+      }
     *abort_flag = 0;
     umma::mbar_fence_init();
   }
@@ -208,7 +224,7 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
     tma::prefetch_map(&tp.tmv);
   }
   __syncthreads();
-  if (warp >= 2) {   // the B operand of QK: query rows (e4m3 hi/lo pairs, or bf16)
+  if (warp >= 2 && warp < 6) {   // the B operand of QK: query rows (e4m3 hi/lo pairs, or bf16)
     for (int g = warp - 2; g < 8; g += 4) {
       float x[4] = {0.f, 0.f, 0.f, 0.f};
       if (g < G) {
@@ -218,7 +234,7 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
       }
       if constexpr (KE == ELEM_E4M3) {
         float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-        amax = warp_max(amax);
+        amax = warp_max_redux(amax);
         const int ex = e4m3_row_exp(amax);
         if (lane == 0) qscale[g] = ldexpf(1.0f, ex);
 #pragma unroll
@@ -309,12 +325,12 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
       const uint32_t qa = umma::smem_u32(qop);
       for (int i = 0; i <= n_tiles; ++i) {
         if (i < n_tiles) {
-          const int s = i % C::NST, u = i / C::NST, bb = i & 1, ub = i >> 1;
+          const int s = i % C::NST, u = i / C::NST, w = i & 1, li = i >> 1, bb = li & 1, ub = li >> 1;
           if (!wait_or_abort(&full[s], u & 1, abort_flag)) break;
-          if (ub > 0 && !wait_or_abort(&s_empty[bb], (ub - 1) & 1, abort_flag)) break;
+          if (ub > 0 && !wait_or_abort(&wb[w].s_empty[bb], (ub - 1) & 1, abort_flag)) break;
           umma::fence_after_sync();
           const uint32_t ka = umma::smem_u32(smem + s * C::STAGE);
-          const uint32_t d = tmem + 16 * bb;
+          const uint32_t d = tmem + 64 * w + 16 * bb;
           if constexpr (KE == ELEM_E4M3) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -330,16 +346,16 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
                                            umma::SWIZZLE_128B),
                                ID_QK, k > 0);
           }
-          umma::mma_commit(&s_full[bb]);
+          umma::mma_commit(&wb[w].s_full[bb]);
         }
         if (i >= 1) {
-          const int j = i - 1, s = j % C::NST, bb = j & 1, ub = j >> 1;
-          if (!wait_or_abort(&p_full[bb], ub & 1, abort_flag)) break;
-          if (ub > 0 && !wait_or_abort(&o_empty[bb], (ub - 1) & 1, abort_flag)) break;
+          const int j = i - 1, s = j % C::NST, w = j & 1, lj = j >> 1, bb = lj & 1, ub = lj >> 1;
+          if (!wait_or_abort(&wb[w].p_full[bb], ub & 1, abort_flag)) break;
+          if (ub > 0 && !wait_or_abort(&wb[w].o_empty[bb], (ub - 1) & 1, abort_flag)) break;
           umma::fence_after_sync();
           const uint32_t va = umma::smem_u32(smem + s * C::STAGE + C::K_TILE);
-          const uint32_t pa = umma::smem_u32(pop0 + bb * C::POP);
-          const uint32_t d = tmem + 32 + 16 * bb;
+          const uint32_t pa = umma::smem_u32(pop0 + (2 * w + bb) * C::POP);
+          const uint32_t d = tmem + 64 * w + 32 + 16 * bb;
           if constexpr (VE == ELEM_E4M3) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -353,16 +369,19 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
                                            umma::SWIZZLE_128B),
                                ID_PV, k > 0);
           }
-          umma::mma_commit(&o_full[bb]);
+          umma::mma_commit(&wb[w].o_full[bb]);
           umma::mma_commit(&empty[s]);
         }
       }
     }
   } else {
-    // ------------------------------------------------ softmax and O update
+    // ------------------------------------- softmax and O update (2 groups)
+    const int wg = (warp - 2) >> 2;                 // warpgroup: even or odd tiles
     const int t = 32 * (warp & 3) + lane;           // TMEM lane of this thread
-    const int sw = warp - 2;                        // 0..3 within the group
+    const int sw = warp & 3;                        // lane quarter
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t s_col = 64 * wg, o_col = 64 * wg + 32;
+    WgBars& B = wb[wg];
     float qs[8];
 #pragma unroll
     for (int g = 0; g < 8; ++g) qs[g] = qscale[g] * p.scale_log2;
@@ -373,20 +392,22 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
     }
     float pf_prev = 1.f;
     bool failed = false;
-    for (int i = 0; i <= n_tiles && !failed; ++i) {
+    const int nl = (n_tiles - wg + 1) / 2;          // tiles of this group
+    for (int li = 0; li <= nl && !failed; ++li) {
       float a_cur[8], b_cur[8];
       float pf_cur = 1.f;
-      if (i < n_tiles) {
-        const int s = i % C::NST, u = i / C::NST, bb = i & 1, ub = i >> 1;
-        bool ok = wait_or_abort(&s_full[bb], ub & 1, abort_flag);
+      if (li < nl) {
+        const int i = 2 * li + wg;
+        const int s = i % C::NST, u = i / C::NST, bb = li & 1, ub = li >> 1;
+        bool ok = wait_or_abort(&B.s_full[bb], ub & 1, abort_flag);
         ok = ok && wait_or_abort(&full[s], u & 1, abort_flag);
-        if (softmax_group_any(!ok)) { failed = true; break; }
+        if (group_any(wg, !ok)) { failed = true; break; }
         umma::fence_after_sync();
         float sc[16];
-        umma::tmem_ld16(tmem + 16 * bb + lane_off, sc);
+        umma::tmem_ld16(tmem + s_col + 16 * bb + lane_off, sc);
         umma::fence_before_sync();
         __syncwarp();
-        if (lane == 0) umma::mbar_arrive(&s_empty[bb]);
+        if (lane == 0) umma::mbar_arrive(&B.s_empty[bb]);
 
         uint8_t* st = smem + s * C::STAGE;
         const float* kss = reinterpret_cast<const float*>(st + C::K_TILE + C::V_TILE);
@@ -397,16 +418,16 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
         const float kf = KE == ELEM_E4M3 ? kss[t] : 1.f;
         const float vsc = VE == ELEM_E4M3 ? (tok_ok ? vss[t] : 0.f) : 1.f;
         float sg[8];
-        float* rb = red + (i & 1) * 36;
+        float* rb = red + (wg * 2 + (li & 1)) * 36;
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const float raw = KE == ELEM_E4M3 ? (sc[g] + sc[g + 8]) : sc[g];
           sg[g] = tok_ok ? raw * (qs[g] * kf) : -INFINITY;
-          const float wm = warp_max(sg[g]);
+          const float wm = warp_max_redux(sg[g]);
           if (lane == 0) rb[sw * 9 + g] = wm;
         }
         if (VE == ELEM_E4M3) {
-          const float vm = warp_max(vsc);
+          const float vm = warp_max_redux(vsc);
           if (lane == 0) rb[sw * 9 + 8] = vm;
         }
         if (!tok_ok) {      // V rows past the sequence end: zero them for PV
@@ -417,7 +438,7 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
             for (int ch = 0; ch < 8; ++ch)
               vrow[(blk * kMmaTile * 128 + t * 128 + ch * 16) / 16] = make_uint4(0, 0, 0, 0);
         }
-        softmax_group_sync();
+        group_sync(wg);
         int pex = 0;
         if (VE == ELEM_E4M3) {
           const float vmax = fmaxf(fmaxf(rb[8], rb[17]), fmaxf(rb[26], rb[35]));
@@ -425,7 +446,8 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
           pf_cur = pow2i(pex);
         }
         const float pinv = pow2i(-pex);
-        uint8_t* pop = pop0 + bb * C::POP;
+        uint8_t* pop = pop0 + (2 * wg + bb) * C::POP;
+        float pb[8];
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const float mt = fmaxf(fmaxf(rb[g], rb[9 + g]), fmaxf(rb[18 + g], rb[27 + g]));
@@ -435,41 +457,50 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
           m_run[g] = mn;
           const float pj = ex2(sg[g] - mt);
           l_thr[g] = l_thr[g] * a_cur[g] + pj * b_cur[g];
-          const float pb = bf16_round(pj * vsc);
-          if constexpr (VE == ELEM_E4M3) {
-            const float ps = pb * pinv;
-            const uint8_t hi = e4m3_rn(ps);
-            const uint8_t lo = e4m3_rn(ps - e4m3_val(hi));
-            pop[sw128_off(g, t, 16)] = hi;
-            pop[sw128_off(g + 8, t, 16)] = lo;
-          } else {
-            *reinterpret_cast<__nv_bfloat16*>(pop + sw128_off(g, t * 2, 16)) = __float2bfloat16_rn(pb);
+          pb[g] = bf16_round(pj * vsc);
+        }
+        if constexpr (VE == ELEM_E4M3) {
+#pragma unroll
+          for (int g = 0; g < 8; g += 2) {
+            const float p0 = pb[g] * pinv, p1 = pb[g + 1] * pinv;
+            const uint32_t hi = e4m3x2_rn(p0, p1);
+            float hv[4];
+            e4m3x4_to_f32_scaled(hi, hv);
+            const uint32_t lo = e4m3x2_rn(p0 - hv[0] * kTwoPow120, p1 - hv[1] * kTwoPow120);
+            pop[sw128_off(g, t, 16)] = (uint8_t)(hi & 0xFF);
+            pop[sw128_off(g + 1, t, 16)] = (uint8_t)(hi >> 8);
+            pop[sw128_off(g + 8, t, 16)] = (uint8_t)(lo & 0xFF);
+            pop[sw128_off(g + 9, t, 16)] = (uint8_t)(lo >> 8);
           }
+        } else {
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            *reinterpret_cast<__nv_bfloat16*>(pop + sw128_off(g, t * 2, 16)) = __float2bfloat16_rn(pb[g]);
         }
         umma::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          umma::mbar_arrive(&p_full[bb]);
+          umma::mbar_arrive(&B.p_full[bb]);
           umma::mbar_arrive(&empty[s]);
         }
       }
-      if (i >= 1) {
-        const int j = i - 1, bb = j & 1, ub = j >> 1;
-        const bool ok = wait_or_abort(&o_full[bb], ub & 1, abort_flag);
-        if (softmax_group_any(!ok)) { failed = true; break; }
+      if (li >= 1) {
+        const int lj = li - 1, bb = lj & 1, ub = lj >> 1;
+        const bool ok = wait_or_abort(&B.o_full[bb], ub & 1, abort_flag);
+        if (group_any(wg, !ok)) { failed = true; break; }
         umma::fence_after_sync();
         float ov[16];
-        umma::tmem_ld16(tmem + 32 + 16 * bb + lane_off, ov);
+        umma::tmem_ld16(tmem + o_col + 16 * bb + lane_off, ov);
         umma::fence_before_sync();
         __syncwarp();
-        if (lane == 0) umma::mbar_arrive(&o_empty[bb]);
+        if (lane == 0) umma::mbar_arrive(&B.o_empty[bb]);
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const float ot = VE == ELEM_E4M3 ? (ov[g] + ov[g + 8]) * pf_prev : ov[g];
           o_run[g] = o_run[g] * a_prev[g] + ot * b_prev[g];
         }
       }
-      if (i < n_tiles) {
+      if (li < nl) {
 #pragma unroll
         for (int g = 0; g < 8; ++g) { a_prev[g] = a_cur[g]; b_prev[g] = b_cur[g]; }
         pf_prev = pf_cur;
@@ -480,29 +511,50 @@ __global__ void __launch_bounds__(192, 1) decode_split_tc(const __grid_constant_
 #pragma unroll
       for (int g = 0; g < 8; ++g) { m_run[g] = -INFINITY; l_thr[g] = 0.f; o_run[g] = 0.f; }
     }
-    // l: per-thread partial sums -> one total per head
+    // l: per-thread partial sums -> one total per head and group
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
       const float ws = warp_sum(l_thr[g]);
-      if (lane == 0) lred[sw * 8 + g] = ws;
+      if (lane == 0) lred[(wg * 4 + sw) * 8 + g] = ws;
     }
-    softmax_group_sync();
+    group_sync(wg);
+    float l_tot[8];
 #pragma unroll
-    for (int g = 0; g < 8; ++g)
-      if (g < G) p.part_o[(part0 + (int64_t)g * S) * D + t] = o_run[g];
-    if (t < G) {
+    for (int g = 0; g < 8; ++g) {
+      const float* lr = lred + wg * 32;
+      l_tot[g] = (lr[g] + lr[8 + g]) + (lr[16 + g] + lr[24 + g]);
+    }
+    // The two groups' running states are merged like two splits: group 1
+    // hands its (m, l, O) to group 0 through shared memory.
+    if (wg == 1) {
 #pragma unroll
-      for (int g = 0; g < 8; ++g)
-        if (g == t) {
-          p.part_m[part0 + (int64_t)g * S] = m_run[g];
-          p.part_l[part0 + (int64_t)g * S] = (lred[g] + lred[8 + g]) + (lred[16 + g] + lred[24 + g]);
+      for (int g = 0; g < 8; ++g) xo[g * D + t] = o_run[g];
+      if (t == 0) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) { xml[g] = m_run[g]; xml[8 + g] = l_tot[g]; }
+      }
+    }
+    asm volatile("bar.sync 3, 256;\n" ::: "memory");
+    if (wg == 0) {
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const float m1 = xml[g], l1 = xml[8 + g];
+        const float M = fmaxf(m_run[g], m1);
+        const float f0 = m_run[g] == -INFINITY ? 0.f : ex2(m_run[g] - M);
+        const float f1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+        const float o = o_run[g] * f0 + xo[g * D + t] * f1;
+        if (g < G) p.part_o[(part0 + (int64_t)g * S) * D + t] = o;
+        if (t == g && g < G) {
+          p.part_m[part0 + (int64_t)g * S] = M;
+          p.part_l[part0 + (int64_t)g * S] = l_tot[g] * f0 + l1 * f1;
         }
+      }
     }
   }
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
-  if (warp == 1) umma::tmem_dealloc(tmem, 64);
+  if (warp == 1) umma::tmem_dealloc(tmem, 128);
 }
 
 // ------------------------------------------------------------ host side --
@@ -558,7 +610,7 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
       !make_map(&tp.tmv, c.v, VE != ELEM_E4M3, rows, box_rows))
     return cudaErrorInvalidValue;
   tp.p = p;
-  decode_split_tc<KE, VE><<<grid, 192, smem, st>>>(tp);
+  decode_split_tc<KE, VE><<<grid, 320, smem, st>>>(tp);
   return cudaGetLastError();
 }
 
