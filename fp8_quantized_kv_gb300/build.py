@@ -31,8 +31,8 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src, extra):
-    obj = os.path.join(OUT, os.path.basename(src) + ".o")
+def _compile(src, extra, out_dir):
+    obj = os.path.join(out_dir, os.path.basename(src) + ".o")
     if _stale(obj, [src] + _headers()):
         tmp = obj + f".tmp{os.getpid()}"
         cmd = [NVCC] + ARCH + FLAGS + extra + ["-c", src, "-o", tmp]
@@ -43,25 +43,32 @@ def _compile(src, extra):
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    os.makedirs(OUT, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, trace: bool = False) -> str:
+    """Build libfp8kv.so (or, with trace=True, libfp8kv_trace.so: the same
+    library with per-tile clock stamps of one CTA of the tensor-core decode
+    kernel, read with fp8kv_trace_read)."""
+    out_dir = OUT + "_trace" if trace else OUT
+    lib = os.path.join(out_dir, "libfp8kv_trace.so" if trace else "libfp8kv.so")
+    os.makedirs(out_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     if force:
-        for o in glob.glob(os.path.join(OUT, "*.o")):
+        for o in glob.glob(os.path.join(out_dir, "*.o")):
             os.remove(o)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if trace:
+        extra = extra + ["-DFP8KV_TRACE"]
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    if force or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, extra, out_dir), srcs))
+    if force or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, trace="--trace" in sys.argv))

@@ -37,7 +37,10 @@
 //   warps 2-5  softmax of tile i, then the O update of tile i-1 (thread =
 //              TMEM lane = token for S, = head dim for O).
 // S, O (TMEM) and P (shared memory) are double-buffered, so QK(i+1), PV(i)
-// and the softmax of tile i+1 overlap.  Every wait is bounded; a wait that
+// and the softmax of tile i+1 overlap.  Each QK and PV is split into four
+// independent MMAs (one per k-step, each with its own TMEM accumulator,
+// summed by the reading threads): dependent thin MMAs would serialise on
+// their latency.  Every wait is bounded; a wait that
 // runs out raises FP8KV_DEVERR_TIMEOUT, the CTA writes an empty partial and
 // leaves.  V rows past the sequence end are zeroed before PV (0 * NaN would
 // poison the product).
@@ -58,7 +61,7 @@ struct TcCfg {
   static constexpr int STAGE = ((K_TILE + V_TILE + 2 * kMmaTile * 4) + 1023) / 1024 * 1024;
   static constexpr int NST = (KE == ELEM_E4M3 && VE == ELEM_E4M3) ? 6 : (VE == ELEM_E4M3 ? 4 : 3);
   static constexpr int QOP = KE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;
-  static constexpr int POP = VE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;
+  static constexpr int POP = VE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;   // [128 tokens][16 or 32 B]
   static constexpr int XO = 8 * 128 * 4;    // group 1's O handed to group 0
   static constexpr int MISC = 2048;
   static constexpr int BYTES = NST * STAGE + QOP + 4 * POP + XO + MISC + 1024;
@@ -106,18 +109,22 @@ __device__ __forceinline__ int e4m3_row_exp(float amax) {
   return e;
 }
 
-// Bounded wait shared by all roles of a CTA: gives up after 2 s of wall time
-// or as soon as another role has given up (abort flag).
+// Bounded wait shared by all roles of a CTA: gives up after ~2 s (SM clock
+// cycles, checked every 64 polls) or as soon as another role has given up
+// (abort flag).
+constexpr long long kWaitLimitCycles = 4000000000ll;
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  constexpr uint64_t kLimitNs = 2000000000ull;
   if (umma::mbar_try(bar, parity)) return true;
-  const uint64_t t0 = umma::globaltimer_ns();
-  while (true) {
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
     if (umma::mbar_try(bar, parity)) return true;
-    if (*abort) return false;
-    if (umma::globaltimer_ns() - t0 > kLimitNs) {
-      *abort = 1;
-      return false;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        *abort = 1;
+        return false;
+      }
     }
   }
 }
@@ -137,6 +144,33 @@ __device__ __forceinline__ bool group_any(int wg, bool pred) {
   return r != 0;
 }
 __device__ __forceinline__ void group_sync(int wg) { asm volatile("bar.sync %0, 128;\n" ::"r"(1 + wg) : "memory"); }
+
+#ifdef FP8KV_TRACE
+// Per-tile clock64 stamps of CTA (0, 0, 0), read by fp8kv_trace_read():
+// slot 8*i + {0: producer issue, 1: QK issue, 2: PV issue, 3: softmax start,
+// 4: P ready (first warp), 5: O folded, 6: P ready (last warp)}; 1010..1014:
+// teardown steps; 1020/1021: kernel begin/end.
+__device__ unsigned long long g_trace[1024];
+// %globaltimer at entry and exit of every CTA (first 4096 CTAs).
+__device__ unsigned long long g_cta_time[4096][2];
+#define TRACE(slot)                                                          \
+  do {                                                                       \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (slot) < 1024) \
+      g_trace[(slot)] = clock64();                                           \
+  } while (0)
+#define TRACE_MAX(slot)                                                      \
+  do {                                                                       \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (slot) < 1024) \
+      atomicMax(&g_trace[(slot)], (unsigned long long)clock64());            \
+  } while (0)
+#else
+#define TRACE(slot) \
+  do {              \
+  } while (0)
+#define TRACE_MAX(slot) \
+  do {                  \
+  } while (0)
+#endif
 
 struct DecodeTmaParams {
   CUtensorMap tmk;
@@ -195,14 +229,62 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
     return;
   }
   const int n_tiles = t_end - t_begin;
+  if (tid == 0) TRACE(1020);
+#ifdef FP8KV_TRACE
+  const int cta_lin = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  if (tid == 0 && cta_lin < 4096) g_cta_time[cta_lin][0] = umma::globaltimer_ns();
+#endif
 
   // ---------------------------------------------------------------- setup
-  for (int i = tid; i < (C::QOP + 4 * C::POP) / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(qop)[i] = make_uint4(0, 0, 0, 0);
-  if (warp == 1) {
-    umma::tmem_alloc(tslot, 128);
-    umma::tmem_relinquish();
-  }
+  // Overlapped before the one CTA-wide barrier: thread 0 initialises the
+  // barriers and issues the first tiles' loads, warp 1 allocates TMEM, warps
+  // 2-5 write the query operand.
+  const int64_t cont_row0 = ((int64_t)b * c.kv_heads + h) * c.max_tokens;
+  // Issue the TMA copies of tile i into its stage (producer thread only).
+  auto produce = [&](int i) {
+    const int s = i % C::NST;
+    uint8_t* st = smem + s * C::STAGE;
+    float* kss = reinterpret_cast<float*>(st + C::K_TILE + C::V_TILE);
+    float* vss = kss + kMmaTile;
+    const int t0 = (t_begin + i) * kMmaTile;
+    const int valid = min(kMmaTile, T - t0);
+    if (!c.paged) {
+      const int nsc = min(kMmaTile, (valid + 15) & ~15);
+      const uint32_t bytes = C::K_TILE + C::V_TILE + (KE == ELEM_E4M3 ? nsc * 4 : 0) +
+                             (VE == ELEM_E4M3 ? nsc * 4 : 0);
+      tma::arrive_expect_tx(&full[s], bytes);
+      const int row = (int)(cont_row0 + t0);
+      tma::load_2d(st, &tp.tmk, 0, row, &full[s]);
+      if (KE != ELEM_E4M3) tma::load_2d(st + kMmaTile * 128, &tp.tmk, 64, row, &full[s]);
+      tma::load_2d(st + C::K_TILE, &tp.tmv, 0, row, &full[s]);
+      if (VE != ELEM_E4M3) tma::load_2d(st + C::K_TILE + kMmaTile * 128, &tp.tmv, 64, row, &full[s]);
+      if (KE == ELEM_E4M3) tma::load_1d(kss, c.k_scale + cont_row0 + t0, nsc * 4, &full[s]);
+      if (VE == ELEM_E4M3) tma::load_1d(vss, c.v_scale + cont_row0 + t0, nsc * 4, &full[s]);
+    } else {
+      const int P = c.page_size;
+      const int np = (valid + P - 1) / P;
+      const uint32_t per_page = P * 128 * (C::KB + C::VB) + P * 4 * ((KE == ELEM_E4M3) + (VE == ELEM_E4M3));
+      tma::arrive_expect_tx(&full[s], per_page * np);
+      for (int j = 0; j < np; ++j) {
+        int page = c.page_table[(int64_t)b * c.max_pages_per_seq + ((t0 >> c.page_shift) + j)];
+        if (page < 0 || page >= c.num_pages) {
+          raise_error(p.err, FP8KV_DEVERR_BAD_PAGE);
+          page = 0;      // read a valid page; the result is flagged as wrong
+        }
+        const int64_t row = ((int64_t)page * c.kv_heads + h) * P;
+        const int off = j * P * 128;
+        tma::load_2d(st + off, &tp.tmk, 0, (int)row, &full[s]);
+        if (KE != ELEM_E4M3) tma::load_2d(st + kMmaTile * 128 + off, &tp.tmk, 64, (int)row, &full[s]);
+        tma::load_2d(st + C::K_TILE + off, &tp.tmv, 0, (int)row, &full[s]);
+        if (VE != ELEM_E4M3)
+          tma::load_2d(st + C::K_TILE + kMmaTile * 128 + off, &tp.tmv, 64, (int)row, &full[s]);
+        if (KE == ELEM_E4M3) tma::load_1d(kss + j * P, c.k_scale + row, P * 4, &full[s]);
+        if (VE == ELEM_E4M3) tma::load_1d(vss + j * P, c.v_scale + row, P * 4, &full[s]);
+      }
+    }
+    TRACE(8 * i + 0);
+  };
+  const int n_first = min(n_tiles, C::NST);
   if (tid == 0) {
     for (int i = 0; i < C::NST; ++i) {
       umma::mbar_init(&full[i], 1);
@@ -218,13 +300,20 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
       }
     *abort_flag = 0;
     umma::mbar_fence_init();
-  }
-  if (tid == 32) {
     tma::prefetch_map(&tp.tmk);
     tma::prefetch_map(&tp.tmv);
+    for (int i = 0; i < n_first; ++i) produce(i);
   }
-  __syncthreads();
-  if (warp >= 2 && warp < 6) {   // the B operand of QK: query rows (e4m3 hi/lo pairs, or bf16)
+  if (warp == 1) {
+    umma::tmem_alloc(tslot, 512);
+    umma::tmem_relinquish();
+  }
+  if (warp >= 2 && warp < 6) {   // zero the operand buffers (group 0 only, then its own barrier)
+    for (int i = tid - 64; i < (C::QOP + 4 * C::POP) / 16; i += 128)
+      reinterpret_cast<uint4*>(qop)[i] = make_uint4(0, 0, 0, 0);
+    group_sync(0);
+  }
+  if (warp >= 2 && warp < 6) {   // query rows -> B operand of QK (e4m3 hi/lo pairs, or bf16)
     for (int g = warp - 2; g < 8; g += 4) {
       float x[4] = {0.f, 0.f, 0.f, 0.f};
       if (g < G) {
@@ -262,56 +351,18 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const int64_t cont_row0 = ((int64_t)b * c.kv_heads + h) * c.max_tokens;
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
+      int issued = n_first;
+      for (int i = n_first; i < n_tiles; ++i) {
         const int s = i % C::NST, u = i / C::NST;
-        if (u > 0 && !wait_or_abort(&empty[s], (u - 1) & 1, abort_flag)) break;
-        uint8_t* st = smem + s * C::STAGE;
-        float* kss = reinterpret_cast<float*>(st + C::K_TILE + C::V_TILE);
-        float* vss = kss + kMmaTile;
-        const int t0 = (t_begin + i) * kMmaTile;
-        const int valid = min(kMmaTile, T - t0);
-        if (!c.paged) {
-          const int nsc = min(kMmaTile, (valid + 15) & ~15);
-          const uint32_t bytes = C::K_TILE + C::V_TILE + (KE == ELEM_E4M3 ? nsc * 4 : 0) +
-                                 (VE == ELEM_E4M3 ? nsc * 4 : 0);
-          tma::arrive_expect_tx(&full[s], bytes);
-          const int row = (int)(cont_row0 + t0);
-          tma::load_2d(st, &tp.tmk, 0, row, &full[s]);
-          if (KE != ELEM_E4M3) tma::load_2d(st + kMmaTile * 128, &tp.tmk, 64, row, &full[s]);
-          tma::load_2d(st + C::K_TILE, &tp.tmv, 0, row, &full[s]);
-          if (VE != ELEM_E4M3) tma::load_2d(st + C::K_TILE + kMmaTile * 128, &tp.tmv, 64, row, &full[s]);
-          if (KE == ELEM_E4M3) tma::load_1d(kss, c.k_scale + cont_row0 + t0, nsc * 4, &full[s]);
-          if (VE == ELEM_E4M3) tma::load_1d(vss, c.v_scale + cont_row0 + t0, nsc * 4, &full[s]);
-        } else {
-          const int P = c.page_size;
-          const int np = (valid + P - 1) / P;
-          const uint32_t per_page = P * 128 * (C::KB + C::VB) + P * 4 * ((KE == ELEM_E4M3) + (VE == ELEM_E4M3));
-          tma::arrive_expect_tx(&full[s], per_page * np);
-          for (int j = 0; j < np; ++j) {
-            int page = c.page_table[(int64_t)b * c.max_pages_per_seq + ((t0 >> c.page_shift) + j)];
-            if (page < 0 || page >= c.num_pages) {
-              raise_error(p.err, FP8KV_DEVERR_BAD_PAGE);
-              page = 0;      // read a valid page; the result is flagged as wrong
-            }
-            const int64_t row = ((int64_t)page * c.kv_heads + h) * P;
-            const int off = j * P * 128;
-            tma::load_2d(st + off, &tp.tmk, 0, (int)row, &full[s]);
-            if (KE != ELEM_E4M3) tma::load_2d(st + kMmaTile * 128 + off, &tp.tmk, 64, (int)row, &full[s]);
-            tma::load_2d(st + C::K_TILE + off, &tp.tmv, 0, (int)row, &full[s]);
-            if (VE != ELEM_E4M3)
-              tma::load_2d(st + C::K_TILE + kMmaTile * 128 + off, &tp.tmv, 64, (int)row, &full[s]);
-            if (KE == ELEM_E4M3) tma::load_1d(kss + j * P, c.k_scale + row, P * 4, &full[s]);
-            if (VE == ELEM_E4M3) tma::load_1d(vss + j * P, c.v_scale + row, P * 4, &full[s]);
-          }
-        }
+        if (!wait_or_abort(&empty[s], (u - 1) & 1, abort_flag)) break;
+        produce(i);
         ++issued;
       }
       // Before leaving, let every copy this thread issued land (only an
       // aborted run has copies that nobody waited for).
       for (int i = max(0, issued - C::NST); i < issued; ++i)
         (void)umma::mbar_wait(&full[i % C::NST], (i / C::NST) & 1, 100000000ull);
+      TRACE(1013);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
@@ -320,57 +371,86 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
           ? umma::idesc(umma::FMT_E4M3, umma::FMT_E4M3, umma::MAJOR_K, umma::MAJOR_K, 128, 16)
           : umma::idesc(umma::FMT_BF16, umma::FMT_BF16, umma::MAJOR_K, umma::MAJOR_K, 128, 16);
       constexpr uint32_t ID_PV = VE == ELEM_E4M3
-          ? umma::idesc(umma::FMT_E4M3, umma::FMT_E4M3, umma::MAJOR_MN, umma::MAJOR_K, 128, 16)
-          : umma::idesc(umma::FMT_BF16, umma::FMT_BF16, umma::MAJOR_MN, umma::MAJOR_K, 128, 16);
+          ? umma::idesc(umma::FMT_E4M3, umma::FMT_E4M3, umma::MAJOR_MN, umma::MAJOR_MN, 128, 16)
+          : umma::idesc(umma::FMT_BF16, umma::FMT_BF16, umma::MAJOR_MN, umma::MAJOR_MN, 128, 16);
       const uint32_t qa = umma::smem_u32(qop);
-      for (int i = 0; i <= n_tiles; ++i) {
-        if (i < n_tiles) {
-          const int s = i % C::NST, u = i / C::NST, w = i & 1, li = i >> 1, bb = li & 1, ub = li >> 1;
-          if (!wait_or_abort(&full[s], u & 1, abort_flag)) break;
-          if (ub > 0 && !wait_or_abort(&wb[w].s_empty[bb], (ub - 1) & 1, abort_flag)) break;
-          umma::fence_after_sync();
-          const uint32_t ka = umma::smem_u32(smem + s * C::STAGE);
-          const uint32_t d = tmem + 64 * w + 16 * bb;
-          if constexpr (KE == ELEM_E4M3) {
+      // Event loop: issue whichever of the next QK and the next PV is ready,
+      // so QK runs up to two tiles ahead of each group's softmax.
+      int nq = 0, np = 0;
+      long long t_prog = clock64();
+      uint32_t idle = 0;
+      while (np < n_tiles) {
+        bool prog = false;
+        if (nq < n_tiles) {
+          const int s = nq % C::NST, u = nq / C::NST, w = nq & 1, li = nq >> 1, bb = li & 1, ub = li >> 1;
+          if (umma::mbar_test(&full[s], u & 1) &&
+              (ub == 0 || umma::mbar_test(&wb[w].s_empty[bb], (ub - 1) & 1))) {
+            umma::fence_after_sync();
+            const uint32_t ka = umma::smem_u32(smem + s * C::STAGE);
+            // four independent accumulators (one per 32-byte k-step) so the
+            // thin MMAs pipeline instead of waiting on each other
+            const uint32_t d = tmem + 256 * w + 64 * bb;
+            if constexpr (KE == ELEM_E4M3) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma::mma_f8_ss(d, umma::sdesc(ka + k * 32, 16, 1024, umma::SWIZZLE_128B),
-                              umma::sdesc(qa + k * 32, 16, 1024, umma::SWIZZLE_128B), ID_QK, k > 0);
-          } else {
+              for (int k = 0; k < 4; ++k)
+                umma::mma_f8_ss(d + 16 * k, umma::sdesc(ka + k * 32, 16, 1024, umma::SWIZZLE_128B),
+                                umma::sdesc(qa + k * 32, 16, 1024, umma::SWIZZLE_128B), ID_QK, 0);
+            } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              umma::mma_f16_ss(d,
-                               umma::sdesc(ka + (k >> 2) * (kMmaTile * 128) + (k & 3) * 32, 16, 1024,
-                                           umma::SWIZZLE_128B),
-                               umma::sdesc(qa + (k >> 2) * (16 * 128) + (k & 3) * 32, 16, 1024,
-                                           umma::SWIZZLE_128B),
-                               ID_QK, k > 0);
+              for (int k = 0; k < 8; ++k)
+                umma::mma_f16_ss(d + 16 * (k & 3),
+                                 umma::sdesc(ka + (k >> 2) * (kMmaTile * 128) + (k & 3) * 32, 16, 1024,
+                                             umma::SWIZZLE_128B),
+                                 umma::sdesc(qa + (k >> 2) * (16 * 128) + (k & 3) * 32, 16, 1024,
+                                             umma::SWIZZLE_128B),
+                                 ID_QK, k >= 4);
+            }
+            umma::mma_commit(&wb[w].s_full[bb]);
+            TRACE(8 * nq + 1);
+            ++nq;
+            prog = true;
           }
-          umma::mma_commit(&wb[w].s_full[bb]);
         }
-        if (i >= 1) {
-          const int j = i - 1, s = j % C::NST, w = j & 1, lj = j >> 1, bb = lj & 1, ub = lj >> 1;
-          if (!wait_or_abort(&wb[w].p_full[bb], ub & 1, abort_flag)) break;
-          if (ub > 0 && !wait_or_abort(&wb[w].o_empty[bb], (ub - 1) & 1, abort_flag)) break;
-          umma::fence_after_sync();
-          const uint32_t va = umma::smem_u32(smem + s * C::STAGE + C::K_TILE);
-          const uint32_t pa = umma::smem_u32(pop0 + (2 * w + bb) * C::POP);
-          const uint32_t d = tmem + 64 * w + 32 + 16 * bb;
-          if constexpr (VE == ELEM_E4M3) {
+        if (np < nq) {
+          const int j = np, s = j % C::NST, w = j & 1, lj = j >> 1, bb = lj & 1, ub = lj >> 1;
+          if (umma::mbar_test(&wb[w].p_full[bb], ub & 1) &&
+              (ub == 0 || umma::mbar_test(&wb[w].o_empty[bb], (ub - 1) & 1))) {
+            umma::fence_after_sync();
+            const uint32_t va = umma::smem_u32(smem + s * C::STAGE + C::K_TILE);
+            const uint32_t pa = umma::smem_u32(pop0 + (2 * w + bb) * C::POP);
+            const uint32_t d = tmem + 256 * w + 128 + 64 * bb;
+            if constexpr (VE == ELEM_E4M3) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma::mma_f8_ss(d, umma::sdesc(va + k * 4 * 1024, 1024, 1024, umma::SWIZZLE_128B),
-                              umma::sdesc(pa + k * 32, 16, 1024, umma::SWIZZLE_128B), ID_PV, k > 0);
-          } else {
+              for (int k = 0; k < 4; ++k)
+                umma::mma_f8_ss(d + 16 * k, umma::sdesc(va + k * 4 * 1024, 1024, 1024, umma::SWIZZLE_128B),
+                                umma::sdesc(pa + k * 512, 128, 128, umma::SWIZZLE_NONE), ID_PV, 0);
+            } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              umma::mma_f16_ss(d, umma::sdesc(va + k * 2 * 1024, kMmaTile * 128, 1024, umma::SWIZZLE_128B),
-                               umma::sdesc(pa + (k >> 2) * (16 * 128) + (k & 3) * 32, 16, 1024,
-                                           umma::SWIZZLE_128B),
-                               ID_PV, k > 0);
+              for (int k = 0; k < 8; ++k)
+                umma::mma_f16_ss(d + 16 * (k & 3),
+                                 umma::sdesc(va + k * 2 * 1024, kMmaTile * 128, 1024, umma::SWIZZLE_128B),
+                                 umma::sdesc(pa + k * 512, 256, 128, umma::SWIZZLE_NONE), ID_PV, k >= 4);
+            }
+            umma::mma_commit(&wb[w].o_full[bb]);
+            umma::mma_commit(&empty[s]);
+            TRACE(8 * np + 2);
+            ++np;
+            prog = true;
           }
-          umma::mma_commit(&wb[w].o_full[bb]);
-          umma::mma_commit(&empty[s]);
+        }
+        if (np == n_tiles) TRACE(1014);
+        if (prog) {
+          idle = 0;
+        } else {
+          __nanosleep(20);   // back off: the polling thread shares an SM sub-partition with softmax warps
+        }
+        if (!prog && (++idle & 63) == 0) {
+          if (idle == 64) t_prog = clock64();
+          if (*abort_flag) break;
+          if (clock64() - t_prog > kWaitLimitCycles) {
+            *abort_flag = 1;
+            break;
+          }
         }
       }
     }
@@ -380,7 +460,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
     const int t = 32 * (warp & 3) + lane;           // TMEM lane of this thread
     const int sw = warp & 3;                        // lane quarter
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t s_col = 64 * wg, o_col = 64 * wg + 32;
+    const uint32_t s_col = 256 * wg, o_col = 256 * wg + 128;
     WgBars& B = wb[wg];
     float qs[8];
 #pragma unroll
@@ -402,9 +482,19 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         bool ok = wait_or_abort(&B.s_full[bb], ub & 1, abort_flag);
         ok = ok && wait_or_abort(&full[s], u & 1, abort_flag);
         if (group_any(wg, !ok)) { failed = true; break; }
+        if (t == 0) TRACE(8 * i + 3);
         umma::fence_after_sync();
         float sc[16];
-        umma::tmem_ld16(tmem + s_col + 16 * bb + lane_off, sc);
+        {
+          uint32_t r[4][16];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) umma::tmem_ld16_nowait(tmem + s_col + 64 * bb + 16 * k + lane_off, r[k]);
+          umma::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            sc[j] = (__uint_as_float(r[0][j]) + __uint_as_float(r[1][j])) +
+                    (__uint_as_float(r[2][j]) + __uint_as_float(r[3][j]));
+        }
         umma::fence_before_sync();
         __syncwarp();
         if (lane == 0) umma::mbar_arrive(&B.s_empty[bb]);
@@ -459,23 +549,29 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
           l_thr[g] = l_thr[g] * a_cur[g] + pj * b_cur[g];
           pb[g] = bf16_round(pj * vsc);
         }
+        // P^T operand, MN-major without swizzle: token t's 16 bytes (e4m3:
+        // hi of heads 0..7 then lo; bf16: heads 0..7) in one 16-byte store.
         if constexpr (VE == ELEM_E4M3) {
+          uint32_t hw[4], lw[4];
 #pragma unroll
           for (int g = 0; g < 8; g += 2) {
             const float p0 = pb[g] * pinv, p1 = pb[g + 1] * pinv;
             const uint32_t hi = e4m3x2_rn(p0, p1);
             float hv[4];
             e4m3x4_to_f32_scaled(hi, hv);
-            const uint32_t lo = e4m3x2_rn(p0 - hv[0] * kTwoPow120, p1 - hv[1] * kTwoPow120);
-            pop[sw128_off(g, t, 16)] = (uint8_t)(hi & 0xFF);
-            pop[sw128_off(g + 1, t, 16)] = (uint8_t)(hi >> 8);
-            pop[sw128_off(g + 8, t, 16)] = (uint8_t)(lo & 0xFF);
-            pop[sw128_off(g + 9, t, 16)] = (uint8_t)(lo >> 8);
+            hw[g >> 1] = hi;
+            lw[g >> 1] = e4m3x2_rn(p0 - hv[0] * kTwoPow120, p1 - hv[1] * kTwoPow120);
           }
+          *reinterpret_cast<uint4*>(pop + t * 16) =
+              make_uint4(hw[0] | (hw[1] << 16), hw[2] | (hw[3] << 16), lw[0] | (lw[1] << 16), lw[2] | (lw[3] << 16));
         } else {
+          uint32_t w4[4];
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
-            *reinterpret_cast<__nv_bfloat16*>(pop + sw128_off(g, t * 2, 16)) = __float2bfloat16_rn(pb[g]);
+          for (int g = 0; g < 8; g += 2) {
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(pb[g], pb[g + 1]);
+            w4[g >> 1] = *reinterpret_cast<const uint32_t*>(&v2);
+          }
+          *reinterpret_cast<uint4*>(pop + (t >> 3) * 256 + (t & 7) * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         umma::fence_proxy_async_smem();
         __syncwarp();
@@ -483,6 +579,8 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
           umma::mbar_arrive(&B.p_full[bb]);
           umma::mbar_arrive(&empty[s]);
         }
+        if (t == 0) TRACE(8 * i + 4);
+        if (lane == 0) TRACE_MAX(8 * i + 6);
       }
       if (li >= 1) {
         const int lj = li - 1, bb = lj & 1, ub = lj >> 1;
@@ -490,7 +588,16 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         if (group_any(wg, !ok)) { failed = true; break; }
         umma::fence_after_sync();
         float ov[16];
-        umma::tmem_ld16(tmem + o_col + 16 * bb + lane_off, ov);
+        {
+          uint32_t r[4][16];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) umma::tmem_ld16_nowait(tmem + o_col + 64 * bb + 16 * k + lane_off, r[k]);
+          umma::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            ov[j] = (__uint_as_float(r[0][j]) + __uint_as_float(r[1][j])) +
+                    (__uint_as_float(r[2][j]) + __uint_as_float(r[3][j]));
+        }
         umma::fence_before_sync();
         __syncwarp();
         if (lane == 0) umma::mbar_arrive(&B.o_empty[bb]);
@@ -499,6 +606,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
           const float ot = VE == ELEM_E4M3 ? (ov[g] + ov[g + 8]) * pf_prev : ov[g];
           o_run[g] = o_run[g] * a_prev[g] + ot * b_prev[g];
         }
+        if (t == 0) TRACE(8 * (2 * lj + wg) + 5);
       }
       if (li < nl) {
 #pragma unroll
@@ -518,6 +626,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
       if (lane == 0) lred[(wg * 4 + sw) * 8 + g] = ws;
     }
     group_sync(wg);
+    if (t == 0 && wg == 0) TRACE(1010);
     float l_tot[8];
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
@@ -535,6 +644,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
       }
     }
     asm volatile("bar.sync 3, 256;\n" ::: "memory");
+    if (t == 0 && wg == 0) TRACE(1011);
     if (wg == 0) {
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
@@ -549,12 +659,17 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
           p.part_l[part0 + (int64_t)g * S] = l_tot[g] * f0 + l1 * f1;
         }
       }
+      if (t == 0) TRACE(1012);
     }
   }
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
-  if (warp == 1) umma::tmem_dealloc(tmem, 128);
+  if (warp == 1) umma::tmem_dealloc(tmem, 512);
+  if (tid == 0) TRACE(1021);
+#ifdef FP8KV_TRACE
+  if (tid == 0 && cta_lin < 4096) g_cta_time[cta_lin][1] = umma::globaltimer_ns();
+#endif
 }
 
 // ------------------------------------------------------------ host side --
@@ -613,6 +728,17 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
   decode_split_tc<KE, VE><<<grid, 320, smem, st>>>(tp);
   return cudaGetLastError();
 }
+
+#ifdef FP8KV_TRACE
+extern "C" __attribute__((visibility("default"))) int fp8kv_trace_read(unsigned long long* out, int n) {
+  if (n > 1024) n = 1024;
+  return cudaMemcpyFromSymbol(out, g_trace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
+}
+extern "C" __attribute__((visibility("default"))) int fp8kv_trace_read_cta(unsigned long long* out, int n) {
+  if (n > 4096) n = 4096;
+  return cudaMemcpyFromSymbol(out, g_cta_time, n * 2 * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int dtype, int batch, cudaStream_t st) {
   dim3 grid(p.num_splits, p.c.kv_heads, batch);
