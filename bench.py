@@ -3,9 +3,11 @@
 
 One step = one decode layer of the batch-16, 8192-token workload (16 query /
 2 KV heads, head_dim 128, e4m3 K and V with per-(token, head) fp32 scales):
-  1. fp8kv_append of the step's new token for every sequence (position 8191),
-  2. fp8kv_decode_split (flash-decoding split kernel, fp32 partials),
-  3. fp8kv_decode_merge (second kernel, bf16 output).
+one fp8kv_decode_step call, which appends the step's new token of every
+sequence (position 8191) and attends over the 8192 cached tokens.  On the
+tensor-core kernel that is one launch (append, flash-decoding split and the
+merge of the fp32 partials all inside it); on the CUDA-core kernel it is
+three (append, split, merge).
 Each step reads a different one of L distinct layer caches (L * 69 MB well
 above the 126 MB L2), so every step streams its cache from HBM.  Steps are
 replayed from CUDA graphs; timing uses CUDA events on the launching stream.
@@ -273,34 +275,22 @@ def run_reference(args, ws, rank):
 # ----------------------------------------------------------------- GPU arm --
 
 class Layer:
-    """One layer: its own cache plus pre-built C-ABI argument tuples."""
+    """One layer: its own cache, zero-filled workspace and pre-built C-ABI
+    argument tuple for fp8kv_decode_step."""
 
-    def __init__(self, cache, q, lens, ws_tensor, out, knew, vnew, sidx, pos, Hq, sm_scale, kernel):
+    def __init__(self, cache, q, lens, ws_tensor, out, knew, vnew, Hq, sm_scale, kernel):
         from fp8_quantized_kv_gb300._lib import get_lib
         self.lib = get_lib()
         self.cache = cache
-        self.keep = (q, lens, ws_tensor, out, knew, vnew, sidx, pos)
+        self.keep = (q, lens, ws_tensor, out, knew, vnew)
         P = lambda t: ctypes.c_void_p(t.data_ptr())
-        self.a_append = (cache.struct_ref, P(knew), P(vnew), P(sidx), P(pos), knew.shape[0])
-        wsb = ws_tensor.numel()
-        self.a_split = (P(q), cache.struct_ref, P(lens), Hq, ctypes.c_float(sm_scale), 0, kernel,
-                        P(ws_tensor), wsb)
-        self.a_merge = (cache.struct_ref, Hq, 0, kernel, P(ws_tensor), wsb, P(out), 0)
+        self.a_step = (P(q), P(knew), P(vnew), cache.struct_ref, P(lens), Hq, ctypes.c_float(sm_scale), 0,
+                       kernel, P(ws_tensor), ws_tensor.numel(), P(out), 0)
 
-    def append(self, s):
-        r = self.lib.fp8kv_append(*self.a_append, s)
+    def step(self, s):
+        r = self.lib.fp8kv_decode_step(*self.a_step, s)
         if r:
-            raise RuntimeError(f"fp8kv_append status {r}")
-
-    def split(self, s):
-        r = self.lib.fp8kv_decode_split(*self.a_split, s)
-        if r:
-            raise RuntimeError(f"fp8kv_decode_split status {r}")
-
-    def merge(self, s):
-        r = self.lib.fp8kv_decode_merge(*self.a_merge, s)
-        if r:
-            raise RuntimeError(f"fp8kv_decode_merge status {r}")
+            raise RuntimeError(f"fp8kv_decode_step status {r}")
 
 
 def build_layers(spec, dtype, L, inp, kernel):
@@ -331,18 +321,17 @@ def build_layers(spec, dtype, L, inp, kernel):
             c = fk.Fp8KVCache(dtype=dtype, layout=0, batch=B, kv_heads=Hkv, head_dim=D,
                               k=clone(base.k), v=clone(base.v), k_scale=clone(base.k_scale),
                               v_scale=clone(base.v_scale), max_tokens=cap)
-        wsb = fk.fp8kv_decode_workspace_bytes(c, Hq, 0, kernel)
-        ws_t = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        wsb = fk.fp8kv_decode_step_workspace_bytes(c, Hq, 0, kernel)
+        ws_t = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
-        layers.append(Layer(c, q, lens, ws_t, out, knew, vnew, new_sidx, new_pos, Hq, 1.0 / math.sqrt(D),
-                            kernel))
+        layers.append(Layer(c, q, lens, ws_t, out, knew, vnew, Hq, 1.0 / math.sqrt(D), kernel))
     torch.cuda.synchronize()
-    return layers, (q, knew, vnew, new_sidx, new_pos, lens)
+    return layers, (q, knew, vnew, lens)
 
 
 def capture(layers, n_steps, with_events):
     """CUDA graph of n_steps steps cycling over the layers; optionally with
-    timing events around each kernel (event-record nodes)."""
+    timing events around each step (event-record nodes)."""
     g = torch.cuda.CUDAGraph()
     evs = []
     s = torch.cuda.Stream()
@@ -353,31 +342,22 @@ def capture(layers, n_steps, with_events):
             for i in range(n_steps):
                 L = layers[i % len(layers)]
                 if with_events:
-                    e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+                    e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
                     e[0].record()
-                L.append(sp)
+                L.step(sp)
                 if with_events:
                     e[1].record()
-                L.split(sp)
-                if with_events:
-                    e[2].record()
-                L.merge(sp)
-                if with_events:
-                    e[3].record()
                     evs.append(e)
     torch.cuda.current_stream().wait_stream(s)
     return g, evs
 
 
 def time_graph_steps(layers, K, chunk, ws):
-    """Time exactly K steps (graph replays); returns (ms total, per-kernel ms)."""
+    """Time exactly K steps replayed from CUDA graphs with no event nodes
+    (the step time), then replay an instrumented copy of one chunk whose
+    event-record nodes bracket every kernel (the per-kernel breakdown)."""
     chunk = max(1, min(chunk, K))
-    try:                                         # event-record graph nodes need `external`
-        torch.cuda.Event(enable_timing=True, external=True)
-        ext = True
-    except TypeError:
-        ext = False
-    g, evs = capture(layers, chunk, ext)
+    g, _ = capture(layers, chunk, False)
     rem = K % chunk
     g_rem = capture(layers, rem, False)[0] if rem else None
     reps = K // chunk
@@ -399,11 +379,15 @@ def time_graph_steps(layers, K, chunk, ws):
     barrier(ws)
     total_ms = start.elapsed_time(end)
     per = None
-    if evs:
-        a = [e[0].elapsed_time(e[1]) for e in evs]
-        sp = [e[1].elapsed_time(e[2]) for e in evs]
-        m = [e[2].elapsed_time(e[3]) for e in evs]
-        per = {"append_ms": statistics.mean(a), "split_ms": statistics.mean(sp), "merge_ms": statistics.mean(m)}
+    try:                                         # event-record graph nodes need `external`
+        torch.cuda.Event(enable_timing=True, external=True)
+        gi, evs = capture(layers, chunk, True)
+        gi.replay()
+        gi.replay()
+        torch.cuda.synchronize()
+        per = {"step_ms": statistics.mean([e[0].elapsed_time(e[1]) for e in evs])}
+    except TypeError:
+        pass
     return total_ms, per, (t_wall0, t_wall1)
 
 
@@ -411,24 +395,21 @@ def e2e_run(layers, host, K, W, kernel):
     """Through the public Python API: pinned host inputs copied in each step,
     the output copied back each step."""
     import fp8_quantized_kv_gb300 as fk
-    q, knew, vnew, sidx, pos, lens = host["dev"]
-    hq, hk, hv, hs, hp, hl = host["pinned"]
+    q, knew, vnew, lens = host["dev"]
+    hq, hk, hv, hl = host["pinned"]
     out_h = host["out"]
     outs = [torch.empty_like(out_h, device="cuda") for _ in layers]
-    wss = [torch.empty(fk.fp8kv_decode_workspace_bytes(L.cache, q.shape[1], 0, kernel), dtype=torch.uint8,
-                       device="cuda") for L in layers]
+    wss = [torch.zeros(fk.fp8kv_decode_step_workspace_bytes(L.cache, q.shape[1], 0, kernel),
+                       dtype=torch.uint8, device="cuda") for L in layers]
 
     def step(i):
         L = layers[i % len(layers)]
         q.copy_(hq, non_blocking=True)
         knew.copy_(hk, non_blocking=True)
         vnew.copy_(hv, non_blocking=True)
-        sidx.copy_(hs, non_blocking=True)
-        pos.copy_(hp, non_blocking=True)
         lens.copy_(hl, non_blocking=True)
-        fk.fp8kv_append(L.cache, knew, vnew, sidx, pos)
-        fk.fp8kv_decode_attention(q, L.cache, lens, out=outs[i % len(layers)],
-                                  workspace=wss[i % len(layers)], kernel=kernel)
+        fk.fp8kv_decode_step(q, knew, vnew, L.cache, lens, out=outs[i % len(layers)],
+                             workspace=wss[i % len(layers)], kernel=kernel)
         out_h.copy_(outs[i % len(layers)], non_blocking=True)
 
     for i in range(W):
@@ -441,7 +422,7 @@ def e2e_run(layers, host, K, W, kernel):
         step(i)
     en.record()
     torch.cuda.synchronize()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hp, hl))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl))
     d2h = out_h.numel() * out_h.element_size()
     return st.elapsed_time(en), h2d, d2h
 
@@ -450,8 +431,7 @@ def measure_variant(spec, dtype, args, ws, inp):
     layers, dev = build_layers(spec, dtype, args.layers, inp, KERNEL_IDS[args.kernel])
     for i in range(max(3, args.warmup)):                      # eager warm-up steps
         L = layers[i % len(layers)]
-        sp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-        L.append(sp); L.split(sp); L.merge(sp)
+        L.step(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()
     total_ms, per, wall = time_graph_steps(layers, args.steps, args.chunk, ws)
     return layers, dev, total_ms, per, wall
@@ -477,7 +457,6 @@ def run_gpu(args, ws, rank):
     clocks = sampler.summary(*wall)
 
     # e2e through the public API with host buffers
-    q, knew, vnew, sidx, pos, lens = dev
     pinned = tuple(t.cpu().pin_memory() for t in dev)
     out_h = torch.empty((spec.batch, spec.q_heads, spec.head_dim), dtype=torch.bfloat16).pin_memory()
     e2e_ms, h2d, d2h = e2e_run(layers, {"dev": dev, "pinned": pinned, "out": out_h}, args.steps, args.warmup,
@@ -487,15 +466,19 @@ def run_gpu(args, ws, rank):
     sampler.stop()
 
     roof = None
+    tensor = args.kernel in ("auto", "tensor_cores")
     if per is not None:
-        achieved = nb["split_kernel"] / (per["split_ms"] * 1e-3) / 1e9
+        # the tensor-core step is one kernel (append + split + merge): its
+        # algorithmic bytes are the whole step's
+        achieved = nb["step"] / (per["step_ms"] * 1e-3) / 1e9
         sha = kernel_source_sha()
-        roof = {"bound": "hbm", "kernel": "decode_split", "achieved": achieved, "peak": peak,
+        roof = {"bound": "hbm", "kernel": "decode_split_tc (fused step)" if tensor else "decode step (3 kernels)",
+                "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} (HBM copy)",
                 "traffic": traffic_from_profile("decode_split_k8v8_b16_ctx8192", sha)
                 if args.dtype == "k8v8" else None,
-                "algorithmic_bytes_per_launch": nb["split_kernel"],
-                "avg_launch_us": per["split_ms"] * 1e3, "source_sha": sha}
+                "algorithmic_bytes_per_launch": nb["step"],
+                "avg_launch_us": per["step_ms"] * 1e3, "source_sha": sha}
 
     controls = {}
     del layers
@@ -509,7 +492,7 @@ def run_gpu(args, ws, rank):
             ob = step_bytes(spec, other, T)
             controls[other] = {"us_per_layer": tms / args.steps * 1e3,
                                "GBps": ob["step"] * args.steps / (tms * 1e-3) / 1e9,
-                               "split_us": None if pr is None else pr["split_ms"] * 1e3}
+                               "step_kernel_us": None if pr is None else pr["step_ms"] * 1e3}
             del ls
             torch.cuda.empty_cache()
 
@@ -533,11 +516,11 @@ def run_gpu(args, ws, rank):
                        "kv_heads": spec.kv_heads, "head_dim": spec.head_dim, "ctx": T,
                        "cache": args.dtype, "layout": "contiguous", "parallelism": f"replicas x{ws}",
                        "kernel": args.kernel,
-                       "step": "append 1 token/seq + decode split + merge",
+                       "step": "fp8kv_decode_step: append 1 token/seq + split + merge",
                        "l2": f"{args.layers} distinct layer caches rotated (inputs larger than L2)"},
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": (1 if tensor else 3) * args.steps,
             "kernels_us": None if per is None else {k.replace("_ms", "_us"): v * 1e3 for k, v in per.items()},
             "clocks": clocks, "controls": controls,
         }

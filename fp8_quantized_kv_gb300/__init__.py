@@ -214,6 +214,39 @@ def fp8kv_decode_merge(cache: Fp8KVCache, q_heads: int, workspace: torch.Tensor,
     return out
 
 
+def fp8kv_decode_step_workspace_bytes(cache: Fp8KVCache, q_heads: int, num_splits: int = 0,
+                                      kernel=0) -> int:
+    return int(get_lib().fp8kv_decode_step_workspace_bytes(cache.struct_ref, q_heads, num_splits,
+                                                           _kernel(kernel)))
+
+
+def fp8kv_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cache: Fp8KVCache,
+                      seq_lens: torch.Tensor, sm_scale: Optional[float] = None, num_splits: int = 0,
+                      out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                      workspace: Optional[torch.Tensor] = None, kernel=0, stream=None):
+    """Append k_new/v_new [B, Hkv, D] at position seq_lens[b]-1 and decode
+    q [B, Hq, D] over seq_lens[b] tokens.  `workspace` must start zero-filled
+    (a fresh one is allocated that way when not given)."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.bfloat16, n)
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Hq, D = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    odt = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    k = _kernel(kernel)
+    if workspace is None:
+        need = fp8kv_decode_step_workspace_bytes(cache, Hq, num_splits, k)
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(get_lib().fp8kv_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), cache.struct_ref, _ptr(seq_lens), Hq, float(sm_scale),
+        num_splits, k, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), odt,
+        _stream(stream)), "fp8kv_decode_step")
+    return out
+
+
 def fp8kv_prefill_attention(q: torch.Tensor, cache: Fp8KVCache, q_pos0: torch.Tensor,
                             sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                             out_dtype=torch.bfloat16, stream=None):
@@ -248,6 +281,7 @@ def fp8kv_status_string(status: int) -> str:
 
 __all__ = ["Fp8KVCache", "Fp8KVError", "fp8kv_quantize", "fp8kv_append",
            "fp8kv_decode_num_splits", "fp8kv_decode_workspace_bytes", "fp8kv_decode_split",
-           "fp8kv_decode_merge", "fp8kv_decode_attention",
+           "fp8kv_decode_merge", "fp8kv_decode_attention", "fp8kv_decode_step",
+           "fp8kv_decode_step_workspace_bytes",
            "fp8kv_prefill_attention", "fp8kv_get_device_error", "fp8kv_status_string",
            "EXPORTS", "K8V8", "K16V8", "K16V16"]

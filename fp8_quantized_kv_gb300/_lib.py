@@ -18,6 +18,8 @@ EXPORTS = (
     "fp8kv_decode_split",
     "fp8kv_decode_merge",
     "fp8kv_decode_attention",
+    "fp8kv_decode_step_workspace_bytes",
+    "fp8kv_decode_step",
     "fp8kv_decode_attention_static",
     "fp8kv_decode_static_scratch_bytes",
     "fp8kv_prefill_attention",
@@ -69,6 +71,8 @@ def get_lib() -> ctypes.CDLL:
         "fp8kv_decode_split": (i32, [vp, cp, vp, i32, f32, i32, i32, vp, sz, vp]),
         "fp8kv_decode_merge": (i32, [cp, i32, i32, i32, vp, sz, vp, i32, vp]),
         "fp8kv_decode_attention": (i32, [vp, cp, vp, i32, f32, i32, i32, vp, sz, vp, i32, vp]),
+        "fp8kv_decode_step_workspace_bytes": (sz, [cp, i32, i32, i32]),
+        "fp8kv_decode_step": (i32, [vp, vp, vp, cp, vp, i32, f32, i32, i32, vp, sz, vp, i32, vp]),
         "fp8kv_decode_attention_static": (i32, [vp, cp, vp, i32, f32, i32, vp, i32, vp]),
         "fp8kv_decode_static_scratch_bytes": (sz, []),
         "fp8kv_prefill_attention": (i32, [vp, cp, vp, i32, i32, f32, vp, i32, vp]),

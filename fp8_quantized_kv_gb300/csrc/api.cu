@@ -235,6 +235,12 @@ fp8kv_status prepare_decode(const void* q, const fp8kv_cache* cache, const int32
   p->num_splits = plan.splits;
   p->chunk_tiles = plan.chunk_tiles;
   p->scale_log2 = sm_scale * kLog2e;
+  p->k_new = nullptr;
+  p->v_new = nullptr;
+  p->counters = nullptr;
+  p->out = nullptr;
+  p->out_f32 = 0;
+  p->fused = 0;
   *resolved = k;
   return FP8KV_OK;
 }
@@ -285,6 +291,48 @@ fp8kv_status fp8kv_decode_attention(const void* q, const fp8kv_cache* cache, con
   if (st != FP8KV_OK) return st;
   return fp8kv_decode_merge(cache, q_heads, num_splits, kernel, workspace, workspace_bytes, out,
                             out_dtype, stream);
+}
+
+size_t fp8kv_decode_step_workspace_bytes(const fp8kv_cache* cache, int32_t q_heads, int32_t num_splits,
+                                         int32_t kernel) {
+  const size_t part = fp8kv_decode_workspace_bytes(cache, q_heads, num_splits, kernel);
+  if (part == 0) return 0;
+  const size_t ctr = ((size_t)cache->batch * cache->kv_heads * sizeof(int) + 15) & ~(size_t)15;
+  return ((part + 15) & ~(size_t)15) + ctr;
+}
+
+fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, const fp8kv_cache* cache,
+                               const int32_t* seq_lens, int32_t q_heads, float sm_scale, int32_t num_splits,
+                               int32_t kernel, void* workspace, size_t workspace_bytes, void* out,
+                               int32_t out_dtype, fp8kv_stream_t stream) {
+  if (out_dtype != FP8KV_OUT_BF16 && out_dtype != FP8KV_OUT_F32) return FP8KV_ERR_INVALID_ARG;
+  DecodeParams p;
+  int k = 0;
+  fp8kv_status st = prepare_decode(q, cache, seq_lens, q_heads, sm_scale, num_splits, kernel, workspace,
+                                   workspace_bytes, true, &p, &k);
+  if (st != FP8KV_OK || cache->batch == 0) return st;
+  if (!out || !k_new || !v_new) return FP8KV_ERR_INVALID_ARG;
+  const size_t need = fp8kv_decode_step_workspace_bytes(cache, q_heads, num_splits, kernel);
+  if (workspace_bytes < need) return FP8KV_ERR_WORKSPACE;
+  p.err = device_error_ptr();
+  if (!p.err) return FP8KV_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (k == FP8KV_KERNEL_TENSOR_CORES) {
+    const size_t part = fp8kv_decode_workspace_bytes(cache, q_heads, num_splits, kernel);
+    p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    p.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + ((part + 15) & ~(size_t)15));
+    p.out = out;
+    p.out_f32 = out_dtype == FP8KV_OUT_F32;
+    p.fused = 1;
+    return cuda_status(launch_decode_mma(p, cache->dtype, cache->batch, s));
+  }
+  cudaError_t e = launch_append_step(p.c, cache->dtype, k_new, v_new, seq_lens, p.err, s);
+  if (e == cudaSuccess) e = launch_decode_fma(p, cache->dtype, cache->batch, s);
+  if (e == cudaSuccess)
+    e = launch_decode_merge(p.part_o, p.part_m, p.part_l, p.num_splits, (int64_t)cache->batch * q_heads,
+                            cache->head_dim, out, out_dtype == FP8KV_OUT_F32, s);
+  return cuda_status(e);
 }
 
 fp8kv_status fp8kv_prefill_attention(const void* q, const fp8kv_cache* cache, const int32_t* q_pos0,

@@ -366,15 +366,20 @@ __global__ void __launch_bounds__(D) decode_merge(const float* __restrict__ part
   }
   __syncthreads();
   const float* po = part_o + bh * S * D + d;
+  // loads of 8 splits issued together per round
   float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-  int s = 0;
-  for (; s + 4 <= Sw; s += 4) {
-    o0 = fmaf(wsh[s], po[(int64_t)s * D], o0);
-    o1 = fmaf(wsh[s + 1], po[(int64_t)(s + 1) * D], o1);
-    o2 = fmaf(wsh[s + 2], po[(int64_t)(s + 2) * D], o2);
-    o3 = fmaf(wsh[s + 3], po[(int64_t)(s + 3) * D], o3);
+  for (int s0 = 0; s0 < Sw; s0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = s0 + k < Sw ? po[(int64_t)(s0 + k) * D] : 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; k += 4) {
+      if (s0 + k < Sw) o0 = fmaf(wsh[s0 + k], v[k], o0);
+      if (s0 + k + 1 < Sw) o1 = fmaf(wsh[s0 + k + 1], v[k + 1], o1);
+      if (s0 + k + 2 < Sw) o2 = fmaf(wsh[s0 + k + 2], v[k + 2], o2);
+      if (s0 + k + 3 < Sw) o3 = fmaf(wsh[s0 + k + 3], v[k + 3], o3);
+    }
   }
-  for (; s < Sw; ++s) o0 = fmaf(wsh[s], po[(int64_t)s * D], o0);
   if (S > kMergeMaxS) {      // rare: more splits than the weight table holds
     float M = -INFINITY;
     for (int k = 0; k < S; ++k) M = fmaxf(M, pm[k]);

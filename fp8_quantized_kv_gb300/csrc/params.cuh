@@ -16,6 +16,13 @@ struct DecodeParams {
   unsigned int* err;         // device error word
   int q_heads, group, num_splits, chunk_tiles;
   float scale_log2;          // sm_scale * log2(e)
+  // Fused decode step (tensor-core kernel only; zero/null otherwise):
+  const __nv_bfloat16* k_new;  // [B][Hkv][D] new token of each sequence, appended at seq_lens[b]-1
+  const __nv_bfloat16* v_new;
+  int* counters;             // [B][Hkv] arrivals of finished splits (zero between calls)
+  void* out;                 // [B][Hq][D] merged output (bf16 or fp32)
+  int out_f32;
+  int fused;
 };
 
 struct PrefillParams {
@@ -33,6 +40,8 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int head_dim, uint8_t* 
 cudaError_t launch_append(const CacheView& c, int dtype, const void* k_new, const void* v_new,
                           const int32_t* seq_idx, const int32_t* pos, int64_t n_tokens,
                           unsigned int* err, cudaStream_t s);
+cudaError_t launch_append_step(const CacheView& c, int dtype, const void* k_new, const void* v_new,
+                               const int32_t* seq_lens, unsigned int* err, cudaStream_t s);
 cudaError_t launch_decode_fma(const DecodeParams& p, int dtype, int batch, cudaStream_t st);
 cudaError_t launch_decode_mma(const DecodeParams& p, int dtype, int batch, cudaStream_t st);
 cudaError_t launch_decode_merge(const float* part_o, const float* part_m, const float* part_l, int S,

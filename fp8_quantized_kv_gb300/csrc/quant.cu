@@ -120,6 +120,40 @@ __global__ void __launch_bounds__(256) append_kernel(CacheView c, const __nv_bfl
   quantize_warp_row<EPL>(v, codes, scale, lane);
 }
 
+// Decode-step append: the new token of sequence b goes to position
+// seq_lens[b] - 1 (the length already counts it).  k_new, v_new: [B][Hkv][D].
+template <int EPL, int KE, int VE>
+__global__ void __launch_bounds__(256) append_step_kernel(CacheView c, const __nv_bfloat16* __restrict__ k_new,
+                                                          const __nv_bfloat16* __restrict__ v_new,
+                                                          const int32_t* __restrict__ seq_lens, unsigned int* err) {
+  constexpr int D = 32 * EPL;
+  const int lane = threadIdx.x & 31;
+  const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t rows = (int64_t)c.batch * c.kv_heads;
+  if (w >= 2 * rows) return;
+  const bool is_v = w >= rows;
+  const int64_t r = is_v ? w - rows : w;
+  const int b = (int)(r / c.kv_heads), h = (int)(r - (int64_t)b * c.kv_heads);
+  const int t = seq_lens[b] - 1;
+  if (t < 0) return;                                   // an empty sequence appends nothing
+  const int64_t dst = cache_row(c, b, h, t, lane == 0 ? err : nullptr);
+  if (dst < 0) return;
+  const __nv_bfloat16* src = (is_v ? v_new : k_new) + r * D;
+  const int kind = is_v ? VE : KE;
+  if (kind == ELEM_BF16) {
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(const_cast<uint8_t*>(is_v ? c.v : c.k)) + dst * D;
+    if (EPL == 4)
+      reinterpret_cast<uint2*>(out)[lane] = reinterpret_cast<const uint2*>(src)[lane];
+    else
+      reinterpret_cast<uint32_t*>(out)[lane] = reinterpret_cast<const uint32_t*>(src)[lane];
+    return;
+  }
+  float v[EPL];
+  load_bf16_slice<EPL>(src, lane, v);
+  quantize_warp_row<EPL>(v, const_cast<uint8_t*>(is_v ? c.v : c.k) + dst * D,
+                         const_cast<float*>(is_v ? c.v_scale : c.k_scale) + dst, lane);
+}
+
 // ------------------------------------------------------------ launchers ---
 cudaError_t launch_quantize(const void* x, int64_t rows, int head_dim, uint8_t* codes, float* scales,
                             cudaStream_t s) {
@@ -157,6 +191,32 @@ cudaError_t launch_append(const CacheView& c, int dtype, const void* k_new, cons
     append_dispatch<4>(dtype, grid, s, c, k, v, seq_idx, pos, n_tokens, err);
   else
     append_dispatch<2>(dtype, grid, s, c, k, v, seq_idx, pos, n_tokens, err);
+  return cudaGetLastError();
+}
+
+template <int EPL>
+static void append_step_dispatch(int dtype, unsigned grid, cudaStream_t s, const CacheView& c,
+                                 const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* lens,
+                                 unsigned int* err) {
+  if (dtype == FP8KV_K8V8)
+    append_step_kernel<EPL, ELEM_E4M3, ELEM_E4M3><<<grid, 256, 0, s>>>(c, k, v, lens, err);
+  else if (dtype == FP8KV_K16V8)
+    append_step_kernel<EPL, ELEM_BF16, ELEM_E4M3><<<grid, 256, 0, s>>>(c, k, v, lens, err);
+  else
+    append_step_kernel<EPL, ELEM_BF16, ELEM_BF16><<<grid, 256, 0, s>>>(c, k, v, lens, err);
+}
+
+cudaError_t launch_append_step(const CacheView& c, int dtype, const void* k_new, const void* v_new,
+                               const int32_t* seq_lens, unsigned int* err, cudaStream_t s) {
+  const int64_t warps_needed = 2 * (int64_t)c.batch * c.kv_heads;
+  if (warps_needed == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)((warps_needed + 7) / 8);
+  const auto* k = (const __nv_bfloat16*)k_new;
+  const auto* v = (const __nv_bfloat16*)v_new;
+  if (c.head_dim == 128)
+    append_step_dispatch<4>(dtype, grid, s, c, k, v, seq_lens, err);
+  else
+    append_step_dispatch<2>(dtype, grid, s, c, k, v, seq_lens, err);
   return cudaGetLastError();
 }
 

@@ -190,6 +190,29 @@ FP8KV_API fp8kv_status fp8kv_decode_merge(const fp8kv_cache *cache, int32_t q_he
                                           size_t workspace_bytes, void *out,
                                           int32_t out_dtype, fp8kv_stream_t stream);
 
+/* One decode step in one call: append the new token of every sequence to
+ * the cache (as fp8kv_append, at position seq_lens[b] - 1: the lengths
+ * already count the new token), then decode attention over seq_lens[b]
+ * tokens, as fp8kv_decode_attention.  On the tensor-core kernel all of it
+ * is one launch: the CTA that owns the new token's tile writes it before
+ * loading that tile, and the last split of each (sequence, KV head) to
+ * finish merges the partials, so no separate append or merge kernel runs.
+ *   k_new, v_new: [batch][kv_heads][head_dim] bf16
+ *   workspace:    fp8kv_decode_step_workspace_bytes() bytes; it also holds
+ *                 one arrival counter per (sequence, KV head), which must be
+ *                 zero before the first call (allocate it zero-filled).
+ *                 Every call that returns FP8KV_OK and whose device error
+ *                 word stays clear leaves the counters zero again; after a
+ *                 timeout, zero the workspace before reusing it.
+ * Other arguments as in fp8kv_decode_attention. */
+FP8KV_API size_t fp8kv_decode_step_workspace_bytes(const fp8kv_cache *cache, int32_t q_heads,
+                                                   int32_t num_splits, int32_t kernel);
+FP8KV_API fp8kv_status fp8kv_decode_step(const void *q, const void *k_new, const void *v_new,
+                                         const fp8kv_cache *cache, const int32_t *seq_lens,
+                                         int32_t q_heads, float sm_scale, int32_t num_splits,
+                                         int32_t kernel, void *workspace, size_t workspace_bytes,
+                                         void *out, int32_t out_dtype, fp8kv_stream_t stream);
+
 /* Decode attention that allocates nothing (the paper has no counterpart:
  * this is a convenience of the library).  Same arguments and results as
  * fp8kv_decode_attention without the workspace: the fp32 partials go to a

@@ -25,6 +25,8 @@ def fill_cache(inp: synth.DecodeInputs, dtype: str, device="cuda", capacity=None
         cache = fk.Fp8KVCache.paged(inp.page_table, inp.num_pages, spec.kv_heads, spec.head_dim,
                                     spec.page_size, dtype, device)
     lens = inp.seq_lens.to(torch.int64)
+    if int(lens.sum()) == 0:
+        return cache
     seq_idx = torch.repeat_interleave(torch.arange(B), lens).to(torch.int32)
     pos = torch.cat([torch.arange(int(n)) for n in lens]).to(torch.int32) if B else torch.zeros(0, dtype=torch.int32)
     fk.fp8kv_append(cache, inp.k.to(device).contiguous(), inp.v.to(device).contiguous(),

@@ -1,0 +1,115 @@
+"""fp8kv_decode_step: append the new token of every sequence and decode in
+one call (one launch on the tensor-core kernel).  Checked against the oracle
+over the full length, the appended rows bit-exact against the oracle's
+quantiser, and against the separate append + decode calls."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_quantized_kv_gb300 import synth
+import fp8_quantized_kv_gb300 as fk
+from kvhelpers import assert_gate, fill_cache, oracle_decode
+
+pytestmark = pytest.mark.gpu
+DTYPES = ["k8v8", "k16v8", "k16v16"]
+
+
+@pytest.fixture(autouse=True)
+def _clear_device_error():
+    fk.fp8kv_get_device_error(clear=True)
+    yield
+
+
+def _split_last_token(inp):
+    """The workload minus each sequence's last token, and those tokens."""
+    lens = inp.seq_lens.to(torch.int64)
+    last = (inp.cu_seqlens[1:] - 1).clamp(min=0)
+    keep = torch.ones(int(inp.cu_seqlens[-1]), dtype=torch.bool)
+    has = lens > 0
+    keep[last[has]] = False
+    prev = synth.DecodeInputs(inp.spec, inp.q, inp.k[keep.to(inp.k.device)], inp.v[keep.to(inp.v.device)],
+                              (inp.seq_lens - has.to(torch.int32)).to(torch.int32),
+                              torch.cat([torch.zeros(1, dtype=torch.int64), torch.cumsum(lens - has.to(torch.int64), 0)]),
+                              inp.page_table, inp.num_pages)
+    B, Hkv, D = len(lens), inp.spec.kv_heads, inp.spec.head_dim
+    knew = torch.zeros(B, Hkv, D, dtype=torch.bfloat16, device=inp.k.device)
+    vnew = torch.zeros_like(knew)
+    knew[has.to(knew.device)] = inp.k[last[has].to(inp.k.device)]
+    vnew[has.to(vnew.device)] = inp.v[last[has].to(inp.v.device)]
+    return prev, knew, vnew
+
+
+def _run(inp, dtype, kernel, num_splits=0, capacity=None):
+    prev, knew, vnew = _split_last_token(inp)
+    cache = fill_cache(prev, dtype, capacity=capacity or max(16, ((inp.max_len + 127) // 128) * 128))
+    lens = inp.seq_lens.cuda()
+    out = fk.fp8kv_decode_step(inp.q.cuda().contiguous(), knew, vnew, cache, lens, num_splits=num_splits,
+                               out_dtype=torch.float32, kernel=kernel)
+    return cache, out, knew, vnew
+
+
+@pytest.mark.parametrize("kernel", ["cuda_cores", "tensor_cores"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_step_ctx8192_full(dtype, kernel):
+    inp = synth.decode_inputs(synth.WORKLOADS["decode_b16_ctx8192"], device="cuda")
+    cache, out, knew, vnew = _run(inp, dtype, kernel)
+    assert fk.fp8kv_get_device_error() == 0
+    assert_gate(out.cpu().numpy(), oracle_decode(inp, dtype, range(16)), f"step {dtype} {kernel}")
+    # the appended row is exactly what the quantiser writes
+    if dtype == "k8v8":
+        codes, scales = oracle.quantize(synth.bf16_bits(knew))
+        got = cache.k[:, :, 8191].cpu().numpy()
+        assert np.array_equal(got, codes)
+        assert np.array_equal(cache.k_scale[:, :, 8191].cpu().numpy().view(np.uint32), scales.view(np.uint32))
+
+
+@pytest.mark.parametrize("kernel", ["cuda_cores", "tensor_cores"])
+def test_step_matches_separate_calls_and_resets_counters(kernel):
+    inp = synth.decode_inputs(synth.WORKLOADS["decode_b16_ctx512"], device="cuda")
+    prev, knew, vnew = _split_last_token(inp)
+    c1 = fill_cache(prev, "k8v8", capacity=512)
+    c2 = fill_cache(prev, "k8v8", capacity=512)
+    lens = inp.seq_lens.cuda()
+    q = inp.q.cuda().contiguous()
+    ws = torch.zeros(fk.fp8kv_decode_step_workspace_bytes(c1, 16, 0, kernel), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):                      # same workspace: the counters must come back to zero
+        outs.append(fk.fp8kv_decode_step(q, knew, vnew, c1, lens, out_dtype=torch.float32, workspace=ws,
+                                         kernel=kernel))
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(ws[-(16 * 2 * 4):]) == 0 or kernel == "cuda_cores"
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    fk.fp8kv_append(c2, knew, vnew, torch.arange(16, dtype=torch.int32, device="cuda"),
+                    (lens - 1).to(torch.int32))
+    sep = fk.fp8kv_decode_attention(q, c2, lens, out_dtype=torch.float32, kernel=kernel)
+    assert torch.equal(c1.k, c2.k) and torch.equal(c1.k_scale, c2.k_scale)
+    rel = ((outs[0].double() - sep.double()).norm(dim=-1) / sep.double().norm(dim=-1)).max().item()
+    assert rel <= 1e-5, rel
+
+
+@pytest.mark.parametrize("kernel", ["cuda_cores", "tensor_cores"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_step_ragged_splits_and_empty(dtype, kernel):
+    lens = (0, 1, 2, 127, 128, 129, 300, 1000, 17, 256)
+    spec = synth.DecodeWorkload("ragged_step", len(lens), 8, 1, 128, seed=25, seq_lens=lens)
+    inp = synth.decode_inputs(spec, device="cuda")
+    for ns in (0, 1, 3):
+        cache, out, _, _ = _run(inp, dtype, kernel, num_splits=ns, capacity=1024)
+        o = out.cpu().numpy()
+        assert np.all(o[0] == 0)
+        assert_gate(o[1:], oracle_decode(inp, dtype, range(1, len(lens))), f"step ragged {dtype} {kernel} {ns}")
+    assert fk.fp8kv_get_device_error() == 0
+
+
+@pytest.mark.parametrize("kernel", ["cuda_cores", "tensor_cores"])
+def test_step_paged(kernel):
+    spec = synth.DecodeWorkload("paged_step", 6, 16, 4, 128, seed=27, len_range=(1, 900), page_size=16,
+                                hostile_keys=True)
+    inp = synth.decode_inputs(spec, device="cuda")
+    prev, knew, vnew = _split_last_token(inp)
+    cache = fill_cache(prev, "k8v8")            # paged pool sized for the full lengths
+    out = fk.fp8kv_decode_step(inp.q.cuda().contiguous(), knew, vnew, cache, inp.seq_lens.cuda(),
+                               out_dtype=torch.float32, kernel=kernel)
+    assert_gate(out.cpu().numpy(), oracle_decode(inp, "k8v8", range(6)), f"step paged {kernel}")
+    assert fk.fp8kv_get_device_error() == 0
