@@ -465,20 +465,24 @@ def run_gpu(args, ws, rank):
     e2e_val = ws * nb["step"] * args.steps / (e2e_ms * 1e-3) / 1e9
     sampler.stop()
 
-    roof = None
     tensor = args.kernel in ("auto", "tensor_cores")
-    if per is not None:
+    roof = None
+    if tensor:
         # the tensor-core step is one kernel (append + split + merge): its
+        # average launch duration is the timed region's time per step (start
+        # and end events around the K back-to-back launches), and its
         # algorithmic bytes are the whole step's
-        achieved = nb["step"] / (per["step_ms"] * 1e-3) / 1e9
+        launch_ms = ms_per_step
+        achieved = nb["step"] / (launch_ms * 1e-3) / 1e9
         sha = kernel_source_sha()
-        roof = {"bound": "hbm", "kernel": "decode_split_tc (fused step)" if tensor else "decode step (3 kernels)",
+        roof = {"bound": "hbm", "kernel": "decode_split_tc (fused decode step)",
                 "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} (HBM copy)",
                 "traffic": traffic_from_profile("decode_split_k8v8_b16_ctx8192", sha)
                 if args.dtype == "k8v8" else None,
                 "algorithmic_bytes_per_launch": nb["step"],
-                "avg_launch_us": per["step_ms"] * 1e3, "source_sha": sha}
+                "avg_launch_us": launch_ms * 1e3, "source_sha": sha,
+                "event_node_step_us": None if per is None else per["step_ms"] * 1e3}
 
     controls = {}
     del layers
