@@ -249,8 +249,9 @@ def fp8kv_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
 
 def fp8kv_prefill_attention(q: torch.Tensor, cache: Fp8KVCache, q_pos0: torch.Tensor,
                             sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                            out_dtype=torch.bfloat16, stream=None):
-    """q [B, n_q, Hq, D] bf16, q_pos0 [B] int32 -> out [B, n_q, Hq, D]."""
+                            out_dtype=torch.bfloat16, kernel="auto", stream=None):
+    """q [B, n_q, Hq, D] bf16, q_pos0 [B] int32 -> out [B, n_q, Hq, D].
+    kernel: "auto", "tensor_cores" (K8V8, head_dim 128) or "cuda_cores"."""
     _need(q, torch.bfloat16, "q")
     _need(q_pos0, torch.int32, "q_pos0")
     B, n_q, Hq, D = q.shape
@@ -260,8 +261,8 @@ def fp8kv_prefill_attention(q: torch.Tensor, cache: Fp8KVCache, q_pos0: torch.Te
         out = torch.empty((B, n_q, Hq, D), dtype=out_dtype, device=q.device)
     odt = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _check(get_lib().fp8kv_prefill_attention(
-        _ptr(q), cache.struct_ref, _ptr(q_pos0), n_q, Hq, float(sm_scale), _ptr(out), odt,
-        _stream(stream)), "fp8kv_prefill_attention")
+        _ptr(q), cache.struct_ref, _ptr(q_pos0), n_q, Hq, float(sm_scale), _kernel(kernel), _ptr(out),
+        odt, _stream(stream)), "fp8kv_prefill_attention")
     return out
 
 

@@ -75,7 +75,7 @@ def get_lib() -> ctypes.CDLL:
         "fp8kv_decode_step": (i32, [vp, vp, vp, cp, vp, i32, f32, i32, i32, vp, sz, vp, i32, vp]),
         "fp8kv_decode_attention_static": (i32, [vp, cp, vp, i32, f32, i32, vp, i32, vp]),
         "fp8kv_decode_static_scratch_bytes": (sz, []),
-        "fp8kv_prefill_attention": (i32, [vp, cp, vp, i32, i32, f32, vp, i32, vp]),
+        "fp8kv_prefill_attention": (i32, [vp, cp, vp, i32, i32, f32, i32, vp, i32, vp]),
         "fp8kv_get_device_error": (i32, [ctypes.POINTER(ctypes.c_uint32), i32]),
         "fp8kv_status_string": (ctypes.c_char_p, [i32]),
     }

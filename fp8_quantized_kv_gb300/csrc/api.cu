@@ -336,8 +336,8 @@ fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_n
 }
 
 fp8kv_status fp8kv_prefill_attention(const void* q, const fp8kv_cache* cache, const int32_t* q_pos0,
-                                     int32_t n_q, int32_t q_heads, float sm_scale, void* out,
-                                     int32_t out_dtype, fp8kv_stream_t stream) {
+                                     int32_t n_q, int32_t q_heads, float sm_scale, int32_t kernel,
+                                     void* out, int32_t out_dtype, fp8kv_stream_t stream) {
   CacheView view;
   fp8kv_status st = check_cache(cache, &view);
   if (st != FP8KV_OK) return st;
@@ -345,6 +345,10 @@ fp8kv_status fp8kv_prefill_attention(const void* q, const fp8kv_cache* cache, co
   if (out_dtype != FP8KV_OUT_BF16 && out_dtype != FP8KV_OUT_F32) return FP8KV_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return FP8KV_ERR_INVALID_ARG;
   if (q_heads / cache->kv_heads > 16) return FP8KV_ERR_UNSUPPORTED;
+  if (kernel < FP8KV_KERNEL_AUTO || kernel > FP8KV_KERNEL_TENSOR_CORES) return FP8KV_ERR_INVALID_ARG;
+  const bool tc_built = cache->dtype == FP8KV_K8V8 && cache->head_dim == 128;
+  if (kernel == FP8KV_KERNEL_TENSOR_CORES && !tc_built) return FP8KV_ERR_UNSUPPORTED;
+  const bool use_tc = kernel == FP8KV_KERNEL_TENSOR_CORES || (kernel == FP8KV_KERNEL_AUTO && tc_built);
   if (cache->batch == 0 || n_q == 0) return FP8KV_OK;
   if (!q || !q_pos0 || !out) return FP8KV_ERR_INVALID_ARG;
   if (n_q > capacity_of(cache)) return FP8KV_ERR_INVALID_ARG;
@@ -361,6 +365,7 @@ fp8kv_status fp8kv_prefill_attention(const void* q, const fp8kv_cache* cache, co
   p.group = q_heads / cache->kv_heads;
   p.out_f32 = out_dtype == FP8KV_OUT_F32;
   p.scale_log2 = sm_scale * kLog2e;
+  if (use_tc) return cuda_status(launch_prefill_tc(p, cache->batch, (cudaStream_t)stream));
   return cuda_status(launch_prefill_fma(p, cache->dtype, cache->batch, (cudaStream_t)stream));
 }
 

@@ -47,5 +47,6 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int dtype, int batch, cudaS
 cudaError_t launch_decode_merge(const float* part_o, const float* part_m, const float* part_l, int S,
                                 int64_t rows, int head_dim, void* out, int out_f32, cudaStream_t st);
 cudaError_t launch_prefill_fma(const PrefillParams& p, int dtype, int batch, cudaStream_t st);
+cudaError_t launch_prefill_tc(const PrefillParams& p, int batch, cudaStream_t st);
 
 }  // namespace fp8kv

@@ -1,0 +1,508 @@
+// prefill_tc.cu -- causal prefill attention over an e4m3 K/V cache on the
+// tcgen05 tensor cores.
+//
+// "03 · 8n — FA-style tiled prefill attention", sections 2.1 and 3.1: query
+// tiles against 64-token KV tiles up to the causal limit, online softmax with
+// running max m, sum l and an O accumulator; a key is valid for the query at
+// position qp iff key <= qp.  FP8 numerics of "FP8 KV cache (fp8_kv, opt-in)",
+// bullet "Math": the K scale folds into the scores and the V scale into P,
+// which is rounded to bf16 before P.V.
+//
+// A CTA owns 128 query rows (two 64-token query tiles: the full-rate tcgen05
+// shape is M = 128) of one query head, and walks the KV tiles of that head's
+// KV head:
+//   S[128 x 64]    = Q . K^T            tcgen05.mma kind::f16 -> TMEM
+//   per row (one thread each, whole row thread-local): s = S * k_scale *
+//     sm_scale, causal mask, running max with lazy rescale, p = 2^(s - m),
+//     l += p, P' = bf16_rn(p * v_scale)
+//   O^T[128 x 128] += V^T . P'^T         tcgen05.mma kind::f16 -> TMEM
+// Operands are f16: the e4m3 K and V codes convert to f16 exactly
+// (cvt.rn.f16x2.e4m3x2); each bf16 query row is scaled by a power of two
+// (exact) into f16's range; the bf16-rounded P' is scaled by one power of two
+// per CTA (from the largest V scale it will see) and converted exactly.  All
+// those scalings are undone in fp32.
+//
+// Warp roles:
+//   warp 0     TMA producer: e4m3 code tiles (64 keys x 128 B, 128-byte
+//              swizzle) and 1-D bulk copies of the scale rows into a ring.
+//   warp 1     TMEM owner and MMA issuer: QK of tile j, then PV of tile j-1.
+//   warps 2-5  softmax, one query row per thread; the output epilogue.
+//   warps 6-9  preparation: codes -> f16 operand tiles (K-major K, MN-major
+//              V; same physical layout), per-key scales; V rows past the
+//              causal end zeroed (0 * NaN would poison P.V).
+// The f16 K/V operands, S (TMEM) and P (shared memory) are double-buffered.
+// O is rescaled in TMEM only when a row's maximum grows by more than 2^8
+// (then P stays <= 2^8 relative to the stale maximum).  Every wait is
+// bounded; a timeout raises FP8KV_DEVERR_TIMEOUT.
+#include "params.cuh"
+#include "tc_common.cuh"
+
+namespace fp8kv {
+
+constexpr int kPfRows = 128;   // query rows per CTA
+constexpr int kPfKeys = 64;    // keys per KV tile
+
+struct PfTcCfg {
+  static constexpr int D = 128;
+  static constexpr int QOP = kPfRows * D * 2;                 // [2 atoms][128 rows][128 B] f16
+  static constexpr int CODES = kPfKeys * D;                    // e4m3 tile [64][128]
+  static constexpr int STAGE = ((2 * CODES + 2 * kPfKeys * 4) + 1023) / 1024 * 1024;
+  static constexpr int NS = 3;
+  static constexpr int OPT = kPfKeys * D * 2;                 // f16 K or V tile [2 atoms][64][128 B]
+  static constexpr int POP = kPfRows * kPfKeys * 2;           // f16 P [128 rows][128 B]
+  static constexpr int COLS = 2 * kPfKeys * 4;                 // per buffer: k and v column scales
+  static constexpr int MISC = 2048;
+  static constexpr int BYTES = QOP + NS * STAGE + 4 * OPT + 2 * POP + 2 * COLS + MISC + 1024;
+  static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+};
+
+struct PrefillTmaParams {
+  CUtensorMap tmk;
+  CUtensorMap tmv;
+  PrefillParams p;
+};
+
+__global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ PrefillTmaParams tp) {
+  using C = PfTcCfg;
+  constexpr int D = 128;
+  const PrefillParams& p = tp.p;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qop = smem;
+  uint8_t* ring = qop + C::QOP;
+  uint8_t* kf = ring + C::NS * C::STAGE;          // [2] f16 K operand
+  uint8_t* vf = kf + 2 * C::OPT;                  // [2] f16 V operand
+  uint8_t* pop = vf + 2 * C::OPT;                 // [2] f16 P operand
+  float* cols = reinterpret_cast<float*>(pop + 2 * C::POP);   // [2][k 64 | v 64]
+  uint8_t* misc = reinterpret_cast<uint8_t*>(cols + 2 * 2 * kPfKeys);
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc);        // [NS] codes landed
+  uint64_t* empty = full + C::NS;                             // [NS] codes consumed by the prep warps
+  uint64_t* op_full = empty + C::NS;                          // [2] f16 K/V operands + scales ready
+  uint64_t* s_full = op_full + 2;                             // [2]
+  uint64_t* s_free = s_full + 2;                              // [2]
+  uint64_t* p_full = s_free + 2;                              // [2]
+  uint64_t* pv_done = p_full + 2;                             // [2] PV of the buffer's tile finished
+  uint64_t* drained = pv_done + 2;                            // final commit of the MMA issuer
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drained + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  int* kp_sh = const_cast<int*>(abort_flag) + 1;
+  float* alpha_sh = reinterpret_cast<float*>(misc + 256);     // [128]
+  float* l_sh = alpha_sh + kPfRows;                           // [128]
+  float* vmax_sh = l_sh + kPfRows;                            // [4]
+
+  const int qt = gridDim.x - 1 - blockIdx.x;      // longest causal range first
+  const int hq = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const CacheView& c = p.c;
+  const int hk = hq / p.group;
+  const int pos0 = p.q_pos0[b];
+  const int i0 = qt * kPfRows;
+  const int last_i = min(p.n_q, i0 + kPfRows) - 1;
+  const int kv_end = pos0 + last_i + 1;
+  if (pos0 < 0 || kv_end > cache_capacity(c)) {
+    if (tid == 0) raise_error(p.err, FP8KV_DEVERR_SEQ_TOO_LONG);
+    return;
+  }
+  const int nkv = (kv_end + kPfKeys - 1) / kPfKeys;
+  const int64_t cont_row0 = ((int64_t)b * c.kv_heads + hk) * c.max_tokens;
+
+  auto produce = [&](int j) {
+    const int s = j % C::NS;
+    uint8_t* st = ring + s * C::STAGE;
+    float* kss = reinterpret_cast<float*>(st + 2 * C::CODES);
+    float* vss = kss + kPfKeys;
+    const int t0 = j * kPfKeys;
+    const int valid = min(kPfKeys, kv_end - t0);
+    if (!c.paged) {
+      const int nsc = min(kPfKeys, (valid + 15) & ~15);
+      tma::arrive_expect_tx(&full[s], 2 * C::CODES + 2 * nsc * 4);
+      const int row = (int)(cont_row0 + t0);
+      tma::load_2d(st, &tp.tmk, 0, row, &full[s]);
+      tma::load_2d(st + C::CODES, &tp.tmv, 0, row, &full[s]);
+      tma::load_1d(kss, c.k_scale + cont_row0 + t0, nsc * 4, &full[s]);
+      tma::load_1d(vss, c.v_scale + cont_row0 + t0, nsc * 4, &full[s]);
+    } else {
+      const int P = c.page_size;
+      const int np = (valid + P - 1) / P;
+      tma::arrive_expect_tx(&full[s], np * (2 * P * 128 + 2 * P * 4));
+      for (int k = 0; k < np; ++k) {
+        int page = c.page_table[(int64_t)b * c.max_pages_per_seq + ((t0 >> c.page_shift) + k)];
+        if (page < 0 || page >= c.num_pages) {
+          raise_error(p.err, FP8KV_DEVERR_BAD_PAGE);
+          page = 0;
+        }
+        const int64_t row = ((int64_t)page * c.kv_heads + hk) * P;
+        tma::load_2d(st + k * P * 128, &tp.tmk, 0, (int)row, &full[s]);
+        tma::load_2d(st + C::CODES + k * P * 128, &tp.tmv, 0, (int)row, &full[s]);
+        tma::load_1d(kss + k * P, c.k_scale + row, P * 4, &full[s]);
+        tma::load_1d(vss + k * P, c.v_scale + row, P * 4, &full[s]);
+      }
+    }
+  };
+
+  // ---------------------------------------------------------------- setup
+  const int n_first = min(nkv, C::NS);
+  if (tid == 0) {
+    for (int i = 0; i < C::NS; ++i) {
+      umma::mbar_init(&full[i], 1);
+      umma::mbar_init(&empty[i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      umma::mbar_init(&op_full[i], 4);
+      umma::mbar_init(&s_full[i], 1);
+      umma::mbar_init(&s_free[i], 4);
+      umma::mbar_init(&p_full[i], 4);
+      umma::mbar_init(&pv_done[i], 1);
+    }
+    umma::mbar_init(drained, 1);
+    *abort_flag = 0;
+    umma::mbar_fence_init();
+    tma::prefetch_map(&tp.tmk);
+    tma::prefetch_map(&tp.tmv);
+    for (int j = 0; j < n_first; ++j) produce(j);
+  }
+  if (warp == 1) {
+    umma::tmem_alloc(tslot, 256);
+    umma::tmem_relinquish();
+  }
+  // softmax warps: this thread's query row -> f16 Q operand, row scale 2^kq
+  const int r = 32 * (warp & 3) + lane;           // query row (softmax warps) / TMEM lane
+  const int qi = i0 + r;
+  const int qpos = qi < p.n_q ? pos0 + qi : -1;
+  int kq = 0;
+  if (warp >= 2 && warp < 6) {
+    uint4 raw[16];
+    if (qi < p.n_q) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.n_q + qi) * p.q_heads + hq) * D);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) raw[k] = src[k];
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) raw[k] = make_uint4(0, 0, 0, 0);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float f2[2];
+        bf16x2_to_f32(w4[u], f2);
+        amax = fmaxf(amax, fmaxf(fabsf(f2[0]), fabsf(f2[1])));
+      }
+    }
+    int e = 0;
+    (void)frexpf(amax * (1.0f / 16384.0f), &e);   // row max -> [2^13, 2^14): inside f16's normal range
+    kq = max(-100, min(100, e));
+    const float qsc = pow2i(-kq);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {                 // 8 elements (one 16-byte f16 chunk) each
+      const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+      uint32_t h[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float f2[2];
+        bf16x2_to_f32(w4[u], f2);
+        const __half2 hv = __floats2half2_rn(f2[0] * qsc, f2[1] * qsc);
+        h[u] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      const int atom = k >> 3, ch = k & 7;
+      *reinterpret_cast<uint4*>(qop + atom * (kPfRows * 128) + r * 128 + ((ch ^ (r & 7)) << 4)) =
+          make_uint4(h[0], h[1], h[2], h[3]);
+    }
+  }
+  // prep warps: one power of two for all of this CTA's P (from the largest
+  // V scale of its keys), so P' stays inside f16's range
+  if (warp >= 6) {
+    const int pt = tid - 192;
+    float vm = 0.f;
+    for (int base = 0; base < kv_end; base += 8 * 128) {   // 8 independent loads in flight
+      float v8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int key = base + 128 * u + pt;
+        const int64_t row = key < kv_end ? cache_row(c, b, hk, key, nullptr) : -1;
+        v8[u] = row >= 0 ? c.v_scale[row] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) vm = fmaxf(vm, v8[u]);
+    }
+    vm = warp_max_redux(vm);
+    if (lane == 0) vmax_sh[warp - 6] = vm;
+    asm volatile("bar.sync 2, 128;\n" ::: "memory");
+    if (pt == 0) {
+      const float v = fmaxf(fmaxf(vmax_sh[0], vmax_sh[1]), fmaxf(vmax_sh[2], vmax_sh[3]));
+      int e = 0;
+      (void)frexpf(v * (1.0f / 128.0f), &e);        // vmax * 2^-e < 128
+      *kp_sh = max(-100, min(100, e));
+    }
+  }
+  umma::fence_proxy_async_smem();
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const int kp = *kp_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = n_first;
+      for (int j = n_first; j < nkv; ++j) {
+        const int s = j % C::NS, u = j / C::NS;
+        if (!wait_or_abort(&empty[s], (u - 1) & 1, abort_flag)) break;
+        produce(j);
+        ++issued;
+      }
+      for (int j = max(0, issued - C::NS); j < issued; ++j)
+        (void)umma::mbar_wait(&full[j % C::NS], (j / C::NS) & 1, 100000000ull);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t ID_QK = umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_K, umma::MAJOR_K, 128, 64);
+      constexpr uint32_t ID_PV = umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_MN, umma::MAJOR_K, 128, 128);
+      const uint32_t qa = umma::smem_u32(qop);
+      for (int j = 0; j <= nkv; ++j) {
+        if (j < nkv) {
+          const int b2 = j & 1, u2 = j >> 1;
+          if (!wait_or_abort(&op_full[b2], u2 & 1, abort_flag)) break;
+          if (u2 > 0 && !wait_or_abort(&s_free[b2], (u2 - 1) & 1, abort_flag)) break;
+          umma::fence_after_sync();
+          const uint32_t ka = umma::smem_u32(kf + b2 * C::OPT);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_f16_ss(tmem + 64 * b2,
+                             umma::sdesc(qa + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
+                             umma::sdesc(ka + (kk >> 2) * (kPfKeys * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
+                             ID_QK, kk > 0);
+          umma::mma_commit(&s_full[b2]);
+        }
+        if (j >= 1) {
+          const int jj = j - 1, b2 = jj & 1, u2 = jj >> 1;
+          if (!wait_or_abort(&p_full[b2], u2 & 1, abort_flag)) break;
+          umma::fence_after_sync();
+          const uint32_t va = umma::smem_u32(vf + b2 * C::OPT);
+          const uint32_t pa = umma::smem_u32(pop + b2 * C::POP);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma::mma_f16_ss(tmem + 128,
+                             umma::sdesc(va + kk * 2048, kPfKeys * 128, 1024, umma::SWIZZLE_128B),
+                             umma::sdesc(pa + kk * 32, 16, 1024, umma::SWIZZLE_128B), ID_PV,
+                             (jj > 0 || kk > 0) ? 1u : 0u);
+          umma::mma_commit(&pv_done[b2]);
+        }
+      }
+      // all issued MMAs complete before TMEM is released (matters only when
+      // a wait above gave up)
+      umma::mma_commit(drained);
+      (void)umma::mbar_wait(drained, 0, 100000000ull);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------- softmax
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const float qsr = pow2i(kq);
+    const float pinv = pow2i(-kp);
+    float m_used = -INFINITY, l = 0.f;
+    bool failed = false;
+    for (int j = 0; j < nkv; ++j) {
+      const int b2 = j & 1, u2 = j >> 1;
+      bool ok = wait_or_abort(&s_full[b2], u2 & 1, abort_flag);
+      ok = ok && wait_or_abort(&op_full[b2], u2 & 1, abort_flag);
+      if (group_any(0, !ok)) { failed = true; break; }
+      umma::fence_after_sync();
+      float sv[64];
+      {
+        uint32_t rr[4][16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) umma::tmem_ld16_nowait(tmem + 64 * b2 + 16 * k + lane_off, rr[k]);
+        umma::tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int u = 0; u < 16; ++u) sv[16 * k + u] = __uint_as_float(rr[k][u]);
+      }
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&s_free[b2]);
+      const float* ksc = cols + b2 * 2 * kPfKeys;
+      const float* vsc = ksc + kPfKeys;
+      const int t0 = j * kPfKeys;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < 64; ++cc) {
+        const bool v_ok = t0 + cc <= qpos;
+        sv[cc] = v_ok ? sv[cc] * ksc[cc] * qsr : -INFINITY;
+        mt = fmaxf(mt, sv[cc]);
+      }
+      // lazy rescale: move the row's reference maximum only when it grows by
+      // more than 2^8 (or on the first tile with a valid key)
+      float alpha = 1.f;
+      if (mt != -INFINITY && (m_used == -INFINITY || mt > m_used + 8.f)) {
+        alpha = m_used == -INFINITY ? 0.f : ex2(m_used - mt);
+        m_used = mt;
+      }
+      float lt = 0.f;
+      uint32_t ph[32];
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 2) {
+        const float p0 = m_used == -INFINITY ? 0.f : ex2(sv[cc] - m_used);
+        const float p1 = m_used == -INFINITY ? 0.f : ex2(sv[cc + 1] - m_used);
+        lt += p0 + p1;
+        const float q0 = bf16_round(p0 * vsc[cc]) * pinv;
+        const float q1 = bf16_round(p1 * vsc[cc + 1]) * pinv;
+        const __half2 hv = __floats2half2_rn(q0, q1);
+        ph[cc >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      l = l * alpha + lt;
+      // O^T columns of rows whose reference moved are rescaled in TMEM once
+      // the previous PV is done
+      const bool need = group_any(0, alpha != 1.f && j > 0);
+      if (need) {
+        alpha_sh[r] = alpha;
+        group_sync(0);
+        const int jp = j - 1;
+        if (!wait_or_abort(&pv_done[jp & 1], (jp >> 1) & 1, abort_flag)) {
+          // the failure is caught by the next group_any
+        }
+        umma::fence_after_sync();
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k) {             // 8 chunks of 16 columns (query rows)
+          uint32_t rr[16];
+          umma::tmem_ld16_nowait(tmem + 128 + 16 * k + lane_off, rr);
+          umma::tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 16; ++u) rr[u] = __float_as_uint(__uint_as_float(rr[u]) * alpha_sh[16 * k + u]);
+          asm volatile(
+              "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+              "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(tmem + 128 + 16 * k + lane_off),
+              "r"(rr[0]), "r"(rr[1]), "r"(rr[2]), "r"(rr[3]), "r"(rr[4]), "r"(rr[5]), "r"(rr[6]), "r"(rr[7]),
+              "r"(rr[8]), "r"(rr[9]), "r"(rr[10]), "r"(rr[11]), "r"(rr[12]), "r"(rr[13]), "r"(rr[14]), "r"(rr[15]));
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+        group_sync(0);                              // alpha_sh reused next tile
+      }
+      // P row -> P operand buffer (free once the PV two tiles back is done)
+      if (u2 > 0 && !wait_or_abort(&pv_done[b2], (u2 - 1) & 1, abort_flag)) { /* caught below */ }
+      uint8_t* prow = pop + b2 * C::POP + r * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8)
+        *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) =
+            make_uint4(ph[4 * c8], ph[4 * c8 + 1], ph[4 * c8 + 2], ph[4 * c8 + 3]);
+      umma::fence_proxy_async_smem();
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&p_full[b2]);
+      if (*abort_flag) { failed = true; }
+      if (group_any(0, failed)) { failed = true; break; }
+    }
+    l_sh[r] = failed ? 0.f : l;
+    group_sync(0);
+    // ------------------------------------------------------------ epilogue
+    if (!failed && nkv > 0) {
+      const int jl = nkv - 1;
+      const bool ok = wait_or_abort(&pv_done[jl & 1], (jl >> 1) & 1, abort_flag);
+      if (!group_any(0, !ok)) {
+        umma::fence_after_sync();
+        const int d = r;                            // O^T lane = head dim
+        const float ofac = pow2i(kp);
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k) {
+          uint32_t rr[16];
+          umma::tmem_ld16_nowait(tmem + 128 + 16 * k + lane_off, rr);
+          umma::tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int row = 16 * k + u, qrow = i0 + row;
+            if (qrow < p.n_q) {
+              const float lr = l_sh[row];
+              const float o = lr > 0.f ? __uint_as_float(rr[u]) * ofac / lr : 0.f;
+              const int64_t oi = (((int64_t)b * p.n_q + qrow) * p.q_heads + hq) * D + d;
+              if (p.out_f32) reinterpret_cast<float*>(p.out)[oi] = o;
+              else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+            }
+          }
+        }
+      } else {
+        failed = true;
+      }
+    }
+    if (failed && r == 0) raise_error(p.err, FP8KV_DEVERR_TIMEOUT);
+  } else {
+    // --------------------------------------------------------- preparation
+    const int pt = tid - 192;
+    const int kr = pt >> 1, hh = pt & 1;          // key row of the tile, half of the head dim
+    bool failed = false;
+    for (int j = 0; j < nkv && !failed; ++j) {
+      const int s = j % C::NS, u = j / C::NS, b2 = j & 1, u2 = j >> 1;
+      bool ok = wait_or_abort(&full[s], u & 1, abort_flag);
+      if (u2 > 0) ok = ok && wait_or_abort(&pv_done[b2], (u2 - 1) & 1, abort_flag);
+      if (group_any(1, !ok)) { failed = true; break; }
+      const uint8_t* st = ring + s * C::STAGE;
+      const float* kss = reinterpret_cast<const float*>(st + 2 * C::CODES);
+      const float* vss = kss + kPfKeys;
+      const int t0 = j * kPfKeys;
+      const bool key_ok = t0 + kr < kv_end;
+#pragma unroll
+      for (int side = 0; side < 2; ++side) {
+        const uint8_t* codes = st + side * C::CODES + kr * 128;
+        uint8_t* dst = (side == 0 ? kf : vf) + b2 * C::OPT + hh * (kPfKeys * 128) + kr * 128;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {           // 16 codes -> two 16-byte f16 chunks
+          const int ch = 4 * hh + cc;
+          uint4 w = *reinterpret_cast<const uint4*>(codes + ((ch ^ (kr & 7)) << 4));
+          uint32_t h[8];
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int u4 = 0; u4 < 4; ++u4) {
+            h[2 * u4] = e4m3x2_to_f16x2((uint16_t)(ww[u4] & 0xFFFF));
+            h[2 * u4 + 1] = e4m3x2_to_f16x2((uint16_t)(ww[u4] >> 16));
+          }
+          if (side == 1 && !key_ok) {
+#pragma unroll
+            for (int u8 = 0; u8 < 8; ++u8) h[u8] = 0u;
+          }
+          const int c0 = 2 * cc, c1 = 2 * cc + 1;   // f16 chunk indices within the 128-byte atom row
+          *reinterpret_cast<uint4*>(dst + ((c0 ^ (kr & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(dst + ((c1 ^ (kr & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+      }
+      if (pt < kPfKeys) {
+        float* cc2 = cols + b2 * 2 * kPfKeys;
+        const bool ok2 = t0 + pt < kv_end;
+        cc2[pt] = ok2 ? kss[pt] * p.scale_log2 : 0.f;
+        cc2[kPfKeys + pt] = ok2 ? vss[pt] : 0.f;
+      }
+      umma::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        umma::mbar_arrive(&op_full[b2]);
+        umma::mbar_arrive(&empty[s]);
+      }
+    }
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  if (warp == 1) umma::tmem_dealloc(tmem, 256);
+}
+
+cudaError_t launch_prefill_tc(const PrefillParams& p, int batch, cudaStream_t st) {
+  constexpr int smem = PfTcCfg::BYTES;
+  cudaError_t e = ensure_smem_optin((const void*)prefill_tc, smem);
+  if (e != cudaSuccess) return e;
+  PrefillTmaParams tp;
+  const CacheView& c = p.c;
+  const int64_t rows = c.paged ? (int64_t)c.num_pages * c.kv_heads * c.page_size
+                               : (int64_t)c.batch * c.kv_heads * c.max_tokens;
+  const int box_rows = c.paged ? c.page_size : kPfKeys;
+  if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  if (!make_map(&tp.tmk, c.k, false, rows, box_rows) || !make_map(&tp.tmv, c.v, false, rows, box_rows))
+    return cudaErrorInvalidValue;
+  tp.p = p;
+  dim3 grid((p.n_q + kPfRows - 1) / kPfRows, p.q_heads, batch);
+  prefill_tc<<<grid, 320, smem, st>>>(tp);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8kv

@@ -1,0 +1,134 @@
+// tc_common.cuh -- helpers shared by the tensor-core (tcgen05) kernels:
+// operand layout offsets, E4M3 and exponent helpers, bounded waits, named
+// barriers of the softmax warpgroups, and TMA tensor-map encoding on the host.
+#pragma once
+
+#include "common.cuh"
+#include "tma.cuh"
+#include "umma.cuh"
+
+namespace fp8kv {
+
+// Byte offset of (row r, byte column c) in a `rows`-row operand stored in the
+// 128-byte-swizzled UMMA layout: 128-byte column blocks are separate
+// [rows][128 B] regions; inside a block, the 16-byte chunk index is XOR-ed
+// with (row % 8).
+__device__ __forceinline__ int sw128_off(int r, int byte_col, int rows) {
+  const int blk = byte_col >> 7, within = byte_col & 127;
+  return blk * rows * 128 + r * 128 + ((((within >> 4) ^ (r & 7))) << 4) + (within & 15);
+}
+
+// Two fp32 -> two E4M3 codes (round to nearest even, saturating); element 0
+// in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_rn(float x0, float x1) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(x1), "f"(x0));
+  return r;
+}
+__device__ __forceinline__ uint8_t e4m3_rn(float x) { return (uint8_t)(e4m3x2_rn(x, 0.f) & 0xFF); }
+__device__ __forceinline__ float e4m3_val(uint8_t c) {
+  float f[4];
+  e4m3x4_to_f32_scaled((uint32_t)c, f);
+  return f[0] * kTwoPow120;
+}
+// 2^e for e in the normal exponent range, by building the bits.
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float warp_max_redux(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(x));
+  return r;
+}
+// Exponent e with amax * 2^-e <= 448 (e = 0 for amax = 0).
+__device__ __forceinline__ int e4m3_row_exp(float amax) {
+  int e = 0;
+  (void)frexpf(amax * (1.0f / 448.0f), &e);
+  return e;
+}
+
+// Bounded wait shared by all roles of a CTA: gives up after ~2 s (SM clock
+// cycles, checked every 64 polls) or as soon as another role has given up
+// (abort flag).
+constexpr long long kWaitLimitCycles = 4000000000ll;
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (umma::mbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    if (umma::mbar_try(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// OR of `pred` over the 128 threads of softmax warpgroup `wg` (named barrier
+// 1 + wg), and a plain barrier over the same threads.
+__device__ __forceinline__ bool group_any(int wg, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(1 + wg)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void group_sync(int wg) { asm volatile("bar.sync %0, 128;\n" ::"r"(1 + wg) : "memory"); }
+
+// Two E4M3 codes (low byte element 0) -> f16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(codes));
+  return r;
+}
+
+// ------------------------------------------------------------ host side --
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    else
+      (void)cudaGetLastError();
+  }
+  return fn;
+}
+
+// Tensor map of a K or V store viewed as [rows][128 elements], boxes of
+// `box_rows` rows by 128 bytes, 128-byte swizzle.
+inline bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(bf16 ? 256 : 128)};
+  const cuuint32_t box[2] = {(cuuint32_t)(bf16 ? 64 : 128), (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace fp8kv

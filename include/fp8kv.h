@@ -242,17 +242,21 @@ FP8KV_API fp8kv_status fp8kv_decode_attention_static(const void *q, const fp8kv_
 FP8KV_API size_t fp8kv_decode_static_scratch_bytes(void);
 
 /* Causal prefill attention over the cache ("03 · 8n — FA-style tiled prefill
- * attention", sections 2-3): 64-token query tiles, online softmax over
- * 64-token KV tiles.  Query i of sequence b sits at absolute position
- * q_pos0[b] + i and attends cache tokens 0..q_pos0[b]+i (the cache must
- * already hold them: append first).
+ * attention", sections 2-3): query tiles, online softmax over 64-token KV
+ * tiles.  Query i of sequence b sits at absolute position q_pos0[b] + i and
+ * attends cache tokens 0..q_pos0[b]+i (the cache must already hold them:
+ * append first).
  *   q:      [batch][n_q][q_heads][head_dim] bf16
  *   q_pos0: [batch] int32 device array
+ *   kernel: FP8KV_KERNEL_* -- TENSOR_CORES (128-query tiles on tcgen05, K8V8
+ *           with head_dim 128 only, else FP8KV_ERR_UNSUPPORTED),
+ *           CUDA_CORES (64-query tiles, every dtype), AUTO (tensor cores
+ *           where built)
  *   out:    [batch][n_q][q_heads][head_dim], bf16 or fp32 per out_dtype */
 FP8KV_API fp8kv_status fp8kv_prefill_attention(const void *q, const fp8kv_cache *cache,
                                      const int32_t *q_pos0, int32_t n_q,
-                                     int32_t q_heads, float sm_scale, void *out,
-                                     int32_t out_dtype, fp8kv_stream_t stream);
+                                     int32_t q_heads, float sm_scale, int32_t kernel,
+                                     void *out, int32_t out_dtype, fp8kv_stream_t stream);
 
 /* Read (and, if `clear` is non-zero, reset) the device error word of the
  * current device.  Synchronous: waits for all work on the device. */

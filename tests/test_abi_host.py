@@ -78,6 +78,13 @@ def test_argument_checks_return_before_any_launch(lib):
     d64 = _cache(head_dim=64)
     assert lib.fp8kv_decode_split(None, r(d64), None, 16, 0.1, 0, 2, None, 0, None) == 2
     assert lib.fp8kv_decode_split(None, r(c), None, 16, 0.1, 0, 3, None, 0, None) == 1
+    # prefill: the tensor-core kernel is built for K8V8 at head_dim 128 only;
+    # a bad kernel id is rejected
+    k16 = _cache(dtype=1, k_scale=None)
+    assert lib.fp8kv_prefill_attention(0x7000, r(k16), 0x8000, 64, 16, 0.1, 2, out, 0, None) == 2
+    assert lib.fp8kv_prefill_attention(0x7000, r(d64), 0x8000, 64, 16, 0.1, 2, out, 0, None) == 2
+    assert lib.fp8kv_prefill_attention(0x7000, r(c), 0x8000, 64, 16, 0.1, 5, out, 0, None) == 1
+    assert lib.fp8kv_prefill_attention(0x7000, r(c), 0x8000, 0, 16, 0.1, 2, out, 0, None) == 0
 
 
 def test_split_plan_and_workspace(lib):

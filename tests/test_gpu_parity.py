@@ -279,7 +279,7 @@ def test_decode_repeat_is_bitwise_stable(kernel):
 
 # ---------------------------------------------------------------- prefill --
 
-def _prefill_case(n_q, pos0, Hq, Hkv, D, dtype, seed, sample_blocks=None):
+def _prefill_case(n_q, pos0, Hq, Hkv, D, dtype, seed, sample_blocks=None, kernel="auto"):
     spec = synth.PrefillWorkload("pf", n_q, Hq, Hkv, D, seed=seed, pos0=pos0)
     pin = synth.prefill_inputs(spec, device="cuda")
     total = pos0 + n_q
@@ -290,7 +290,7 @@ def _prefill_case(n_q, pos0, Hq, Hkv, D, dtype, seed, sample_blocks=None):
                     torch.arange(total, dtype=torch.int32, device="cuda"))
     out = fk.fp8kv_prefill_attention(pin.q[None].contiguous(), cache,
                                      torch.tensor([pos0], dtype=torch.int32, device="cuda"),
-                                     out_dtype=torch.float32)[0].cpu().numpy()
+                                     out_dtype=torch.float32, kernel=kernel)[0].cpu().numpy()
     kb = synth.bf16_bits(pin.k).transpose(1, 0, 2)
     vb = synth.bf16_bits(pin.v).transpose(1, 0, 2)
     if dtype == "k8v8":
@@ -308,7 +308,12 @@ def _prefill_case(n_q, pos0, Hq, Hkv, D, dtype, seed, sample_blocks=None):
 
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_prefill_small_ragged(dtype):
-    _prefill_case(200, 0, 4, 2, 128, dtype, seed=31)
+    _prefill_case(200, 0, 4, 2, 128, dtype, seed=31, kernel="cuda_cores")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_small_ragged_k8v8_both_kernels(kernel):
+    _prefill_case(200, 0, 4, 2, 128, "k8v8", seed=31, kernel=kernel)
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -316,10 +321,11 @@ def test_prefill_with_prefix_offset(dtype):
     _prefill_case(77, 37, 6, 2, 64, dtype, seed=32)
 
 
-def test_prefill_2048_full_sampled():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_2048_full_sampled(kernel):
     """Causal prefill at full size (2048 tokens, 28 q / 4 KV heads), oracle on
     sampled query blocks that straddle tile boundaries."""
-    _prefill_case(2048, 0, 28, 4, 128, "k8v8", seed=4,
+    _prefill_case(2048, 0, 28, 4, 128, "k8v8", seed=4, kernel=kernel,
                   sample_blocks=[(0, 70), (1000, 1090), (1980, 2048)])
 
 
