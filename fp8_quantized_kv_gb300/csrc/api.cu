@@ -241,6 +241,7 @@ fp8kv_status prepare_decode(const void* q, const fp8kv_cache* cache, const int32
   p->out = nullptr;
   p->out_f32 = 0;
   p->fused = 0;
+  p->cluster = 0;
   *resolved = k;
   return FP8KV_OK;
 }

@@ -44,6 +44,14 @@
 // runs out raises FP8KV_DEVERR_TIMEOUT, the CTA writes an empty partial and
 // leaves.  V rows past the sequence end are zeroed before PV (0 * NaN would
 // poison the product).
+//
+// The fused decode step (append + split + merge in one launch) merges the
+// splits of a (sequence, KV head) in one of two ways.  With 2..8 splits whose
+// clusters all fit on the GPU at once, the splits run as one thread-block
+// cluster and exchange their partials through distributed shared memory
+// (cluster_exchange: each rank merges a slice of the head dimension).
+// Otherwise every split writes its partial to global memory and the last
+// one to finish, found with an atomic counter, merges them all.
 #include "params.cuh"
 #include "tc_common.cuh"
 
@@ -62,7 +70,7 @@ struct TcCfg {
   static constexpr int QOP = KE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;
   static constexpr int POP = VE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;   // [128 tokens][16 or 32 B]
   static constexpr int XO = 8 * 128 * 4;    // group 1's O handed to group 0
-  static constexpr int MISC = 3072;
+  static constexpr int MISC = 6656;         // barriers, small tables, cluster receive buffers
   static constexpr int BYTES = NST * STAGE + QOP + 4 * POP + XO + MISC + 1024;
   static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
@@ -105,6 +113,104 @@ __device__ unsigned long long g_cta_time[4096][8];   // start, end, published, l
   } while (0)
 #endif
 
+// Merge of the fused step when the splits of one (sequence, KV head) run as
+// one thread-block cluster (split = cluster rank, S <= 8).  Rank r owns the
+// four-dim groups [g4_lo(r), g4_lo(r+1)) of the head dimension, all 8 heads.
+// Each rank stages its split's O as [head][dim] in shared memory and pushes
+// every (head, four-dim group) as one 16-byte st.async into the owning
+// rank's receive buffer ([sender][head][group]); thread t < S pushes the
+// split's (m, l) to rank t.  Every st.async counts down the receiver's
+// mbarrier, whose transaction count was armed at setup with all the bytes
+// it will get.  Each rank then waits for its slice and merges it from local
+// shared memory, one (head, four-dim group) output per thread: one one-way
+// trip over the cluster network, no cluster-wide barrier.  Called by the 128
+// merging threads (warps 2-5, thread t = dim t of the partial) of every CTA;
+// `stage` is [8][128] floats of this CTA's shared memory that is idle now.
+__device__ __forceinline__ int g4_lo(int r, int S) { return (32 * r) / S; }
+
+__device__ __noinline__ void cluster_exchange(const DecodeParams& p, float* rx_ml, float* rx_o, uint64_t* rx_bar,
+                                              float* stage, const float (&Og)[8], const float (&Mg)[8],
+                                              const float (&Lg)[8], int b, int h, int G, int t,
+                                              volatile int* abort) {
+  constexpr int D = 128;
+  const int S = p.num_splits;
+  const int k = (int)cluster_rank();
+  if (t == 0) TRACE(1002);
+#pragma unroll
+  for (int g = 0; g < 8; ++g) stage[g * D + t] = Og[g];
+  group_sync(0);
+  // (the caller passed the cluster barrier after setup: every rank's receive
+  // barrier is initialised and armed)
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int c = t + 128 * j, g = c >> 5, q = c & 31;   // head g, four-dim group q
+    int r = 0;
+#pragma unroll
+    for (int u = 1; u < 8; ++u)
+      if (u < S && g4_lo(u, S) <= q) r = u;
+    const int lo = g4_lo(r, S), n4 = g4_lo(r + 1, S) - lo;
+    const float4 v = *reinterpret_cast<const float4*>(stage + g * D + 4 * q);
+    st_async_v4(mapa_u32(umma::smem_u32(rx_o + 4 * ((k * 8 + g) * n4 + (q - lo))), (uint32_t)r), v,
+                mapa_u32(umma::smem_u32(rx_bar), (uint32_t)r));
+  }
+  if (t < S) {
+    const uint32_t bar_t = mapa_u32(umma::smem_u32(rx_bar), (uint32_t)t);
+    const uint32_t dml = mapa_u32(umma::smem_u32(rx_ml + k * 16), (uint32_t)t);
+    st_async_v4(dml, make_float4(Mg[0], Mg[1], Mg[2], Mg[3]), bar_t);
+    st_async_v4(dml + 16, make_float4(Mg[4], Mg[5], Mg[6], Mg[7]), bar_t);
+    st_async_v4(dml + 32, make_float4(Lg[0], Lg[1], Lg[2], Lg[3]), bar_t);
+    st_async_v4(dml + 48, make_float4(Lg[4], Lg[5], Lg[6], Lg[7]), bar_t);
+  }
+  if (t == 0) TRACE(1003);
+  const bool ok = wait_cluster(rx_bar, 0, abort);
+  if (t == 0) TRACE(1004);
+  if (!ok) {
+    if (t == 0) raise_error(p.err, FP8KV_DEVERR_TIMEOUT);
+    return;
+  }
+  const int mlo = g4_lo(k, S), m4 = g4_lo(k + 1, S) - mlo;
+  if (t < 8 * m4) {
+    const int g = t / m4, j = t - g * m4;
+    float M = -INFINITY;
+    for (int kk = 0; kk < S; ++kk) M = fmaxf(M, rx_ml[kk * 16 + g]);
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int kk = 0; kk < S; ++kk) {
+      const float mk = rx_ml[kk * 16 + g];
+      const float w = mk == -INFINITY ? 0.f : ex2(mk - M);
+      const float4 v = *reinterpret_cast<const float4*>(rx_o + 4 * ((kk * 8 + g) * m4 + j));
+      L += w * rx_ml[kk * 16 + 8 + g];
+      o.x += w * v.x; o.y += w * v.y; o.z += w * v.z; o.w += w * v.w;
+    }
+    if (g < G) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const int64_t oi = ((int64_t)b * p.q_heads + (int64_t)h * G + g) * D + 4 * (mlo + j);
+      const float r4[4] = {o.x * inv, o.y * inv, o.z * inv, o.w * inv};
+      if ((reinterpret_cast<uintptr_t>(p.out) & 15) != 0) {   // caller's buffer not 16-byte aligned
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (p.out_f32) reinterpret_cast<float*>(p.out)[oi + e] = r4[e];
+          else reinterpret_cast<__nv_bfloat16*>(p.out)[oi + e] = __float2bfloat16_rn(r4[e]);
+        }
+      } else if (p.out_f32) {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi) = make_float4(r4[0], r4[1], r4[2], r4[3]);
+      } else {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(r4[0], r4[1]);
+        const __nv_bfloat162 c = __floats2bfloat162_rn(r4[2], r4[3]);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&c));
+      }
+    }
+  }
+  if (t == 0) TRACE(1005);
+}
+
+// Bytes a rank receives in the cluster merge: S senders x (8 heads x its
+// four-dim groups x 16 bytes + 16 (m, l) floats).
+__device__ __forceinline__ uint32_t cluster_rx_bytes(int rank, int S) {
+  return (uint32_t)(S * (128 * (g4_lo(rank + 1, S) - g4_lo(rank, S)) + 64));
+}
+
 template <int KE, int VE>
 __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant__ DecodeTmaParams tp) {
   using C = TcCfg<KE, VE>;
@@ -120,13 +226,16 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
   uint64_t* empty = full + 8;                              // [8]
   WgBars* wb = reinterpret_cast<WgBars*>(empty + 8);       // [2]
   uint64_t* appended = reinterpret_cast<uint64_t*>(wb + 2);   // new token written (fused step)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(appended + 1);
+  uint64_t* rx_bar = appended + 1;                         // cluster merge: this rank's slice received
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(rx_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tslot + 2);
   float* qscale = reinterpret_cast<float*>(misc + 512);    // [8]
   float* red = qscale + 8;                                 // [wg][2][4][9]
-  float* lred = red + 144;                                 // [wg][4][8]; later the merge's (m, l) table
-  float* xml = lred + 256;                                 // [16]: m and l of warpgroup 1
+  float* lred = red + 144;                                 // [wg][4][8]
+  float* xml = lred + 64;                                  // [16]: m and l of warpgroup 1
+  float* rx_ml = reinterpret_cast<float*>(misc + 1536);    // [sender][m 8 | l 8]
+  float* rx_o = reinterpret_cast<float*>(misc + 2048);     // [sender][dim of this rank's slice][8 heads]
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -144,6 +253,25 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
   const int t_end = min(t_begin + p.chunk_tiles, tiles);
   const int64_t part0 = ((int64_t)b * p.q_heads + (int64_t)h * G) * S + split;
   if (t_begin >= t_end) {
+    if (p.cluster) {
+      // no tiles: an empty partial (m = -inf, l = 0) in the cluster merge
+      if (tid == 0) {
+        *abort_flag = 0;
+        umma::mbar_init(rx_bar, 1);
+        tma::arrive_expect_tx(rx_bar, cluster_rx_bytes((int)cluster_rank(), S));
+        umma::mbar_fence_init();
+      }
+      __syncthreads();
+      cluster_arrive_relaxed();
+      if (tid >= 64 && tid < 192) {
+        cluster_wait();
+        float Og[8], Mg[8], Lg[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) { Og[g] = 0.f; Mg[g] = -INFINITY; Lg[g] = 0.f; }
+        cluster_exchange(p, rx_ml, rx_o, rx_bar, xo, Og, Mg, Lg, b, h, G, tid - 64, abort_flag);
+      }
+      return;
+    }
     if (p.fused) {
       // No partial: splits without work take no part in the merge.  A
       // sequence with no tokens gets its zero output from split 0.
@@ -239,6 +367,10 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         umma::mbar_init(&wb[w].o_empty[i], 4);
       }
     umma::mbar_init(appended, 1);
+    if (p.cluster) {
+      umma::mbar_init(rx_bar, 1);
+      tma::arrive_expect_tx(rx_bar, cluster_rx_bytes(split, S));
+    }
     *abort_flag = 0;
     *last_flag = 0;
     umma::mbar_fence_init();
@@ -289,6 +421,12 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
   __syncthreads();
   umma::fence_after_sync();
   const uint32_t tmem = *tslot;
+  if (p.cluster) {
+    // every rank's receive barrier initialised: the merging warps wait for
+    // that here, while the first tiles are still in flight
+    cluster_arrive_relaxed();
+    if (warp >= 2 && warp < 6) cluster_wait();
+  }
 
   if (appender && warp == 6) {
     // Quantise and write the new token's K and V rows (the arithmetic of
@@ -614,6 +752,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
     }
     // The two groups' running states are merged like two splits: group 1
     // hands its (m, l, O) to group 0 through shared memory.
+    if (t == 0 && wg == 1) TRACE(1000);
     if (wg == 1) {
 #pragma unroll
       for (int g = 0; g < 8; ++g) xo[g * D + t] = o_run[g];
@@ -637,7 +776,10 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         Mg[g] = M;
         Lg[g] = l_tot[g] * f0 + l1 * f1;
       }
-      if (p.fused && n_busy == 1) {
+      if (t == 0) TRACE(1001);
+      if (p.cluster) {
+        cluster_exchange(p, rx_ml, rx_o, rx_bar, xo, Og, Mg, Lg, b, h, G, t, abort_flag);
+      } else if (p.fused && n_busy == 1) {
         // the only split of this sequence: normalise and write the output
 #pragma unroll
         for (int g = 0; g < 8; ++g)
@@ -786,6 +928,8 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
       if (t == 0) TRACE(1012);
     }
   }
+  // (threads other than the merging ones arrived at the cluster barrier at
+  // setup and never wait on it: they arrive only once)
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
@@ -797,6 +941,40 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
 }
 
 // ------------------------------------------------------------ host side --
+
+// True when every cluster of grid.x CTAs (one per (sequence, KV head)) can
+// be resident at once, so the cluster launch runs in a single wave like the
+// plain launch.  Cached per device, kernel and grid shape.
+static bool cluster_fits(const void* fn, dim3 grid, int smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { (void)cudaGetLastError(); return false; }
+  struct Key { int dev; const void* fn; unsigned x; };
+  static Key keys[16];
+  static int vals[16];
+  static int n = 0;
+  int max_clusters = -1;
+  for (int i = 0; i < n; ++i)
+    if (keys[i].dev == dev && keys[i].fn == fn && keys[i].x == grid.x) max_clusters = vals[i];
+  if (max_clusters < 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(320);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = grid.x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      max_clusters = 0;
+    }
+    if (n < 16) { keys[n] = Key{dev, fn, grid.x}; vals[n] = max_clusters; ++n; }
+  }
+  return (long long)max_clusters >= (long long)grid.y * grid.z;
+}
 
 template <int KE, int VE>
 static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st) {
@@ -813,6 +991,26 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
       !make_map(&tp.tmv, c.v, VE != ELEM_E4M3, rows, box_rows))
     return cudaErrorInvalidValue;
   tp.p = p;
+  tp.p.cluster = 0;
+  const void* fn = (const void*)decode_split_tc<KE, VE>;
+  if (p.fused && p.num_splits >= 2 && p.num_splits <= 8 && cluster_fits(fn, grid, smem)) {
+    tp.p.cluster = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(320);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = grid.x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e2 = cudaLaunchKernelEx(&cfg, decode_split_tc<KE, VE>, tp);
+    if (e2 != cudaSuccess) (void)cudaGetLastError();
+    return e2;
+  }
   decode_split_tc<KE, VE><<<grid, 320, smem, st>>>(tp);
   return cudaGetLastError();
 }

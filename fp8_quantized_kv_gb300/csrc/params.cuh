@@ -23,6 +23,7 @@ struct DecodeParams {
   void* out;                 // [B][Hq][D] merged output (bf16 or fp32)
   int out_f32;
   int fused;
+  int cluster;               // fused step launched with the splits of a (sequence, KV head) as one cluster
 };
 
 struct PrefillParams {

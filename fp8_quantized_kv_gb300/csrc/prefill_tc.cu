@@ -13,14 +13,15 @@
 // KV head:
 //   S[128 x 64]    = Q . K^T            tcgen05.mma kind::f16 -> TMEM
 //   per row (one thread each, whole row thread-local): s = S * k_scale *
-//     sm_scale, causal mask, running max with lazy rescale, p = 2^(s - m),
-//     l += p, P' = bf16_rn(p * v_scale)
+//     sm_scale, causal mask (diagonal tiles only), running max with lazy
+//     rescale, p = 2^(s - m), l += p, P' = p * v_scale
 //   O^T[128 x 128] += V^T . P'^T         tcgen05.mma kind::f16 -> TMEM
 // Operands are f16: the e4m3 K and V codes convert to f16 exactly
 // (cvt.rn.f16x2.e4m3x2); each bf16 query row is scaled by a power of two
-// (exact) into f16's range; the bf16-rounded P' is scaled by one power of two
-// per CTA (from the largest V scale it will see) and converted exactly.  All
-// those scalings are undone in fp32.
+// (exact) into f16's range.  P' is rounded once, to the 16-bit operand of the
+// P.V product as the method asks, but to f16 (11-bit significand, 8x finer
+// than bf16) after one power-of-two scaling per CTA chosen from the largest V
+// scale it will see.  All those scalings are undone in fp32.
 //
 // Warp roles:
 //   warp 0     TMA producer: e4m3 code tiles (64 keys x 128 B, 128-byte
@@ -47,14 +48,31 @@ struct PfTcCfg {
   static constexpr int QOP = kPfRows * D * 2;                 // [2 atoms][128 rows][128 B] f16
   static constexpr int CODES = kPfKeys * D;                    // e4m3 tile [64][128]
   static constexpr int STAGE = ((2 * CODES + 2 * kPfKeys * 4) + 1023) / 1024 * 1024;
-  static constexpr int NS = 3;
+  static constexpr int NS = 2;                                 // e4m3 code stages
+  static constexpr int NOP = 3;                                // f16 K/V operand buffers
   static constexpr int OPT = kPfKeys * D * 2;                 // f16 K or V tile [2 atoms][64][128 B]
   static constexpr int POP = kPfRows * kPfKeys * 2;           // f16 P [128 rows][128 B]
   static constexpr int COLS = 2 * kPfKeys * 4;                 // per buffer: k and v column scales
   static constexpr int MISC = 2048;
-  static constexpr int BYTES = QOP + NS * STAGE + 4 * OPT + 2 * POP + 2 * COLS + MISC + 1024;
+  static constexpr int BYTES = QOP + NS * STAGE + 2 * NOP * OPT + 2 * POP + NOP * COLS + MISC + 1024;
   static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
+
+#ifdef FP8KV_TRACE
+// Per-tile clock64 stamps of CTA (0, 0, 0) (the longest query tile):
+// slot 8*j + {0: TMA issue, 1: QK issue, 2: PV issue, 3: operands ready,
+// 4: softmax has S, 5: P ready}; 1010: epilogue start; 1020/1021: begin/end.
+__device__ unsigned long long g_pf_trace[1024];
+#define PF_TRACE(slot)                                                               \
+  do {                                                                               \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (slot) < 1024)      \
+      g_pf_trace[(slot)] = clock64();                                                \
+  } while (0)
+#else
+#define PF_TRACE(slot) \
+  do {                 \
+  } while (0)
+#endif
 
 struct PrefillTmaParams {
   CUtensorMap tmk;
@@ -70,18 +88,19 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qop = smem;
   uint8_t* ring = qop + C::QOP;
-  uint8_t* kf = ring + C::NS * C::STAGE;          // [2] f16 K operand
-  uint8_t* vf = kf + 2 * C::OPT;                  // [2] f16 V operand
-  uint8_t* pop = vf + 2 * C::OPT;                 // [2] f16 P operand
-  float* cols = reinterpret_cast<float*>(pop + 2 * C::POP);   // [2][k 64 | v 64]
-  uint8_t* misc = reinterpret_cast<uint8_t*>(cols + 2 * 2 * kPfKeys);
+  uint8_t* kf = ring + C::NS * C::STAGE;          // [NOP] f16 K operand
+  uint8_t* vf = kf + C::NOP * C::OPT;             // [NOP] f16 V operand
+  uint8_t* pop = vf + C::NOP * C::OPT;            // [2] f16 P operand
+  float* cols = reinterpret_cast<float*>(pop + 2 * C::POP);   // [NOP][k 64 | v 64]
+  uint8_t* misc = reinterpret_cast<uint8_t*>(cols + C::NOP * 2 * kPfKeys);
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);        // [NS] codes landed
   uint64_t* empty = full + C::NS;                             // [NS] codes consumed by the prep warps
-  uint64_t* op_full = empty + C::NS;                          // [2] f16 K/V operands + scales ready
-  uint64_t* s_full = op_full + 2;                             // [2]
+  uint64_t* op_full = empty + C::NS;                          // [NOP] f16 K/V operands + scales ready
+  uint64_t* op_free = op_full + C::NOP;                       // [NOP] PV of the buffer's tile finished
+  uint64_t* s_full = op_free + C::NOP;                        // [2]
   uint64_t* s_free = s_full + 2;                              // [2]
   uint64_t* p_full = s_free + 2;                              // [2]
-  uint64_t* pv_done = p_full + 2;                             // [2] PV of the buffer's tile finished
+  uint64_t* pv_done = p_full + 2;                             // [2] PV of the P buffer's tile finished
   uint64_t* drained = pv_done + 2;                            // final commit of the MMA issuer
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drained + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
@@ -107,6 +126,7 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
   const int64_t cont_row0 = ((int64_t)b * c.kv_heads + hk) * c.max_tokens;
 
   auto produce = [&](int j) {
+    PF_TRACE(8 * j + 0);
     const int s = j % C::NS;
     uint8_t* st = ring + s * C::STAGE;
     float* kss = reinterpret_cast<float*>(st + 2 * C::CODES);
@@ -142,13 +162,17 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
 
   // ---------------------------------------------------------------- setup
   const int n_first = min(nkv, C::NS);
+  if (tid == 0) PF_TRACE(1020);
   if (tid == 0) {
     for (int i = 0; i < C::NS; ++i) {
       umma::mbar_init(&full[i], 1);
       umma::mbar_init(&empty[i], 4);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NOP; ++i) {
       umma::mbar_init(&op_full[i], 4);
+      umma::mbar_init(&op_free[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       umma::mbar_init(&s_full[i], 1);
       umma::mbar_init(&s_free[i], 4);
       umma::mbar_init(&p_full[i], 4);
@@ -250,7 +274,7 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       int issued = n_first;
       for (int j = n_first; j < nkv; ++j) {
         const int s = j % C::NS, u = j / C::NS;
-        if (!wait_or_abort(&empty[s], (u - 1) & 1, abort_flag)) break;
+        if (!wait_fast(&empty[s], (u - 1) & 1, abort_flag)) break;
         produce(j);
         ++issued;
       }
@@ -263,34 +287,44 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       constexpr uint32_t ID_QK = umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_K, umma::MAJOR_K, 128, 64);
       constexpr uint32_t ID_PV = umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_MN, umma::MAJOR_K, 128, 128);
       const uint32_t qa = umma::smem_u32(qop);
-      for (int j = 0; j <= nkv; ++j) {
-        if (j < nkv) {
-          const int b2 = j & 1, u2 = j >> 1;
-          if (!wait_or_abort(&op_full[b2], u2 & 1, abort_flag)) break;
-          if (u2 > 0 && !wait_or_abort(&s_free[b2], (u2 - 1) & 1, abort_flag)) break;
-          umma::fence_after_sync();
-          const uint32_t ka = umma::smem_u32(kf + b2 * C::OPT);
+      // QK of tile j+1 goes out before PV of tile j, so the tensor core works
+      // on the next scores while the softmax warps turn tile j into P
+      auto qk = [&](int j) -> bool {
+        const int b2 = j & 1, u2 = j >> 1, ob = j % C::NOP, ou = j / C::NOP;
+        if (!wait_fast(&op_full[ob], ou & 1, abort_flag)) return false;
+        if (u2 > 0 && !wait_fast(&s_free[b2], (u2 - 1) & 1, abort_flag)) return false;
+        umma::fence_after_sync();
+        PF_TRACE(8 * j + 1);
+        const uint32_t ka = umma::smem_u32(kf + ob * C::OPT);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma::mma_f16_ss(tmem + 64 * b2,
-                             umma::sdesc(qa + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
-                             umma::sdesc(ka + (kk >> 2) * (kPfKeys * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
-                             ID_QK, kk > 0);
-          umma::mma_commit(&s_full[b2]);
-        }
-        if (j >= 1) {
-          const int jj = j - 1, b2 = jj & 1, u2 = jj >> 1;
-          if (!wait_or_abort(&p_full[b2], u2 & 1, abort_flag)) break;
-          umma::fence_after_sync();
-          const uint32_t va = umma::smem_u32(vf + b2 * C::OPT);
-          const uint32_t pa = umma::smem_u32(pop + b2 * C::POP);
+        for (int kk = 0; kk < 8; ++kk)
+          umma::mma_f16_ss(tmem + 64 * b2,
+                           umma::sdesc(qa + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
+                           umma::sdesc(ka + (kk >> 2) * (kPfKeys * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
+                           ID_QK, kk > 0);
+        umma::mma_commit(&s_full[b2]);
+        return true;
+      };
+      auto pv = [&](int j) -> bool {
+        const int b2 = j & 1, u2 = j >> 1, ob = j % C::NOP;
+        if (!wait_fast(&p_full[b2], u2 & 1, abort_flag)) return false;
+        umma::fence_after_sync();
+        PF_TRACE(8 * j + 2);
+        const uint32_t va = umma::smem_u32(vf + ob * C::OPT);
+        const uint32_t pa = umma::smem_u32(pop + b2 * C::POP);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma::mma_f16_ss(tmem + 128,
-                             umma::sdesc(va + kk * 2048, kPfKeys * 128, 1024, umma::SWIZZLE_128B),
-                             umma::sdesc(pa + kk * 32, 16, 1024, umma::SWIZZLE_128B), ID_PV,
-                             (jj > 0 || kk > 0) ? 1u : 0u);
-          umma::mma_commit(&pv_done[b2]);
+        for (int kk = 0; kk < 4; ++kk)
+          umma::mma_f16_ss(tmem + 128, umma::sdesc(va + kk * 2048, kPfKeys * 128, 1024, umma::SWIZZLE_128B),
+                           umma::sdesc(pa + kk * 32, 16, 1024, umma::SWIZZLE_128B), ID_PV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+        umma::mma_commit(&pv_done[b2]);
+        umma::mma_commit(&op_free[ob]);
+        return true;
+      };
+      if (qk(0)) {
+        for (int j = 0; j < nkv; ++j) {
+          if (j + 1 < nkv && !qk(j + 1)) break;
+          if (!pv(j)) break;
         }
       }
       // all issued MMAs complete before TMEM is released (matters only when
@@ -302,15 +336,16 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
     // ------------------------------------------------------------- softmax
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float qsr = pow2i(kq);
-    const float pinv = pow2i(-kp);
+    const int qpos_min = pos0 + i0;                 // smallest position among this CTA's queries
     float m_used = -INFINITY, l = 0.f;
     bool failed = false;
     for (int j = 0; j < nkv; ++j) {
-      const int b2 = j & 1, u2 = j >> 1;
-      bool ok = wait_or_abort(&s_full[b2], u2 & 1, abort_flag);
-      ok = ok && wait_or_abort(&op_full[b2], u2 & 1, abort_flag);
+      const int b2 = j & 1, u2 = j >> 1, ob = j % C::NOP;
+      bool ok = wait_fast(&s_full[b2], u2 & 1, abort_flag);
+      ok = ok && wait_fast(&op_full[ob], (j / C::NOP) & 1, abort_flag);
       if (group_any(0, !ok)) { failed = true; break; }
       umma::fence_after_sync();
+      if (r == 0) PF_TRACE(8 * j + 4);
       float sv[64];
       {
         uint32_t rr[4][16];
@@ -325,16 +360,31 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       umma::fence_before_sync();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&s_free[b2]);
-      const float* ksc = cols + b2 * 2 * kPfKeys;
-      const float* vsc = ksc + kPfKeys;
-      const int t0 = j * kPfKeys;
-      float mt = -INFINITY;
+      // t = S * k_scale * sm_scale * log2(e); the row's 2^kq comes in below
+      const float4* kc4 = reinterpret_cast<const float4*>(cols + ob * 2 * kPfKeys);
+      const float4* vc4 = kc4 + kPfKeys / 4;
 #pragma unroll
-      for (int cc = 0; cc < 64; ++cc) {
-        const bool v_ok = t0 + cc <= qpos;
-        sv[cc] = v_ok ? sv[cc] * ksc[cc] * qsr : -INFINITY;
-        mt = fmaxf(mt, sv[cc]);
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 kc = kc4[c4];
+        sv[4 * c4 + 0] *= kc.x;
+        sv[4 * c4 + 1] *= kc.y;
+        sv[4 * c4 + 2] *= kc.z;
+        sv[4 * c4 + 3] *= kc.w;
       }
+      const int t0 = j * kPfKeys;
+      if (t0 + kPfKeys - 1 > qpos_min) {             // causal edge: keys past this row's position drop out
+#pragma unroll
+        for (int cc = 0; cc < 64; ++cc) sv[cc] = t0 + cc <= qpos ? sv[cc] : -INFINITY;
+      }
+      float m8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8[k] = fmaxf(sv[k], sv[k + 8]);
+#pragma unroll
+      for (int cc = 16; cc < 64; cc += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], sv[cc + k]);
+      float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      mt *= qsr;
       // lazy rescale: move the row's reference maximum only when it grows by
       // more than 2^8 (or on the first tile with a valid key)
       float alpha = 1.f;
@@ -342,19 +392,27 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
         alpha = m_used == -INFINITY ? 0.f : ex2(m_used - mt);
         m_used = mt;
       }
-      float lt = 0.f;
+      const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t ph[32];
 #pragma unroll
-      for (int cc = 0; cc < 64; cc += 2) {
-        const float p0 = m_used == -INFINITY ? 0.f : ex2(sv[cc] - m_used);
-        const float p1 = m_used == -INFINITY ? 0.f : ex2(sv[cc + 1] - m_used);
-        lt += p0 + p1;
-        const float q0 = bf16_round(p0 * vsc[cc]) * pinv;
-        const float q1 = bf16_round(p1 * vsc[cc + 1]) * pinv;
-        const __half2 hv = __floats2half2_rn(q0, q1);
-        ph[cc >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 vc = vc4[c4];
+        const float p0 = ex2_ftz(fmaf(sv[4 * c4 + 0], qsr, neg_m));
+        const float p1 = ex2_ftz(fmaf(sv[4 * c4 + 1], qsr, neg_m));
+        const float p2 = ex2_ftz(fmaf(sv[4 * c4 + 2], qsr, neg_m));
+        const float p3 = ex2_ftz(fmaf(sv[4 * c4 + 3], qsr, neg_m));
+        l4[0] += p0;
+        l4[1] += p1;
+        l4[2] += p2;
+        l4[3] += p3;
+        // P' = p * v_scale * 2^-kp, rounded once to the f16 operand
+        const __half2 h01 = __floats2half2_rn(p0 * vc.x, p1 * vc.y);
+        const __half2 h23 = __floats2half2_rn(p2 * vc.z, p3 * vc.w);
+        ph[2 * c4] = *reinterpret_cast<const uint32_t*>(&h01);
+        ph[2 * c4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
       }
-      l = l * alpha + lt;
+      l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
       // O^T columns of rows whose reference moved are rescaled in TMEM once
       // the previous PV is done
       const bool need = group_any(0, alpha != 1.f && j > 0);
@@ -362,7 +420,7 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
         alpha_sh[r] = alpha;
         group_sync(0);
         const int jp = j - 1;
-        if (!wait_or_abort(&pv_done[jp & 1], (jp >> 1) & 1, abort_flag)) {
+        if (!wait_fast(&pv_done[jp & 1], (jp >> 1) & 1, abort_flag)) {
           // the failure is caught by the next group_any
         }
         umma::fence_after_sync();
@@ -383,7 +441,7 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
         group_sync(0);                              // alpha_sh reused next tile
       }
       // P row -> P operand buffer (free once the PV two tiles back is done)
-      if (u2 > 0 && !wait_or_abort(&pv_done[b2], (u2 - 1) & 1, abort_flag)) { /* caught below */ }
+      if (u2 > 0 && !wait_fast(&pv_done[b2], (u2 - 1) & 1, abort_flag)) { /* caught below */ }
       uint8_t* prow = pop + b2 * C::POP + r * 128;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8)
@@ -393,12 +451,14 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       umma::fence_before_sync();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&p_full[b2]);
+      if (r == 0) PF_TRACE(8 * j + 5);
       if (*abort_flag) { failed = true; }
       if (group_any(0, failed)) { failed = true; break; }
     }
     l_sh[r] = failed ? 0.f : l;
     group_sync(0);
     // ------------------------------------------------------------ epilogue
+    if (r == 0) PF_TRACE(1010);
     if (!failed && nkv > 0) {
       const int jl = nkv - 1;
       const bool ok = wait_or_abort(&pv_done[jl & 1], (jl >> 1) & 1, abort_flag);
@@ -432,11 +492,12 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
     // --------------------------------------------------------- preparation
     const int pt = tid - 192;
     const int kr = pt >> 1, hh = pt & 1;          // key row of the tile, half of the head dim
+    const float vfac = pow2i(-kp);                // keeps p * v_scale inside f16's range
     bool failed = false;
     for (int j = 0; j < nkv && !failed; ++j) {
-      const int s = j % C::NS, u = j / C::NS, b2 = j & 1, u2 = j >> 1;
-      bool ok = wait_or_abort(&full[s], u & 1, abort_flag);
-      if (u2 > 0) ok = ok && wait_or_abort(&pv_done[b2], (u2 - 1) & 1, abort_flag);
+      const int s = j % C::NS, u = j / C::NS, ob = j % C::NOP, ou = j / C::NOP;
+      bool ok = wait_fast(&full[s], u & 1, abort_flag);
+      if (ou > 0) ok = ok && wait_fast(&op_free[ob], (ou - 1) & 1, abort_flag);
       if (group_any(1, !ok)) { failed = true; break; }
       const uint8_t* st = ring + s * C::STAGE;
       const float* kss = reinterpret_cast<const float*>(st + 2 * C::CODES);
@@ -446,7 +507,7 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
 #pragma unroll
       for (int side = 0; side < 2; ++side) {
         const uint8_t* codes = st + side * C::CODES + kr * 128;
-        uint8_t* dst = (side == 0 ? kf : vf) + b2 * C::OPT + hh * (kPfKeys * 128) + kr * 128;
+        uint8_t* dst = (side == 0 ? kf : vf) + ob * C::OPT + hh * (kPfKeys * 128) + kr * 128;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {           // 16 codes -> two 16-byte f16 chunks
           const int ch = 4 * hh + cc;
@@ -468,15 +529,16 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
         }
       }
       if (pt < kPfKeys) {
-        float* cc2 = cols + b2 * 2 * kPfKeys;
+        float* cc2 = cols + ob * 2 * kPfKeys;
         const bool ok2 = t0 + pt < kv_end;
         cc2[pt] = ok2 ? kss[pt] * p.scale_log2 : 0.f;
-        cc2[kPfKeys + pt] = ok2 ? vss[pt] : 0.f;
+        cc2[kPfKeys + pt] = ok2 ? vss[pt] * vfac : 0.f;
       }
       umma::fence_proxy_async_smem();
       __syncwarp();
+      if (pt == 0) PF_TRACE(8 * j + 3);
       if (lane == 0) {
-        umma::mbar_arrive(&op_full[b2]);
+        umma::mbar_arrive(&op_full[ob]);
         umma::mbar_arrive(&empty[s]);
       }
     }
@@ -485,7 +547,15 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
   __syncthreads();
   umma::fence_after_sync();
   if (warp == 1) umma::tmem_dealloc(tmem, 256);
+  if (tid == 0) PF_TRACE(1021);
 }
+
+#ifdef FP8KV_TRACE
+extern "C" __attribute__((visibility("default"))) int fp8kv_trace_read_prefill(unsigned long long* out, int n) {
+  if (n > 1024) n = 1024;
+  return cudaMemcpyFromSymbol(out, g_pf_trace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, int batch, cudaStream_t st) {
   constexpr int smem = PfTcCfg::BYTES;

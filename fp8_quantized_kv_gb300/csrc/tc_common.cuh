@@ -38,6 +38,12 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
+// 2^x with results below 2^-126 flushed to zero.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float warp_max_redux(float x) {
   float r;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(x));
@@ -70,6 +76,23 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
+// As wait_or_abort, but each poll resumes as soon as the phase completes
+// (no suspend-time hint): for hand-offs on the critical path of a pipeline.
+__device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (umma::mbar_try_wake(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    if (umma::mbar_try_wake(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // OR of `pred` over the 128 threads of softmax warpgroup `wg` (named barrier
 // 1 + wg), and a plain barrier over the same threads.
 __device__ __forceinline__ bool group_any(int wg, bool pred) {
@@ -85,6 +108,62 @@ __device__ __forceinline__ bool group_any(int wg, bool pred) {
   return r != 0;
 }
 __device__ __forceinline__ void group_sync(int wg) { asm volatile("bar.sync %0, 128;\n" ::"r"(1 + wg) : "memory"); }
+
+// ------------------------------------------------------------- clusters --
+// Cluster-wide barrier, split into arrive and wait (acquire).  Arrive is
+// relaxed: used after fence.mbarrier_init, when the only thing to publish is
+// the initialisation of barriers that other CTAs will signal.  A thread that
+// arrives once and never again need not wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;\n" ::: "memory"); }
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t saddr, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(ra) : "r"(saddr), "r"(rank));
+  return ra;
+}
+// 16-byte store into another CTA's shared memory; completes 16 bytes of the
+// transaction count of the mbarrier `rbar` in that CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];\n"
+               ::"r"(raddr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar)
+               : "memory");
+}
+// Bounded wait (as wait_fast) with cluster-scope acquire: for data that other
+// CTAs of the cluster delivered with st.async.
+__device__ __forceinline__ bool mbar_try_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done)
+      : "r"(umma::smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_cluster(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
 
 // Two E4M3 codes (low byte element 0) -> f16x2, exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {

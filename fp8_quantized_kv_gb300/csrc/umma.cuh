@@ -156,6 +156,20 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// The same poll without a suspend-time hint: the hardware's own limit
+// applies and the thread resumes as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wake(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Non-blocking test of the phase with the given parity.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t done;

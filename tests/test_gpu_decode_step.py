@@ -94,7 +94,9 @@ def test_step_ragged_splits_and_empty(dtype, kernel):
     lens = (0, 1, 2, 127, 128, 129, 300, 1000, 17, 256)
     spec = synth.DecodeWorkload("ragged_step", len(lens), 8, 1, 128, seed=25, seq_lens=lens)
     inp = synth.decode_inputs(spec, device="cuda")
-    for ns in (0, 1, 3):
+    # 2..8 splits: the tensor-core step merges inside a thread-block cluster;
+    # more splits (12, and the automatic count here): through global partials
+    for ns in (0, 1, 2, 3, 8, 12):
         cache, out, _, _ = _run(inp, dtype, kernel, num_splits=ns, capacity=1024)
         o = out.cpu().numpy()
         assert np.all(o[0] == 0)
@@ -113,3 +115,24 @@ def test_step_paged(kernel):
                                out_dtype=torch.float32, kernel=kernel)
     assert_gate(out.cpu().numpy(), oracle_decode(inp, "k8v8", range(6)), f"step paged {kernel}")
     assert fk.fp8kv_get_device_error() == 0
+
+
+def test_step_split_invariance_cluster_and_global_merge():
+    """The fused tensor-core step at 1 split (no merge), 2-8 splits (merge in
+    a thread-block cluster) and 12-16 splits (merge through global partials)
+    agrees within the split-merge bar of 1e-5 relative."""
+    spec = synth.DecodeWorkload("inv_step", 4, 16, 2, 128, seed=29, seq_lens=(4096, 3000, 2049, 1))
+    inp = synth.decode_inputs(spec, device="cuda")
+    prev, knew, vnew = _split_last_token(inp)
+    q = inp.q.cuda().contiguous()
+    lens = inp.seq_lens.cuda()
+    outs = {}
+    for ns in (1, 2, 4, 5, 8, 12, 16):
+        cache = fill_cache(prev, "k8v8", capacity=4096)
+        outs[ns] = fk.fp8kv_decode_step(q, knew, vnew, cache, lens, num_splits=ns, out_dtype=torch.float32,
+                                        kernel="tensor_cores").double()
+    assert fk.fp8kv_get_device_error() == 0
+    ref = outs[1]
+    for ns, o in outs.items():
+        rel = ((o - ref).norm(dim=-1) / ref.norm(dim=-1)).max().item()
+        assert rel <= 1e-5, (ns, rel)
