@@ -40,7 +40,7 @@ KERNEL_IDS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
 PAGE_NUMBER_GBS = 550.0   # the pages' figure for this workload (RTX 5070 Ti, Triton, codes only)
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=4000)
@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--kernel", default="auto", choices=["auto", "cuda_cores", "tensor_cores"])
     ap.add_argument("--no-controls", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ------------------------------------------------------------ distributed --
@@ -85,6 +85,14 @@ def max_over_ranks(x, ws):
     t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(bytes_per_step, steps, local_ms, ws):
+    """Whole-job figure of the timed region: the slowest rank's time, and the
+    bytes every rank processed (each rank runs its own copy of the workload:
+    weak scaling) per second of that time, in GB/s."""
+    t_max = max_over_ranks(local_ms, ws)
+    return t_max, ws * bytes_per_step * steps / (t_max * 1e-3) / 1e9
 
 
 # ----------------------------------------------------------------- bytes --
@@ -449,10 +457,9 @@ def run_gpu(args, ws, rank):
     time.sleep(0.3)
 
     layers, dev, total_ms, per, wall = measure_variant(spec, args.dtype, args, ws, inp)
-    t_max = max_over_ranks(total_ms, ws)
     nb = step_bytes(spec, args.dtype, T)
+    t_max, value = aggregate(nb["step"], args.steps, total_ms, ws)
     ms_per_step = t_max / args.steps
-    value = ws * nb["step"] * args.steps / (t_max * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
     clocks = sampler.summary(*wall)
 
@@ -461,8 +468,7 @@ def run_gpu(args, ws, rank):
     out_h = torch.empty((spec.batch, spec.q_heads, spec.head_dim), dtype=torch.bfloat16).pin_memory()
     e2e_ms, h2d, d2h = e2e_run(layers, {"dev": dev, "pinned": pinned, "out": out_h}, args.steps, args.warmup,
                                KERNEL_IDS[args.kernel])
-    e2e_ms = max_over_ranks(e2e_ms, ws)
-    e2e_val = ws * nb["step"] * args.steps / (e2e_ms * 1e-3) / 1e9
+    e2e_ms, e2e_val = aggregate(nb["step"], args.steps, e2e_ms, ws)
     sampler.stop()
 
     tensor = args.kernel in ("auto", "tensor_cores")
