@@ -127,11 +127,14 @@ __device__ unsigned long long g_cta_time[4096][8];   // start, end, published, l
 // merging threads (warps 2-5, thread t = dim t of the partial) of every CTA;
 // `stage` is [8][128] floats of this CTA's shared memory that is idle now.
 __device__ __forceinline__ int g4_lo(int r, int S) { return (32 * r) / S; }
+// Owner rank of four-dim group q: the largest r with g4_lo(r, S) <= q, i.e.
+// floor(32 r / S) <= q  <=>  r < (q + 1) S / 32.
+__device__ __forceinline__ int g4_owner(int q, int S) { return ((q + 1) * S - 1) >> 5; }
 
 __device__ __noinline__ void cluster_exchange(const DecodeParams& p, float* rx_ml, float* rx_o, uint64_t* rx_bar,
-                                              float* stage, const float (&Og)[8], const float (&Mg)[8],
-                                              const float (&Lg)[8], int b, int h, int G, int t,
-                                              volatile int* abort) {
+                                              const int* slice, float* stage, const float (&Og)[8],
+                                              const float (&Mg)[8], const float (&Lg)[8], int b, int h, int G,
+                                              int t, volatile int* abort) {
   constexpr int D = 128;
   const int S = p.num_splits;
   const int k = (int)cluster_rank();
@@ -144,11 +147,8 @@ __device__ __noinline__ void cluster_exchange(const DecodeParams& p, float* rx_m
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int c = t + 128 * j, g = c >> 5, q = c & 31;   // head g, four-dim group q
-    int r = 0;
-#pragma unroll
-    for (int u = 1; u < 8; ++u)
-      if (u < S && g4_lo(u, S) <= q) r = u;
-    const int lo = g4_lo(r, S), n4 = g4_lo(r + 1, S) - lo;
+    const int r = g4_owner(q, S);
+    const int lo = slice[r], n4 = slice[r + 1] - lo;
     const float4 v = *reinterpret_cast<const float4*>(stage + g * D + 4 * q);
     st_async_v4(mapa_u32(umma::smem_u32(rx_o + 4 * ((k * 8 + g) * n4 + (q - lo))), (uint32_t)r), v,
                 mapa_u32(umma::smem_u32(rx_bar), (uint32_t)r));
@@ -168,9 +168,12 @@ __device__ __noinline__ void cluster_exchange(const DecodeParams& p, float* rx_m
     if (t == 0) raise_error(p.err, FP8KV_DEVERR_TIMEOUT);
     return;
   }
-  const int mlo = g4_lo(k, S), m4 = g4_lo(k + 1, S) - mlo;
+  const int mlo = slice[k], m4 = slice[k + 1] - mlo;
   if (t < 8 * m4) {
-    const int g = t / m4, j = t - g * m4;
+    int g = 0;          // t / m4 without a division: m4 <= 16, t < 128
+#pragma unroll
+    for (int u = 1; u < 8; ++u) g += t >= u * m4;
+    const int j = t - g * m4;
     float M = -INFINITY;
     for (int kk = 0; kk < S; ++kk) M = fmaxf(M, rx_ml[kk * 16 + g]);
     float L = 0.f;
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
   float* red = qscale + 8;                                 // [wg][2][4][9]
   float* lred = red + 144;                                 // [wg][4][8]
   float* xml = lred + 64;                                  // [16]: m and l of warpgroup 1
+  int* slice_tab = reinterpret_cast<int*>(misc + 1472);    // [9] first four-dim group of each rank
   float* rx_ml = reinterpret_cast<float*>(misc + 1536);    // [sender][m 8 | l 8]
   float* rx_o = reinterpret_cast<float*>(misc + 2048);     // [sender][dim of this rank's slice][8 heads]
 
@@ -260,6 +264,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         umma::mbar_init(rx_bar, 1);
         tma::arrive_expect_tx(rx_bar, cluster_rx_bytes((int)cluster_rank(), S));
         umma::mbar_fence_init();
+        for (int r = 0; r <= S; ++r) slice_tab[r] = g4_lo(r, S);
       }
       __syncthreads();
       cluster_arrive_relaxed();
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         float Og[8], Mg[8], Lg[8];
 #pragma unroll
         for (int g = 0; g < 8; ++g) { Og[g] = 0.f; Mg[g] = -INFINITY; Lg[g] = 0.f; }
-        cluster_exchange(p, rx_ml, rx_o, rx_bar, xo, Og, Mg, Lg, b, h, G, tid - 64, abort_flag);
+        cluster_exchange(p, rx_ml, rx_o, rx_bar, slice_tab, xo, Og, Mg, Lg, b, h, G, tid - 64, abort_flag);
       }
       return;
     }
@@ -354,10 +359,15 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
   };
   const int n_first = min(min(n_tiles, C::NST), i_new);
   if (tid == 0) {
+    // the ring's barriers first, so the first loads go out as early as possible
     for (int i = 0; i < C::NST; ++i) {
       umma::mbar_init(&full[i], 1);
       umma::mbar_init(&empty[i], 1 + 4);     // PV commit + the four warps of the owning group
     }
+    *abort_flag = 0;
+    *last_flag = 0;
+    umma::mbar_fence_init();
+    for (int i = 0; i < n_first; ++i) produce(i);
     for (int w = 0; w < 2; ++w)
       for (int i = 0; i < 2; ++i) {
         umma::mbar_init(&wb[w].s_full[i], 1);
@@ -370,13 +380,9 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
     if (p.cluster) {
       umma::mbar_init(rx_bar, 1);
       tma::arrive_expect_tx(rx_bar, cluster_rx_bytes(split, S));
+      for (int r = 0; r <= S; ++r) slice_tab[r] = g4_lo(r, S);
     }
-    *abort_flag = 0;
-    *last_flag = 0;
     umma::mbar_fence_init();
-    tma::prefetch_map(&tp.tmk);
-    tma::prefetch_map(&tp.tmv);
-    for (int i = 0; i < n_first; ++i) produce(i);
   }
   if (warp == 1) {
     umma::tmem_alloc(tslot, 512);
@@ -428,10 +434,12 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
     if (warp >= 2 && warp < 6) cluster_wait();
   }
 
-  if (appender && warp == 6) {
+  if (appender && warp == 0) {
     // Quantise and write the new token's K and V rows (the arithmetic of
     // fp8kv_append: amax/448 with IEEE division, RNE saturating encode),
-    // then publish them to the TMA loads of the producer.
+    // then publish them to the TMA loads of the producer.  The producer warp
+    // does it: its first loads are in flight and no ring slot frees up for
+    // a few microseconds, while the softmax warps start on the first tiles.
     const int tpos = T - 1;
     const int64_t row = cache_row(c, b, h, tpos, lane == 0 ? p.err : nullptr);
     if (row >= 0) {
@@ -764,7 +772,6 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
     asm volatile("bar.sync 3, 256;\n" ::: "memory");
     if (t == 0 && wg == 0) TRACE(1011);
     if (wg == 0) {
-      const int n_busy = (tiles + p.chunk_tiles - 1) / p.chunk_tiles;   // splits with work
       float Mg[8], Lg[8], Og[8];
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
@@ -777,8 +784,10 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         Lg[g] = l_tot[g] * f0 + l1 * f1;
       }
       if (t == 0) TRACE(1001);
+      // splits with work (only the global-memory merge needs it)
+      const int n_busy = p.cluster ? 0 : (tiles + p.chunk_tiles - 1) / p.chunk_tiles;
       if (p.cluster) {
-        cluster_exchange(p, rx_ml, rx_o, rx_bar, xo, Og, Mg, Lg, b, h, G, t, abort_flag);
+        cluster_exchange(p, rx_ml, rx_o, rx_bar, slice_tab, xo, Og, Mg, Lg, b, h, G, t, abort_flag);
       } else if (p.fused && n_busy == 1) {
         // the only split of this sequence: normalise and write the output
 #pragma unroll
