@@ -52,6 +52,8 @@ def parse(argv=None):
     ap.add_argument("--kernel", default="auto", choices=["auto", "cuda_cores", "tensor_cores"])
     ap.add_argument("--no-controls", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-steps", type=int, default=200)
+    ap.add_argument("--no-prefill", action="store_true")
     return ap.parse_args(argv)
 
 
@@ -187,6 +189,23 @@ def hbm_peak():
     except (OSError, ValueError, TypeError):
         pass
     return 6800.0, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 tensor-core peak in TFLOP/s (f16 runs at the same rate):
+    the burst figure of MEASURED_PEAKS.json when present, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("bf16_tflops", "bf16_TFLOPs", "bf16"):
+            if key in d:
+                v = d[key]
+                v = v.get("value") if isinstance(v, dict) else v
+                return float(v), "measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return 1900.0, "fallback"
 
 
 def kernel_source_sha():
@@ -435,6 +454,60 @@ def e2e_run(layers, host, K, W, kernel):
     return st.elapsed_time(en), h2d, d2h
 
 
+def measure_prefill(args, ws):
+    """Causal prefill of the 2048-token, 28 q / 4 KV head workload over a K8/V8
+    cache (tensor-core kernel).  Eight independent copies (Q, cache, output:
+    ~250 MB, above L2) are rotated; the timed region is `args.prefill_steps`
+    launches between CUDA events on the launching stream."""
+    import fp8_quantized_kv_gb300 as fk
+    spec = synth.PREFILL_WORKLOADS["prefill_2048"]
+    n, Hq, Hkv, D = spec.n_tokens, spec.q_heads, spec.kv_heads, spec.head_dim
+    pin = synth.prefill_inputs(spec, device="cuda")
+    sets = []
+    for _ in range(8):
+        cache = fk.Fp8KVCache.contiguous(1, Hkv, D, n, "k8v8")
+        fk.fp8kv_append(cache, pin.k.contiguous(), pin.v.contiguous(),
+                        torch.zeros(n, dtype=torch.int32, device="cuda"),
+                        torch.arange(n, dtype=torch.int32, device="cuda"))
+        q = pin.q[None].contiguous().clone()
+        out = torch.empty(1, n, Hq, D, dtype=torch.bfloat16, device="cuda")
+        sets.append((cache, q, out))
+    p0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def run(i):
+        cache, q, out = sets[i % len(sets)]
+        fk.fp8kv_prefill_attention(q, cache, p0, out=out, kernel="tensor_cores", stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        run(i)
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K = args.prefill_steps
+    e0.record(stream)
+    for i in range(K):
+        run(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    if fk.fp8kv_get_device_error() != 0:
+        raise RuntimeError("prefill raised a device error")
+    flops = 4.0 * D * Hq * n * (n + 1) / 2
+    t_max, _ = aggregate(0, K, e0.elapsed_time(e1), ws)
+    us = t_max / K * 1e3
+    achieved = flops / (us * 1e-6) / 1e12
+    peak, kind = tensor_peak()
+    return {"workload": "prefill_2048", "batch": 1, "tokens": n, "q_heads": Hq, "kv_heads": Hkv,
+            "head_dim": D, "cache": "k8v8", "kernel": "prefill_tc", "launches": K,
+            "us_per_launch": us, "value": ws * achieved, "unit": "TFLOP/s",
+            "l2": "8 input sets rotated (~250 MB, above L2)",
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_kind": f"{kind} (dense bf16; f16 operands run at the same rate)",
+                         "traffic": None, "algorithmic_flops_per_launch": flops}}
+
+
 def measure_variant(spec, dtype, args, ws, inp):
     layers, dev = build_layers(spec, dtype, args.layers, inp, KERNEL_IDS[args.kernel])
     for i in range(max(3, args.warmup)):                      # eager warm-up steps
@@ -506,6 +579,8 @@ def run_gpu(args, ws, rank):
             del ls
             torch.cuda.empty_cache()
 
+    prefill = None if args.no_prefill else measure_prefill(args, ws)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         host_inp = synth.decode_inputs(spec, device="cpu", seq_lens=[T] * 8)
@@ -532,7 +607,7 @@ def run_gpu(args, ws, rank):
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": (1 if tensor else 3) * args.steps,
             "kernels_us": None if per is None else {k.replace("_ms", "_us"): v * 1e3 for k, v in per.items()},
-            "clocks": clocks, "controls": controls,
+            "clocks": clocks, "controls": controls, "prefill": prefill,
         }
         print(json.dumps(line), flush=True)
 

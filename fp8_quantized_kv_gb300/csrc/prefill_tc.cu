@@ -6,7 +6,7 @@
 // running max m, sum l and an O accumulator; a key is valid for the query at
 // position qp iff key <= qp.  FP8 numerics of "FP8 KV cache (fp8_kv, opt-in)",
 // bullet "Math": the K scale folds into the scores and the V scale into P,
-// which is rounded to bf16 before P.V.
+// which is rounded to a 16-bit operand before P.V.
 //
 // A CTA owns 128 query rows (two 64-token query tiles: the full-rate tcgen05
 // shape is M = 128) of one query head, and walks the KV tiles of that head's
@@ -16,24 +16,31 @@
 //     sm_scale, causal mask (diagonal tiles only), running max with lazy
 //     rescale, p = 2^(s - m), l += p, P' = p * v_scale
 //   O^T[128 x 128] += V^T . P'^T         tcgen05.mma kind::f16 -> TMEM
+// Two softmax warpgroups take alternate KV tiles (even, odd), each with its
+// own running (m, l) and its own O accumulator, so the softmax of two tiles
+// runs at once; the two states are combined per row in the epilogue, as two
+// flash-decoding splits are.
 // Operands are f16: the e4m3 K and V codes convert to f16 exactly
 // (cvt.rn.f16x2.e4m3x2); each bf16 query row is scaled by a power of two
 // (exact) into f16's range.  P' is rounded once, to the 16-bit operand of the
-// P.V product as the method asks, but to f16 (11-bit significand, 8x finer
-// than bf16) after one power-of-two scaling per CTA chosen from the largest V
-// scale it will see.  All those scalings are undone in fp32.
+// P.V product, as f16 (11-bit significand, 8x finer than bf16; the page's own
+// prefill keeps its probabilities in f16, section 2.4) after one power-of-two
+// scaling per CTA chosen from the largest V scale it will see.  All those
+// scalings are undone in fp32.
 //
 // Warp roles:
-//   warp 0     TMA producer: e4m3 code tiles (64 keys x 128 B, 128-byte
-//              swizzle) and 1-D bulk copies of the scale rows into a ring.
-//   warp 1     TMEM owner and MMA issuer: QK of tile j, then PV of tile j-1.
-//   warps 2-5  softmax, one query row per thread; the output epilogue.
-//   warps 6-9  preparation: codes -> f16 operand tiles (K-major K, MN-major
-//              V; same physical layout), per-key scales; V rows past the
-//              causal end zeroed (0 * NaN would poison P.V).
-// The f16 K/V operands, S (TMEM) and P (shared memory) are double-buffered.
-// O is rescaled in TMEM only when a row's maximum grows by more than 2^8
-// (then P stays <= 2^8 relative to the stale maximum).  Every wait is
+//   warp 0      TMA producer: e4m3 code tiles (64 keys x 128 B, 128-byte
+//               swizzle) and 1-D bulk copies of the scale rows into a ring.
+//   warp 1      TMEM owner and MMA issuer: an event loop issuing each QK
+//               and each PV as soon as its operands are ready.
+//   warps 2-5   softmax of the even tiles, warps 6-9 of the odd tiles (one
+//               query row per thread); then the output epilogue.
+//   warps 10-13 preparation: codes -> f16 operand tiles (K-major K, MN-major
+//               V; same physical layout), per-key scales; V rows past the
+//               causal end zeroed (0 * NaN would poison P.V).
+// TMEM: S of each group double-buffered (4 x 64 columns), one O^T per group
+// (2 x 128).  O is rescaled in TMEM only when a row's maximum grows by more
+// than 2^8 (then P stays <= 2^8 relative to the stale maximum).  Every wait is
 // bounded; a timeout raises FP8KV_DEVERR_TIMEOUT.
 #include "params.cuh"
 #include "tc_common.cuh"
@@ -42,18 +49,19 @@ namespace fp8kv {
 
 constexpr int kPfRows = 128;   // query rows per CTA
 constexpr int kPfKeys = 64;    // keys per KV tile
+constexpr int kPfThreads = 448;
 
 struct PfTcCfg {
   static constexpr int D = 128;
   static constexpr int QOP = kPfRows * D * 2;                 // [2 atoms][128 rows][128 B] f16
   static constexpr int CODES = kPfKeys * D;                    // e4m3 tile [64][128]
   static constexpr int STAGE = ((2 * CODES + 2 * kPfKeys * 4) + 1023) / 1024 * 1024;
-  static constexpr int NS = 2;                                 // e4m3 code stages
+  static constexpr int NS = 3;                                 // e4m3 code stages
   static constexpr int NOP = 3;                                // f16 K/V operand buffers
   static constexpr int OPT = kPfKeys * D * 2;                 // f16 K or V tile [2 atoms][64][128 B]
-  static constexpr int POP = kPfRows * kPfKeys * 2;           // f16 P [128 rows][128 B]
+  static constexpr int POP = kPfRows * kPfKeys * 2;           // f16 P [128 rows][128 B], one per group
   static constexpr int COLS = 2 * kPfKeys * 4;                 // per buffer: k and v column scales
-  static constexpr int MISC = 2048;
+  static constexpr int MISC = 4096;
   static constexpr int BYTES = QOP + NS * STAGE + 2 * NOP * OPT + 2 * POP + NOP * COLS + MISC + 1024;
   static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
@@ -80,7 +88,21 @@ struct PrefillTmaParams {
   PrefillParams p;
 };
 
-__global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ PrefillTmaParams tp) {
+// OR of `pred` over the 256 softmax threads (named barrier 3).
+__device__ __forceinline__ bool pair_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 3, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constant__ PrefillTmaParams tp) {
   using C = PfTcCfg;
   constexpr int D = 128;
   const PrefillParams& p = tp.p;
@@ -90,24 +112,25 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
   uint8_t* ring = qop + C::QOP;
   uint8_t* kf = ring + C::NS * C::STAGE;          // [NOP] f16 K operand
   uint8_t* vf = kf + C::NOP * C::OPT;             // [NOP] f16 V operand
-  uint8_t* pop = vf + C::NOP * C::OPT;            // [2] f16 P operand
+  uint8_t* pop = vf + C::NOP * C::OPT;            // [group] f16 P operand
   float* cols = reinterpret_cast<float*>(pop + 2 * C::POP);   // [NOP][k 64 | v 64]
   uint8_t* misc = reinterpret_cast<uint8_t*>(cols + C::NOP * 2 * kPfKeys);
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);        // [NS] codes landed
   uint64_t* empty = full + C::NS;                             // [NS] codes consumed by the prep warps
   uint64_t* op_full = empty + C::NS;                          // [NOP] f16 K/V operands + scales ready
   uint64_t* op_free = op_full + C::NOP;                       // [NOP] PV of the buffer's tile finished
-  uint64_t* s_full = op_free + C::NOP;                        // [2]
-  uint64_t* s_free = s_full + 2;                              // [2]
-  uint64_t* p_full = s_free + 2;                              // [2]
-  uint64_t* pv_done = p_full + 2;                             // [2] PV of the P buffer's tile finished
+  uint64_t* s_full = op_free + C::NOP;                        // [group][2]
+  uint64_t* s_free = s_full + 4;                              // [group][2]
+  uint64_t* p_full = s_free + 4;                              // [group]
+  uint64_t* pv_done = p_full + 2;                             // [group] PV of the group's last tile finished
   uint64_t* drained = pv_done + 2;                            // final commit of the MMA issuer
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drained + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   int* kp_sh = const_cast<int*>(abort_flag) + 1;
-  float* alpha_sh = reinterpret_cast<float*>(misc + 256);     // [128]
-  float* l_sh = alpha_sh + kPfRows;                           // [128]
-  float* vmax_sh = l_sh + kPfRows;                            // [4]
+  float* alpha_sh = reinterpret_cast<float*>(misc + 256);     // [group][128]
+  float* m_sh = reinterpret_cast<float*>(misc + 1280);        // [group][128] final reference maxima
+  float* l_sh = reinterpret_cast<float*>(misc + 2304);        // [group][128] final row sums
+  float* vmax_sh = reinterpret_cast<float*>(misc + 3328);     // [4]
 
   const int qt = gridDim.x - 1 - blockIdx.x;      // longest causal range first
   const int hq = blockIdx.y, b = blockIdx.z;
@@ -168,60 +191,58 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       umma::mbar_init(&full[i], 1);
       umma::mbar_init(&empty[i], 4);
     }
+    *abort_flag = 0;
+    umma::mbar_fence_init();
+    for (int j = 0; j < n_first; ++j) produce(j);
     for (int i = 0; i < C::NOP; ++i) {
       umma::mbar_init(&op_full[i], 4);
       umma::mbar_init(&op_free[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       umma::mbar_init(&s_full[i], 1);
       umma::mbar_init(&s_free[i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
       umma::mbar_init(&p_full[i], 4);
       umma::mbar_init(&pv_done[i], 1);
     }
     umma::mbar_init(drained, 1);
-    *abort_flag = 0;
     umma::mbar_fence_init();
-    tma::prefetch_map(&tp.tmk);
-    tma::prefetch_map(&tp.tmv);
-    for (int j = 0; j < n_first; ++j) produce(j);
   }
   if (warp == 1) {
-    umma::tmem_alloc(tslot, 256);
+    umma::tmem_alloc(tslot, 512);
     umma::tmem_relinquish();
   }
   // softmax warps: this thread's query row -> f16 Q operand, row scale 2^kq
+  // (both groups compute the row's scale; each writes one 64-dim atom)
   const int r = 32 * (warp & 3) + lane;           // query row (softmax warps) / TMEM lane
+  const int wg = (warp - 2) >> 2;                 // softmax group: tiles j with j % 2 == wg
   const int qi = i0 + r;
   const int qpos = qi < p.n_q ? pos0 + qi : -1;
   int kq = 0;
-  if (warp >= 2 && warp < 6) {
-    uint4 raw[16];
-    if (qi < p.n_q) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.n_q + qi) * p.q_heads + hq) * D);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) raw[k] = src[k];
-    } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) raw[k] = make_uint4(0, 0, 0, 0);
-    }
+  if (warp >= 2 && warp < 10) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.n_q + (qi < p.n_q ? qi : 0)) * p.q_heads + hq) * D);
+    uint4 mine[8];
     float amax = 0.f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+      const uint4 w = qi < p.n_q ? src[k] : make_uint4(0, 0, 0, 0);
+      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         float f2[2];
         bf16x2_to_f32(w4[u], f2);
         amax = fmaxf(amax, fmaxf(fabsf(f2[0]), fabsf(f2[1])));
       }
+      if ((k >> 3) == wg) mine[k & 7] = w;
     }
     int e = 0;
     (void)frexpf(amax * (1.0f / 16384.0f), &e);   // row max -> [2^13, 2^14): inside f16's normal range
     kq = max(-100, min(100, e));
     const float qsc = pow2i(-kq);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {                 // 8 elements (one 16-byte f16 chunk) each
-      const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+    for (int ch = 0; ch < 8; ++ch) {               // 8 elements (one 16-byte f16 chunk) each
+      const uint32_t w4[4] = {mine[ch].x, mine[ch].y, mine[ch].z, mine[ch].w};
       uint32_t h[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -230,15 +251,14 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
         const __half2 hv = __floats2half2_rn(f2[0] * qsc, f2[1] * qsc);
         h[u] = *reinterpret_cast<const uint32_t*>(&hv);
       }
-      const int atom = k >> 3, ch = k & 7;
-      *reinterpret_cast<uint4*>(qop + atom * (kPfRows * 128) + r * 128 + ((ch ^ (r & 7)) << 4)) =
+      *reinterpret_cast<uint4*>(qop + wg * (kPfRows * 128) + r * 128 + ((ch ^ (r & 7)) << 4)) =
           make_uint4(h[0], h[1], h[2], h[3]);
     }
   }
   // prep warps: one power of two for all of this CTA's P (from the largest
   // V scale of its keys), so P' stays inside f16's range
-  if (warp >= 6) {
-    const int pt = tid - 192;
+  if (warp >= 10) {
+    const int pt = tid - 320;
     float vm = 0.f;
     for (int base = 0; base < kv_end; base += 8 * 128) {   // 8 independent loads in flight
       float v8[8];
@@ -252,8 +272,8 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       for (int u = 0; u < 8; ++u) vm = fmaxf(vm, v8[u]);
     }
     vm = warp_max_redux(vm);
-    if (lane == 0) vmax_sh[warp - 6] = vm;
-    asm volatile("bar.sync 2, 128;\n" ::: "memory");
+    if (lane == 0) vmax_sh[warp - 10] = vm;
+    asm volatile("bar.sync 4, 128;\n" ::: "memory");
     if (pt == 0) {
       const float v = fmaxf(fmaxf(vmax_sh[0], vmax_sh[1]), fmaxf(vmax_sh[2], vmax_sh[3]));
       int e = 0;
@@ -287,44 +307,65 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       constexpr uint32_t ID_QK = umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_K, umma::MAJOR_K, 128, 64);
       constexpr uint32_t ID_PV = umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_MN, umma::MAJOR_K, 128, 128);
       const uint32_t qa = umma::smem_u32(qop);
-      // QK of tile j+1 goes out before PV of tile j, so the tensor core works
-      // on the next scores while the softmax warps turn tile j into P
-      auto qk = [&](int j) -> bool {
-        const int b2 = j & 1, u2 = j >> 1, ob = j % C::NOP, ou = j / C::NOP;
-        if (!wait_fast(&op_full[ob], ou & 1, abort_flag)) return false;
-        if (u2 > 0 && !wait_fast(&s_free[b2], (u2 - 1) & 1, abort_flag)) return false;
-        umma::fence_after_sync();
-        PF_TRACE(8 * j + 1);
-        const uint32_t ka = umma::smem_u32(kf + ob * C::OPT);
+      // tile j: group w = j % 2, its local index lj = j / 2, S buffer lj % 2.
+      // Event loop: issue whichever of the next QK and the next PV is ready
+      // (non-blocking tests), so neither waits behind the other: a PV goes
+      // out as soon as its P lands, which frees the f16 operand buffer the
+      // preparation warps need next.
+      int nq = 0, np = 0;
+      long long t_idle = 0;
+      uint32_t idle = 0;
+      while (np < nkv) {
+        bool prog = false;
+        if (nq < nkv) {
+          const int j = nq, w = j & 1, lj = j >> 1, bb = lj & 1, ub = lj >> 1, ob = j % C::NOP, ou = j / C::NOP;
+          if (umma::mbar_test(&op_full[ob], ou & 1) &&
+              (ub == 0 || umma::mbar_test(&s_free[2 * w + bb], (ub - 1) & 1))) {
+            umma::fence_after_sync();
+            PF_TRACE(8 * j + 1);
+            const uint32_t ka = umma::smem_u32(kf + ob * C::OPT);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma::mma_f16_ss(tmem + 64 * b2,
-                           umma::sdesc(qa + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
-                           umma::sdesc(ka + (kk >> 2) * (kPfKeys * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
-                           ID_QK, kk > 0);
-        umma::mma_commit(&s_full[b2]);
-        return true;
-      };
-      auto pv = [&](int j) -> bool {
-        const int b2 = j & 1, u2 = j >> 1, ob = j % C::NOP;
-        if (!wait_fast(&p_full[b2], u2 & 1, abort_flag)) return false;
-        umma::fence_after_sync();
-        PF_TRACE(8 * j + 2);
-        const uint32_t va = umma::smem_u32(vf + ob * C::OPT);
-        const uint32_t pa = umma::smem_u32(pop + b2 * C::POP);
+            for (int kk = 0; kk < 8; ++kk)
+              umma::mma_f16_ss(tmem + 64 * (2 * w + bb),
+                               umma::sdesc(qa + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
+                               umma::sdesc(ka + (kk >> 2) * (kPfKeys * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
+                               ID_QK, kk > 0);
+            umma::mma_commit(&s_full[2 * w + bb]);
+            ++nq;
+            prog = true;
+          }
+        }
+        if (np < nq) {
+          const int j = np, w = j & 1, lj = j >> 1, ob = j % C::NOP;
+          if (umma::mbar_test(&p_full[w], lj & 1)) {
+            umma::fence_after_sync();
+            PF_TRACE(8 * j + 2);
+            const uint32_t va = umma::smem_u32(vf + ob * C::OPT);
+            const uint32_t pa = umma::smem_u32(pop + w * C::POP);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma::mma_f16_ss(tmem + 128, umma::sdesc(va + kk * 2048, kPfKeys * 128, 1024, umma::SWIZZLE_128B),
-                           umma::sdesc(pa + kk * 32, 16, 1024, umma::SWIZZLE_128B), ID_PV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-        umma::mma_commit(&pv_done[b2]);
-        umma::mma_commit(&op_free[ob]);
-        return true;
-      };
-      if (qk(0)) {
-        for (int j = 0; j < nkv; ++j) {
-          if (j + 1 < nkv && !qk(j + 1)) break;
-          if (!pv(j)) break;
+            for (int kk = 0; kk < 4; ++kk)
+              umma::mma_f16_ss(tmem + 256 + 128 * w,
+                               umma::sdesc(va + kk * 2048, kPfKeys * 128, 1024, umma::SWIZZLE_128B),
+                               umma::sdesc(pa + kk * 32, 16, 1024, umma::SWIZZLE_128B), ID_PV,
+                               (lj > 0 || kk > 0) ? 1u : 0u);
+            umma::mma_commit(&pv_done[w]);
+            umma::mma_commit(&op_free[ob]);
+            ++np;
+            prog = true;
+          }
+        }
+        if (prog) {
+          idle = 0;
+          continue;
+        }
+        __nanosleep(20);     // the polling thread shares an SM sub-partition with softmax warps
+        if ((++idle & 63) == 0) {                    // bounded: give up after ~2 s without progress
+          if (idle == 64) t_idle = clock64();
+          if (*abort_flag) break;
+          if (clock64() - t_idle > kWaitLimitCycles) {
+            *abort_flag = 1;
+            break;
+          }
         }
       }
       // all issued MMAs complete before TMEM is released (matters only when
@@ -332,25 +373,30 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       umma::mma_commit(drained);
       (void)umma::mbar_wait(drained, 0, 100000000ull);
     }
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ------------------------------------------------------------- softmax
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float qsr = pow2i(kq);
     const int qpos_min = pos0 + i0;                 // smallest position among this CTA's queries
+    const int my_tiles = (nkv - wg + 1) >> 1;       // tiles j = 2 lj + wg < nkv
+    const uint32_t s_base = tmem + 64 * (2 * wg), o_base = tmem + 256 + 128 * wg;
+    float* my_alpha = alpha_sh + wg * kPfRows;
+    uint8_t* my_p = pop + wg * C::POP;
     float m_used = -INFINITY, l = 0.f;
     bool failed = false;
-    for (int j = 0; j < nkv; ++j) {
-      const int b2 = j & 1, u2 = j >> 1, ob = j % C::NOP;
-      bool ok = wait_fast(&s_full[b2], u2 & 1, abort_flag);
+    for (int lj = 0; lj < my_tiles; ++lj) {
+      const int j = 2 * lj + wg, bb = lj & 1, ub = lj >> 1, ob = j % C::NOP;
+      bool ok = wait_fast(&s_full[2 * wg + bb], ub & 1, abort_flag);
       ok = ok && wait_fast(&op_full[ob], (j / C::NOP) & 1, abort_flag);
-      if (group_any(0, !ok)) { failed = true; break; }
+      ok = ok && !*abort_flag;
+      if (group_any(wg, !ok)) { failed = true; break; }
       umma::fence_after_sync();
       if (r == 0) PF_TRACE(8 * j + 4);
       float sv[64];
       {
         uint32_t rr[4][16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) umma::tmem_ld16_nowait(tmem + 64 * b2 + 16 * k + lane_off, rr[k]);
+        for (int k = 0; k < 4; ++k) umma::tmem_ld16_nowait(s_base + 64 * bb + 16 * k + lane_off, rr[k]);
         umma::tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -359,7 +405,7 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       }
       umma::fence_before_sync();
       __syncwarp();
-      if (lane == 0) umma::mbar_arrive(&s_free[b2]);
+      if (lane == 0) umma::mbar_arrive(&s_free[2 * wg + bb]);
       // t = S * k_scale * sm_scale * log2(e); the row's 2^kq comes in below
       const float4* kc4 = reinterpret_cast<const float4*>(cols + ob * 2 * kPfKeys);
       const float4* vc4 = kc4 + kPfKeys / 4;
@@ -378,13 +424,10 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       }
       float m8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) m8[k] = fmaxf(sv[k], sv[k + 8]);
+      for (int k = 0; k < 8; ++k) m8[k] = fmaxf(fmaxf(sv[k], sv[k + 8]), fmaxf(sv[k + 16], sv[k + 24]));
 #pragma unroll
-      for (int cc = 16; cc < 64; cc += 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], sv[cc + k]);
-      float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      mt *= qsr;
+      for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], fmaxf(fmaxf(sv[k + 32], sv[k + 40]), fmaxf(sv[k + 48], sv[k + 56])));
+      const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * qsr;
       // lazy rescale: move the row's reference maximum only when it grows by
       // more than 2^8 (or on the first tile with a valid key)
       float alpha = 1.f;
@@ -413,36 +456,31 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
         ph[2 * c4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
       }
       l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-      // O^T columns of rows whose reference moved are rescaled in TMEM once
-      // the previous PV is done
-      const bool need = group_any(0, alpha != 1.f && j > 0);
-      if (need) {
-        alpha_sh[r] = alpha;
-        group_sync(0);
-        const int jp = j - 1;
-        if (!wait_fast(&pv_done[jp & 1], (jp >> 1) & 1, abort_flag)) {
-          // the failure is caught by the next group_any
-        }
+      // this group's previous P.V (tile j-2) must be done before its O is
+      // rescaled and before its P buffer is overwritten
+      if (lj > 0 && !wait_fast(&pv_done[wg], (lj - 1) & 1, abort_flag)) { /* caught at the next tile */ }
+      if (group_any(wg, alpha != 1.f && lj > 0)) {
+        // O^T columns of rows whose reference moved are rescaled in TMEM
+        my_alpha[r] = alpha;
+        group_sync(wg);
         umma::fence_after_sync();
 #pragma unroll 1
         for (int k = 0; k < 8; ++k) {             // 8 chunks of 16 columns (query rows)
           uint32_t rr[16];
-          umma::tmem_ld16_nowait(tmem + 128 + 16 * k + lane_off, rr);
+          umma::tmem_ld16_nowait(o_base + 16 * k + lane_off, rr);
           umma::tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < 16; ++u) rr[u] = __float_as_uint(__uint_as_float(rr[u]) * alpha_sh[16 * k + u]);
+          for (int u = 0; u < 16; ++u) rr[u] = __float_as_uint(__uint_as_float(rr[u]) * my_alpha[16 * k + u]);
           asm volatile(
               "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-              "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(tmem + 128 + 16 * k + lane_off),
+              "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(o_base + 16 * k + lane_off),
               "r"(rr[0]), "r"(rr[1]), "r"(rr[2]), "r"(rr[3]), "r"(rr[4]), "r"(rr[5]), "r"(rr[6]), "r"(rr[7]),
               "r"(rr[8]), "r"(rr[9]), "r"(rr[10]), "r"(rr[11]), "r"(rr[12]), "r"(rr[13]), "r"(rr[14]), "r"(rr[15]));
         }
         asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-        group_sync(0);                              // alpha_sh reused next tile
+        group_sync(wg);                             // my_alpha reused next tile
       }
-      // P row -> P operand buffer (free once the PV two tiles back is done)
-      if (u2 > 0 && !wait_fast(&pv_done[b2], (u2 - 1) & 1, abort_flag)) { /* caught below */ }
-      uint8_t* prow = pop + b2 * C::POP + r * 128;
+      uint8_t* prow = my_p + r * 128;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8)
         *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) =
@@ -450,47 +488,56 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       umma::fence_proxy_async_smem();
       umma::fence_before_sync();
       __syncwarp();
-      if (lane == 0) umma::mbar_arrive(&p_full[b2]);
+      if (lane == 0) umma::mbar_arrive(&p_full[wg]);
       if (r == 0) PF_TRACE(8 * j + 5);
-      if (*abort_flag) { failed = true; }
-      if (group_any(0, failed)) { failed = true; break; }
     }
-    l_sh[r] = failed ? 0.f : l;
-    group_sync(0);
+    m_sh[wg * kPfRows + r] = failed ? -INFINITY : m_used;
+    l_sh[wg * kPfRows + r] = failed ? 0.f : l;
     // ------------------------------------------------------------ epilogue
-    if (r == 0) PF_TRACE(1010);
-    if (!failed && nkv > 0) {
-      const int jl = nkv - 1;
-      const bool ok = wait_or_abort(&pv_done[jl & 1], (jl >> 1) & 1, abort_flag);
-      if (!group_any(0, !ok)) {
-        umma::fence_after_sync();
-        const int d = r;                            // O^T lane = head dim
-        const float ofac = pow2i(kp);
+    // both groups' states are visible after this barrier; a failure in
+    // either group skips the epilogue in both
+    bool any_fail = pair_any(failed);
+    if (r == 0 && wg == 0) PF_TRACE(1010);
+    const int n0 = (nkv + 1) >> 1, n1 = nkv >> 1;   // tiles of each group
+    if (!any_fail) {
+      bool ok = n0 == 0 || wait_or_abort(&pv_done[0], (n0 - 1) & 1, abort_flag);
+      ok = ok && (n1 == 0 || wait_or_abort(&pv_done[1], (n1 - 1) & 1, abort_flag));
+      any_fail = pair_any(!ok);
+    }
+    if (!any_fail) {
+      umma::fence_after_sync();
+      const int d = r;                              // O^T lane = head dim
+      const float ofac = pow2i(kp);
 #pragma unroll 1
-        for (int k = 0; k < 8; ++k) {
-          uint32_t rr[16];
-          umma::tmem_ld16_nowait(tmem + 128 + 16 * k + lane_off, rr);
-          umma::tmem_wait_ld();
+      for (int k = 4 * wg; k < 4 * wg + 4; ++k) {   // this group writes 64 of the 128 query rows
+        uint32_t r0[16], r1[16];
+        if (n0 > 0) umma::tmem_ld16_nowait(tmem + 256 + 16 * k + lane_off, r0);
+        if (n1 > 0) umma::tmem_ld16_nowait(tmem + 384 + 16 * k + lane_off, r1);
+        umma::tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int row = 16 * k + u, qrow = i0 + row;
-            if (qrow < p.n_q) {
-              const float lr = l_sh[row];
-              const float o = lr > 0.f ? __uint_as_float(rr[u]) * ofac / lr : 0.f;
-              const int64_t oi = (((int64_t)b * p.n_q + qrow) * p.q_heads + hq) * D + d;
-              if (p.out_f32) reinterpret_cast<float*>(p.out)[oi] = o;
-              else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
-            }
+        for (int u = 0; u < 16; ++u) {
+          const int row = 16 * k + u, qrow = i0 + row;
+          if (qrow < p.n_q) {
+            const float ma = m_sh[row], mb = m_sh[kPfRows + row];
+            const float M = fmaxf(ma, mb);
+            const float fa = ma == -INFINITY ? 0.f : ex2(ma - M);
+            const float fb = mb == -INFINITY ? 0.f : ex2(mb - M);
+            const float L = l_sh[row] * fa + l_sh[kPfRows + row] * fb;
+            float o = 0.f;
+            if (n0 > 0 && fa != 0.f) o += __uint_as_float(r0[u]) * fa;
+            if (n1 > 0 && fb != 0.f) o += __uint_as_float(r1[u]) * fb;
+            o = L > 0.f ? o * ofac / L : 0.f;
+            const int64_t oi = (((int64_t)b * p.n_q + qrow) * p.q_heads + hq) * D + d;
+            if (p.out_f32) reinterpret_cast<float*>(p.out)[oi] = o;
+            else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
           }
         }
-      } else {
-        failed = true;
       }
     }
-    if (failed && r == 0) raise_error(p.err, FP8KV_DEVERR_TIMEOUT);
+    if (any_fail && r == 0 && wg == 0) raise_error(p.err, FP8KV_DEVERR_TIMEOUT);
   } else {
     // --------------------------------------------------------- preparation
-    const int pt = tid - 192;
+    const int pt = tid - 320;
     const int kr = pt >> 1, hh = pt & 1;          // key row of the tile, half of the head dim
     const float vfac = pow2i(-kp);                // keeps p * v_scale inside f16's range
     bool failed = false;
@@ -498,7 +545,7 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
       const int s = j % C::NS, u = j / C::NS, ob = j % C::NOP, ou = j / C::NOP;
       bool ok = wait_fast(&full[s], u & 1, abort_flag);
       if (ou > 0) ok = ok && wait_fast(&op_free[ob], (ou - 1) & 1, abort_flag);
-      if (group_any(1, !ok)) { failed = true; break; }
+      if (group_any(3, !ok)) { failed = true; break; }
       const uint8_t* st = ring + s * C::STAGE;
       const float* kss = reinterpret_cast<const float*>(st + 2 * C::CODES);
       const float* vss = kss + kPfKeys;
@@ -546,7 +593,7 @@ __global__ void __launch_bounds__(320, 1) prefill_tc(const __grid_constant__ Pre
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
-  if (warp == 1) umma::tmem_dealloc(tmem, 256);
+  if (warp == 1) umma::tmem_dealloc(tmem, 512);
   if (tid == 0) PF_TRACE(1021);
 }
 
@@ -571,7 +618,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int batch, cudaStream_t st
     return cudaErrorInvalidValue;
   tp.p = p;
   dim3 grid((p.n_q + kPfRows - 1) / kPfRows, p.q_heads, batch);
-  prefill_tc<<<grid, 320, smem, st>>>(tp);
+  prefill_tc<<<grid, kPfThreads, smem, st>>>(tp);
   return cudaGetLastError();
 }
 
