@@ -11,7 +11,7 @@
 // A CTA owns 128 query rows (two 64-token query tiles: the full-rate tcgen05
 // shape is M = 128) of one query head, and walks the KV tiles of that head's
 // KV head:
-//   S[128 x 64]    = Q . K^T            tcgen05.mma kind::f16 -> TMEM
+//   S[128 x 64]    = (Q_hi + Q_lo) . K^T  tcgen05.mma kind::f8f6f4 -> TMEM
 //   per row (one thread each, whole row thread-local): s = S * k_scale *
 //     sm_scale, causal mask (diagonal tiles only), running max with lazy
 //     rescale, p = 2^(s - m), l += p, P' = p * v_scale
@@ -20,9 +20,12 @@
 // own running (m, l) and its own O accumulator, so the softmax of two tiles
 // runs at once; the two states are combined per row in the epilogue, as two
 // flash-decoding splits are.
-// Operands are f16: the e4m3 K and V codes convert to f16 exactly
-// (cvt.rn.f16x2.e4m3x2); each bf16 query row is scaled by a power of two
-// (exact) into f16's range.  P' is rounded once, to the 16-bit operand of the
+// QK runs on the e4m3 K tile as it lands in shared memory ("FP8 KV
+// attention: hardware paths and tile preparation", section "Use a native
+// narrow QK path": no K preparation), with each bf16 query row, after a
+// power-of-two scaling that puts its largest magnitude at most 448, written
+// as two e4m3 terms (hi = e4m3(x), lo = e4m3(x - hi)).  P.V is kind::f16:
+// the e4m3 V codes convert to f16 exactly (cvt.rn.f16x2.e4m3x2).  P' is rounded once, to the 16-bit operand of the
 // P.V product, as f16 (11-bit significand, 8x finer than bf16; the page's own
 // prefill keeps its probabilities in f16, section 2.4) after one power-of-two
 // scaling per CTA chosen from the largest V scale it will see.  All those
@@ -31,13 +34,15 @@
 // Warp roles:
 //   warp 0      TMA producer: e4m3 code tiles (64 keys x 128 B, 128-byte
 //               swizzle) and 1-D bulk copies of the scale rows into a ring.
-//   warp 1      TMEM owner and MMA issuer: an event loop issuing each QK
-//               and each PV as soon as its operands are ready.
+//   warp 1      TMEM owner and QK issuer (one thread).
+//   warp 14     PV issuer (one thread): QK and PV each wait only for their
+//               own operands.
 //   warps 2-5   softmax of the even tiles, warps 6-9 of the odd tiles (one
 //               query row per thread); then the output epilogue.
-//   warps 10-13 preparation: codes -> f16 operand tiles (K-major K, MN-major
-//               V; same physical layout), per-key scales; V rows past the
-//               causal end zeroed (0 * NaN would poison P.V).
+//   warps 10-13 preparation: V codes -> f16 operand tiles (MN-major), per-key
+//               scales; V rows past the causal end zeroed (0 * NaN would
+//               poison P.V).
+//   warp 15     idle.
 // TMEM: S of each group double-buffered (4 x 64 columns), one O^T per group
 // (2 x 128).  O is rescaled in TMEM only when a row's maximum grows by more
 // than 2^8 (then P stays <= 2^8 relative to the stale maximum).  Every wait is
@@ -49,20 +54,20 @@ namespace fp8kv {
 
 constexpr int kPfRows = 128;   // query rows per CTA
 constexpr int kPfKeys = 64;    // keys per KV tile
-constexpr int kPfThreads = 448;
+constexpr int kPfThreads = 512;
 
 struct PfTcCfg {
   static constexpr int D = 128;
-  static constexpr int QOP = kPfRows * D * 2;                 // [2 atoms][128 rows][128 B] f16
+  static constexpr int QOP = 2 * kPfRows * D;                 // [hi, lo][128 rows][128 B] e4m3
   static constexpr int CODES = kPfKeys * D;                    // e4m3 tile [64][128]
   static constexpr int STAGE = ((2 * CODES + 2 * kPfKeys * 4) + 1023) / 1024 * 1024;
-  static constexpr int NS = 3;                                 // e4m3 code stages
-  static constexpr int NOP = 3;                                // f16 K/V operand buffers
-  static constexpr int OPT = kPfKeys * D * 2;                 // f16 K or V tile [2 atoms][64][128 B]
+  static constexpr int NS = 4;                                 // e4m3 code stages
+  static constexpr int NOP = 4;                                // f16 V operand buffers
+  static constexpr int OPT = kPfKeys * D * 2;                 // f16 V tile [2 atoms][64][128 B]
   static constexpr int POP = kPfRows * kPfKeys * 2;           // f16 P [128 rows][128 B], one per group
   static constexpr int COLS = 2 * kPfKeys * 4;                 // per buffer: k and v column scales
   static constexpr int MISC = 4096;
-  static constexpr int BYTES = QOP + NS * STAGE + 2 * NOP * OPT + 2 * POP + NOP * COLS + MISC + 1024;
+  static constexpr int BYTES = QOP + NS * STAGE + NOP * OPT + 2 * POP + NOP * COLS + MISC + 1024;
   static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
@@ -110,21 +115,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qop = smem;
   uint8_t* ring = qop + C::QOP;
-  uint8_t* kf = ring + C::NS * C::STAGE;          // [NOP] f16 K operand
-  uint8_t* vf = kf + C::NOP * C::OPT;             // [NOP] f16 V operand
+  uint8_t* vf = ring + C::NS * C::STAGE;          // [NOP] f16 V operand
   uint8_t* pop = vf + C::NOP * C::OPT;            // [group] f16 P operand
   float* cols = reinterpret_cast<float*>(pop + 2 * C::POP);   // [NOP][k 64 | v 64]
   uint8_t* misc = reinterpret_cast<uint8_t*>(cols + C::NOP * 2 * kPfKeys);
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);        // [NS] codes landed
-  uint64_t* empty = full + C::NS;                             // [NS] codes consumed by the prep warps
-  uint64_t* op_full = empty + C::NS;                          // [NOP] f16 K/V operands + scales ready
+  uint64_t* empty = full + C::NS;                             // [NS] K read by QK, V converted by the prep warps
+  uint64_t* op_full = empty + C::NS;                          // [NOP] f16 V operand + scales ready
   uint64_t* op_free = op_full + C::NOP;                       // [NOP] PV of the buffer's tile finished
   uint64_t* s_full = op_free + C::NOP;                        // [group][2]
   uint64_t* s_free = s_full + 4;                              // [group][2]
   uint64_t* p_full = s_free + 4;                              // [group]
   uint64_t* pv_done = p_full + 2;                             // [group] PV of the group's last tile finished
-  uint64_t* drained = pv_done + 2;                            // final commit of the MMA issuer
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(drained + 1);
+  uint64_t* drained = pv_done + 2;                            // [2] final commits of the two MMA issuers
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drained + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   int* kp_sh = const_cast<int*>(abort_flag) + 1;
   float* alpha_sh = reinterpret_cast<float*>(misc + 256);     // [group][128]
@@ -189,7 +193,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   if (tid == 0) {
     for (int i = 0; i < C::NS; ++i) {
       umma::mbar_init(&full[i], 1);
-      umma::mbar_init(&empty[i], 4);
+      umma::mbar_init(&empty[i], 1 + 4);       // QK commit + the four prep warps
     }
     *abort_flag = 0;
     umma::mbar_fence_init();
@@ -206,15 +210,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
       umma::mbar_init(&p_full[i], 4);
       umma::mbar_init(&pv_done[i], 1);
     }
-    umma::mbar_init(drained, 1);
+    umma::mbar_init(&drained[0], 1);
+    umma::mbar_init(&drained[1], 1);
     umma::mbar_fence_init();
   }
   if (warp == 1) {
     umma::tmem_alloc(tslot, 512);
     umma::tmem_relinquish();
   }
-  // softmax warps: this thread's query row -> f16 Q operand, row scale 2^kq
-  // (both groups compute the row's scale; each writes one 64-dim atom)
+  // softmax warps: this thread's query row -> the QK A operand as two e4m3
+  // terms (hi = e4m3(x), lo = e4m3(x - hi)) after scaling the row by 2^-kq so
+  // its largest magnitude is at most 448; both groups compute the row's
+  // scale, each writes 64 of the 128 dims of both terms
   const int r = 32 * (warp & 3) + lane;           // query row (softmax warps) / TMEM lane
   const int wg = (warp - 2) >> 2;                 // softmax group: tiles j with j % 2 == wg
   const int qi = i0 + r;
@@ -236,28 +243,35 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
       }
       if ((k >> 3) == wg) mine[k & 7] = w;
     }
-    int e = 0;
-    (void)frexpf(amax * (1.0f / 16384.0f), &e);   // row max -> [2^13, 2^14): inside f16's normal range
-    kq = max(-100, min(100, e));
+    kq = max(-100, min(100, e4m3_row_exp(amax)));
     const float qsc = pow2i(-kq);
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {               // 8 elements (one 16-byte f16 chunk) each
-      const uint32_t w4[4] = {mine[ch].x, mine[ch].y, mine[ch].z, mine[ch].w};
-      uint32_t h[4];
+    for (int c16 = 0; c16 < 4; ++c16) {            // 16 dims (one 16-byte e4m3 chunk) each
+      uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float f2[2];
-        bf16x2_to_f32(w4[u], f2);
-        const __half2 hv = __floats2half2_rn(f2[0] * qsc, f2[1] * qsc);
-        h[u] = *reinterpret_cast<const uint32_t*>(&hv);
+      for (int u = 0; u < 4; ++u) {                // 4 dims at a time
+        const uint4 w = mine[2 * c16 + (u >> 1)];
+        const uint32_t wa = (u & 1) ? w.z : w.x, wb = (u & 1) ? w.w : w.y;
+        float f2[2], g2[2];
+        bf16x2_to_f32(wa, f2);
+        bf16x2_to_f32(wb, g2);
+        const float x0 = f2[0] * qsc, x1 = f2[1] * qsc, x2 = g2[0] * qsc, x3 = g2[1] * qsc;
+        const uint32_t h = e4m3x2_rn(x0, x1) | (e4m3x2_rn(x2, x3) << 16);
+        float hv[4];
+        e4m3x4_to_f32_scaled(h, hv);
+        hi[u] = h;
+        lo[u] = e4m3x2_rn(x0 - hv[0] * kTwoPow120, x1 - hv[1] * kTwoPow120) |
+                (e4m3x2_rn(x2 - hv[2] * kTwoPow120, x3 - hv[3] * kTwoPow120) << 16);
       }
-      *reinterpret_cast<uint4*>(qop + wg * (kPfRows * 128) + r * 128 + ((ch ^ (r & 7)) << 4)) =
-          make_uint4(h[0], h[1], h[2], h[3]);
+      const int ch = 4 * wg + c16;
+      const int off = r * 128 + ((ch ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(qop + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(qop + kPfRows * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
   }
   // prep warps: one power of two for all of this CTA's P (from the largest
   // V scale of its keys), so P' stays inside f16's range
-  if (warp >= 10) {
+  if (warp >= 10 && warp < 14) {
     const int pt = tid - 320;
     float vm = 0.f;
     for (int base = 0; base < kv_end; base += 8 * 128) {   // 8 independent loads in flight
@@ -304,76 +318,58 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t ID_QK = umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_K, umma::MAJOR_K, 128, 64);
-      constexpr uint32_t ID_PV = umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_MN, umma::MAJOR_K, 128, 128);
+      constexpr uint32_t ID_QK = umma::idesc(umma::FMT_E4M3, umma::FMT_E4M3, umma::MAJOR_K, umma::MAJOR_K, 128, 64);
       const uint32_t qa = umma::smem_u32(qop);
-      // tile j: group w = j % 2, its local index lj = j / 2, S buffer lj % 2.
-      // Event loop: issue whichever of the next QK and the next PV is ready
-      // (non-blocking tests), so neither waits behind the other: a PV goes
-      // out as soon as its P lands, which frees the f16 operand buffer the
-      // preparation warps need next.
-      int nq = 0, np = 0;
-      long long t_idle = 0;
-      uint32_t idle = 0;
-      while (np < nkv) {
-        bool prog = false;
-        if (nq < nkv) {
-          const int j = nq, w = j & 1, lj = j >> 1, bb = lj & 1, ub = lj >> 1, ob = j % C::NOP, ou = j / C::NOP;
-          if (umma::mbar_test(&op_full[ob], ou & 1) &&
-              (ub == 0 || umma::mbar_test(&s_free[2 * w + bb], (ub - 1) & 1))) {
-            umma::fence_after_sync();
-            PF_TRACE(8 * j + 1);
-            const uint32_t ka = umma::smem_u32(kf + ob * C::OPT);
+      // QK issuer.  Tile j: group w = j % 2, its local index lj = j / 2, S
+      // buffer lj % 2.  The PVs are issued by another warp (warp 14), so a
+      // QK waiting for its K tile never holds up a PV and vice versa.
+      for (int j = 0; j < nkv; ++j) {
+        const int w = j & 1, lj = j >> 1, bb = lj & 1, ub = lj >> 1, s = j % C::NS, u = j / C::NS;
+        if (!wait_fast(&full[s], u & 1, abort_flag)) break;
+        if (ub > 0 && !wait_fast(&s_free[2 * w + bb], (ub - 1) & 1, abort_flag)) break;
+        umma::fence_after_sync();
+        PF_TRACE(8 * j + 1);
+        // S = (Q_hi + Q_lo) . K: the e4m3 K codes are the B operand as they
+        // landed (K-major, 128-byte swizzle), 32 dims per MMA
+        const uint32_t ka = umma::smem_u32(ring + s * C::STAGE);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma::mma_f16_ss(tmem + 64 * (2 * w + bb),
-                               umma::sdesc(qa + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
-                               umma::sdesc(ka + (kk >> 2) * (kPfKeys * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
-                               ID_QK, kk > 0);
-            umma::mma_commit(&s_full[2 * w + bb]);
-            ++nq;
-            prog = true;
-          }
-        }
-        if (np < nq) {
-          const int j = np, w = j & 1, lj = j >> 1, ob = j % C::NOP;
-          if (umma::mbar_test(&p_full[w], lj & 1)) {
-            umma::fence_after_sync();
-            PF_TRACE(8 * j + 2);
-            const uint32_t va = umma::smem_u32(vf + ob * C::OPT);
-            const uint32_t pa = umma::smem_u32(pop + w * C::POP);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma::mma_f16_ss(tmem + 256 + 128 * w,
-                               umma::sdesc(va + kk * 2048, kPfKeys * 128, 1024, umma::SWIZZLE_128B),
-                               umma::sdesc(pa + kk * 32, 16, 1024, umma::SWIZZLE_128B), ID_PV,
-                               (lj > 0 || kk > 0) ? 1u : 0u);
-            umma::mma_commit(&pv_done[w]);
-            umma::mma_commit(&op_free[ob]);
-            ++np;
-            prog = true;
-          }
-        }
-        if (prog) {
-          idle = 0;
-          continue;
-        }
-        __nanosleep(20);     // the polling thread shares an SM sub-partition with softmax warps
-        if ((++idle & 63) == 0) {                    // bounded: give up after ~2 s without progress
-          if (idle == 64) t_idle = clock64();
-          if (*abort_flag) break;
-          if (clock64() - t_idle > kWaitLimitCycles) {
-            *abort_flag = 1;
-            break;
-          }
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          umma::mma_f8_ss(tmem + 64 * (2 * w + bb),
+                          umma::sdesc(qa + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
+                          umma::sdesc(ka + (kk & 3) * 32, 16, 1024, umma::SWIZZLE_128B), ID_QK, kk > 0);
+        umma::mma_commit(&s_full[2 * w + bb]);
+        umma::mma_commit(&empty[s]);
       }
       // all issued MMAs complete before TMEM is released (matters only when
       // a wait above gave up)
-      umma::mma_commit(drained);
-      (void)umma::mbar_wait(drained, 0, 100000000ull);
+      umma::mma_commit(&drained[0]);
+      (void)umma::mbar_wait(&drained[0], 0, 100000000ull);
     }
-  } else if (warp < 10) {
+  } else if (warp == 14) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_PV = umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_MN, umma::MAJOR_K, 128, 128);
+      for (int j = 0; j < nkv; ++j) {
+        const int w = j & 1, lj = j >> 1, ob = j % C::NOP, ou = j / C::NOP;
+        if (!wait_fast(&p_full[w], lj & 1, abort_flag)) break;
+        if (!wait_fast(&op_full[ob], ou & 1, abort_flag)) break;
+        umma::fence_after_sync();
+        PF_TRACE(8 * j + 2);
+        const uint32_t va = umma::smem_u32(vf + ob * C::OPT);
+        const uint32_t pa = umma::smem_u32(pop + w * C::POP);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma::mma_f16_ss(tmem + 256 + 128 * w, umma::sdesc(va + kk * 2048, kPfKeys * 128, 1024, umma::SWIZZLE_128B),
+                           umma::sdesc(pa + kk * 32, 16, 1024, umma::SWIZZLE_128B), ID_PV,
+                           (lj > 0 || kk > 0) ? 1u : 0u);
+        umma::mma_commit(&pv_done[w]);
+        umma::mma_commit(&op_free[ob]);
+      }
+      // this thread's MMAs complete before TMEM is released
+      umma::mma_commit(&drained[1]);
+      (void)umma::mbar_wait(&drained[1], 0, 100000000ull);
+    }
+  } else if (warp >= 2 && warp < 10) {
     // ------------------------------------------------------------- softmax
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float qsr = pow2i(kq);
@@ -535,7 +531,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
       }
     }
     if (any_fail && r == 0 && wg == 0) raise_error(p.err, FP8KV_DEVERR_TIMEOUT);
-  } else {
+  } else if (warp >= 10 && warp < 14) {
     // --------------------------------------------------------- preparation
     const int pt = tid - 320;
     const int kr = pt >> 1, hh = pt & 1;          // key row of the tile, half of the head dim
@@ -551,10 +547,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
       const float* vss = kss + kPfKeys;
       const int t0 = j * kPfKeys;
       const bool key_ok = t0 + kr < kv_end;
-#pragma unroll
-      for (int side = 0; side < 2; ++side) {
-        const uint8_t* codes = st + side * C::CODES + kr * 128;
-        uint8_t* dst = (side == 0 ? kf : vf) + ob * C::OPT + hh * (kPfKeys * 128) + kr * 128;
+      {
+        const uint8_t* codes = st + C::CODES + kr * 128;
+        uint8_t* dst = vf + ob * C::OPT + hh * (kPfKeys * 128) + kr * 128;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {           // 16 codes -> two 16-byte f16 chunks
           const int ch = 4 * hh + cc;
@@ -566,7 +561,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
             h[2 * u4] = e4m3x2_to_f16x2((uint16_t)(ww[u4] & 0xFFFF));
             h[2 * u4 + 1] = e4m3x2_to_f16x2((uint16_t)(ww[u4] >> 16));
           }
-          if (side == 1 && !key_ok) {
+          if (!key_ok) {
 #pragma unroll
             for (int u8 = 0; u8 < 8; ++u8) h[u8] = 0u;
           }
@@ -598,6 +593,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
 }
 
 #ifdef FP8KV_TRACE
+extern "C" __attribute__((visibility("default"))) int fp8kv_trace_clear_prefill() {
+  static unsigned long long zero[1024];
+  return cudaMemcpyToSymbol(g_pf_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : -1;
+}
 extern "C" __attribute__((visibility("default"))) int fp8kv_trace_read_prefill(unsigned long long* out, int n) {
   if (n > 1024) n = 1024;
   return cudaMemcpyFromSymbol(out, g_pf_trace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
