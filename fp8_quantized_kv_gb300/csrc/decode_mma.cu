@@ -243,6 +243,10 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {                                 // the TMA unit fetches the maps while the CTA sets up
+    tma::prefetch_map(&tp.tmk);
+    tma::prefetch_map(&tp.tmv);
+  }
   const CacheView& c = p.c;
   const int G = p.group, S = p.num_splits;
 

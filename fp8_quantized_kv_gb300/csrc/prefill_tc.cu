@@ -136,9 +136,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   float* l_sh = reinterpret_cast<float*>(misc + 2304);        // [group][128] final row sums
   float* vmax_sh = reinterpret_cast<float*>(misc + 3328);     // [4]
 
-  const int qt = gridDim.x - 1 - blockIdx.x;      // longest causal range first
-  const int hq = blockIdx.y, b = blockIdx.z;
+  // grid (query head, sequence, query tile), the tile index slowest and
+  // reversed: the CTAs with the longest causal ranges launch first
+  const int hq = blockIdx.x, b = blockIdx.y, qt = gridDim.z - 1 - blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {                                 // the TMA unit fetches the maps while the CTA sets up
+    tma::prefetch_map(&tp.tmk);
+    tma::prefetch_map(&tp.tmv);
+  }
   const CacheView& c = p.c;
   const int hk = hq / p.group;
   const int pos0 = p.q_pos0[b];
@@ -616,7 +621,9 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int batch, cudaStream_t st
   if (!make_map(&tp.tmk, c.k, false, rows, box_rows) || !make_map(&tp.tmv, c.v, false, rows, box_rows))
     return cudaErrorInvalidValue;
   tp.p = p;
-  dim3 grid((p.n_q + kPfRows - 1) / kPfRows, p.q_heads, batch);
+  const int n_qt = (p.n_q + kPfRows - 1) / kPfRows;
+  if (n_qt > 65535) return cudaErrorInvalidValue;
+  dim3 grid(p.q_heads, batch, n_qt);
   prefill_tc<<<grid, kPfThreads, smem, st>>>(tp);
   return cudaGetLastError();
 }
