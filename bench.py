@@ -38,6 +38,10 @@ WORKLOAD = "decode_b16_ctx8192"
 METRIC = "decode attn KV-read GB/s (% of HBM peak) and µs/layer at B16 ctx8192, 1 GB300"
 KERNEL_IDS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
 PAGE_NUMBER_GBS = 550.0   # the pages' figure for this workload (RTX 5070 Ti, Triton, codes only)
+# fp8kv_decode_step flag: each layer's step streams its own cache while the
+# previous layer's step finishes (programmatic dependent launch); the layers'
+# caches are distinct, as in a model
+STEP_EARLY_CACHE_READ = 1
 
 
 def parse(argv=None):
@@ -53,6 +57,8 @@ def parse(argv=None):
     ap.add_argument("--no-controls", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-steps", type=int, default=200)
+    ap.add_argument("--plain-launch", action="store_true",
+                    help="launch every step only after the previous one finished (no early cache read)")
     ap.add_argument("--no-prefill", action="store_true")
     return ap.parse_args(argv)
 
@@ -305,14 +311,14 @@ class Layer:
     """One layer: its own cache, zero-filled workspace and pre-built C-ABI
     argument tuple for fp8kv_decode_step."""
 
-    def __init__(self, cache, q, lens, ws_tensor, out, knew, vnew, Hq, sm_scale, kernel):
+    def __init__(self, cache, q, lens, ws_tensor, out, knew, vnew, Hq, sm_scale, kernel, flags):
         from fp8_quantized_kv_gb300._lib import get_lib
         self.lib = get_lib()
         self.cache = cache
         self.keep = (q, lens, ws_tensor, out, knew, vnew)
         P = lambda t: ctypes.c_void_p(t.data_ptr())
         self.a_step = (P(q), P(knew), P(vnew), cache.struct_ref, P(lens), Hq, ctypes.c_float(sm_scale), 0,
-                       kernel, P(ws_tensor), ws_tensor.numel(), P(out), 0)
+                       kernel, P(ws_tensor), ws_tensor.numel(), P(out), 0, ctypes.c_uint32(flags))
 
     def step(self, s):
         r = self.lib.fp8kv_decode_step(*self.a_step, s)
@@ -320,7 +326,7 @@ class Layer:
             raise RuntimeError(f"fp8kv_decode_step status {r}")
 
 
-def build_layers(spec, dtype, L, inp, kernel):
+def build_layers(spec, dtype, L, inp, kernel, flags=0):
     import fp8_quantized_kv_gb300 as fk
     B, Hq, Hkv, D = spec.batch, spec.q_heads, spec.kv_heads, spec.head_dim
     T = spec.seq_lens[0]
@@ -351,7 +357,7 @@ def build_layers(spec, dtype, L, inp, kernel):
         wsb = fk.fp8kv_decode_step_workspace_bytes(c, Hq, 0, kernel)
         ws_t = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
-        layers.append(Layer(c, q, lens, ws_t, out, knew, vnew, Hq, 1.0 / math.sqrt(D), kernel))
+        layers.append(Layer(c, q, lens, ws_t, out, knew, vnew, Hq, 1.0 / math.sqrt(D), kernel, flags))
     torch.cuda.synchronize()
     return layers, (q, knew, vnew, lens)
 
@@ -508,8 +514,10 @@ def measure_prefill(args, ws):
                          "traffic": None, "algorithmic_flops_per_launch": flops}}
 
 
-def measure_variant(spec, dtype, args, ws, inp):
-    layers, dev = build_layers(spec, dtype, args.layers, inp, KERNEL_IDS[args.kernel])
+def measure_variant(spec, dtype, args, ws, inp, flags=None):
+    if flags is None:
+        flags = 0 if args.plain_launch else STEP_EARLY_CACHE_READ
+    layers, dev = build_layers(spec, dtype, args.layers, inp, KERNEL_IDS[args.kernel], flags)
     for i in range(max(3, args.warmup)):                      # eager warm-up steps
         L = layers[i % len(layers)]
         L.step(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
@@ -563,6 +571,15 @@ def run_gpu(args, ws, rank):
                 "avg_launch_us": launch_ms * 1e3, "source_sha": sha,
                 "event_node_step_us": None if per is None else per["step_ms"] * 1e3}
 
+    plain = None
+    if not args.plain_launch and tensor:
+        del layers
+        torch.cuda.empty_cache()
+        layers, _, pms, _, _ = measure_variant(spec, args.dtype, args, ws, inp, flags=0)
+        pms, pval = aggregate(nb["step"], args.steps, pms, ws)
+        plain = {"us_per_layer": pms / args.steps * 1e3, "GBps": pval,
+                 "note": "every step launched after the previous one finished"}
+
     controls = {}
     del layers
     torch.cuda.empty_cache()
@@ -602,12 +619,14 @@ def run_gpu(args, ws, rank):
                        "cache": args.dtype, "layout": "contiguous", "parallelism": f"replicas x{ws}",
                        "kernel": args.kernel,
                        "step": "fp8kv_decode_step: append 1 token/seq + split + merge",
+            "launch": "plain" if args.plain_launch or not tensor else
+                      "programmatic dependent launch: a step streams its layer's cache while the previous step finishes (FP8KV_STEP_EARLY_CACHE_READ)",
                        "l2": f"{args.layers} distinct layer caches rotated (inputs larger than L2)"},
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": (1 if tensor else 3) * args.steps,
             "kernels_us": None if per is None else {k.replace("_ms", "_us"): v * 1e3 for k, v in per.items()},
-            "clocks": clocks, "controls": controls, "prefill": prefill,
+            "clocks": clocks, "controls": controls, "plain_launch": plain, "prefill": prefill,
         }
         print(json.dumps(line), flush=True)
 

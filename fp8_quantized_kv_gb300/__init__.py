@@ -26,6 +26,7 @@ LAYOUT_CONTIGUOUS, LAYOUT_PAGED = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
 
 DEVERR_SEQ_TOO_LONG, DEVERR_BAD_PAGE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+STEP_EARLY_CACHE_READ = 0x1
 KERNEL_AUTO, KERNEL_CUDA_CORES, KERNEL_TENSOR_CORES = 0, 1, 2
 KERNELS = {"auto": KERNEL_AUTO, "cuda_cores": KERNEL_CUDA_CORES, "tensor_cores": KERNEL_TENSOR_CORES}
 
@@ -223,10 +224,13 @@ def fp8kv_decode_step_workspace_bytes(cache: Fp8KVCache, q_heads: int, num_split
 def fp8kv_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cache: Fp8KVCache,
                       seq_lens: torch.Tensor, sm_scale: Optional[float] = None, num_splits: int = 0,
                       out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
-                      workspace: Optional[torch.Tensor] = None, kernel=0, stream=None):
+                      workspace: Optional[torch.Tensor] = None, kernel=0, early_cache_read=False,
+                      stream=None):
     """Append k_new/v_new [B, Hkv, D] at position seq_lens[b]-1 and decode
     q [B, Hq, D] over seq_lens[b] tokens.  `workspace` must start zero-filled
-    (a fresh one is allocated that way when not given)."""
+    (a fresh one is allocated that way when not given).  early_cache_read:
+    FP8KV_STEP_EARLY_CACHE_READ (the kernel issued just before on the stream
+    must not write this cache or seq_lens)."""
     for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new")):
         _need(t, torch.bfloat16, n)
     _need(seq_lens, torch.int32, "seq_lens")
@@ -243,7 +247,7 @@ def fp8kv_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     _check(get_lib().fp8kv_decode_step(
         _ptr(q), _ptr(k_new), _ptr(v_new), cache.struct_ref, _ptr(seq_lens), Hq, float(sm_scale),
         num_splits, k, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), odt,
-        _stream(stream)), "fp8kv_decode_step")
+        STEP_EARLY_CACHE_READ if early_cache_read else 0, _stream(stream)), "fp8kv_decode_step")
     return out
 
 

@@ -62,6 +62,7 @@ def get_lib() -> ctypes.CDLL:
             "(the FP8-KV kernels have no fallback)")
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    u32 = ctypes.c_uint32
     cp = ctypes.POINTER(CacheStruct)
     sig = {
         "fp8kv_quantize": (i32, [vp, i64, i32, vp, vp, vp]),
@@ -72,7 +73,7 @@ def get_lib() -> ctypes.CDLL:
         "fp8kv_decode_merge": (i32, [cp, i32, i32, i32, vp, sz, vp, i32, vp]),
         "fp8kv_decode_attention": (i32, [vp, cp, vp, i32, f32, i32, i32, vp, sz, vp, i32, vp]),
         "fp8kv_decode_step_workspace_bytes": (sz, [cp, i32, i32, i32]),
-        "fp8kv_decode_step": (i32, [vp, vp, vp, cp, vp, i32, f32, i32, i32, vp, sz, vp, i32, vp]),
+        "fp8kv_decode_step": (i32, [vp, vp, vp, cp, vp, i32, f32, i32, i32, vp, sz, vp, i32, u32, vp]),
         "fp8kv_decode_attention_static": (i32, [vp, cp, vp, i32, f32, i32, vp, i32, vp]),
         "fp8kv_decode_static_scratch_bytes": (sz, []),
         "fp8kv_prefill_attention": (i32, [vp, cp, vp, i32, i32, f32, i32, vp, i32, vp]),

@@ -242,6 +242,7 @@ fp8kv_status prepare_decode(const void* q, const fp8kv_cache* cache, const int32
   p->out_f32 = 0;
   p->fused = 0;
   p->cluster = 0;
+  p->pdl = 0;
   *resolved = k;
   return FP8KV_OK;
 }
@@ -305,8 +306,9 @@ size_t fp8kv_decode_step_workspace_bytes(const fp8kv_cache* cache, int32_t q_hea
 fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_new, const fp8kv_cache* cache,
                                const int32_t* seq_lens, int32_t q_heads, float sm_scale, int32_t num_splits,
                                int32_t kernel, void* workspace, size_t workspace_bytes, void* out,
-                               int32_t out_dtype, fp8kv_stream_t stream) {
+                               int32_t out_dtype, uint32_t flags, fp8kv_stream_t stream) {
   if (out_dtype != FP8KV_OUT_BF16 && out_dtype != FP8KV_OUT_F32) return FP8KV_ERR_INVALID_ARG;
+  if (flags & ~FP8KV_STEP_EARLY_CACHE_READ) return FP8KV_ERR_INVALID_ARG;
   DecodeParams p;
   int k = 0;
   fp8kv_status st = prepare_decode(q, cache, seq_lens, q_heads, sm_scale, num_splits, kernel, workspace,
@@ -326,6 +328,7 @@ fp8kv_status fp8kv_decode_step(const void* q, const void* k_new, const void* v_n
     p.out = out;
     p.out_f32 = out_dtype == FP8KV_OUT_F32;
     p.fused = 1;
+    p.pdl = (flags & FP8KV_STEP_EARLY_CACHE_READ) ? 1 : 0;
     return cuda_status(launch_decode_mma(p, cache->dtype, cache->batch, s));
   }
   cudaError_t e = launch_append_step(p.c, cache->dtype, k_new, v_new, seq_lens, p.err, s);

@@ -113,6 +113,12 @@ __device__ unsigned long long g_cta_time[4096][8];   // start, end, published, l
   } while (0)
 #endif
 
+// Programmatic dependent launch: wait for the kernel issued before this one
+// on the stream (its writes visible), and let the next one be scheduled.
+// Both are no-ops when the launch carries no programmatic dependency.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 // Merge of the fused step when the splits of one (sequence, KV head) run as
 // one thread-block cluster (split = cluster rank, S <= 8).  Rank r owns the
 // four-dim groups [g4_lo(r), g4_lo(r+1)) of the head dimension, all 8 heads.
@@ -261,6 +267,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
   const int t_end = min(t_begin + p.chunk_tiles, tiles);
   const int64_t part0 = ((int64_t)b * p.q_heads + (int64_t)h * G) * S + split;
   if (t_begin >= t_end) {
+    if (p.pdl) grid_dep_wait();                   // writes below
     if (p.cluster) {
       // no tiles: an empty partial (m = -inf, l = 0) in the cluster merge
       if (tid == 0) {
@@ -391,6 +398,12 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
   if (warp == 1) {
     umma::tmem_alloc(tslot, 512);
     umma::tmem_relinquish();
+  }
+  if (p.pdl) {
+    // the first cache tiles are in flight; q, k_new and v_new, and every
+    // write, wait for the previous kernel on the stream
+    grid_dep_wait();
+    if (tid == 0) grid_dep_launch();
   }
   if (warp >= 2 && warp < 6) {   // zero the operand buffers (group 0 only, then its own barrier)
     for (int i = tid - 64; i < (C::QOP + 4 * C::POP) / 16; i += 128)
@@ -1006,26 +1019,31 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
   tp.p = p;
   tp.p.cluster = 0;
   const void* fn = (const void*)decode_split_tc<KE, VE>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(320);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
   if (p.fused && p.num_splits >= 2 && p.num_splits <= 8 && cluster_fits(fn, grid, smem)) {
     tp.p.cluster = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(320);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = grid.x;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e2 = cudaLaunchKernelEx(&cfg, decode_split_tc<KE, VE>, tp);
-    if (e2 != cudaSuccess) (void)cudaGetLastError();
-    return e2;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = grid.x;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
-  decode_split_tc<KE, VE><<<grid, 320, smem, st>>>(tp);
-  return cudaGetLastError();
+  if (p.pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  const cudaError_t e2 = cudaLaunchKernelEx(&cfg, decode_split_tc<KE, VE>, tp);
+  if (e2 != cudaSuccess) (void)cudaGetLastError();
+  return e2;
 }
 
 #ifdef FP8KV_TRACE

@@ -24,6 +24,7 @@ struct DecodeParams {
   int out_f32;
   int fused;
   int cluster;               // fused step launched with the splits of a (sequence, KV head) as one cluster
+  int pdl;                   // fused step launched as a programmatic dependent of the previous kernel
 };
 
 struct PrefillParams {

@@ -204,6 +204,7 @@ FP8KV_API fp8kv_status fp8kv_decode_merge(const fp8kv_cache *cache, int32_t q_he
  *                 Every call that returns FP8KV_OK and whose device error
  *                 word stays clear leaves the counters zero again; after a
  *                 timeout, zero the workspace before reusing it.
+ *   flags:        0, or FP8KV_STEP_EARLY_CACHE_READ (below).
  * Other arguments as in fp8kv_decode_attention. */
 FP8KV_API size_t fp8kv_decode_step_workspace_bytes(const fp8kv_cache *cache, int32_t q_heads,
                                                    int32_t num_splits, int32_t kernel);
@@ -211,7 +212,19 @@ FP8KV_API fp8kv_status fp8kv_decode_step(const void *q, const void *k_new, const
                                          const fp8kv_cache *cache, const int32_t *seq_lens,
                                          int32_t q_heads, float sm_scale, int32_t num_splits,
                                          int32_t kernel, void *workspace, size_t workspace_bytes,
-                                         void *out, int32_t out_dtype, fp8kv_stream_t stream);
+                                         void *out, int32_t out_dtype, uint32_t flags,
+                                         fp8kv_stream_t stream);
+
+/* Flag of fp8kv_decode_step (tensor-core kernel; ignored by the CUDA-core
+ * kernel): the step may start before the kernel issued just before it on
+ * the stream has finished (programmatic dependent launch).  It then reads
+ * seq_lens and starts streaming the cache rows already appended before this
+ * call while that kernel runs, and waits for it before it reads q, k_new or
+ * v_new and before it writes anything (the new rows, the workspace, out).
+ * Set it only when the kernel issued just before on the stream writes
+ * neither this cache nor seq_lens -- as in a model, where the step follows
+ * the query/key/value projection and every layer has its own cache. */
+#define FP8KV_STEP_EARLY_CACHE_READ 1u
 
 /* Decode attention that allocates nothing (the paper has no counterpart:
  * this is a convenience of the library).  Same arguments and results as

@@ -78,6 +78,9 @@ def test_argument_checks_return_before_any_launch(lib):
     d64 = _cache(head_dim=64)
     assert lib.fp8kv_decode_split(None, r(d64), None, 16, 0.1, 0, 2, None, 0, None) == 2
     assert lib.fp8kv_decode_split(None, r(c), None, 16, 0.1, 0, 3, None, 0, None) == 1
+    # decode step: unknown flag bits are rejected before anything else
+    assert lib.fp8kv_decode_step(0x7000, 0x7000, 0x7000, r(c), 0x8000, 16, 0.1, 0, 2, 0x9000, 1 << 30,
+                                 out, 0, 2, None) == 1
     # prefill: the tensor-core kernel is built for K8V8 at head_dim 128 only;
     # a bad kernel id is rejected
     k16 = _cache(dtype=1, k_scale=None)

@@ -136,3 +136,30 @@ def test_step_split_invariance_cluster_and_global_merge():
     for ns, o in outs.items():
         rel = ((o - ref).norm(dim=-1) / ref.norm(dim=-1)).max().item()
         assert rel <= 1e-5, (ns, rel)
+
+
+def test_step_early_cache_read_matches_plain_launch():
+    """Back-to-back steps over four layer caches with
+    FP8KV_STEP_EARLY_CACHE_READ (each step streams its cache while the step
+    before it finishes) give the same outputs and the same appended rows as
+    plain launches."""
+    inp = synth.decode_inputs(synth.WORKLOADS["decode_b16_ctx512"], device="cuda")
+    prev, knew, vnew = _split_last_token(inp)
+    q = inp.q.cuda().contiguous()
+    lens = inp.seq_lens.cuda()
+    results = {}
+    for early in (False, True):
+        caches = [fill_cache(prev, "k8v8", capacity=512) for _ in range(4)]
+        outs = [torch.empty(16, 16, 128, dtype=torch.float32, device="cuda") for _ in range(4)]
+        for rep in range(3):
+            for i, c in enumerate(caches):
+                fk.fp8kv_decode_step(q, knew, vnew, c, lens, out=outs[i], kernel="tensor_cores",
+                                     early_cache_read=early)
+        torch.cuda.synchronize()
+        results[early] = (outs, caches)
+    assert fk.fp8kv_get_device_error() == 0
+    for i in range(4):
+        assert torch.equal(results[False][0][i], results[True][0][i])
+        assert torch.equal(results[False][1][i].k, results[True][1][i].k)
+        assert torch.equal(results[False][1][i].v_scale, results[True][1][i].v_scale)
+    assert_gate(results[True][0][0].cpu().numpy(), oracle_decode(inp, "k8v8", range(16)), "early cache read")
