@@ -511,7 +511,9 @@ def measure_prefill(args, ws):
             "l2": "8 input sets rotated (~250 MB, above L2)",
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_kind": f"{kind} (dense bf16; f16 operands run at the same rate)",
-                         "traffic": None, "algorithmic_flops_per_launch": flops}}
+                         "traffic": traffic_from_profile("prefill_k8v8_2048", kernel_source_sha()),
+                         "traffic_unit": "DRAM bytes per launch",
+                         "algorithmic_flops_per_launch": flops}}
 
 
 def measure_variant(spec, dtype, args, ws, inp, flags=None):
