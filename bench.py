@@ -60,6 +60,7 @@ def parse(argv=None):
     ap.add_argument("--plain-launch", action="store_true",
                     help="launch every step only after the previous one finished (no early cache read)")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-shapes", action="store_true")
     return ap.parse_args(argv)
 
 
@@ -516,6 +517,71 @@ def measure_prefill(args, ws):
                          "algorithmic_flops_per_launch": flops}}
 
 
+def measure_shapes(args):
+    """The decode step on the other decode workloads: batch 16 at 512 tokens
+    (40 rotated layer caches, above L2) and the paged batch-64 serving decode
+    (lengths U[1024, 16384], 16-token pages, hostile keys; one 1.2-1.7 GB
+    cache), K8/V8 and K16/V8, on each kernel.  Plain launches, CUDA-graph
+    replay, CUDA events on the launching stream."""
+    import fp8_quantized_kv_gb300 as fk
+    res = {}
+    for wl, n_layers, K in (("decode_b16_ctx512", 40, 400), ("paged_b64_hostile", 1, 20)):
+        spec = synth.WORKLOADS[wl]
+        inp = synth.decode_inputs(spec, device="cuda")
+        B, Hq, Hkv, D = spec.batch, spec.q_heads, spec.kv_heads, spec.head_dim
+        lens64 = inp.seq_lens.to(torch.int64)
+        sidx = torch.repeat_interleave(torch.arange(B), lens64).to(torch.int32).cuda()
+        pos = torch.cat([torch.arange(int(n)) for n in lens64]).to(torch.int32).cuda()
+        last = (inp.cu_seqlens[1:] - 1).cuda()
+        knew, vnew = inp.k[last].contiguous(), inp.v[last].contiguous()
+        lens = inp.seq_lens.cuda()
+        q = inp.q.contiguous()
+        res[wl] = {"group": spec.group, "tokens": int(lens64.sum())}
+        for dtype in ("k8v8", "k16v8"):
+            k8, v8 = dtype == "k8v8", True
+            row = D * ((1 if k8 else 2) + 1) + 4 * (int(k8) + int(v8))
+            nbytes = int(lens64.sum()) * Hkv * row + 2 * B * Hq * D * 2 + B * Hkv * (2 * D * 2 + row)
+            caches = []
+            for _ in range(n_layers):
+                if spec.page_size is None:
+                    c = fk.Fp8KVCache.contiguous(B, Hkv, D, int(lens64.max()), dtype)
+                else:
+                    c = fk.Fp8KVCache.paged(inp.page_table, inp.num_pages, Hkv, D, spec.page_size, dtype)
+                fk.fp8kv_append(c, inp.k.contiguous(), inp.v.contiguous(), sidx, pos)
+                caches.append(c)
+            out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+            res[wl][dtype] = {"algorithmic_bytes": nbytes}
+            for kname in ("cuda_cores", "tensor_cores"):
+                wss = [torch.zeros(fk.fp8kv_decode_step_workspace_bytes(c, Hq, 0, kname), dtype=torch.uint8,
+                                   device="cuda") for c in caches]
+
+                def step(i):
+                    fk.fp8kv_decode_step(q, knew, vnew, caches[i % n_layers], lens, out=out,
+                                         workspace=wss[i % n_layers], kernel=kname)
+                for i in range(max(3, args.warmup)):
+                    step(i)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for i in range(K):
+                        step(i)
+                g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                us = e0.elapsed_time(e1) / K * 1e3
+                res[wl][dtype][kname] = {"us_per_step": us, "GBps": nbytes / (us * 1e-6) / 1e9}
+                del g, wss
+            del caches
+            torch.cuda.empty_cache()
+        if fk.fp8kv_get_device_error() != 0:
+            raise RuntimeError(f"{wl}: device error")
+    return res
+
+
 def measure_variant(spec, dtype, args, ws, inp, flags=None):
     if flags is None:
         flags = 0 if args.plain_launch else STEP_EARLY_CACHE_READ
@@ -599,6 +665,7 @@ def run_gpu(args, ws, rank):
             torch.cuda.empty_cache()
 
     prefill = None if args.no_prefill else measure_prefill(args, ws)
+    shapes = None if args.no_shapes else measure_shapes(args)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -629,6 +696,7 @@ def run_gpu(args, ws, rank):
             "gpu_launches": (1 if tensor else 3) * args.steps,
             "kernels_us": None if per is None else {k.replace("_ms", "_us"): v * 1e3 for k, v in per.items()},
             "clocks": clocks, "controls": controls, "plain_launch": plain, "prefill": prefill,
+            "shapes": shapes,
         }
         print(json.dumps(line), flush=True)
 

@@ -324,7 +324,19 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
   // barriers and issues the first tiles' loads, warp 1 allocates TMEM, warps
   // 2-5 write the query operand.
   const int64_t cont_row0 = ((int64_t)b * c.kv_heads + h) * c.max_tokens;
-  // Issue the TMA copies of tile i into its stage (producer thread only).
+  // Issue the TMA copies of tile i into its stage.  Called by all 32 lanes
+  // of warp 0.  Contiguous layout: lane 0 issues the tile's few copies.
+  // Paged layout: lane j issues page j's copies (K and V boxes, scale rows),
+  // lane 0 arms the stage's barrier (the transaction count is signed, so a
+  // copy may land first); each lane holds its page id of the next tile,
+  // loaded one tile ahead so the table lookup overlaps the wait for a stage.
+  int my_page = 0;
+  auto load_page = [&](int i) {
+    if (!c.paged || i >= n_tiles) return;
+    const int t0 = (t_begin + i) * kMmaTile;
+    const int np = (min(kMmaTile, T - t0) + c.page_size - 1) / c.page_size;
+    if (lane < np) my_page = c.page_table[(int64_t)b * c.max_pages_per_seq + (t0 >> c.page_shift) + lane];
+  };
   auto produce = [&](int i) {
     const int s = i % C::NST;
     uint8_t* st = smem + s * C::STAGE;
@@ -333,40 +345,43 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
     const int t0 = (t_begin + i) * kMmaTile;
     const int valid = min(kMmaTile, T - t0);
     if (!c.paged) {
-      const int nsc = min(kMmaTile, (valid + 15) & ~15);
-      const uint32_t bytes = C::K_TILE + C::V_TILE + (KE == ELEM_E4M3 ? nsc * 4 : 0) +
-                             (VE == ELEM_E4M3 ? nsc * 4 : 0);
-      tma::arrive_expect_tx(&full[s], bytes);
-      const int row = (int)(cont_row0 + t0);
-      tma::load_2d(st, &tp.tmk, 0, row, &full[s]);
-      if (KE != ELEM_E4M3) tma::load_2d(st + kMmaTile * 128, &tp.tmk, 64, row, &full[s]);
-      tma::load_2d(st + C::K_TILE, &tp.tmv, 0, row, &full[s]);
-      if (VE != ELEM_E4M3) tma::load_2d(st + C::K_TILE + kMmaTile * 128, &tp.tmv, 64, row, &full[s]);
-      if (KE == ELEM_E4M3) tma::load_1d(kss, c.k_scale + cont_row0 + t0, nsc * 4, &full[s]);
-      if (VE == ELEM_E4M3) tma::load_1d(vss, c.v_scale + cont_row0 + t0, nsc * 4, &full[s]);
+      if (lane == 0) {
+        const int nsc = min(kMmaTile, (valid + 15) & ~15);
+        const uint32_t bytes = C::K_TILE + C::V_TILE + (KE == ELEM_E4M3 ? nsc * 4 : 0) +
+                               (VE == ELEM_E4M3 ? nsc * 4 : 0);
+        tma::arrive_expect_tx(&full[s], bytes);
+        const int row = (int)(cont_row0 + t0);
+        tma::load_2d(st, &tp.tmk, 0, row, &full[s]);
+        if (KE != ELEM_E4M3) tma::load_2d(st + kMmaTile * 128, &tp.tmk, 64, row, &full[s]);
+        tma::load_2d(st + C::K_TILE, &tp.tmv, 0, row, &full[s]);
+        if (VE != ELEM_E4M3) tma::load_2d(st + C::K_TILE + kMmaTile * 128, &tp.tmv, 64, row, &full[s]);
+        if (KE == ELEM_E4M3) tma::load_1d(kss, c.k_scale + cont_row0 + t0, nsc * 4, &full[s]);
+        if (VE == ELEM_E4M3) tma::load_1d(vss, c.v_scale + cont_row0 + t0, nsc * 4, &full[s]);
+      }
     } else {
       const int P = c.page_size;
       const int np = (valid + P - 1) / P;
       const uint32_t per_page = P * 128 * (C::KB + C::VB) + P * 4 * ((KE == ELEM_E4M3) + (VE == ELEM_E4M3));
-      tma::arrive_expect_tx(&full[s], per_page * np);
-      for (int j = 0; j < np; ++j) {
-        int page = c.page_table[(int64_t)b * c.max_pages_per_seq + ((t0 >> c.page_shift) + j)];
+      int page = my_page;
+      load_page(i + 1);
+      if (lane == 0) tma::arrive_expect_tx(&full[s], per_page * np);
+      if (lane < np) {
         if (page < 0 || page >= c.num_pages) {
           raise_error(p.err, FP8KV_DEVERR_BAD_PAGE);
           page = 0;      // read a valid page; the result is flagged as wrong
         }
         const int64_t row = ((int64_t)page * c.kv_heads + h) * P;
-        const int off = j * P * 128;
+        const int off = lane * P * 128;
         tma::load_2d(st + off, &tp.tmk, 0, (int)row, &full[s]);
         if (KE != ELEM_E4M3) tma::load_2d(st + kMmaTile * 128 + off, &tp.tmk, 64, (int)row, &full[s]);
         tma::load_2d(st + C::K_TILE + off, &tp.tmv, 0, (int)row, &full[s]);
         if (VE != ELEM_E4M3)
           tma::load_2d(st + C::K_TILE + kMmaTile * 128 + off, &tp.tmv, 64, (int)row, &full[s]);
-        if (KE == ELEM_E4M3) tma::load_1d(kss + j * P, c.k_scale + row, P * 4, &full[s]);
-        if (VE == ELEM_E4M3) tma::load_1d(vss + j * P, c.v_scale + row, P * 4, &full[s]);
+        if (KE == ELEM_E4M3) tma::load_1d(kss + lane * P, c.k_scale + row, P * 4, &full[s]);
+        if (VE == ELEM_E4M3) tma::load_1d(vss + lane * P, c.v_scale + row, P * 4, &full[s]);
       }
     }
-    TRACE(8 * i + 0);
+    if (lane == 0) TRACE(8 * i + 0);
   };
   const int n_first = min(min(n_tiles, C::NST), i_new);
   if (tid == 0) {
@@ -378,7 +393,13 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
     *abort_flag = 0;
     *last_flag = 0;
     umma::mbar_fence_init();
+  }
+  if (warp == 0) {
+    __syncwarp();
+    load_page(0);
     for (int i = 0; i < n_first; ++i) produce(i);
+  }
+  if (tid == 0) {
     for (int w = 0; w < 2; ++w)
       for (int i = 0; i < 2; ++i) {
         umma::mbar_init(&wb[w].s_full[i], 1);
@@ -491,17 +512,22 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int issued = n_first;
-      for (int i = n_first; i < n_tiles; ++i) {
-        const int s = i % C::NST, u = i / C::NST;
-        if (u > 0 && !wait_or_abort(&empty[s], (u - 1) & 1, abort_flag)) break;
-        if (i == i_new && !wait_or_abort(appended, 0, abort_flag)) break;
-        produce(i);
-        ++issued;
+    // (the whole warp: lane 0 waits for each stage and the others follow it)
+    int issued = n_first;
+    for (int i = n_first; i < n_tiles; ++i) {
+      const int s = i % C::NST, u = i / C::NST;
+      bool ok = true;
+      if (lane == 0) {
+        ok = u == 0 || wait_or_abort(&empty[s], (u - 1) & 1, abort_flag);
+        ok = ok && (i != i_new || wait_or_abort(appended, 0, abort_flag));
       }
-      // Before leaving, let every copy this thread issued land (only an
-      // aborted run has copies that nobody waited for).
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      produce(i);
+      ++issued;
+    }
+    // Before leaving, let every copy this warp issued land (only an aborted
+    // run has copies that nobody waited for).
+    if (lane == 0) {
       for (int i = max(0, issued - C::NST); i < issued; ++i)
         (void)umma::mbar_wait(&full[i % C::NST], (i / C::NST) & 1, 100000000ull);
       TRACE(1013);

@@ -81,10 +81,11 @@ typedef enum {
 
 typedef enum { FP8KV_OUT_BF16 = 0, FP8KV_OUT_F32 = 1 } fp8kv_out_dtype;
 
-/* Which split kernel a decode call runs.  AUTO picks per shape: the tensor
- * cores for head_dim 128 with 5 to 8 query heads per KV head, the CUDA cores
- * otherwise.  The tensor-core kernel (tcgen05) walks 128-token tiles and
- * needs head_dim 128; the CUDA-core kernel walks 64-token tiles. */
+/* Which split kernel a decode call runs.  AUTO picks the tensor cores
+ * wherever that kernel is built (head_dim 128, 1 to 8 query heads per KV
+ * head: it was measured faster at every group size), the CUDA cores
+ * otherwise.  The tensor-core kernel (tcgen05) walks 128-token tiles; the
+ * CUDA-core kernel walks 64-token tiles. */
 typedef enum {
   FP8KV_KERNEL_AUTO = 0,
   FP8KV_KERNEL_CUDA_CORES = 1,
