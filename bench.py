@@ -61,6 +61,7 @@ def parse(argv=None):
                     help="launch every step only after the previous one finished (no early cache read)")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-shapes", action="store_true")
+    ap.add_argument("--no-interval", action="store_true")
     return ap.parse_args(argv)
 
 
@@ -582,6 +583,69 @@ def measure_shapes(args):
     return res
 
 
+def measure_interval(args):
+    """Steady-state tile initiation interval of the tensor-core decode split:
+    the slope of the step time against the context length (2K-16K tokens) at
+    a fixed 4 splits, batch 16, 16 q / 2 KV heads, head_dim 128, times the
+    tokens a CTA covers per 128-token tile.  Per cache dtype; 8 rotated layer
+    caches, plain launches, CUDA-graph replay."""
+    import fp8_quantized_kv_gb300 as fk
+    ctxs = (2048, 4096, 8192, 16384)
+    S = 4
+    res = {}
+    spec0 = synth.WORKLOADS[WORKLOAD]
+    B, Hq, Hkv, D = spec0.batch, spec0.q_heads, spec0.kv_heads, spec0.head_dim
+    for dtype in ("k8v8", "k16v8", "k16v16"):
+        pts = []
+        for T in ctxs:
+            spec = synth.DecodeWorkload("ii", B, Hq, Hkv, D, seed=2, seq_lens=(T,) * B)
+            inp = synth.decode_inputs(spec, device="cuda")
+            sidx = torch.repeat_interleave(torch.arange(B), torch.full((B,), T)).to(torch.int32).cuda()
+            pos = torch.arange(T, dtype=torch.int32).repeat(B).cuda()
+            knew, vnew = inp.k[T - 1::T].contiguous(), inp.v[T - 1::T].contiguous()
+            lens = inp.seq_lens.cuda()
+            q = inp.q.contiguous()
+            caches = []
+            for _ in range(8):
+                c = fk.Fp8KVCache.contiguous(B, Hkv, D, T, dtype)
+                fk.fp8kv_append(c, inp.k.contiguous(), inp.v.contiguous(), sidx, pos)
+                caches.append(c)
+            out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+            wss = [torch.zeros(fk.fp8kv_decode_step_workspace_bytes(c, Hq, S, "tensor_cores"), dtype=torch.uint8,
+                               device="cuda") for c in caches]
+
+            def step(i):
+                fk.fp8kv_decode_step(q, knew, vnew, caches[i % 8], lens, out=out, workspace=wss[i % 8],
+                                     num_splits=S, kernel="tensor_cores")
+            for i in range(5):
+                step(i)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(200):
+                    step(i)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            pts.append((T, e0.elapsed_time(e1) / 200 * 1e3))
+            del g, caches, wss
+            torch.cuda.empty_cache()
+        n = len(pts)
+        mx = sum(t for t, _ in pts) / n
+        my = sum(u for _, u in pts) / n
+        slope = sum((t - mx) * (u - my) for t, u in pts) / sum((t - mx) ** 2 for t, _ in pts)   # us per token
+        res[dtype] = {"us_at_ctx": {str(t): u for t, u in pts}, "fixed_us": my - slope * mx,
+                      "interval_us_per_tile": slope * 128 * S,
+                      "note": "one CTA's 128-token tile; 128 CTAs stream at once"}
+    if fk.fp8kv_get_device_error() != 0:
+        raise RuntimeError("interval sweep: device error")
+    return res
+
+
 def measure_variant(spec, dtype, args, ws, inp, flags=None):
     if flags is None:
         flags = 0 if args.plain_launch else STEP_EARLY_CACHE_READ
@@ -666,6 +730,7 @@ def run_gpu(args, ws, rank):
 
     prefill = None if args.no_prefill else measure_prefill(args, ws)
     shapes = None if args.no_shapes else measure_shapes(args)
+    interval = None if args.no_interval else measure_interval(args)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -696,7 +761,7 @@ def run_gpu(args, ws, rank):
             "gpu_launches": (1 if tensor else 3) * args.steps,
             "kernels_us": None if per is None else {k.replace("_ms", "_us"): v * 1e3 for k, v in per.items()},
             "clocks": clocks, "controls": controls, "plain_launch": plain, "prefill": prefill,
-            "shapes": shapes,
+            "shapes": shapes, "initiation_interval": interval,
         }
         print(json.dumps(line), flush=True)
 
