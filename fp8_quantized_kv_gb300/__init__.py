@@ -20,8 +20,8 @@ import torch
 
 from ._lib import EXPORTS, CacheStruct, get_lib
 
-K8V8, K16V8, K16V16 = 0, 1, 2
-DTYPES = {"k8v8": K8V8, "k16v8": K16V8, "k16v16": K16V16}
+K8V8, K16V8, K16V16, K8V16 = 0, 1, 2, 3
+DTYPES = {"k8v8": K8V8, "k16v8": K16V8, "k16v16": K16V16, "k8v16": K8V16}
 LAYOUT_CONTIGUOUS, LAYOUT_PAGED = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
 
@@ -96,7 +96,7 @@ class Fp8KVCache:
     @staticmethod
     def _alloc(dtype, lead, head_dim, device):
         dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
-        k8, v8 = dt == K8V8, dt != K16V16
+        k8, v8 = dt in (K8V8, K8V16), dt in (K8V8, K16V8)
         kel = torch.uint8 if k8 else torch.bfloat16
         vel = torch.uint8 if v8 else torch.bfloat16
         k = torch.zeros(lead + (head_dim,), dtype=kel, device=device)
@@ -289,4 +289,4 @@ __all__ = ["Fp8KVCache", "Fp8KVError", "fp8kv_quantize", "fp8kv_append",
            "fp8kv_decode_merge", "fp8kv_decode_attention", "fp8kv_decode_step",
            "fp8kv_decode_step_workspace_bytes",
            "fp8kv_prefill_attention", "fp8kv_get_device_error", "fp8kv_status_string",
-           "EXPORTS", "K8V8", "K16V8", "K16V16"]
+           "EXPORTS", "K8V8", "K16V8", "K16V16", "K8V16"]

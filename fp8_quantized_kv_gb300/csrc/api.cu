@@ -47,13 +47,13 @@ static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 static fp8kv_status check_cache(const fp8kv_cache* c, CacheView* view) {
   if (c == nullptr) return FP8KV_ERR_INVALID_ARG;
-  if (c->dtype < FP8KV_K8V8 || c->dtype > FP8KV_K16V16) return FP8KV_ERR_INVALID_ARG;
+  if (c->dtype < FP8KV_K8V8 || c->dtype > FP8KV_K8V16) return FP8KV_ERR_INVALID_ARG;
   if (c->layout != FP8KV_LAYOUT_CONTIGUOUS && c->layout != FP8KV_LAYOUT_PAGED) return FP8KV_ERR_INVALID_ARG;
   if (c->batch < 0 || c->kv_heads <= 0 || c->head_dim <= 0) return FP8KV_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return FP8KV_ERR_UNSUPPORTED;
   if (c->k == nullptr || c->v == nullptr) return FP8KV_ERR_INVALID_ARG;
-  const bool k8 = c->dtype == FP8KV_K8V8;
-  const bool v8 = c->dtype != FP8KV_K16V16;
+  const bool k8 = c->dtype == FP8KV_K8V8 || c->dtype == FP8KV_K8V16;
+  const bool v8 = c->dtype == FP8KV_K8V8 || c->dtype == FP8KV_K16V8;
   if (k8 != (c->k_scale != nullptr) || v8 != (c->v_scale != nullptr)) return FP8KV_ERR_INVALID_ARG;
   // 16-byte vector copies read the cache: every base pointer must be aligned
   const uintptr_t align = (uintptr_t)c->k | (uintptr_t)c->v | (uintptr_t)c->k_scale |

@@ -418,6 +418,7 @@ template <int D>
 static cudaError_t launch_fma_d(const DecodeParams& p, int dtype, dim3 grid, cudaStream_t st) {
   if (dtype == FP8KV_K8V8) return launch_fma_g<D, ELEM_E4M3, ELEM_E4M3>(p, grid, st);
   if (dtype == FP8KV_K16V8) return launch_fma_g<D, ELEM_BF16, ELEM_E4M3>(p, grid, st);
+  if (dtype == FP8KV_K8V16) return launch_fma_g<D, ELEM_E4M3, ELEM_BF16>(p, grid, st);
   return launch_fma_g<D, ELEM_BF16, ELEM_BF16>(p, grid, st);
 }
 

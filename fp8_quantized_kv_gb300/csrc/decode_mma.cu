@@ -66,13 +66,14 @@ struct TcCfg {
   static constexpr int K_TILE = kMmaTile * D * KB;
   static constexpr int V_TILE = kMmaTile * D * VB;
   static constexpr int STAGE = ((K_TILE + V_TILE + 2 * kMmaTile * 4) + 1023) / 1024 * 1024;
-  static constexpr int NST = (KE == ELEM_E4M3 && VE == ELEM_E4M3) ? 6 : (VE == ELEM_E4M3 ? 4 : 3);
+  static constexpr int NST = (KE == ELEM_E4M3 && VE == ELEM_E4M3) ? 6 : (KE == VE ? 3 : 4);
   static constexpr int QOP = KE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;
   static constexpr int POP = VE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;   // [128 tokens][16 or 32 B]
   static constexpr int XO = 8 * 128 * 4;    // group 1's O handed to group 0
   static constexpr int MISC = 6656;         // barriers, small tables, cluster receive buffers
   static constexpr int BYTES = NST * STAGE + QOP + 4 * POP + XO + MISC + 1024;
   static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+  static_assert(NST * STAGE >= (8 * 48 * D + 2 * 8 * 48) * 4, "ring too small to stage 48 partials for the merge");
 };
 
 struct DecodeTmaParams {
@@ -1087,6 +1088,7 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int dtype, int batch, cudaS
   dim3 grid(p.num_splits, p.c.kv_heads, batch);
   if (dtype == FP8KV_K8V8) return launch_tc_t<ELEM_E4M3, ELEM_E4M3>(p, grid, st);
   if (dtype == FP8KV_K16V8) return launch_tc_t<ELEM_BF16, ELEM_E4M3>(p, grid, st);
+  if (dtype == FP8KV_K8V16) return launch_tc_t<ELEM_E4M3, ELEM_BF16>(p, grid, st);
   return launch_tc_t<ELEM_BF16, ELEM_BF16>(p, grid, st);
 }
 

@@ -175,6 +175,8 @@ static void append_dispatch(int dtype, unsigned grid, cudaStream_t s, const Cach
     append_kernel<EPL, ELEM_E4M3, ELEM_E4M3><<<grid, 256, 0, s>>>(c, k, v, si, ps, n, err);
   else if (dtype == FP8KV_K16V8)
     append_kernel<EPL, ELEM_BF16, ELEM_E4M3><<<grid, 256, 0, s>>>(c, k, v, si, ps, n, err);
+  else if (dtype == FP8KV_K8V16)
+    append_kernel<EPL, ELEM_E4M3, ELEM_BF16><<<grid, 256, 0, s>>>(c, k, v, si, ps, n, err);
   else
     append_kernel<EPL, ELEM_BF16, ELEM_BF16><<<grid, 256, 0, s>>>(c, k, v, si, ps, n, err);
 }
@@ -202,6 +204,8 @@ static void append_step_dispatch(int dtype, unsigned grid, cudaStream_t s, const
     append_step_kernel<EPL, ELEM_E4M3, ELEM_E4M3><<<grid, 256, 0, s>>>(c, k, v, lens, err);
   else if (dtype == FP8KV_K16V8)
     append_step_kernel<EPL, ELEM_BF16, ELEM_E4M3><<<grid, 256, 0, s>>>(c, k, v, lens, err);
+  else if (dtype == FP8KV_K8V16)
+    append_step_kernel<EPL, ELEM_E4M3, ELEM_BF16><<<grid, 256, 0, s>>>(c, k, v, lens, err);
   else
     append_step_kernel<EPL, ELEM_BF16, ELEM_BF16><<<grid, 256, 0, s>>>(c, k, v, lens, err);
 }

@@ -67,7 +67,8 @@ typedef enum {
 typedef enum {
   FP8KV_K8V8 = 0,    /* K codes, V codes (symmetric FP8)            */
   FP8KV_K16V8 = 1,   /* K bf16, V codes (no K transform)           */
-  FP8KV_K16V16 = 2   /* K bf16, V bf16 (the bf16-cache control)     */
+  FP8KV_K16V16 = 2,  /* K bf16, V bf16 (the bf16-cache control)     */
+  FP8KV_K8V16 = 3    /* K codes, V bf16 (the remaining control)     */
 } fp8kv_kv_dtype;
 
 typedef enum {

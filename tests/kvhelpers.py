@@ -34,6 +34,16 @@ def fill_cache(inp: synth.DecodeInputs, dtype: str, device="cuda", capacity=None
     return cache
 
 
+def k_fp8(dtype: str) -> bool:
+    """Whether the cache dtype stores K as e4m3 codes (else bf16)."""
+    return dtype in ("k8v8", "k8v16")
+
+
+def v_fp8(dtype: str) -> bool:
+    """Whether the cache dtype stores V as e4m3 codes (else bf16)."""
+    return dtype in ("k8v8", "k16v8")
+
+
 def seq_bits(inp: synth.DecodeInputs, which: str, b: int):
     """bf16 bits of sequence b's K or V rows, as [Hkv, T_b, D]."""
     t = inp.k if which == "k" else inp.v
@@ -45,7 +55,7 @@ def oracle_kv(inp: synth.DecodeInputs, dtype: str, b: int):
     """fp64 K and V of sequence b as the cache holds them: e4m3 round trip
     for an FP8 side, the bf16 value for a bf16 side.  [Hkv, T_b, D]."""
     out = []
-    for which, fp8 in (("k", dtype == "k8v8"), ("v", dtype != "k16v16")):
+    for which, fp8 in (("k", k_fp8(dtype)), ("v", v_fp8(dtype))):
         bits = seq_bits(inp, which, b)
         if fp8:
             c, s = oracle.quantize(bits)

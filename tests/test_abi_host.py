@@ -90,6 +90,20 @@ def test_argument_checks_return_before_any_launch(lib):
     assert lib.fp8kv_prefill_attention(0x7000, r(c), 0x8000, 0, 16, 0.1, 2, out, 0, None) == 0
 
 
+def test_cache_dtype_and_scale_pointers(lib):
+    # each dtype wants a scale row exactly for its e4m3 sides:
+    # K8V8 both, K16V8 V only, K16V16 none, K8V16 K only; ids past K8V16 are unknown
+    r = ctypes.byref
+    for dtype, k8, v8 in ((0, 1, 1), (1, 0, 1), (2, 0, 0), (3, 1, 0)):
+        for ks in (0, 1):
+            for vs in (0, 1):
+                c = _cache(dtype=dtype, k_scale=0x3000 if ks else None, v_scale=0x4000 if vs else None)
+                want = 64 if (ks, vs) == (k8, v8) else 0
+                assert lib.fp8kv_decode_num_splits(r(c), 16, 64, 2) == want, (dtype, ks, vs)
+    assert lib.fp8kv_decode_num_splits(r(_cache(dtype=4)), 16, 64, 2) == 0
+    assert lib.fp8kv_decode_num_splits(r(_cache(dtype=-1)), 16, 64, 2) == 0
+
+
 def test_split_plan_and_workspace(lib):
     c = _cache()
     r = ctypes.byref

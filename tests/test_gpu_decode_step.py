@@ -12,7 +12,7 @@ import fp8_quantized_kv_gb300 as fk
 from kvhelpers import assert_gate, fill_cache, oracle_decode
 
 pytestmark = pytest.mark.gpu
-DTYPES = ["k8v8", "k16v8", "k16v16"]
+DTYPES = ["k8v8", "k16v8", "k16v16", "k8v16"]
 
 
 @pytest.fixture(autouse=True)

@@ -14,10 +14,11 @@ import torch
 import oracle
 from fp8_quantized_kv_gb300 import synth
 import fp8_quantized_kv_gb300 as fk
-from kvhelpers import (assert_gate, fill_cache, gpu_decode, oracle_decode, oracle_kv, seq_bits)
+from kvhelpers import (assert_gate, fill_cache, gpu_decode, k_fp8, oracle_decode, oracle_kv, seq_bits,
+                       v_fp8)
 
 pytestmark = pytest.mark.gpu
-DTYPES = ["k8v8", "k16v8", "k16v16"]
+DTYPES = ["k8v8", "k16v8", "k16v16", "k8v16"]
 KERNELS = ["cuda_cores", "tensor_cores"]
 
 
@@ -83,7 +84,7 @@ def test_append_bit_exact(dtype, paged):
     assert fk.fp8kv_get_device_error() == 0
     for b in range(3):
         T = int(inp.seq_lens[b])
-        for which, fp8 in (("k", dtype == "k8v8"), ("v", dtype != "k16v16")):
+        for which, fp8 in (("k", k_fp8(dtype)), ("v", v_fp8(dtype))):
             store = cache.k if which == "k" else cache.v
             if store.dtype == torch.bfloat16:
                 store = store.view(torch.int16)
@@ -293,11 +294,8 @@ def _prefill_case(n_q, pos0, Hq, Hkv, D, dtype, seed, sample_blocks=None, kernel
                                      out_dtype=torch.float32, kernel=kernel)[0].cpu().numpy()
     kb = synth.bf16_bits(pin.k).transpose(1, 0, 2)
     vb = synth.bf16_bits(pin.v).transpose(1, 0, 2)
-    if dtype == "k8v8":
-        k = oracle.dequantize(*oracle.quantize(kb))
-    else:
-        k = oracle.bf16_to_double(kb)
-    v = oracle.bf16_to_double(vb) if dtype == "k16v16" else oracle.dequantize(*oracle.quantize(vb))
+    k = oracle.dequantize(*oracle.quantize(kb)) if k_fp8(dtype) else oracle.bf16_to_double(kb)
+    v = oracle.dequantize(*oracle.quantize(vb)) if v_fp8(dtype) else oracle.bf16_to_double(vb)
     q = oracle.bf16_to_double(synth.bf16_bits(pin.q))
     sm = 1 / math.sqrt(D)
     blocks = sample_blocks or [(0, n_q)]
