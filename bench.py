@@ -36,7 +36,8 @@ from fp8_quantized_kv_gb300 import synth  # noqa: E402
 
 WORKLOAD = "decode_b16_ctx8192"
 METRIC = "decode attn KV-read GB/s (% of HBM peak) and µs/layer at B16 ctx8192, 1 GB300"
-KERNEL_IDS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
+KERNEL_IDS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2, "tensor_cores_k_f16": 3,
+              "tensor_cores_k_f16_producer": 4}
 PAGE_NUMBER_GBS = 550.0   # the pages' figure for this workload (RTX 5070 Ti, Triton, codes only)
 # fp8kv_decode_step flag: each layer's step streams its own cache while the
 # previous layer's step finishes (programmatic dependent launch); the layers'
@@ -53,7 +54,7 @@ def parse(argv=None):
     ap.add_argument("--dtype", default="k8v8", choices=["k8v8", "k16v8", "k16v16", "k8v16"])
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--chunk", type=int, default=200)
-    ap.add_argument("--kernel", default="auto", choices=["auto", "cuda_cores", "tensor_cores"])
+    ap.add_argument("--kernel", default="auto", choices=list(KERNEL_IDS))
     ap.add_argument("--no-controls", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-steps", type=int, default=200)
@@ -646,10 +647,11 @@ def measure_interval(args):
     return res
 
 
-def measure_variant(spec, dtype, args, ws, inp, flags=None):
+def measure_variant(spec, dtype, args, ws, inp, flags=None, kernel=None):
     if flags is None:
         flags = 0 if args.plain_launch else STEP_EARLY_CACHE_READ
-    layers, dev = build_layers(spec, dtype, args.layers, inp, KERNEL_IDS[args.kernel], flags)
+    kid = KERNEL_IDS[args.kernel if kernel is None else kernel]
+    layers, dev = build_layers(spec, dtype, args.layers, inp, kid, flags)
     for i in range(max(3, args.warmup)):                      # eager warm-up steps
         L = layers[i % len(layers)]
         L.step(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
@@ -684,7 +686,7 @@ def run_gpu(args, ws, rank):
     e2e_ms, e2e_val = aggregate(nb["step"], args.steps, e2e_ms, ws)
     sampler.stop()
 
-    tensor = args.kernel in ("auto", "tensor_cores")
+    tensor = args.kernel != "cuda_cores"
     roof = None
     if tensor:
         # the tensor-core step is one kernel (append + split + merge): its
@@ -728,6 +730,24 @@ def run_gpu(args, ws, rank):
             del ls
             torch.cuda.empty_cache()
 
+    # where K is prepared: the native e4m3 QK against the transform path (each
+    # K tile converted to f16 in shared memory, 16-bit QK), same step, same
+    # launch mode
+    transform = None
+    if not args.no_controls and args.dtype == "k8v8" and args.kernel in ("auto", "tensor_cores"):
+        transform = {"native_e4m3_qk": {"us_per_layer": ms_per_step * 1e3, "GBps": value}}
+        for kname, who in (("tensor_cores_k_f16", "the softmax warpgroup that owns the tile"),
+                           ("tensor_cores_k_f16_producer", "the TMA producer warp")):
+            ls, _, xms, _, _ = measure_variant(spec, "k8v8", args, ws, inp, kernel=kname)
+            xms = max_over_ranks(xms, ws)
+            transform[kname] = {"us_per_layer": xms / args.steps * 1e3,
+                                "GBps": nb["step"] * args.steps / (xms * 1e-3) / 1e9,
+                                "converted_by": who}
+            del ls
+            torch.cuda.empty_cache()
+        transform["note"] = ("transform path: each K tile converted to f16 in shared memory, QK as kind::f16 "
+                             "on an f16 query; 4 cache stages instead of 6 (the two f16 K buffers take the room)")
+
     prefill = None if args.no_prefill else measure_prefill(args, ws)
     shapes = None if args.no_shapes else measure_shapes(args)
     interval = None if args.no_interval else measure_interval(args)
@@ -760,7 +780,8 @@ def run_gpu(args, ws, rank):
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": (1 if tensor else 3) * args.steps,
             "kernels_us": None if per is None else {k.replace("_ms", "_us"): v * 1e3 for k, v in per.items()},
-            "clocks": clocks, "controls": controls, "plain_launch": plain, "prefill": prefill,
+            "clocks": clocks, "controls": controls, "transform_path": transform, "plain_launch": plain,
+            "prefill": prefill,
             "shapes": shapes, "initiation_interval": interval,
         }
         print(json.dumps(line), flush=True)

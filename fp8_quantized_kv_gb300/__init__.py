@@ -28,7 +28,10 @@ OUT_BF16, OUT_F32 = 0, 1
 DEVERR_SEQ_TOO_LONG, DEVERR_BAD_PAGE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 STEP_EARLY_CACHE_READ = 0x1
 KERNEL_AUTO, KERNEL_CUDA_CORES, KERNEL_TENSOR_CORES = 0, 1, 2
-KERNELS = {"auto": KERNEL_AUTO, "cuda_cores": KERNEL_CUDA_CORES, "tensor_cores": KERNEL_TENSOR_CORES}
+KERNEL_TENSOR_CORES_K_F16, KERNEL_TENSOR_CORES_K_F16_PRODUCER = 3, 4
+KERNELS = {"auto": KERNEL_AUTO, "cuda_cores": KERNEL_CUDA_CORES, "tensor_cores": KERNEL_TENSOR_CORES,
+           "tensor_cores_k_f16": KERNEL_TENSOR_CORES_K_F16,
+           "tensor_cores_k_f16_producer": KERNEL_TENSOR_CORES_K_F16_PRODUCER}
 
 STATUS_NAMES = {0: "FP8KV_OK", 1: "FP8KV_ERR_INVALID_ARG", 2: "FP8KV_ERR_UNSUPPORTED",
                 3: "FP8KV_ERR_WORKSPACE", 4: "FP8KV_ERR_CUDA", 5: "FP8KV_ERR_TIMEOUT",
@@ -169,7 +172,8 @@ def fp8kv_decode_attention(q: torch.Tensor, cache: Fp8KVCache, seq_lens: torch.T
                            out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
                            workspace: Optional[torch.Tensor] = None, kernel=0, stream=None):
     """q [B, Hq, D] bf16, seq_lens [B] int32 -> out [B, Hq, D] (bf16 or fp32).
-    kernel: "auto" / "cuda_cores" / "tensor_cores" (or 0 / 1 / 2)."""
+    kernel: "auto" / "cuda_cores" / "tensor_cores" / "tensor_cores_k_f16" /
+    "tensor_cores_k_f16_producer" (or 0 .. 4)."""
     _need(q, torch.bfloat16, "q")
     _need(seq_lens, torch.int32, "seq_lens")
     B, Hq, D = q.shape

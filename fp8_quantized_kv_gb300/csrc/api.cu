@@ -105,6 +105,8 @@ static int resolve_kernel(const fp8kv_cache* c, int q_heads, int requested) {
   const int G = q_heads / c->kv_heads;
   const bool mma_ok = c->head_dim == 128 && G >= 1 && G <= 8;
   if (requested == FP8KV_KERNEL_TENSOR_CORES) return mma_ok ? FP8KV_KERNEL_TENSOR_CORES : 0;
+  if (requested == FP8KV_KERNEL_TENSOR_CORES_K_F16 || requested == FP8KV_KERNEL_TENSOR_CORES_K_F16_PRODUCER)
+    return mma_ok && c->dtype == FP8KV_K8V8 ? requested : 0;
   if (requested == FP8KV_KERNEL_CUDA_CORES) return FP8KV_KERNEL_CUDA_CORES;
   if (requested != FP8KV_KERNEL_AUTO) return 0;
   // measured on the B16 decode (G 1, 2, 4, 8) and the paged B64 decode
@@ -113,7 +115,7 @@ static int resolve_kernel(const fp8kv_cache* c, int q_heads, int requested) {
 }
 
 static SplitPlan plan_splits(const fp8kv_cache* c, int requested, int kernel) {
-  const bool tc = kernel == FP8KV_KERNEL_TENSOR_CORES;
+  const bool tc = kernel >= FP8KV_KERNEL_TENSOR_CORES;
   const int tile = tc ? 128 : kTileTokens;
   const int max_tiles = (capacity_of(c) + tile - 1) / tile;
   if (max_tiles <= 0) return {1, 1, tile, kernel};
@@ -218,7 +220,7 @@ fp8kv_status prepare_decode(const void* q, const fp8kv_cache* cache, const int32
   fp8kv_status st = check_cache(cache, &view);
   if (st != FP8KV_OK) return st;
   if (q_heads <= 0 || q_heads % cache->kv_heads != 0 || num_splits < 0) return FP8KV_ERR_INVALID_ARG;
-  if (kernel < FP8KV_KERNEL_AUTO || kernel > FP8KV_KERNEL_TENSOR_CORES) return FP8KV_ERR_INVALID_ARG;
+  if (kernel < FP8KV_KERNEL_AUTO || kernel > FP8KV_KERNEL_TENSOR_CORES_K_F16_PRODUCER) return FP8KV_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return FP8KV_ERR_INVALID_ARG;
   const int G = q_heads / cache->kv_heads;
   if (G > 8) return FP8KV_ERR_UNSUPPORTED;
@@ -250,7 +252,8 @@ fp8kv_status prepare_decode(const void* q, const fp8kv_cache* cache, const int32
   p->fused = 0;
   p->cluster = 0;
   p->pdl = 0;
-  *resolved = k;
+  p->k_f16 = k == FP8KV_KERNEL_TENSOR_CORES_K_F16 ? 1 : k == FP8KV_KERNEL_TENSOR_CORES_K_F16_PRODUCER ? 2 : 0;
+  *resolved = k >= FP8KV_KERNEL_TENSOR_CORES ? FP8KV_KERNEL_TENSOR_CORES : k;
   return FP8KV_OK;
 }
 

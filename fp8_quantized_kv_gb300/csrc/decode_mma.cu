@@ -52,6 +52,8 @@
 // (cluster_exchange: each rank merges a slice of the head dimension).
 // Otherwise every split writes its partial to global memory and the last
 // one to finish, found with an atomic counter, merges them all.
+#include <cuda_fp16.h>
+
 #include "params.cuh"
 #include "tc_common.cuh"
 
@@ -59,21 +61,33 @@ namespace fp8kv {
 
 constexpr int kMmaTile = 128;
 
-template <int KE, int VE>
+// XK: where K is prepared (an ablation).  XK_NATIVE: QK is the native e4m3
+// MMA on the query's e4m3 hi/lo pair.  On the transform path each landed
+// e4m3 K tile is converted to f16 in shared memory and QK runs as kind::f16
+// on an f16 query, the conversion done by the producer warp (XK_PRODUCER)
+// or by the softmax warpgroup that owns the tile (XK_CONSUMER).  The K scale
+// stays in score space on every path.
+enum : int { XK_NATIVE = 0, XK_PRODUCER = 1, XK_CONSUMER = 2 };
+
+template <int KE, int VE, int XK = XK_NATIVE>
 struct TcCfg {
   static constexpr int D = 128;
+  static constexpr bool QHL = KE == ELEM_E4M3 && XK == XK_NATIVE;   // query as an e4m3 hi/lo pair
   static constexpr int KB = KE == ELEM_E4M3 ? 1 : 2, VB = VE == ELEM_E4M3 ? 1 : 2;
   static constexpr int K_TILE = kMmaTile * D * KB;
   static constexpr int V_TILE = kMmaTile * D * VB;
   static constexpr int STAGE = ((K_TILE + V_TILE + 2 * kMmaTile * 4) + 1023) / 1024 * 1024;
-  static constexpr int NST = (KE == ELEM_E4M3 && VE == ELEM_E4M3) ? 6 : (KE == VE ? 3 : 4);
-  static constexpr int QOP = KE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;
+  static constexpr int NST = XK != XK_NATIVE ? 4 : (KE == ELEM_E4M3 && VE == ELEM_E4M3) ? 6 : (KE == VE ? 3 : 4);
+  static constexpr int KCV = XK != XK_NATIVE ? 2 * kMmaTile * D * 2 : 0;   // two converted f16 K tiles
+  static constexpr int QOP = QHL ? 16 * 128 : 2 * 16 * 128;
   static constexpr int POP = VE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;   // [128 tokens][16 or 32 B]
   static constexpr int XO = 8 * 128 * 4;    // group 1's O handed to group 0
   static constexpr int MISC = 6656;         // barriers, small tables, cluster receive buffers
-  static constexpr int BYTES = NST * STAGE + QOP + 4 * POP + XO + MISC + 1024;
+  static constexpr int BYTES = NST * STAGE + KCV + QOP + 4 * POP + XO + MISC + 1024;
   static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
-  static_assert(NST * STAGE >= (8 * 48 * D + 2 * 8 * 48) * 4, "ring too small to stage 48 partials for the merge");
+  static_assert(NST * STAGE + KCV >= (8 * 48 * D + 2 * 8 * 48) * 4,
+                "ring too small to stage 48 partials for the merge");
+  static_assert(XK == XK_NATIVE || KE == ELEM_E4M3, "the K transform converts e4m3 codes");
 };
 
 struct DecodeTmaParams {
@@ -221,14 +235,50 @@ __device__ __forceinline__ uint32_t cluster_rx_bytes(int rank, int S) {
   return (uint32_t)(S * (128 * (g4_lo(rank + 1, S) - g4_lo(rank, S)) + 64));
 }
 
-template <int KE, int VE>
+// One e4m3 K tile (K-major, 128-byte swizzle: row r = token, 16-byte chunk
+// c = dims 16c..16c+15 at chunk position c ^ (r & 7)) -> the f16 K operand:
+// two 64-dim atoms of the same swizzle (atom a holds dims 64a..64a+63, one
+// 128-byte row per token).  Every e4m3 value is exact in f16.  Called by the
+// NT threads (32: one warp, 128: a warpgroup), idx = 0..NT-1: thread = (row,
+// chunk), so each group of eight consecutive threads reads one whole 128-byte
+// row.  Eight rows' loads are issued before any store (the compiler cannot
+// move a load above a store to the same shared memory), so their latencies
+// overlap.
+template <int NT>
+__device__ __forceinline__ void k_tile_to_f16(const uint8_t* src, uint8_t* dst, int idx) {
+  constexpr int RP = NT / 8;                      // rows per pass
+  const int c = idx & 7, a = c >> 2, c0 = 2 * (c & 3);
+#pragma unroll 1
+  for (int r0 = idx >> 3; r0 < kMmaTile; r0 += 8 * RP) {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = r0 + RP * j;
+      v[j] = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = r0 + RP * j;
+      uint8_t* row = dst + a * (kMmaTile * 128) + r * 128;
+      *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) =
+          make_uint4(e4m3x2_to_f16x2((uint16_t)v[j].x), e4m3x2_to_f16x2((uint16_t)(v[j].x >> 16)),
+                     e4m3x2_to_f16x2((uint16_t)v[j].y), e4m3x2_to_f16x2((uint16_t)(v[j].y >> 16)));
+      *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) =
+          make_uint4(e4m3x2_to_f16x2((uint16_t)v[j].z), e4m3x2_to_f16x2((uint16_t)(v[j].z >> 16)),
+                     e4m3x2_to_f16x2((uint16_t)v[j].w), e4m3x2_to_f16x2((uint16_t)(v[j].w >> 16)));
+    }
+  }
+}
+
+template <int KE, int VE, int XK>
 __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant__ DecodeTmaParams tp) {
-  using C = TcCfg<KE, VE>;
+  using C = TcCfg<KE, VE, XK>;
   constexpr int D = 128;
   const DecodeParams& p = tp.p;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* qop = smem + C::NST * C::STAGE;
+  uint8_t* kcv = smem + C::NST * C::STAGE;                  // [2] f16 K tiles (transform path)
+  uint8_t* qop = kcv + C::KCV;
   uint8_t* pop0 = qop + C::QOP;                            // [wg][buffer] P operands
   float* xo = reinterpret_cast<float*>(pop0 + 4 * C::POP);   // [8][128]
   uint8_t* misc = pop0 + 4 * C::POP + C::XO;
@@ -240,6 +290,8 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
   uint32_t* tslot = reinterpret_cast<uint32_t*>(rx_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tslot + 2);
+  uint64_t* kc_full = reinterpret_cast<uint64_t*>(misc + 320);   // [2] transform path: f16 K tile ready
+  uint64_t* kc_empty = kc_full + 2;                              // [2] its QK completed
   float* qscale = reinterpret_cast<float*>(misc + 512);    // [8]
   float* red = qscale + 8;                                 // [wg][2][4][9]
   float* lred = red + 144;                                 // [wg][4][8]
@@ -410,6 +462,11 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         umma::mbar_init(&wb[w].o_empty[i], 4);
       }
     umma::mbar_init(appended, 1);
+    if (XK != XK_NATIVE)
+      for (int i = 0; i < 2; ++i) {
+        umma::mbar_init(&kc_full[i], XK == XK_CONSUMER ? 4 : 1);   // the owning group's four warps
+        umma::mbar_init(&kc_empty[i], 1);
+      }
     if (p.cluster) {
       umma::mbar_init(rx_bar, 1);
       tma::arrive_expect_tx(rx_bar, cluster_rx_bytes(split, S));
@@ -440,7 +497,19 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[e] = __bfloat162float(qr[e]);
       }
-      if constexpr (KE == ELEM_E4M3) {
+      if constexpr (XK != XK_NATIVE) {
+        // f16 query for the f16 QK: each head's row scaled by a power of two
+        // so its largest magnitude lies in [2^14, 2^15) (bf16 -> f16 exact)
+        float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+        amax = warp_max_redux(amax);
+        int e = 0;
+        (void)frexpf(amax, &e);
+        const int ex = e - 15;
+        if (lane == 0) qscale[g] = ldexpf(1.0f, ex);
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4)
+          *reinterpret_cast<__half*>(qop + sw128_off(g, (lane * 4 + e4) * 2, 16)) = __float2half_rn(ldexpf(x[e4], -ex));
+      } else if constexpr (KE == ELEM_E4M3) {
         float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
         amax = warp_max_redux(amax);
         const int ex = e4m3_row_exp(amax);
@@ -515,16 +584,69 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
     // ------------------------------------------------------------ producer
     // (the whole warp: lane 0 waits for each stage and the others follow it)
     int issued = n_first;
-    for (int i = n_first; i < n_tiles; ++i) {
-      const int s = i % C::NST, u = i / C::NST;
-      bool ok = true;
-      if (lane == 0) {
-        ok = u == 0 || wait_or_abort(&empty[s], (u - 1) & 1, abort_flag);
-        ok = ok && (i != i_new || wait_or_abort(appended, 0, abort_flag));
+    if constexpr (XK != XK_PRODUCER) {
+      for (int i = n_first; i < n_tiles; ++i) {
+        const int s = i % C::NST, u = i / C::NST;
+        bool ok = true;
+        if (lane == 0) {
+          ok = u == 0 || wait_or_abort(&empty[s], (u - 1) & 1, abort_flag);
+          ok = ok && (i != i_new || wait_or_abort(appended, 0, abort_flag));
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        produce(i);
+        ++issued;
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      produce(i);
-      ++issued;
+    } else {
+      // Transform path: issue tiles as stages free up and convert each
+      // landed K tile into the free f16 buffer, whichever is ready first.
+      int nc = 0;
+      long long t_prog = clock64();
+      uint32_t idle = 0;
+      while (nc < n_tiles) {
+        bool prog = false;
+        if (issued < n_tiles) {
+          const int i = issued, s = i % C::NST, u = i / C::NST;
+          int ready = 0;
+          if (lane == 0)
+            ready = (u == 0 || umma::mbar_test(&empty[s], (u - 1) & 1)) &&
+                    (i != i_new || umma::mbar_test(appended, 0));
+          if (__shfl_sync(0xffffffffu, ready, 0)) {
+            produce(i);
+            ++issued;
+            prog = true;
+          }
+        }
+        if (nc < issued) {
+          const int s = nc % C::NST, u = nc / C::NST, kb = nc & 1, ku = nc >> 1;
+          int ready = 0;
+          if (lane == 0)
+            ready = umma::mbar_test(&full[s], u & 1) && (ku == 0 || umma::mbar_test(&kc_empty[kb], (ku - 1) & 1));
+          if (__shfl_sync(0xffffffffu, ready, 0)) {
+            k_tile_to_f16<32>(smem + s * C::STAGE, kcv + kb * (kMmaTile * D * 2), lane);
+            umma::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              umma::mbar_arrive(&kc_full[kb]);
+              TRACE(8 * nc + 7);
+            }
+            ++nc;
+            prog = true;
+          }
+        }
+        if (prog) {
+          idle = 0;
+          continue;
+        }
+        __nanosleep(20);
+        if ((++idle & 63) == 0) {
+          if (idle == 64) t_prog = clock64();
+          if (*abort_flag) break;
+          if (clock64() - t_prog > kWaitLimitCycles) {
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
     }
     // Before leaving, let every copy this warp issued land (only an aborted
     // run has copies that nobody waited for).
@@ -552,14 +674,27 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         bool prog = false;
         if (nq < n_tiles) {
           const int s = nq % C::NST, u = nq / C::NST, w = nq & 1, li = nq >> 1, bb = li & 1, ub = li >> 1;
-          if (umma::mbar_test(&full[s], u & 1) &&
-              (ub == 0 || umma::mbar_test(&wb[w].s_empty[bb], (ub - 1) & 1))) {
+          const bool k_ready = XK != XK_NATIVE ? umma::mbar_test(&kc_full[nq & 1], (nq >> 1) & 1)
+                                               : umma::mbar_test(&full[s], u & 1);
+          if (k_ready && (ub == 0 || umma::mbar_test(&wb[w].s_empty[bb], (ub - 1) & 1))) {
             umma::fence_after_sync();
-            const uint32_t ka = umma::smem_u32(smem + s * C::STAGE);
+            const uint32_t ka =
+                umma::smem_u32(XK != XK_NATIVE ? kcv + (nq & 1) * (kMmaTile * D * 2) : smem + s * C::STAGE);
             // four independent accumulators (one per 32-byte k-step) so the
             // thin MMAs pipeline instead of waiting on each other
             const uint32_t d = tmem + 256 * w + 64 * bb;
-            if constexpr (KE == ELEM_E4M3) {
+            if constexpr (XK != XK_NATIVE) {
+              constexpr uint32_t ID_F16 =
+                  umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_K, umma::MAJOR_K, 128, 16);
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                umma::mma_f16_ss(d + 16 * (k & 3),
+                                 umma::sdesc(ka + (k >> 2) * (kMmaTile * 128) + (k & 3) * 32, 16, 1024,
+                                             umma::SWIZZLE_128B),
+                                 umma::sdesc(qa + (k >> 2) * (16 * 128) + (k & 3) * 32, 16, 1024,
+                                             umma::SWIZZLE_128B),
+                                 ID_F16, k >= 4);
+            } else if constexpr (KE == ELEM_E4M3) {
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 umma::mma_f8_ss(d + 16 * k, umma::sdesc(ka + k * 32, 16, 1024, umma::SWIZZLE_128B),
@@ -575,6 +710,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
                                  ID_QK, k >= 4);
             }
             umma::mma_commit(&wb[w].s_full[bb]);
+            if (XK == XK_PRODUCER) umma::mma_commit(&kc_empty[nq & 1]);
             TRACE(8 * nq + 1);
             ++nq;
             prog = true;
@@ -583,7 +719,8 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         if (np < nq) {
           const int j = np, s = j % C::NST, w = j & 1, lj = j >> 1, bb = lj & 1, ub = lj >> 1;
           if (umma::mbar_test(&wb[w].p_full[bb], ub & 1) &&
-              (ub == 0 || umma::mbar_test(&wb[w].o_empty[bb], (ub - 1) & 1))) {
+              (ub == 0 || umma::mbar_test(&wb[w].o_empty[bb], (ub - 1) & 1)) &&
+              (XK == XK_NATIVE || umma::mbar_test(&full[s], (j / C::NST) & 1))) {
             umma::fence_after_sync();
             const uint32_t va = umma::smem_u32(smem + s * C::STAGE + C::K_TILE);
             const uint32_t pa = umma::smem_u32(pop0 + (2 * w + bb) * C::POP);
@@ -648,6 +785,16 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
       if (li < nl) {
         const int i = 2 * li + wg;
         const int s = i % C::NST, u = i / C::NST, bb = li & 1, ub = li >> 1;
+        if constexpr (XK == XK_CONSUMER) {
+          // convert this tile's K into the group's own f16 buffer (free: the
+          // group consumed the S of its previous tile, so that QK is done)
+          const bool landed = wait_or_abort(&full[s], u & 1, abort_flag);
+          if (group_any(wg, !landed)) { failed = true; break; }
+          k_tile_to_f16<128>(smem + s * C::STAGE, kcv + wg * (kMmaTile * D * 2), t);
+          umma::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) umma::mbar_arrive(&kc_full[wg]);
+        }
         bool ok = wait_or_abort(&B.s_full[bb], ub & 1, abort_flag);
         ok = ok && wait_or_abort(&full[s], u & 1, abort_flag);
         if (group_any(wg, !ok)) { failed = true; break; }
@@ -680,7 +827,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         float* rb = red + (wg * 2 + (li & 1)) * 36;
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          const float raw = KE == ELEM_E4M3 ? (sc[g] + sc[g + 8]) : sc[g];
+          const float raw = C::QHL ? (sc[g] + sc[g + 8]) : sc[g];
           sg[g] = tok_ok ? raw * (qs[g] * kf) : -INFINITY;
           const float wm = warp_max_redux(sg[g]);
           if (lane == 0) rb[sw * 9 + g] = wm;
@@ -1029,10 +1176,10 @@ static bool cluster_fits(const void* fn, dim3 grid, int smem) {
   return (long long)max_clusters >= (long long)grid.y * grid.z;
 }
 
-template <int KE, int VE>
+template <int KE, int VE, int XK = XK_NATIVE>
 static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st) {
-  constexpr int smem = TcCfg<KE, VE>::BYTES;
-  cudaError_t e = ensure_smem_optin((const void*)decode_split_tc<KE, VE>, smem);
+  constexpr int smem = TcCfg<KE, VE, XK>::BYTES;
+  cudaError_t e = ensure_smem_optin((const void*)decode_split_tc<KE, VE, XK>, smem);
   if (e != cudaSuccess) return e;
   DecodeTmaParams tp;
   const CacheView& c = p.c;
@@ -1045,7 +1192,7 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
     return cudaErrorInvalidValue;
   tp.p = p;
   tp.p.cluster = 0;
-  const void* fn = (const void*)decode_split_tc<KE, VE>;
+  const void* fn = (const void*)decode_split_tc<KE, VE, XK>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(320);
@@ -1068,7 +1215,7 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  const cudaError_t e2 = cudaLaunchKernelEx(&cfg, decode_split_tc<KE, VE>, tp);
+  const cudaError_t e2 = cudaLaunchKernelEx(&cfg, decode_split_tc<KE, VE, XK>, tp);
   if (e2 != cudaSuccess) (void)cudaGetLastError();
   return e2;
 }
@@ -1086,7 +1233,11 @@ extern "C" __attribute__((visibility("default"))) int fp8kv_trace_read_cta(unsig
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int dtype, int batch, cudaStream_t st) {
   dim3 grid(p.num_splits, p.c.kv_heads, batch);
-  if (dtype == FP8KV_K8V8) return launch_tc_t<ELEM_E4M3, ELEM_E4M3>(p, grid, st);
+  if (dtype == FP8KV_K8V8) {
+    if (p.k_f16 == 1) return launch_tc_t<ELEM_E4M3, ELEM_E4M3, XK_CONSUMER>(p, grid, st);
+    if (p.k_f16 == 2) return launch_tc_t<ELEM_E4M3, ELEM_E4M3, XK_PRODUCER>(p, grid, st);
+    return launch_tc_t<ELEM_E4M3, ELEM_E4M3>(p, grid, st);
+  }
   if (dtype == FP8KV_K16V8) return launch_tc_t<ELEM_BF16, ELEM_E4M3>(p, grid, st);
   if (dtype == FP8KV_K8V16) return launch_tc_t<ELEM_E4M3, ELEM_BF16>(p, grid, st);
   return launch_tc_t<ELEM_BF16, ELEM_BF16>(p, grid, st);

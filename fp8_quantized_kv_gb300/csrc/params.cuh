@@ -25,6 +25,8 @@ struct DecodeParams {
   int fused;
   int cluster;               // fused step launched with the splits of a (sequence, KV head) as one cluster
   int pdl;                   // fused step launched as a programmatic dependent of the previous kernel
+  int k_f16;                 // tensor-core kernel on the transform path (K converted to f16 on chip):
+                             // 0 no, 1 by the softmax warpgroups, 2 by the producer warp
 };
 
 struct PrefillParams {

@@ -90,7 +90,20 @@ typedef enum { FP8KV_OUT_BF16 = 0, FP8KV_OUT_F32 = 1 } fp8kv_out_dtype;
 typedef enum {
   FP8KV_KERNEL_AUTO = 0,
   FP8KV_KERNEL_CUDA_CORES = 1,
-  FP8KV_KERNEL_TENSOR_CORES = 2
+  FP8KV_KERNEL_TENSOR_CORES = 2,
+  /* Decode only, K8V8 at head_dim 128: the tensor-core kernel on the
+   * transform path.  Each landed e4m3 K tile is converted to f16 in shared
+   * memory and QK runs as a 16-bit MMA on an f16 query, in place of the
+   * native e4m3 QK; V, P and the merge are unchanged.  _K_F16: the softmax
+   * warpgroup that owns the tile converts it; _K_F16_PRODUCER: the TMA
+   * producer warp does.  Comparison points for where the K preparation runs
+   * ("FP8 KV attention: hardware paths and tile preparation", sections
+   * "Measure the BF16-Q/FP8-KV transform path" and "Pipeline the existing
+   * transform"); AUTO never picks them.  Rejected (FP8KV_ERR_UNSUPPORTED)
+   * for other dtypes and head dims, and by the prefill
+   * (FP8KV_ERR_INVALID_ARG). */
+  FP8KV_KERNEL_TENSOR_CORES_K_F16 = 3,
+  FP8KV_KERNEL_TENSOR_CORES_K_F16_PRODUCER = 4
 } fp8kv_decode_kernel;
 
 /* Device error word bits (fp8kv_get_device_error). */

@@ -104,6 +104,27 @@ def test_cache_dtype_and_scale_pointers(lib):
     assert lib.fp8kv_decode_num_splits(r(_cache(dtype=-1)), 16, 64, 2) == 0
 
 
+def test_transform_path_kernel_ids(lib):
+    # kernels 3 and 4 (tensor cores, K converted to f16 on chip): K8V8 at
+    # head_dim 128 only, planned like the tensor-core kernel; unknown ids rejected
+    r = ctypes.byref
+    c = _cache()
+    for kid in (3, 4):
+        assert lib.fp8kv_decode_num_splits(r(c), 16, 0, kid) == lib.fp8kv_decode_num_splits(r(c), 16, 0, 2)
+        assert (lib.fp8kv_decode_workspace_bytes(r(c), 16, 0, kid)
+                == lib.fp8kv_decode_workspace_bytes(r(c), 16, 0, 2))
+        assert lib.fp8kv_decode_num_splits(r(_cache(dtype=1, k_scale=None)), 16, 0, kid) == 0
+        assert lib.fp8kv_decode_num_splits(r(_cache(dtype=3, v_scale=None)), 16, 0, kid) == 0
+        assert lib.fp8kv_decode_num_splits(r(_cache(head_dim=64)), 16, 0, kid) == 0
+    assert lib.fp8kv_decode_num_splits(r(c), 16, 0, 5) == 0
+    out = 0x6000
+    assert lib.fp8kv_decode_split(None, r(c), None, 16, 0.1, 0, 5, None, 0, None) == 1
+    assert lib.fp8kv_decode_split(None, r(_cache(dtype=2, k_scale=None, v_scale=None)), None, 16, 0.1, 0, 3,
+                                  None, 0, None) == 2
+    # the prefill has no transform-path kernel
+    assert lib.fp8kv_prefill_attention(0x7000, r(c), 0x8000, 64, 16, 0.1, 3, out, 0, None) == 1
+
+
 def test_split_plan_and_workspace(lib):
     c = _cache()
     r = ctypes.byref
