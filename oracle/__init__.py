@@ -15,6 +15,8 @@ Sources (page title, section):
     the error report ``fp8_kv_error``.
   * "03 · 8n — FA-style tiled prefill attention", sections 2.1 and 3.1: causal
     prefill masking by position and GQA slicing.
+  * "FP8 KV attention: hardware paths and tile preparation", section "Measure
+    block-scaled QK": MXFP8 keys, one E8M0 scale per 32-element block.
 """
 import ctypes
 import os
@@ -45,6 +47,8 @@ def _load():
         lib.fp8kv_oracle_bf16_to_double.argtypes = [c_u16_p, i64, c_dbl_p]
         lib.fp8kv_oracle_quantize.argtypes = [c_u16_p, i64, i32, c_u8_p, c_f32_p]
         lib.fp8kv_oracle_dequantize.argtypes = [c_u8_p, c_f32_p, i64, i32, c_dbl_p]
+        lib.fp8kv_oracle_mx_quantize.argtypes = [c_u16_p, i64, i32, c_u8_p, c_u8_p]
+        lib.fp8kv_oracle_mx_dequantize.argtypes = [c_u8_p, c_u8_p, i64, i32, c_dbl_p]
         lib.fp8kv_oracle_gather_paged.restype = ctypes.c_int
         lib.fp8kv_oracle_gather_paged.argtypes = [
             c_u8_p, i32, i32, i32, i32, c_i32_p, i32, i32, i32, c_u8_p]
@@ -124,6 +128,39 @@ def dequantize(codes, scales):
     out = np.empty(c.shape, dtype=np.float64)
     lib.fp8kv_oracle_dequantize(_ptr(c, ctypes.c_uint8), _ptr(s, ctypes.c_float),
                                 rows, d, _ptr(out, ctypes.c_double))
+    return out
+
+
+# ----------------------------------------------------------------- MXFP8 --
+
+def mx_quantize(x_bits):
+    """Rows of bf16 bits [..., D] (D a multiple of 32) -> (codes u8 [..., D],
+    E8M0 bytes u8 [..., D/32]): one power-of-two scale per 32-element block,
+    the smallest with amax <= 448 * scale ("FP8 KV attention: hardware paths
+    and tile preparation", section "Measure block-scaled QK")."""
+    lib = _load()
+    x = _c(x_bits, np.uint16)
+    d = x.shape[-1]
+    assert d % 32 == 0
+    rows = x.size // d if d else 0
+    codes = np.empty(x.shape, dtype=np.uint8)
+    scales = np.empty(x.shape[:-1] + (d // 32,), dtype=np.uint8)
+    lib.fp8kv_oracle_mx_quantize(_ptr(x, ctypes.c_uint16), rows, d,
+                                 _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8))
+    return codes, scales
+
+
+def mx_dequantize(codes, scales):
+    """codes [..., D] and E8M0 bytes [..., D/32] -> fp64 values [..., D]."""
+    lib = _load()
+    c = _c(codes, np.uint8)
+    s = _c(scales, np.uint8)
+    d = c.shape[-1]
+    rows = c.size // d if d else 0
+    assert s.size == rows * (d // 32)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib.fp8kv_oracle_mx_dequantize(_ptr(c, ctypes.c_uint8), _ptr(s, ctypes.c_uint8),
+                                   rows, d, _ptr(out, ctypes.c_double))
     return out
 
 

@@ -37,6 +37,17 @@
  *  - Causal prefill ("03 · 8n", section 3.1, masked positions): query i at
  *    absolute position pos0 + i attends keys j <= pos0 + i.
  *
+ *  - MXFP8 block scales ("FP8 KV attention: hardware paths and tile
+ *    preparation", section "Measure block-scaled QK": D = C + (SFA*A)@(SFB*B)
+ *    with one E8M0 scale per 32-element block).  The page does not say how a
+ *    block's scale is chosen; the reading taken is the per-token rule of the
+ *    fp8_kv page (the scale maps amax to 448) restricted to the powers of two
+ *    an E8M0 byte can hold: X = 2^E with E the smallest integer such that
+ *    amax <= 448 * 2^E, clamped to [-127, 127], so no element saturates.
+ *    Each element is encoded from the fp32 product x * 2^-E.  The byte is
+ *    E + 127 (an all-zero block gets E = -127, byte 0).  Dequantisation:
+ *    decode(code) * 2^E.
+ *
  *  - Paged addressing: token t of sequence b lives in page
  *    page_table[b][t / page_size] at offset t % page_size ("FP8 KV attention:
  *    hardware paths and tile preparation", section "Collect the profiler
@@ -141,6 +152,53 @@ void fp8kv_oracle_dequantize(const uint8_t *codes, const float *scales,
   for (int64_t r = 0; r < rows; ++r)
     for (int i = 0; i < d; ++i)
       out[r * d + i] = fp8kv_oracle_e4m3_decode(codes[r * d + i]) * (double)scales[r];
+}
+
+/* ------------------------------------------------------------- MXFP8 -- */
+
+/* Exponent E of a block's E8M0 scale: the smallest integer with
+ * amax <= 448 * 2^E, clamped to [-127, 127].  With amax = m * 2^e,
+ * m in [0.5, 1) (frexp): 448 * 2^(e-9) = 0.875 * 2^e, so E = e - 9 when
+ * m <= 0.875 and E = e - 8 otherwise. */
+static int mx_block_exponent(float amax) {
+  if (amax == 0.0f) return -127;
+  int e = 0;
+  const float m = frexpf(amax, &e);
+  int E = m <= 0.875f ? e - 9 : e - 8;
+  if (E < -127) E = -127;
+  if (E > 127) E = 127;
+  return E;
+}
+
+/* Rows of d bf16 values (d a multiple of 32) -> e4m3 codes and one E8M0
+ * byte per 32-element block: scales[r * (d / 32) + blk]. */
+void fp8kv_oracle_mx_quantize(const uint16_t *x, int64_t rows, int d,
+                              uint8_t *codes, uint8_t *scales) {
+  const int nb = d / 32;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int blk = 0; blk < nb; ++blk) {
+      const uint16_t *xb = x + r * d + blk * 32;
+      float amax = 0.0f;
+      for (int i = 0; i < 32; ++i) {
+        const float a = fabsf(bf16_bits_to_float(xb[i]));
+        if (a > amax) amax = a;
+      }
+      const int E = mx_block_exponent(amax);
+      scales[r * nb + blk] = (uint8_t)(E + 127);
+      const float inv = ldexpf(1.0f, -E);      /* exact: a power of two */
+      for (int i = 0; i < 32; ++i)
+        codes[r * d + blk * 32 + i] = fp8kv_oracle_e4m3_encode(bf16_bits_to_float(xb[i]) * inv);
+    }
+}
+
+/* codes x 2^(byte - 127) per 32-element block -> fp64 values. */
+void fp8kv_oracle_mx_dequantize(const uint8_t *codes, const uint8_t *scales,
+                                int64_t rows, int d, double *out) {
+  const int nb = d / 32;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int i = 0; i < d; ++i)
+      out[r * d + i] = fp8kv_oracle_e4m3_decode(codes[r * d + i]) *
+                       ldexp(1.0, (int)scales[r * nb + i / 32] - 127);
 }
 
 /* ---------------------------------------------------------- paged cache -- */

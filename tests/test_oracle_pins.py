@@ -180,6 +180,91 @@ def test_quantize_zero_row_and_single_spike():
     assert np.all(codes[2] == 0x7E) and scales[2] == np.float32(1.0) / np.float32(448)
 
 
+# ----------------------------------------------------------------- MXFP8 --
+
+def _mx_worked_row():
+    kv = {}
+    with open(os.path.join(GOLDEN, "mx_quantize_worked_row.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                key, *vals = line.split()
+                kv[key] = [int(h, 16) for h in vals]
+    return kv
+
+
+def test_mx_quantize_worked_row():
+    kv = _mx_worked_row()
+    assert len(kv["input"]) == 128 and len(kv["codes"]) == 128 and len(kv["e8m0"]) == 4
+    codes, scales = oracle.mx_quantize(np.array(kv["input"], dtype=np.uint16)[None, :])
+    assert [int(c) for c in codes[0]] == kv["codes"]
+    assert [int(b) for b in scales[0]] == kv["e8m0"]
+
+
+def _mx_rows(seed, n=256, d=128):
+    """bf16 rows whose 32-element blocks span 2^-140 .. 2^120 in magnitude,
+    with zero blocks, single spikes and bf16 subnormals."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(n, d, generator=g) * torch.exp2(torch.randint(-140, 120, (n, d // 32), generator=g)
+                                                  .float().repeat_interleave(32, dim=1))
+    x[::17, :32] = 0.0
+    x[5::23, 40] = 1e30
+    return synth.bf16_bits(x.to(torch.bfloat16))
+
+
+def test_mx_scale_is_the_smallest_power_of_two_that_fits():
+    bits = _mx_rows(11)
+    x = oracle.bf16_to_double(bits).reshape(-1, 4, 32)
+    _, scales = oracle.mx_quantize(bits)
+    E = scales.reshape(-1, 4).astype(np.int64) - 127
+    amax = np.abs(x).max(axis=-1)
+    X = np.ldexp(1.0, E)
+    assert np.all(amax <= 448.0 * X)
+    nz = amax > 0
+    # one power of two smaller would overflow 448 (unless E is already -127)
+    assert np.all((amax[nz] > 448.0 * X[nz] / 2) | (E[nz] == -127))
+    assert np.all(E[~nz] == -127)
+
+
+def test_mx_elements_are_nearest_e4m3_of_the_scaled_value():
+    bits = _mx_rows(12)
+    x = oracle.bf16_to_double(bits)
+    codes, scales = oracle.mx_quantize(bits)
+    X = np.ldexp(1.0, scales.astype(np.int64) - 127).repeat(32, axis=-1)
+    deq = oracle.mx_dequantize(codes, scales)
+    assert np.array_equal(deq, oracle.e4m3_decode(codes) * X)
+    # brute force: the dequantised value is a nearest E4M3 grid point of x/X
+    grid = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    grid = np.unique(grid[np.isfinite(grid)])
+    y = (x / X).ravel()
+    d_best = np.abs(grid[None, :] - y[:, None]).min(axis=1)
+    got = (deq / X).ravel()
+    # fp32 rounding of x * 2^-E only matters below the fp32 normal range
+    assert np.all(np.abs(got - y) <= d_best * (1 + 1e-12) + 2.0 ** -149)
+    # and never beyond half the top binade's spacing (16) times X
+    assert np.all(np.abs(deq - x) <= 16 * X)
+
+
+def test_mx_round_trip_is_exact_on_the_grid():
+    bits = _mx_rows(13)
+    codes, scales = oracle.mx_quantize(bits)
+    deq = oracle.mx_dequantize(codes, scales)
+    again = synth.bf16_bits(torch.from_numpy(deq).to(torch.bfloat16))
+    assert np.array_equal(oracle.bf16_to_double(again), deq)        # the grid fits in bf16 here
+    c2, s2 = oracle.mx_quantize(again)
+    assert np.array_equal(oracle.mx_dequantize(c2, s2), deq)
+
+
+def test_mx_scaling_by_powers_of_two_moves_only_the_scale():
+    g = torch.Generator().manual_seed(14)
+    x = torch.randn(32, 128, generator=g).to(torch.bfloat16)
+    c0, s0 = oracle.mx_quantize(synth.bf16_bits(x))
+    for k in (-20, -3, 5, 40):
+        ck, sk = oracle.mx_quantize(synth.bf16_bits(x * (2.0 ** k)))
+        assert np.array_equal(ck, c0)
+        assert np.array_equal(sk.astype(int), s0.astype(int) + k)
+
+
 # ------------------------------------------------------------- attention --
 
 def _brute_attention(q, k, v, sm_scale):
