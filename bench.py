@@ -51,7 +51,7 @@ def parse(argv=None):
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="fp8kv", choices=["fp8kv", "reference"])
-    ap.add_argument("--dtype", default="k8v8", choices=["k8v8", "k16v8", "k16v16", "k8v16"])
+    ap.add_argument("--dtype", default="k8v8", choices=["k8v8", "k16v8", "k16v16", "k8v16", "mxk8v8"])
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--chunk", type=int, default=200)
     ap.add_argument("--kernel", default="auto", choices=list(KERNEL_IDS))
@@ -112,7 +112,7 @@ def step_bytes(spec, dtype, T):
     """Algorithmic bytes of one step: KV codes (or bf16) + scales read, Q read,
     O written (bf16), plus the appended token's rows (bf16 in, cache out)."""
     B, Hq, Hkv, D = spec.batch, spec.q_heads, spec.kv_heads, spec.head_dim
-    k8, v8 = dtype in ("k8v8", "k8v16"), dtype in ("k8v8", "k16v8")
+    k8, v8 = dtype in ("k8v8", "k8v16", "mxk8v8"), dtype in ("k8v8", "k16v8", "mxk8v8")
     row_bytes = D * ((1 if k8 else 2) + (1 if v8 else 2)) + 4 * (int(k8) + int(v8))
     kv = B * Hkv * T * row_bytes
     qo = 2 * B * Hq * D * 2
@@ -596,7 +596,7 @@ def measure_interval(args):
     res = {}
     spec0 = synth.WORKLOADS[WORKLOAD]
     B, Hq, Hkv, D = spec0.batch, spec0.q_heads, spec0.kv_heads, spec0.head_dim
-    for dtype in ("k8v8", "k16v8", "k8v16", "k16v16"):
+    for dtype in ("k8v8", "mxk8v8", "k16v8", "k8v16", "k16v16"):
         pts = []
         for T in ctxs:
             spec = synth.DecodeWorkload("ii", B, Hq, Hkv, D, seed=2, seq_lens=(T,) * B)
@@ -718,7 +718,7 @@ def run_gpu(args, ws, rank):
     del layers
     torch.cuda.empty_cache()
     if not args.no_controls:
-        for other in ("k8v8", "k16v8", "k8v16", "k16v16"):
+        for other in ("k8v8", "mxk8v8", "k16v8", "k8v16", "k16v16"):
             if other == args.dtype:
                 continue
             ls, _, tms, pr, _ = measure_variant(spec, other, args, ws, inp)

@@ -20,8 +20,8 @@ import torch
 
 from ._lib import EXPORTS, CacheStruct, get_lib
 
-K8V8, K16V8, K16V16, K8V16 = 0, 1, 2, 3
-DTYPES = {"k8v8": K8V8, "k16v8": K16V8, "k16v16": K16V16, "k8v16": K8V16}
+K8V8, K16V8, K16V16, K8V16, MXK8V8 = 0, 1, 2, 3, 4
+DTYPES = {"k8v8": K8V8, "k16v8": K16V8, "k16v16": K16V16, "k8v16": K8V16, "mxk8v8": MXK8V8}
 LAYOUT_CONTIGUOUS, LAYOUT_PAGED = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
 
@@ -99,12 +99,15 @@ class Fp8KVCache:
     @staticmethod
     def _alloc(dtype, lead, head_dim, device):
         dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
-        k8, v8 = dt in (K8V8, K8V16), dt in (K8V8, K16V8)
+        k8, v8 = dt in (K8V8, K8V16, MXK8V8), dt in (K8V8, K16V8, MXK8V8)
         kel = torch.uint8 if k8 else torch.bfloat16
         vel = torch.uint8 if v8 else torch.bfloat16
         k = torch.zeros(lead + (head_dim,), dtype=kel, device=device)
         v = torch.zeros(lead + (head_dim,), dtype=vel, device=device)
-        ks = torch.zeros(lead, dtype=torch.float32, device=device) if k8 else None
+        if dt == MXK8V8:    # the four E8M0 block bytes of each row in its 4-byte slot
+            ks = torch.zeros(lead + (4,), dtype=torch.uint8, device=device)
+        else:
+            ks = torch.zeros(lead, dtype=torch.float32, device=device) if k8 else None
         vs = torch.zeros(lead, dtype=torch.float32, device=device) if v8 else None
         return k, v, ks, vs
 
@@ -138,6 +141,22 @@ def fp8kv_quantize(x: torch.Tensor, codes: Optional[torch.Tensor] = None,
         scales = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
     _check(get_lib().fp8kv_quantize(_ptr(x), rows, D, _ptr(codes), _ptr(scales), _stream(stream)),
            "fp8kv_quantize")
+    return codes, scales
+
+
+def fp8kv_quantize_mx(x: torch.Tensor, codes: Optional[torch.Tensor] = None,
+                      scales: Optional[torch.Tensor] = None, stream=None):
+    """bf16 rows [..., D] (D 64 or 128) -> (uint8 codes [..., D], uint8 E8M0
+    block scales [..., D/32]): MXFP8, one power-of-two scale per 32 elements."""
+    _need(x, torch.bfloat16, "x")
+    D = x.shape[-1]
+    rows = x.numel() // D if D else 0
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(x.shape[:-1] + (max(D // 32, 1),), dtype=torch.uint8, device=x.device)
+    _check(get_lib().fp8kv_quantize_mx(_ptr(x), rows, D, _ptr(codes), _ptr(scales), _stream(stream)),
+           "fp8kv_quantize_mx")
     return codes, scales
 
 
@@ -288,9 +307,9 @@ def fp8kv_status_string(status: int) -> str:
     return get_lib().fp8kv_status_string(status).decode()
 
 
-__all__ = ["Fp8KVCache", "Fp8KVError", "fp8kv_quantize", "fp8kv_append",
+__all__ = ["Fp8KVCache", "Fp8KVError", "fp8kv_quantize", "fp8kv_quantize_mx", "fp8kv_append",
            "fp8kv_decode_num_splits", "fp8kv_decode_workspace_bytes", "fp8kv_decode_split",
            "fp8kv_decode_merge", "fp8kv_decode_attention", "fp8kv_decode_step",
            "fp8kv_decode_step_workspace_bytes",
            "fp8kv_prefill_attention", "fp8kv_get_device_error", "fp8kv_status_string",
-           "EXPORTS", "K8V8", "K16V8", "K16V16", "K8V16"]
+           "EXPORTS", "K8V8", "K16V8", "K16V16", "K8V16", "MXK8V8"]

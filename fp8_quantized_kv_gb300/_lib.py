@@ -12,6 +12,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libfp8kv.so")
 
 EXPORTS = (
     "fp8kv_quantize",
+    "fp8kv_quantize_mx",
     "fp8kv_append",
     "fp8kv_decode_num_splits",
     "fp8kv_decode_workspace_bytes",
@@ -66,6 +67,7 @@ def get_lib() -> ctypes.CDLL:
     cp = ctypes.POINTER(CacheStruct)
     sig = {
         "fp8kv_quantize": (i32, [vp, i64, i32, vp, vp, vp]),
+        "fp8kv_quantize_mx": (i32, [vp, i64, i32, vp, vp, vp]),
         "fp8kv_append": (i32, [cp, vp, vp, vp, vp, i64, vp]),
         "fp8kv_decode_num_splits": (i32, [cp, i32, i32, i32]),
         "fp8kv_decode_workspace_bytes": (sz, [cp, i32, i32, i32]),

@@ -47,13 +47,14 @@ static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 static fp8kv_status check_cache(const fp8kv_cache* c, CacheView* view) {
   if (c == nullptr) return FP8KV_ERR_INVALID_ARG;
-  if (c->dtype < FP8KV_K8V8 || c->dtype > FP8KV_K8V16) return FP8KV_ERR_INVALID_ARG;
+  if (c->dtype < FP8KV_K8V8 || c->dtype > FP8KV_MXK8V8) return FP8KV_ERR_INVALID_ARG;
   if (c->layout != FP8KV_LAYOUT_CONTIGUOUS && c->layout != FP8KV_LAYOUT_PAGED) return FP8KV_ERR_INVALID_ARG;
   if (c->batch < 0 || c->kv_heads <= 0 || c->head_dim <= 0) return FP8KV_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return FP8KV_ERR_UNSUPPORTED;
+  if (c->dtype == FP8KV_MXK8V8 && c->head_dim != 128) return FP8KV_ERR_UNSUPPORTED;
   if (c->k == nullptr || c->v == nullptr) return FP8KV_ERR_INVALID_ARG;
-  const bool k8 = c->dtype == FP8KV_K8V8 || c->dtype == FP8KV_K8V16;
-  const bool v8 = c->dtype == FP8KV_K8V8 || c->dtype == FP8KV_K16V8;
+  const bool k8 = c->dtype == FP8KV_K8V8 || c->dtype == FP8KV_K8V16 || c->dtype == FP8KV_MXK8V8;
+  const bool v8 = c->dtype == FP8KV_K8V8 || c->dtype == FP8KV_K16V8 || c->dtype == FP8KV_MXK8V8;
   if (k8 != (c->k_scale != nullptr) || v8 != (c->v_scale != nullptr)) return FP8KV_ERR_INVALID_ARG;
   // 16-byte vector copies read the cache: every base pointer must be aligned
   const uintptr_t align = (uintptr_t)c->k | (uintptr_t)c->v | (uintptr_t)c->k_scale |
@@ -104,6 +105,11 @@ struct SplitPlan { int splits, chunk_tiles, tile, kernel; };
 static int resolve_kernel(const fp8kv_cache* c, int q_heads, int requested) {
   const int G = q_heads / c->kv_heads;
   const bool mma_ok = c->head_dim == 128 && G >= 1 && G <= 8;
+  // MXFP8 keys: the tensor-core kernel only (its QK already keeps one
+  // accumulator per 32-dim block, where the block scales apply)
+  if (c->dtype == FP8KV_MXK8V8)
+    return (requested == FP8KV_KERNEL_AUTO || requested == FP8KV_KERNEL_TENSOR_CORES) && mma_ok
+               ? FP8KV_KERNEL_TENSOR_CORES : 0;
   if (requested == FP8KV_KERNEL_TENSOR_CORES) return mma_ok ? FP8KV_KERNEL_TENSOR_CORES : 0;
   if (requested == FP8KV_KERNEL_TENSOR_CORES_K_F16 || requested == FP8KV_KERNEL_TENSOR_CORES_K_F16_PRODUCER)
     return mma_ok && c->dtype == FP8KV_K8V8 ? requested : 0;
@@ -172,6 +178,14 @@ fp8kv_status fp8kv_quantize(const void* x, int64_t rows, int32_t head_dim, uint8
   if (head_dim != 64 && head_dim != 128) return FP8KV_ERR_UNSUPPORTED;
   if (rows > 0 && (x == nullptr || codes == nullptr || scales == nullptr)) return FP8KV_ERR_INVALID_ARG;
   return cuda_status(launch_quantize(x, rows, head_dim, codes, scales, (cudaStream_t)stream));
+}
+
+fp8kv_status fp8kv_quantize_mx(const void* x, int64_t rows, int32_t head_dim, uint8_t* codes, uint8_t* scales,
+                               fp8kv_stream_t stream) {
+  if (rows < 0) return FP8KV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return FP8KV_ERR_UNSUPPORTED;
+  if (rows > 0 && (x == nullptr || codes == nullptr || scales == nullptr)) return FP8KV_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_mx(x, rows, head_dim, codes, scales, (cudaStream_t)stream));
 }
 
 fp8kv_status fp8kv_append(const fp8kv_cache* cache, const void* k_new, const void* v_new,
@@ -360,6 +374,7 @@ fp8kv_status fp8kv_prefill_attention(const void* q, const fp8kv_cache* cache, co
   if (!std::isfinite(sm_scale)) return FP8KV_ERR_INVALID_ARG;
   if (q_heads / cache->kv_heads > 16) return FP8KV_ERR_UNSUPPORTED;
   if (kernel < FP8KV_KERNEL_AUTO || kernel > FP8KV_KERNEL_TENSOR_CORES) return FP8KV_ERR_INVALID_ARG;
+  if (cache->dtype == FP8KV_MXK8V8) return FP8KV_ERR_UNSUPPORTED;     // decode only
   const bool tc_built = cache->dtype == FP8KV_K8V8 && cache->head_dim == 128;
   if (kernel == FP8KV_KERNEL_TENSOR_CORES && !tc_built) return FP8KV_ERR_UNSUPPORTED;
   const bool use_tc = kernel == FP8KV_KERNEL_TENSOR_CORES || (kernel == FP8KV_KERNEL_AUTO && tc_built);

@@ -15,7 +15,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTwoPow120 = 1.329227995784916e36f;   // 2^120, exact in fp32
 
 // Cache element kinds, resolved at compile time per kernel instance.
-enum : int { ELEM_E4M3 = 0, ELEM_BF16 = 1 };
+// ELEM_MX: e4m3 codes with one E8M0 (power-of-two) scale per 32-element
+// block of the row, the block scales of a row packed into its 4-byte scale
+// slot (byte b = block b); K side only.
+enum : int { ELEM_E4M3 = 0, ELEM_BF16 = 1, ELEM_MX = 2 };
 
 // Plain-data view of a cache, passed by value to kernels.
 struct CacheView {
@@ -90,6 +93,26 @@ __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
+}
+
+// ----------------------------------------------------------------- MXFP8 --
+// Block scale of an MXFP8 block ("FP8 KV attention: hardware paths and tile
+// preparation", section "Measure block-scaled QK": one E8M0 scale per 32
+// elements): X = 2^E with E the smallest integer such that amax <= 448 * 2^E,
+// clamped to [-127, 127], so no element saturates.  With amax = m * 2^e,
+// m in [0.5, 1): 448 * 2^(e-9) = 0.875 * 2^e, hence E = e - 9 if m <= 0.875,
+// else e - 8.  An all-zero block takes E = -127.
+__device__ __forceinline__ int mx_block_exp(float amax) {
+  if (amax == 0.f) return -127;
+  int e = 0;
+  const float m = frexpf(amax, &e);
+  const int E = m <= 0.875f ? e - 9 : e - 8;
+  return max(-127, min(127, E));
+}
+
+// Power of two 2^k for k in [-149, 127], exact.
+__device__ __forceinline__ float pow2_exact(int k) {
+  return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
 }
 
 // Location of cache row (sequence b, KV head h, token t) in elements of

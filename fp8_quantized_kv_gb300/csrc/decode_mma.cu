@@ -72,12 +72,14 @@ enum : int { XK_NATIVE = 0, XK_PRODUCER = 1, XK_CONSUMER = 2 };
 template <int KE, int VE, int XK = XK_NATIVE>
 struct TcCfg {
   static constexpr int D = 128;
-  static constexpr bool QHL = KE == ELEM_E4M3 && XK == XK_NATIVE;   // query as an e4m3 hi/lo pair
-  static constexpr int KB = KE == ELEM_E4M3 ? 1 : 2, VB = VE == ELEM_E4M3 ? 1 : 2;
+  static constexpr bool K8 = KE != ELEM_BF16;                       // K as 8-bit codes (e4m3 or MXFP8)
+  static constexpr bool KMX = KE == ELEM_MX;                         // per-32-dim block scales on K
+  static constexpr bool QHL = K8 && XK == XK_NATIVE;                 // query as an e4m3 hi/lo pair
+  static constexpr int KB = K8 ? 1 : 2, VB = VE == ELEM_E4M3 ? 1 : 2;
   static constexpr int K_TILE = kMmaTile * D * KB;
   static constexpr int V_TILE = kMmaTile * D * VB;
   static constexpr int STAGE = ((K_TILE + V_TILE + 2 * kMmaTile * 4) + 1023) / 1024 * 1024;
-  static constexpr int NST = XK != XK_NATIVE ? 4 : (KE == ELEM_E4M3 && VE == ELEM_E4M3) ? 6 : (KE == VE ? 3 : 4);
+  static constexpr int NST = XK != XK_NATIVE ? 4 : (K8 && VE == ELEM_E4M3) ? 6 : (K8 == (VE == ELEM_E4M3) ? 3 : 4);
   static constexpr int KCV = XK != XK_NATIVE ? 2 * kMmaTile * D * 2 : 0;   // two converted f16 K tiles
   static constexpr int QOP = QHL ? 16 * 128 : 2 * 16 * 128;
   static constexpr int POP = VE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;   // [128 tokens][16 or 32 B]
@@ -400,21 +402,21 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
     if (!c.paged) {
       if (lane == 0) {
         const int nsc = min(kMmaTile, (valid + 15) & ~15);
-        const uint32_t bytes = C::K_TILE + C::V_TILE + (KE == ELEM_E4M3 ? nsc * 4 : 0) +
+        const uint32_t bytes = C::K_TILE + C::V_TILE + (C::K8 ? nsc * 4 : 0) +
                                (VE == ELEM_E4M3 ? nsc * 4 : 0);
         tma::arrive_expect_tx(&full[s], bytes);
         const int row = (int)(cont_row0 + t0);
         tma::load_2d(st, &tp.tmk, 0, row, &full[s]);
-        if (KE != ELEM_E4M3) tma::load_2d(st + kMmaTile * 128, &tp.tmk, 64, row, &full[s]);
+        if (!C::K8) tma::load_2d(st + kMmaTile * 128, &tp.tmk, 64, row, &full[s]);
         tma::load_2d(st + C::K_TILE, &tp.tmv, 0, row, &full[s]);
         if (VE != ELEM_E4M3) tma::load_2d(st + C::K_TILE + kMmaTile * 128, &tp.tmv, 64, row, &full[s]);
-        if (KE == ELEM_E4M3) tma::load_1d(kss, c.k_scale + cont_row0 + t0, nsc * 4, &full[s]);
+        if (C::K8) tma::load_1d(kss, c.k_scale + cont_row0 + t0, nsc * 4, &full[s]);
         if (VE == ELEM_E4M3) tma::load_1d(vss, c.v_scale + cont_row0 + t0, nsc * 4, &full[s]);
       }
     } else {
       const int P = c.page_size;
       const int np = (valid + P - 1) / P;
-      const uint32_t per_page = P * 128 * (C::KB + C::VB) + P * 4 * ((KE == ELEM_E4M3) + (VE == ELEM_E4M3));
+      const uint32_t per_page = P * 128 * (C::KB + C::VB) + P * 4 * ((int)C::K8 + (VE == ELEM_E4M3));
       int page = my_page;
       load_page(i + 1);
       if (lane == 0) tma::arrive_expect_tx(&full[s], per_page * np);
@@ -426,11 +428,11 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         const int64_t row = ((int64_t)page * c.kv_heads + h) * P;
         const int off = lane * P * 128;
         tma::load_2d(st + off, &tp.tmk, 0, (int)row, &full[s]);
-        if (KE != ELEM_E4M3) tma::load_2d(st + kMmaTile * 128 + off, &tp.tmk, 64, (int)row, &full[s]);
+        if (!C::K8) tma::load_2d(st + kMmaTile * 128 + off, &tp.tmk, 64, (int)row, &full[s]);
         tma::load_2d(st + C::K_TILE + off, &tp.tmv, 0, (int)row, &full[s]);
         if (VE != ELEM_E4M3)
           tma::load_2d(st + C::K_TILE + kMmaTile * 128 + off, &tp.tmv, 64, (int)row, &full[s]);
-        if (KE == ELEM_E4M3) tma::load_1d(kss + lane * P, c.k_scale + row, P * 4, &full[s]);
+        if (C::K8) tma::load_1d(kss + lane * P, c.k_scale + row, P * 4, &full[s]);
         if (VE == ELEM_E4M3) tma::load_1d(vss + lane * P, c.v_scale + row, P * 4, &full[s]);
       }
     }
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
 #pragma unroll
         for (int e4 = 0; e4 < 4; ++e4)
           *reinterpret_cast<__half*>(qop + sw128_off(g, (lane * 4 + e4) * 2, 16)) = __float2half_rn(ldexpf(x[e4], -ex));
-      } else if constexpr (KE == ELEM_E4M3) {
+      } else if constexpr (C::K8) {
         float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
         amax = warp_max_redux(amax);
         const int ex = e4m3_row_exp(amax);
@@ -555,7 +557,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
       for (int side = 0; side < 2; ++side) {
         const __nv_bfloat16* src = (side == 0 ? p.k_new : p.v_new) + ((int64_t)b * c.kv_heads + h) * D + lane * 4;
         const uint2 raw = *reinterpret_cast<const uint2*>(src);
-        const bool fp8 = side == 0 ? KE == ELEM_E4M3 : VE == ELEM_E4M3;
+        const bool fp8 = side == 0 ? C::K8 : VE == ELEM_E4M3;
         uint8_t* dst = const_cast<uint8_t*>(side == 0 ? c.k : c.v);
         if (!fp8) {
           *reinterpret_cast<uint2*>(dst + (row * D + lane * 4) * 2) = raw;
@@ -564,14 +566,26 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
           bf16x2_to_f32(raw.x, t2); x[0] = t2[0]; x[1] = t2[1];
           bf16x2_to_f32(raw.y, t2); x[2] = t2[0]; x[3] = t2[1];
           float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-          amax = warp_max(amax);
-          const float scale = __fdiv_rn(amax, 448.0f);
-          uint32_t packed = 0;
-          if (amax != 0.f)
-            packed = e4m3x2_rn(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale)) |
-                     (e4m3x2_rn(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale)) << 16);
-          *reinterpret_cast<uint32_t*>(dst + row * D + lane * 4) = packed;
-          if (lane == 0) const_cast<float*>(side == 0 ? c.k_scale : c.v_scale)[row] = scale;
+          if (C::KMX && side == 0) {
+            // MXFP8 key: the arithmetic of fp8kv_quantize_mx, block = 8 lanes
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const int E = mx_block_exp(amax);
+            const float inv = pow2_exact(-E);
+            *reinterpret_cast<uint32_t*>(dst + row * D + lane * 4) =
+                e4m3x2_rn(x[0] * inv, x[1] * inv) | (e4m3x2_rn(x[2] * inv, x[3] * inv) << 16);
+            if ((lane & 7) == 0)
+              reinterpret_cast<uint8_t*>(const_cast<float*>(c.k_scale) + row)[lane >> 3] = (uint8_t)(E + 127);
+          } else {
+            amax = warp_max(amax);
+            const float scale = __fdiv_rn(amax, 448.0f);
+            uint32_t packed = 0;
+            if (amax != 0.f)
+              packed = e4m3x2_rn(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale)) |
+                       (e4m3x2_rn(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale)) << 16);
+            *reinterpret_cast<uint32_t*>(dst + row * D + lane * 4) = packed;
+            if (lane == 0) const_cast<float*>(side == 0 ? c.k_scale : c.v_scale)[row] = scale;
+          }
         }
       }
     }
@@ -658,7 +672,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t ID_QK = KE == ELEM_E4M3
+      constexpr uint32_t ID_QK = C::K8
           ? umma::idesc(umma::FMT_E4M3, umma::FMT_E4M3, umma::MAJOR_K, umma::MAJOR_K, 128, 16)
           : umma::idesc(umma::FMT_BF16, umma::FMT_BF16, umma::MAJOR_K, umma::MAJOR_K, 128, 16);
       constexpr uint32_t ID_PV = VE == ELEM_E4M3
@@ -694,7 +708,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
                                  umma::sdesc(qa + (k >> 2) * (16 * 128) + (k & 3) * 32, 16, 1024,
                                              umma::SWIZZLE_128B),
                                  ID_F16, k >= 4);
-            } else if constexpr (KE == ELEM_E4M3) {
+            } else if constexpr (C::K8) {
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 umma::mma_f8_ss(d + 16 * k, umma::sdesc(ka + k * 32, 16, 1024, umma::SWIZZLE_128B),
@@ -806,10 +820,24 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
 #pragma unroll
           for (int k = 0; k < 4; ++k) umma::tmem_ld16_nowait(tmem + s_col + 64 * bb + 16 * k + lane_off, r[k]);
           umma::tmem_wait_ld();
+          if constexpr (C::KMX) {
+            // MXFP8 keys: accumulator k holds dims 32k..32k+31 of the dot
+            // product, so the key's E8M0 block scale k applies to it here
+            // (the block-scaled product, summed over the four blocks)
+            const uint32_t e8 = reinterpret_cast<const uint32_t*>(smem + s * C::STAGE + C::K_TILE + C::V_TILE)[t];
+            float w[4];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            sc[j] = (__uint_as_float(r[0][j]) + __uint_as_float(r[1][j])) +
-                    (__uint_as_float(r[2][j]) + __uint_as_float(r[3][j]));
+            for (int k = 0; k < 4; ++k) w[k] = pow2_exact((int)((e8 >> (8 * k)) & 0xFF) - 127);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              sc[j] = (w[0] * __uint_as_float(r[0][j]) + w[1] * __uint_as_float(r[1][j])) +
+                      (w[2] * __uint_as_float(r[2][j]) + w[3] * __uint_as_float(r[3][j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              sc[j] = (__uint_as_float(r[0][j]) + __uint_as_float(r[1][j])) +
+                      (__uint_as_float(r[2][j]) + __uint_as_float(r[3][j]));
+          }
         }
         umma::fence_before_sync();
         __syncwarp();
@@ -821,7 +849,7 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
         const int t0 = (t_begin + i) * kMmaTile;
         const int valid = min(kMmaTile, T - t0);
         const bool tok_ok = t < valid;
-        const float kf = KE == ELEM_E4M3 ? kss[t] : 1.f;
+        const float kf = KE == ELEM_E4M3 ? kss[t] : 1.f;     // (MXFP8: block scales applied above)
         const float vsc = VE == ELEM_E4M3 ? (tok_ok ? vss[t] : 0.f) : 1.f;
         float sg[8];
         float* rb = red + (wg * 2 + (li & 1)) * 36;
@@ -1187,7 +1215,7 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
                                : (int64_t)c.batch * c.kv_heads * c.max_tokens;
   const int box_rows = c.paged ? c.page_size : kMmaTile;
   if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  if (!make_map(&tp.tmk, c.k, KE != ELEM_E4M3, rows, box_rows) ||
+  if (!make_map(&tp.tmk, c.k, KE == ELEM_BF16, rows, box_rows) ||
       !make_map(&tp.tmv, c.v, VE != ELEM_E4M3, rows, box_rows))
     return cudaErrorInvalidValue;
   tp.p = p;
@@ -1240,6 +1268,7 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int dtype, int batch, cudaS
   }
   if (dtype == FP8KV_K16V8) return launch_tc_t<ELEM_BF16, ELEM_E4M3>(p, grid, st);
   if (dtype == FP8KV_K8V16) return launch_tc_t<ELEM_E4M3, ELEM_BF16>(p, grid, st);
+  if (dtype == FP8KV_MXK8V8) return launch_tc_t<ELEM_MX, ELEM_E4M3>(p, grid, st);
   return launch_tc_t<ELEM_BF16, ELEM_BF16>(p, grid, st);
 }
 

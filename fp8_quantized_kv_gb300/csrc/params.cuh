@@ -41,6 +41,8 @@ struct PrefillParams {
 
 cudaError_t launch_quantize(const void* x, int64_t rows, int head_dim, uint8_t* codes, float* scales,
                             cudaStream_t s);
+cudaError_t launch_quantize_mx(const void* x, int64_t rows, int head_dim, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t s);
 cudaError_t launch_append(const CacheView& c, int dtype, const void* k_new, const void* v_new,
                           const int32_t* seq_idx, const int32_t* pos, int64_t n_tokens,
                           unsigned int* err, cudaStream_t s);

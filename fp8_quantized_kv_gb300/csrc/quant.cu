@@ -48,6 +48,32 @@ __device__ __forceinline__ void quantize_warp_row(const float (&x)[EPL], uint8_t
   if (lane == 0) *scale_out = scale;
 }
 
+// MXFP8 row held by a warp (EPL elements per lane): block b is lanes
+// [b*32/EPL, (b+1)*32/EPL).  The block amax is a shuffle max over its lanes;
+// each element is encoded from the fp32 product x * 2^-E (exact unless the
+// product is below the fp32 normal range); the first lane of each block
+// writes its E8M0 byte E + 127 to scale_row[b].
+template <int EPL>
+__device__ __forceinline__ void mx_quantize_warp_row(const float (&x)[EPL], uint8_t* codes_row,
+                                                     uint8_t* scale_row, int lane) {
+  constexpr int LPB = 32 / EPL;                 // lanes per 32-element block
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int o = 1; o < LPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int E = mx_block_exp(amax);
+  const float inv = pow2_exact(-E);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; i += 2) packed |= (uint32_t)cvt_e4m3x2(x[i] * inv, x[i + 1] * inv) << (8 * i);
+  if (EPL == 4)
+    *reinterpret_cast<uint32_t*>(codes_row + lane * 4) = packed;
+  else
+    *reinterpret_cast<uint16_t*>(codes_row + lane * 2) = (uint16_t)packed;
+  if (lane % LPB == 0) scale_row[lane / LPB] = (uint8_t)(E + 127);
+}
+
 template <int EPL>
 __device__ __forceinline__ void load_bf16_slice(const __nv_bfloat16* row, int lane, float (&x)[EPL]) {
   if (EPL == 4) {
@@ -76,6 +102,21 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const __nv_bfloat16*
   float v[EPL];
   load_bf16_slice<EPL>(x + row * D, lane, v);
   quantize_warp_row<EPL>(v, codes + row * D, scales + row, lane);
+}
+
+// Standalone MXFP8 quantiser: rows of D = 32*EPL values -> codes and D/32
+// E8M0 bytes per row.
+template <int EPL>
+__global__ void __launch_bounds__(256) quantize_mx_rows_kernel(const __nv_bfloat16* __restrict__ x,
+                                                               int64_t rows, uint8_t* __restrict__ codes,
+                                                               uint8_t* __restrict__ scales) {
+  constexpr int D = 32 * EPL;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  float v[EPL];
+  load_bf16_slice<EPL>(x + row * D, lane, v);
+  mx_quantize_warp_row<EPL>(v, codes + row * D, scales + row * (D / 32), lane);
 }
 
 // Append: warp per (token, KV head, K-or-V) row.  KE/VE: element kind of the
@@ -117,7 +158,10 @@ __global__ void __launch_bounds__(256) append_kernel(CacheView c, const __nv_bfl
   load_bf16_slice<EPL>(src, lane, v);
   uint8_t* codes = const_cast<uint8_t*>(is_v ? c.v : c.k) + dst * D;
   float* scale = const_cast<float*>(is_v ? c.v_scale : c.k_scale) + dst;
-  quantize_warp_row<EPL>(v, codes, scale, lane);
+  if (kind == ELEM_MX)
+    mx_quantize_warp_row<EPL>(v, codes, reinterpret_cast<uint8_t*>(scale), lane);
+  else
+    quantize_warp_row<EPL>(v, codes, scale, lane);
 }
 
 // Decode-step append: the new token of sequence b goes to position
@@ -150,8 +194,12 @@ __global__ void __launch_bounds__(256) append_step_kernel(CacheView c, const __n
   }
   float v[EPL];
   load_bf16_slice<EPL>(src, lane, v);
-  quantize_warp_row<EPL>(v, const_cast<uint8_t*>(is_v ? c.v : c.k) + dst * D,
-                         const_cast<float*>(is_v ? c.v_scale : c.k_scale) + dst, lane);
+  uint8_t* codes = const_cast<uint8_t*>(is_v ? c.v : c.k) + dst * D;
+  float* scale = const_cast<float*>(is_v ? c.v_scale : c.k_scale) + dst;
+  if (kind == ELEM_MX)
+    mx_quantize_warp_row<EPL>(v, codes, reinterpret_cast<uint8_t*>(scale), lane);
+  else
+    quantize_warp_row<EPL>(v, codes, scale, lane);
 }
 
 // ------------------------------------------------------------ launchers ---
@@ -167,6 +215,18 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int head_dim, uint8_t* 
   return cudaGetLastError();
 }
 
+cudaError_t launch_quantize_mx(const void* x, int64_t rows, int head_dim, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int warps = 8;
+  const unsigned grid = (unsigned)((rows + warps - 1) / warps);
+  if (head_dim == 128)
+    quantize_mx_rows_kernel<4><<<grid, 32 * warps, 0, s>>>((const __nv_bfloat16*)x, rows, codes, scales);
+  else
+    quantize_mx_rows_kernel<2><<<grid, 32 * warps, 0, s>>>((const __nv_bfloat16*)x, rows, codes, scales);
+  return cudaGetLastError();
+}
+
 template <int EPL>
 static void append_dispatch(int dtype, unsigned grid, cudaStream_t s, const CacheView& c,
                             const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* si,
@@ -177,6 +237,8 @@ static void append_dispatch(int dtype, unsigned grid, cudaStream_t s, const Cach
     append_kernel<EPL, ELEM_BF16, ELEM_E4M3><<<grid, 256, 0, s>>>(c, k, v, si, ps, n, err);
   else if (dtype == FP8KV_K8V16)
     append_kernel<EPL, ELEM_E4M3, ELEM_BF16><<<grid, 256, 0, s>>>(c, k, v, si, ps, n, err);
+  else if (dtype == FP8KV_MXK8V8)
+    append_kernel<EPL, ELEM_MX, ELEM_E4M3><<<grid, 256, 0, s>>>(c, k, v, si, ps, n, err);
   else
     append_kernel<EPL, ELEM_BF16, ELEM_BF16><<<grid, 256, 0, s>>>(c, k, v, si, ps, n, err);
 }
@@ -206,6 +268,8 @@ static void append_step_dispatch(int dtype, unsigned grid, cudaStream_t s, const
     append_step_kernel<EPL, ELEM_BF16, ELEM_E4M3><<<grid, 256, 0, s>>>(c, k, v, lens, err);
   else if (dtype == FP8KV_K8V16)
     append_step_kernel<EPL, ELEM_E4M3, ELEM_BF16><<<grid, 256, 0, s>>>(c, k, v, lens, err);
+  else if (dtype == FP8KV_MXK8V8)
+    append_step_kernel<EPL, ELEM_MX, ELEM_E4M3><<<grid, 256, 0, s>>>(c, k, v, lens, err);
   else
     append_step_kernel<EPL, ELEM_BF16, ELEM_BF16><<<grid, 256, 0, s>>>(c, k, v, lens, err);
 }

@@ -68,7 +68,14 @@ typedef enum {
   FP8KV_K8V8 = 0,    /* K codes, V codes (symmetric FP8)            */
   FP8KV_K16V8 = 1,   /* K bf16, V codes (no K transform)           */
   FP8KV_K16V16 = 2,  /* K bf16, V bf16 (the bf16-cache control)     */
-  FP8KV_K8V16 = 3    /* K codes, V bf16 (the remaining control)     */
+  FP8KV_K8V16 = 3,   /* K codes, V bf16 (the remaining control)     */
+  /* K as MXFP8: e4m3 codes with one E8M0 (power-of-two) scale per 32-dim
+   * block, the four block bytes of a row in its 4-byte k_scale slot (byte b
+   * = dims 32b..32b+31), as fp8kv_quantize_mx writes them; V codes with an
+   * fp32 scale per row.  head_dim 128 and the tensor-core decode only
+   * ("FP8 KV attention: hardware paths and tile preparation", section
+   * "Measure block-scaled QK"). */
+  FP8KV_MXK8V8 = 4
 } fp8kv_kv_dtype;
 
 typedef enum {
@@ -128,7 +135,8 @@ typedef struct {
   int32_t reserved;
   void *k;                    /* e4m3 codes (uint8) or bf16, layout above      */
   void *v;
-  float *k_scale;             /* fp32 per (token, KV head); NULL if K is bf16  */
+  float *k_scale;             /* fp32 per (token, KV head); NULL if K is bf16;
+                                 FP8KV_MXK8V8: the row's four E8M0 bytes      */
   float *v_scale;             /* NULL if V is bf16                             */
   const int32_t *page_table;  /* paged: [batch][max_pages_per_seq]; else NULL  */
 } fp8kv_cache;
@@ -143,6 +151,20 @@ typedef struct {
 FP8KV_API fp8kv_status fp8kv_quantize(const void *x, int64_t rows, int32_t head_dim,
                             uint8_t *codes, float *scales,
                             fp8kv_stream_t stream);
+
+/* Quantise `rows` rows of `head_dim` bf16 values into MXFP8: E4M3 codes and
+ * one E8M0 byte per 32-element block ("FP8 KV attention: hardware paths and
+ * tile preparation", section "Measure block-scaled QK").  Block scale
+ * X = 2^E, E the smallest integer with amax(|block|) <= 448 * 2^E, clamped
+ * to [-127, 127] (no element saturates; an all-zero block gets E = -127);
+ * byte = E + 127; code = round-to-nearest-even encode of the fp32 product
+ * x * 2^-E (the sign of a zero is kept).
+ *   x:      [rows][head_dim] bf16      codes: [rows][head_dim] uint8
+ *   scales: [rows][head_dim / 32] uint8 (E8M0)
+ * head_dim 64 or 128 (else FP8KV_ERR_UNSUPPORTED). */
+FP8KV_API fp8kv_status fp8kv_quantize_mx(const void *x, int64_t rows, int32_t head_dim,
+                               uint8_t *codes, uint8_t *scales,
+                               fp8kv_stream_t stream);
 
 /* Append new tokens to the cache: each (token, KV head) row of K and of V is
  * quantised as in fp8kv_quantize (or copied, for a bf16 side) and written

@@ -35,13 +35,13 @@ def fill_cache(inp: synth.DecodeInputs, dtype: str, device="cuda", capacity=None
 
 
 def k_fp8(dtype: str) -> bool:
-    """Whether the cache dtype stores K as e4m3 codes (else bf16)."""
+    """Whether the cache dtype stores K as e4m3 codes with a per-row scale."""
     return dtype in ("k8v8", "k8v16")
 
 
 def v_fp8(dtype: str) -> bool:
     """Whether the cache dtype stores V as e4m3 codes (else bf16)."""
-    return dtype in ("k8v8", "k16v8")
+    return dtype in ("k8v8", "k16v8", "mxk8v8")
 
 
 def seq_bits(inp: synth.DecodeInputs, which: str, b: int):
@@ -57,7 +57,9 @@ def oracle_kv(inp: synth.DecodeInputs, dtype: str, b: int):
     out = []
     for which, fp8 in (("k", k_fp8(dtype)), ("v", v_fp8(dtype))):
         bits = seq_bits(inp, which, b)
-        if fp8:
+        if which == "k" and dtype == "mxk8v8":
+            out.append(oracle.mx_dequantize(*oracle.mx_quantize(bits)))
+        elif fp8:
             c, s = oracle.quantize(bits)
             out.append(oracle.dequantize(c, s))
         else:

@@ -92,16 +92,35 @@ def test_argument_checks_return_before_any_launch(lib):
 
 def test_cache_dtype_and_scale_pointers(lib):
     # each dtype wants a scale row exactly for its e4m3 sides:
-    # K8V8 both, K16V8 V only, K16V16 none, K8V16 K only; ids past K8V16 are unknown
+    # K8V8 both, K16V8 V only, K16V16 none, K8V16 K only, MXK8V8 both (the K
+    # row's E8M0 bytes); ids past MXK8V8 are unknown
     r = ctypes.byref
-    for dtype, k8, v8 in ((0, 1, 1), (1, 0, 1), (2, 0, 0), (3, 1, 0)):
+    for dtype, k8, v8 in ((0, 1, 1), (1, 0, 1), (2, 0, 0), (3, 1, 0), (4, 1, 1)):
         for ks in (0, 1):
             for vs in (0, 1):
                 c = _cache(dtype=dtype, k_scale=0x3000 if ks else None, v_scale=0x4000 if vs else None)
                 want = 64 if (ks, vs) == (k8, v8) else 0
                 assert lib.fp8kv_decode_num_splits(r(c), 16, 64, 2) == want, (dtype, ks, vs)
-    assert lib.fp8kv_decode_num_splits(r(_cache(dtype=4)), 16, 64, 2) == 0
+    assert lib.fp8kv_decode_num_splits(r(_cache(dtype=5)), 16, 64, 2) == 0
     assert lib.fp8kv_decode_num_splits(r(_cache(dtype=-1)), 16, 64, 2) == 0
+
+
+def test_mxfp8_cache_is_tensor_core_decode_only(lib):
+    r = ctypes.byref
+    mx = _cache(dtype=4)
+    assert lib.fp8kv_decode_num_splits(r(mx), 16, 0, 0) == lib.fp8kv_decode_num_splits(r(_cache()), 16, 0, 2)
+    assert lib.fp8kv_decode_num_splits(r(mx), 16, 0, 2) > 0
+    for kid in (1, 3, 4):                        # CUDA cores, transform paths
+        assert lib.fp8kv_decode_num_splits(r(mx), 16, 0, kid) == 0
+    assert lib.fp8kv_decode_split(None, r(mx), None, 16, 0.1, 0, 1, None, 0, None) == 2
+    assert lib.fp8kv_decode_num_splits(r(_cache(dtype=4, head_dim=64)), 16, 0, 0) == 0
+    out = 0x6000
+    assert lib.fp8kv_prefill_attention(0x7000, r(mx), 0x8000, 64, 16, 0.1, 0, out, 0, None) == 2
+    # the standalone MX quantiser checks its arguments on the host
+    assert lib.fp8kv_quantize_mx(None, -1, 128, None, None, None) == 1
+    assert lib.fp8kv_quantize_mx(None, 10, 96, None, None, None) == 2
+    assert lib.fp8kv_quantize_mx(None, 10, 128, None, None, None) == 1
+    assert lib.fp8kv_quantize_mx(None, 0, 128, None, None, None) == 0
 
 
 def test_transform_path_kernel_ids(lib):
