@@ -48,6 +48,7 @@ def _load():
         lib.fp8kv_oracle_quantize.argtypes = [c_u16_p, i64, i32, c_u8_p, c_f32_p]
         lib.fp8kv_oracle_dequantize.argtypes = [c_u8_p, c_f32_p, i64, i32, c_dbl_p]
         lib.fp8kv_oracle_mx_quantize.argtypes = [c_u16_p, i64, i32, c_u8_p, c_u8_p]
+        lib.fp8kv_oracle_quantize_residual.argtypes = [c_u16_p, c_f32_p, i64, i32, i64, i32, c_u8_p, c_f32_p]
         lib.fp8kv_oracle_mx_dequantize.argtypes = [c_u8_p, c_u8_p, i64, i32, c_dbl_p]
         lib.fp8kv_oracle_gather_paged.restype = ctypes.c_int
         lib.fp8kv_oracle_gather_paged.argtypes = [
@@ -129,6 +130,29 @@ def dequantize(codes, scales):
     lib.fp8kv_oracle_dequantize(_ptr(c, ctypes.c_uint8), _ptr(s, ctypes.c_float),
                                 rows, d, _ptr(out, ctypes.c_double))
     return out
+
+
+# ------------------------------------------------------ pre-bias residual --
+
+def quantize_residual(x_bits, bias):
+    """Key rows [Hkv, T, D] (bf16 bits) and a per-KV-head fp32 bias [Hkv, D] ->
+    codes and fp32 scales of the residual fp32(k) - bias ("Fused KV-cache
+    quantization", section "Bias-aware symmetric FP8")."""
+    lib = _load()
+    x = _c(x_bits, np.uint16)
+    b = _c(bias, np.float32)
+    heads, T, d = x.shape
+    assert b.shape == (heads, d)
+    codes = np.empty(x.shape, dtype=np.uint8)
+    scales = np.empty(x.shape[:-1], dtype=np.float32)
+    lib.fp8kv_oracle_quantize_residual(_ptr(x, ctypes.c_uint16), _ptr(b, ctypes.c_float), heads * T, heads, T, d,
+                                       _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_float))
+    return codes, scales
+
+
+def residual_keys(codes, scales, bias):
+    """The keys a residual cache represents: dequant(r) + bias, fp64 [Hkv, T, D]."""
+    return dequantize(codes, scales) + np.asarray(bias, dtype=np.float64)[:, None, :]
 
 
 # ----------------------------------------------------------------- MXFP8 --

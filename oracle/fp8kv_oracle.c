@@ -48,6 +48,15 @@
  *    E + 127 (an all-zero block gets E = -127, byte 0).  Dequantisation:
  *    decode(code) * 2^E.
  *
+ *  - Pre-bias residual keys ("Fused KV-cache quantization", section
+ *    "Bias-aware symmetric FP8"; "FP8 KV attention: hardware paths and tile
+ *    preparation", section "Treat numerical safety and kernel speed as
+ *    separate gates"): the cache quantises the residual r = k - b of each key
+ *    row against a fixed per-KV-head bias b kept exact in fp32, with the
+ *    per-row rule above applied to the fp32 residual (r = fp32(k) - b, one
+ *    IEEE fp32 subtraction per element).  The key the cache represents is
+ *    dequant(r) + b, reconstructed here in fp64.
+ *
  *  - Paged addressing: token t of sequence b lives in page
  *    page_table[b][t / page_size] at offset t % page_size ("FP8 KV attention:
  *    hardware paths and tile preparation", section "Collect the profiler
@@ -140,6 +149,32 @@ void fp8kv_oracle_quantize(const uint16_t *x, int64_t rows, int d,
         codes[r * d + i] = 0x00;
       } else {
         float y = bf16_bits_to_float(xr[i]) / scale;
+        codes[r * d + i] = fp8kv_oracle_e4m3_encode(y);
+      }
+    }
+  }
+}
+
+/* Residual rows: r = fp32(x) - bias (bias: d fp32 values shared by the rows
+ * of one KV head; row r uses bias + ((r / rows_per_head) % heads) * d, i.e.
+ * rows ordered [..][heads][rows_per_head]), then the per-row rule of
+ * fp8kv_oracle_quantize on the fp32 residual. */
+void fp8kv_oracle_quantize_residual(const uint16_t *x, const float *bias, int64_t rows, int heads,
+                                    int64_t rows_per_head, int d, uint8_t *codes, float *scales) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const float *br = bias + ((r / rows_per_head) % heads) * d;
+    float amax = 0.0f;
+    for (int i = 0; i < d; ++i) {
+      const float a = fabsf(bf16_bits_to_float(x[r * d + i]) - br[i]);
+      if (a > amax) amax = a;
+    }
+    const float scale = amax / 448.0f;
+    scales[r] = scale;
+    for (int i = 0; i < d; ++i) {
+      if (amax == 0.0f) {
+        codes[r * d + i] = 0x00;
+      } else {
+        const float y = (bf16_bits_to_float(x[r * d + i]) - br[i]) / scale;
         codes[r * d + i] = fp8kv_oracle_e4m3_encode(y);
       }
     }

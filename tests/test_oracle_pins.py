@@ -180,6 +180,71 @@ def test_quantize_zero_row_and_single_spike():
     assert np.all(codes[2] == 0x7E) and scales[2] == np.float32(1.0) / np.float32(448)
 
 
+# ------------------------------------------------------ pre-bias residual --
+
+def test_residual_worked_row():
+    kv = {}
+    with open(os.path.join(GOLDEN, "residual_worked_row.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                key, *vals = line.split()
+                kv[key] = vals
+    x = np.array([int(h, 16) for h in kv["input"]], dtype=np.uint16)[None, None, :]
+    b = np.array([float(v) for v in kv["bias"]], dtype=np.float32)[None, :]
+    codes, scales = oracle.quantize_residual(x, b)
+    assert [int(c) for c in codes[0, 0]] == [int(h, 16) for h in kv["codes"]]
+    assert scales.view(np.uint32)[0, 0] == int(kv["scale_bits"][0], 16)
+
+
+def test_residual_reduces_to_plain_quantisation():
+    g = torch.Generator().manual_seed(15)
+    # exact in bf16: small-integer residuals plus a per-head integer bias
+    r = torch.randint(-40, 41, (2, 50, 128), generator=g).float()
+    b = torch.randint(-64, 65, (2, 128), generator=g).float()
+    k_bits = synth.bf16_bits((r + b[:, None, :]).to(torch.bfloat16))
+    assert np.array_equal(oracle.bf16_to_double(k_bits), (r + b[:, None, :]).numpy())
+    codes, scales = oracle.quantize_residual(k_bits, b.numpy())
+    rc, rs = oracle.quantize(synth.bf16_bits(r.to(torch.bfloat16)))
+    assert np.array_equal(codes, rc) and np.array_equal(scales, rs)
+    # a zero bias is the plain per-row rule on the keys themselves
+    c0, s0 = oracle.quantize_residual(k_bits, np.zeros((2, 128), np.float32))
+    pc, ps = oracle.quantize(k_bits)
+    assert np.array_equal(c0, pc) and np.array_equal(s0, ps)
+
+
+def test_residual_reconstruction_bound_and_bias_exactness():
+    g = torch.Generator().manual_seed(16)
+    b = (torch.randn(2, 128, generator=g) * 30).float()
+    k = (b[:, None, :] + torch.randn(2, 64, 128, generator=g)).to(torch.bfloat16)
+    bits = synth.bf16_bits(k)
+    codes, scales = oracle.quantize_residual(bits, b.numpy())
+    kk = oracle.bf16_to_double(bits)
+    rec = oracle.residual_keys(codes, scales, b.numpy())
+    r = kk - b.numpy().astype(np.float64)[:, None, :]
+    # within 1/16 of the residual's row maximum (e4m3 half-ulp at the top binade
+    # is 16/448 of it) plus the fp32 rounding of the subtraction
+    bound = np.abs(r).max(axis=-1, keepdims=True) / 16 + np.abs(kk) * 2.0 ** -23
+    assert np.all(np.abs(rec - kk) <= bound)
+    # the residual keeps far more of the token-varying part than quantising k
+    plain = oracle.dequantize(*oracle.quantize(bits))
+    assert np.linalg.norm(rec - kk) < 0.2 * np.linalg.norm(plain - kk)
+
+
+def test_constant_key_bias_cancels_in_attention():
+    # the score correction q.b is the same for every key of a row, so
+    # attention over dequant(r) equals attention over dequant(r) + b
+    rng = np.random.default_rng(17)
+    q = rng.standard_normal((2, 8, 64))
+    k = rng.standard_normal((2, 2, 40, 64))
+    v = rng.standard_normal((2, 2, 40, 64))
+    b = rng.standard_normal((2, 64)) * 50
+    lens = np.array([40, 23], np.int32)
+    a = oracle.decode_attention(q, k, v, lens, 0.125)
+    c = oracle.decode_attention(q, k + b[None, :, None, :], v, lens, 0.125)
+    assert np.allclose(a, c, rtol=0, atol=1e-9)
+
+
 # ----------------------------------------------------------------- MXFP8 --
 
 def _mx_worked_row():
