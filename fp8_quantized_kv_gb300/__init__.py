@@ -70,13 +70,16 @@ class Fp8KVCache:
     that describes them.  Layouts are those of include/fp8kv.h."""
 
     def __init__(self, *, dtype, layout, batch, kv_heads, head_dim, k, v, k_scale, v_scale,
-                 max_tokens=0, page_size=0, num_pages=0, page_table=None):
+                 max_tokens=0, page_size=0, num_pages=0, page_table=None, k_bias=None):
         self.dtype = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
         self.layout = layout
         self.batch, self.kv_heads, self.head_dim = batch, kv_heads, head_dim
         self.max_tokens, self.page_size, self.num_pages = max_tokens, page_size, num_pages
         self.k, self.v, self.k_scale, self.v_scale = k, v, k_scale, v_scale
         self.page_table = page_table
+        if k_bias is not None:
+            _need(k_bias, torch.float32, "k_bias")
+        self.k_bias = k_bias
         self._struct = CacheStruct(
             dtype=self.dtype, layout=layout, batch=batch, kv_heads=kv_heads, head_dim=head_dim,
             max_tokens=max_tokens, page_size=page_size, num_pages=num_pages,
@@ -84,7 +87,8 @@ class Fp8KVCache:
             k=k.data_ptr(), v=v.data_ptr(),
             k_scale=None if k_scale is None else k_scale.data_ptr(),
             v_scale=None if v_scale is None else v_scale.data_ptr(),
-            page_table=None if page_table is None else page_table.data_ptr())
+            page_table=None if page_table is None else page_table.data_ptr(),
+            k_bias=None if k_bias is None else k_bias.data_ptr())
 
     @property
     def struct_ref(self):
@@ -112,17 +116,19 @@ class Fp8KVCache:
         return k, v, ks, vs
 
     @classmethod
-    def contiguous(cls, batch, kv_heads, head_dim, max_tokens, dtype="k8v8", device="cuda"):
+    def contiguous(cls, batch, kv_heads, head_dim, max_tokens, dtype="k8v8", device="cuda", k_bias=None):
+        """k_bias: optional [kv_heads, head_dim] fp32 key bias; the cache then
+        holds pre-bias residual keys (include/fp8kv.h, fp8kv_cache.k_bias)."""
         k, v, ks, vs = cls._alloc(dtype, (batch, kv_heads, max_tokens), head_dim, device)
-        return cls(dtype=dtype, layout=LAYOUT_CONTIGUOUS, batch=batch, kv_heads=kv_heads,
+        return cls(dtype=dtype, layout=LAYOUT_CONTIGUOUS, batch=batch, kv_heads=kv_heads, k_bias=k_bias,
                    head_dim=head_dim, k=k, v=v, k_scale=ks, v_scale=vs, max_tokens=max_tokens)
 
     @classmethod
     def paged(cls, page_table: torch.Tensor, num_pages, kv_heads, head_dim, page_size=16,
-              dtype="k8v8", device="cuda"):
+              dtype="k8v8", device="cuda", k_bias=None):
         pt = page_table.to(device=device, dtype=torch.int32).contiguous()
         k, v, ks, vs = cls._alloc(dtype, (num_pages, kv_heads, page_size), head_dim, device)
-        return cls(dtype=dtype, layout=LAYOUT_PAGED, batch=pt.shape[0], kv_heads=kv_heads,
+        return cls(dtype=dtype, layout=LAYOUT_PAGED, batch=pt.shape[0], kv_heads=kv_heads, k_bias=k_bias,
                    head_dim=head_dim, k=k, v=v, k_scale=ks, v_scale=vs, page_size=page_size,
                    num_pages=num_pages, page_table=pt)
 

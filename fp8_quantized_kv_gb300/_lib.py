@@ -47,6 +47,7 @@ class CacheStruct(ctypes.Structure):
         ("k_scale", ctypes.c_void_p),
         ("v_scale", ctypes.c_void_p),
         ("page_table", ctypes.c_void_p),
+        ("k_bias", ctypes.c_void_p),
     ]
 
 

@@ -56,9 +56,10 @@ static fp8kv_status check_cache(const fp8kv_cache* c, CacheView* view) {
   const bool k8 = c->dtype == FP8KV_K8V8 || c->dtype == FP8KV_K8V16 || c->dtype == FP8KV_MXK8V8;
   const bool v8 = c->dtype == FP8KV_K8V8 || c->dtype == FP8KV_K16V8 || c->dtype == FP8KV_MXK8V8;
   if (k8 != (c->k_scale != nullptr) || v8 != (c->v_scale != nullptr)) return FP8KV_ERR_INVALID_ARG;
+  if (c->k_bias != nullptr && c->dtype != FP8KV_K8V8 && c->dtype != FP8KV_K8V16) return FP8KV_ERR_INVALID_ARG;
   // 16-byte vector copies read the cache: every base pointer must be aligned
   const uintptr_t align = (uintptr_t)c->k | (uintptr_t)c->v | (uintptr_t)c->k_scale |
-                          (uintptr_t)c->v_scale | (uintptr_t)c->page_table;
+                          (uintptr_t)c->v_scale | (uintptr_t)c->page_table | (uintptr_t)c->k_bias;
   if (align & 15) return FP8KV_ERR_INVALID_ARG;
   std::memset(view, 0, sizeof(*view));
   if (c->layout == FP8KV_LAYOUT_CONTIGUOUS) {
@@ -81,6 +82,7 @@ static fp8kv_status check_cache(const fp8kv_cache* c, CacheView* view) {
   view->v = static_cast<const uint8_t*>(c->v);
   view->k_scale = c->k_scale;
   view->v_scale = c->v_scale;
+  view->k_bias = c->k_bias;
   view->batch = c->batch;
   view->kv_heads = c->kv_heads;
   view->head_dim = c->head_dim;

@@ -27,6 +27,7 @@ struct CacheView {
   const float* k_scale;
   const float* v_scale;
   const int32_t* page_table;
+  const float* k_bias;             // pre-bias residual keys: [kv_heads][head_dim], or null
   int batch, kv_heads, head_dim;
   int max_tokens;                  // contiguous capacity
   int page_size, page_shift, num_pages, max_pages_per_seq;

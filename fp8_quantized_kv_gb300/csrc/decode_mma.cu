@@ -565,6 +565,10 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
           float x[4], t2[2];
           bf16x2_to_f32(raw.x, t2); x[0] = t2[0]; x[1] = t2[1];
           bf16x2_to_f32(raw.y, t2); x[2] = t2[0]; x[3] = t2[1];
+          if (side == 0 && c.k_bias != nullptr) {      // pre-bias residual key
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] -= c.k_bias[h * D + lane * 4 + e];
+          }
           float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
           if (C::KMX && side == 0) {
             // MXFP8 key: the arithmetic of fp8kv_quantize_mx, block = 8 lanes

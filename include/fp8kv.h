@@ -139,6 +139,17 @@ typedef struct {
                                  FP8KV_MXK8V8: the row's four E8M0 bytes      */
   float *v_scale;             /* NULL if V is bf16                             */
   const int32_t *page_table;  /* paged: [batch][max_pages_per_seq]; else NULL  */
+  /* Pre-bias residual keys ("Fused KV-cache quantization", section
+   * "Bias-aware symmetric FP8"): NULL, or [kv_heads][head_dim] fp32, a fixed
+   * key bias b kept exact.  Appends then quantise each K row's residual
+   * fp32(k) - b with the per-row rule, so a large bias no longer sets the
+   * row's scale.  Only for FP8KV_K8V8 and FP8KV_K8V16 (else
+   * FP8KV_ERR_INVALID_ARG).  Attention reads the residual codes as the keys:
+   * the dropped score term q.b is the same for every key a query row sees,
+   * so it cancels in the softmax.  b is one vector per KV head for all
+   * positions; a bias rotated with the key's position (a bias added before a
+   * rotary embedding, with the cache holding rotated keys) is not this. */
+  const float *k_bias;
 } fp8kv_cache;
 
 /* Quantise `rows` rows of `head_dim` bf16 values into E4M3 codes and one fp32

@@ -123,6 +123,16 @@ def test_mxfp8_cache_is_tensor_core_decode_only(lib):
     assert lib.fp8kv_quantize_mx(None, 0, 128, None, None, None) == 0
 
 
+def test_key_bias_checks(lib):
+    # pre-bias residual keys: K8V8 and K8V16 only, 16-byte aligned
+    r = ctypes.byref
+    assert lib.fp8kv_decode_num_splits(r(_cache(k_bias=0x5000)), 16, 0, 0) > 0
+    assert lib.fp8kv_decode_num_splits(r(_cache(dtype=3, v_scale=None, k_bias=0x5000)), 16, 0, 0) > 0
+    assert lib.fp8kv_decode_num_splits(r(_cache(dtype=1, k_scale=None, k_bias=0x5000)), 16, 0, 0) == 0
+    assert lib.fp8kv_decode_num_splits(r(_cache(dtype=4, k_bias=0x5000)), 16, 0, 0) == 0
+    assert lib.fp8kv_decode_num_splits(r(_cache(k_bias=0x5004)), 16, 0, 0) == 0
+
+
 def test_transform_path_kernel_ids(lib):
     # kernels 3 and 4 (tensor cores, K converted to f16 on chip): K8V8 at
     # head_dim 128 only, planned like the tensor-core kernel; unknown ids rejected
