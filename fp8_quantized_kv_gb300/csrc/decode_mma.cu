@@ -32,8 +32,10 @@
 //   warp 0     TMA producer: 128-byte-swizzled tensor loads of the K and V
 //              tiles straight into the UMMA operand layout, 1-D bulk copies
 //              of the scale rows; a ring of NST stages (full/empty mbarriers).
-//   warp 1     TMEM owner and MMA issuer (one thread): QK of tile i, then
-//              PV of tile i-1.
+//   warp 1     TMEM owner and QK issuer (one thread).
+//   warp 10    PV issuer (one thread).  Issuing a few tcgen05.mma costs the
+//              issuing thread a fraction of a microsecond; one thread issuing
+//              both QK and PV set the tile interval, two run side by side.
 //   warps 2-5  softmax of tile i, then the O update of tile i-1 (thread =
 //              TMEM lane = token for S, = head dim for O).
 // S, O (TMEM) and P (shared memory) are double-buffered, so QK(i+1), PV(i)
@@ -60,6 +62,9 @@
 namespace fp8kv {
 
 constexpr int kMmaTile = 128;
+// warp 0 TMA producer, warp 1 QK issuer and TMEM owner, warps 2-9 softmax,
+// warp 10 PV issuer
+constexpr int kTcThreads = 352;
 
 // XK: where K is prepared (an ablation).  XK_NATIVE: QK is the native e4m3
 // MMA on the query's e4m3 hi/lo pair.  On the transform path each landed
@@ -273,7 +278,7 @@ __device__ __forceinline__ void k_tile_to_f16(const uint8_t* src, uint8_t* dst, 
 }
 
 template <int KE, int VE, int XK>
-__global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant__ DecodeTmaParams tp) {
+__global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_constant__ DecodeTmaParams tp) {
   using C = TcCfg<KE, VE, XK>;
   constexpr int D = 128;
   const DecodeParams& p = tp.p;
@@ -674,109 +679,91 @@ __global__ void __launch_bounds__(320, 1) decode_split_tc(const __grid_constant_
       TRACE(1013);
     }
   } else if (warp == 1) {
-    // ----------------------------------------------------------------- MMA
+    // -------------------------------------------------------- QK issuer
+    // One thread issues every QK; the PV issuer is warp 10.  An issue of a
+    // few tcgen05.mma takes a fraction of a microsecond of the issuing
+    // thread, so QK and PV each get their own thread and run side by side.
     if (lane == 0) {
       constexpr uint32_t ID_QK = C::K8
           ? umma::idesc(umma::FMT_E4M3, umma::FMT_E4M3, umma::MAJOR_K, umma::MAJOR_K, 128, 16)
           : umma::idesc(umma::FMT_BF16, umma::FMT_BF16, umma::MAJOR_K, umma::MAJOR_K, 128, 16);
+      const uint32_t qa = umma::smem_u32(qop);
+      for (int nq = 0; nq < n_tiles; ++nq) {
+        const int s = nq % C::NST, u = nq / C::NST, w = nq & 1, li = nq >> 1, bb = li & 1, ub = li >> 1;
+        bool ok = XK != XK_NATIVE ? wait_fast(&kc_full[nq & 1], (nq >> 1) & 1, abort_flag)
+                                  : wait_fast(&full[s], u & 1, abort_flag);
+        ok = ok && (ub == 0 || wait_fast(&wb[w].s_empty[bb], (ub - 1) & 1, abort_flag));
+        if (!ok) break;
+        umma::fence_after_sync();
+        const uint32_t ka =
+            umma::smem_u32(XK != XK_NATIVE ? kcv + (nq & 1) * (kMmaTile * D * 2) : smem + s * C::STAGE);
+        // four independent accumulators (one per 32-byte k-step) so the
+        // thin MMAs pipeline instead of waiting on each other
+        const uint32_t d = tmem + 256 * w + 64 * bb;
+        if constexpr (XK != XK_NATIVE) {
+          constexpr uint32_t ID_F16 =
+              umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_K, umma::MAJOR_K, 128, 16);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma::mma_f16_ss(d + 16 * (k & 3),
+                             umma::sdesc(ka + (k >> 2) * (kMmaTile * 128) + (k & 3) * 32, 16, 1024,
+                                         umma::SWIZZLE_128B),
+                             umma::sdesc(qa + (k >> 2) * (16 * 128) + (k & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
+                             ID_F16, k >= 4);
+        } else if constexpr (C::K8) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma::mma_f8_ss(d + 16 * k, umma::sdesc(ka + k * 32, 16, 1024, umma::SWIZZLE_128B),
+                            umma::sdesc(qa + k * 32, 16, 1024, umma::SWIZZLE_128B), ID_QK, 0);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma::mma_f16_ss(d + 16 * (k & 3),
+                             umma::sdesc(ka + (k >> 2) * (kMmaTile * 128) + (k & 3) * 32, 16, 1024,
+                                         umma::SWIZZLE_128B),
+                             umma::sdesc(qa + (k >> 2) * (16 * 128) + (k & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
+                             ID_QK, k >= 4);
+        }
+        umma::mma_commit(&wb[w].s_full[bb]);
+        if (XK == XK_PRODUCER) umma::mma_commit(&kc_empty[nq & 1]);
+        TRACE(8 * nq + 1);
+      }
+    }
+  } else if (warp == 10) {
+    // -------------------------------------------------------- PV issuer
+    if (lane == 0) {
       constexpr uint32_t ID_PV = VE == ELEM_E4M3
           ? umma::idesc(umma::FMT_E4M3, umma::FMT_E4M3, umma::MAJOR_MN, umma::MAJOR_MN, 128, 16)
           : umma::idesc(umma::FMT_BF16, umma::FMT_BF16, umma::MAJOR_MN, umma::MAJOR_MN, 128, 16);
-      const uint32_t qa = umma::smem_u32(qop);
-      // Event loop: issue whichever of the next QK and the next PV is ready,
-      // so QK runs up to two tiles ahead of each group's softmax.
-      int nq = 0, np = 0;
-      long long t_prog = clock64();
-      uint32_t idle = 0;
-      while (np < n_tiles) {
-        bool prog = false;
-        if (nq < n_tiles) {
-          const int s = nq % C::NST, u = nq / C::NST, w = nq & 1, li = nq >> 1, bb = li & 1, ub = li >> 1;
-          const bool k_ready = XK != XK_NATIVE ? umma::mbar_test(&kc_full[nq & 1], (nq >> 1) & 1)
-                                               : umma::mbar_test(&full[s], u & 1);
-          if (k_ready && (ub == 0 || umma::mbar_test(&wb[w].s_empty[bb], (ub - 1) & 1))) {
-            umma::fence_after_sync();
-            const uint32_t ka =
-                umma::smem_u32(XK != XK_NATIVE ? kcv + (nq & 1) * (kMmaTile * D * 2) : smem + s * C::STAGE);
-            // four independent accumulators (one per 32-byte k-step) so the
-            // thin MMAs pipeline instead of waiting on each other
-            const uint32_t d = tmem + 256 * w + 64 * bb;
-            if constexpr (XK != XK_NATIVE) {
-              constexpr uint32_t ID_F16 =
-                  umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_K, umma::MAJOR_K, 128, 16);
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % C::NST, w = j & 1, lj = j >> 1, bb = lj & 1, ub = lj >> 1;
+        // P ready implies S ready, which implies the tile landed; the
+        // transform path's QK did not read the stage itself, so wait for it
+        bool ok = wait_fast(&wb[w].p_full[bb], ub & 1, abort_flag);
+        ok = ok && (ub == 0 || wait_fast(&wb[w].o_empty[bb], (ub - 1) & 1, abort_flag));
+        ok = ok && (XK == XK_NATIVE || wait_fast(&full[s], (j / C::NST) & 1, abort_flag));
+        if (!ok) break;
+        if (XK == XK_NATIVE) TRACE(8 * j + 7);
+        umma::fence_after_sync();
+        const uint32_t va = umma::smem_u32(smem + s * C::STAGE + C::K_TILE);
+        const uint32_t pa = umma::smem_u32(pop0 + (2 * w + bb) * C::POP);
+        const uint32_t d = tmem + 256 * w + 128 + 64 * bb;
+        if constexpr (VE == ELEM_E4M3) {
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                umma::mma_f16_ss(d + 16 * (k & 3),
-                                 umma::sdesc(ka + (k >> 2) * (kMmaTile * 128) + (k & 3) * 32, 16, 1024,
-                                             umma::SWIZZLE_128B),
-                                 umma::sdesc(qa + (k >> 2) * (16 * 128) + (k & 3) * 32, 16, 1024,
-                                             umma::SWIZZLE_128B),
-                                 ID_F16, k >= 4);
-            } else if constexpr (C::K8) {
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                umma::mma_f8_ss(d + 16 * k, umma::sdesc(ka + k * 32, 16, 1024, umma::SWIZZLE_128B),
-                                umma::sdesc(qa + k * 32, 16, 1024, umma::SWIZZLE_128B), ID_QK, 0);
-            } else {
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                umma::mma_f16_ss(d + 16 * (k & 3),
-                                 umma::sdesc(ka + (k >> 2) * (kMmaTile * 128) + (k & 3) * 32, 16, 1024,
-                                             umma::SWIZZLE_128B),
-                                 umma::sdesc(qa + (k >> 2) * (16 * 128) + (k & 3) * 32, 16, 1024,
-                                             umma::SWIZZLE_128B),
-                                 ID_QK, k >= 4);
-            }
-            umma::mma_commit(&wb[w].s_full[bb]);
-            if (XK == XK_PRODUCER) umma::mma_commit(&kc_empty[nq & 1]);
-            TRACE(8 * nq + 1);
-            ++nq;
-            prog = true;
-          }
-        }
-        if (np < nq) {
-          const int j = np, s = j % C::NST, w = j & 1, lj = j >> 1, bb = lj & 1, ub = lj >> 1;
-          if (umma::mbar_test(&wb[w].p_full[bb], ub & 1) &&
-              (ub == 0 || umma::mbar_test(&wb[w].o_empty[bb], (ub - 1) & 1)) &&
-              (XK == XK_NATIVE || umma::mbar_test(&full[s], (j / C::NST) & 1))) {
-            umma::fence_after_sync();
-            const uint32_t va = umma::smem_u32(smem + s * C::STAGE + C::K_TILE);
-            const uint32_t pa = umma::smem_u32(pop0 + (2 * w + bb) * C::POP);
-            const uint32_t d = tmem + 256 * w + 128 + 64 * bb;
-            if constexpr (VE == ELEM_E4M3) {
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                umma::mma_f8_ss(d + 16 * k, umma::sdesc(va + k * 4 * 1024, 1024, 1024, umma::SWIZZLE_128B),
-                                umma::sdesc(pa + k * 512, 128, 128, umma::SWIZZLE_NONE), ID_PV, 0);
-            } else {
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                umma::mma_f16_ss(d + 16 * (k & 3),
-                                 umma::sdesc(va + k * 2 * 1024, kMmaTile * 128, 1024, umma::SWIZZLE_128B),
-                                 umma::sdesc(pa + k * 512, 256, 128, umma::SWIZZLE_NONE), ID_PV, k >= 4);
-            }
-            umma::mma_commit(&wb[w].o_full[bb]);
-            umma::mma_commit(&empty[s]);
-            TRACE(8 * np + 2);
-            ++np;
-            prog = true;
-          }
-        }
-        if (np == n_tiles) TRACE(1014);
-        if (prog) {
-          idle = 0;
+          for (int k = 0; k < 4; ++k)
+            umma::mma_f8_ss(d + 16 * k, umma::sdesc(va + k * 4 * 1024, 1024, 1024, umma::SWIZZLE_128B),
+                            umma::sdesc(pa + k * 512, 128, 128, umma::SWIZZLE_NONE), ID_PV, 0);
         } else {
-          __nanosleep(20);   // back off: the polling thread shares an SM sub-partition with softmax warps
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma::mma_f16_ss(d + 16 * (k & 3), umma::sdesc(va + k * 2 * 1024, kMmaTile * 128, 1024, umma::SWIZZLE_128B),
+                             umma::sdesc(pa + k * 512, 256, 128, umma::SWIZZLE_NONE), ID_PV, k >= 4);
         }
-        if (!prog && (++idle & 63) == 0) {
-          if (idle == 64) t_prog = clock64();
-          if (*abort_flag) break;
-          if (clock64() - t_prog > kWaitLimitCycles) {
-            *abort_flag = 1;
-            break;
-          }
-        }
+        umma::mma_commit(&wb[w].o_full[bb]);
+        umma::mma_commit(&empty[s]);
+        TRACE(8 * j + 2);
       }
+      TRACE(1014);
     }
   } else {
     // ------------------------------------- softmax and O update (2 groups)
@@ -1190,7 +1177,7 @@ static bool cluster_fits(const void* fn, dim3 grid, int smem) {
   if (max_clusters < 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(320);
+    cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1227,7 +1214,7 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
   const void* fn = (const void*)decode_split_tc<KE, VE, XK>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(320);
+  cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
