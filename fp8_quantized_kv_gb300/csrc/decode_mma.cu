@@ -800,8 +800,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
           __syncwarp();
           if (lane == 0) umma::mbar_arrive(&kc_full[wg]);
         }
-        bool ok = wait_or_abort(&B.s_full[bb], ub & 1, abort_flag);
-        ok = ok && wait_or_abort(&full[s], u & 1, abort_flag);
+        // hand-offs on the critical path: poll without a suspend-time hint
+        bool ok = wait_fast(&B.s_full[bb], ub & 1, abort_flag);
+        ok = ok && wait_fast(&full[s], u & 1, abort_flag);
         if (group_any(wg, !ok)) { failed = true; break; }
         if (t == 0) TRACE(8 * i + 3);
         umma::fence_after_sync();
@@ -919,7 +920,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
       }
       if (li >= 1) {
         const int lj = li - 1, bb = lj & 1, ub = lj >> 1;
-        const bool ok = wait_or_abort(&B.o_full[bb], ub & 1, abort_flag);
+        const bool ok = wait_fast(&B.o_full[bb], ub & 1, abort_flag);
         if (group_any(wg, !ok)) { failed = true; break; }
         umma::fence_after_sync();
         float ov[16];
