@@ -159,7 +159,7 @@ __device__ __forceinline__ int g4_lo(int r, int S) { return (32 * r) / S; }
 // floor(32 r / S) <= q  <=>  r < (q + 1) S / 32.
 __device__ __forceinline__ int g4_owner(int q, int S) { return ((q + 1) * S - 1) >> 5; }
 
-__device__ __noinline__ void cluster_exchange(const DecodeParams& p, float* rx_ml, float* rx_o, uint64_t* rx_bar,
+__device__ __forceinline__ void cluster_exchange(const DecodeParams& p, float* rx_ml, float* rx_o, uint64_t* rx_bar,
                                               const int* slice, float* stage, const float (&Og)[8],
                                               const float (&Mg)[8], const float (&Lg)[8], int b, int h, int G,
                                               int t, volatile int* abort) {
