@@ -522,8 +522,8 @@ def measure_prefill(args, ws):
 def measure_shapes(args):
     """The decode step on the other decode workloads: batch 16 at 512 tokens
     (40 rotated layer caches, above L2) and the paged batch-64 serving decode
-    (lengths U[1024, 16384], 16-token pages, hostile keys; one 1.2-1.7 GB
-    cache), K8/V8 and K16/V8, on each kernel.  Plain launches, CUDA-graph
+    (lengths U[1024, 16384], 16-token pages, hostile keys; one 1.2-2.3 GB
+    cache), the four cache dtypes, on each kernel.  Plain launches, CUDA-graph
     replay, CUDA events on the launching stream."""
     import fp8_quantized_kv_gb300 as fk
     res = {}
@@ -539,9 +539,9 @@ def measure_shapes(args):
         lens = inp.seq_lens.cuda()
         q = inp.q.contiguous()
         res[wl] = {"group": spec.group, "tokens": int(lens64.sum())}
-        for dtype in ("k8v8", "k16v8"):
-            k8, v8 = dtype == "k8v8", True
-            row = D * ((1 if k8 else 2) + 1) + 4 * (int(k8) + int(v8))
+        for dtype in ("k8v8", "k16v8", "k8v16", "k16v16"):
+            k8, v8 = dtype in ("k8v8", "k8v16"), dtype in ("k8v8", "k16v8")
+            row = D * ((1 if k8 else 2) + (1 if v8 else 2)) + 4 * (int(k8) + int(v8))
             nbytes = int(lens64.sum()) * Hkv * row + 2 * B * Hq * D * 2 + B * Hkv * (2 * D * 2 + row)
             caches = []
             for _ in range(n_layers):
@@ -647,11 +647,11 @@ def measure_interval(args):
     return res
 
 
-def measure_variant(spec, dtype, args, ws, inp, flags=None, kernel=None):
+def measure_variant(spec, dtype, args, ws, inp, flags=None, kernel=None, n_layers=None):
     if flags is None:
         flags = 0 if args.plain_launch else STEP_EARLY_CACHE_READ
     kid = KERNEL_IDS[args.kernel if kernel is None else kernel]
-    layers, dev = build_layers(spec, dtype, args.layers, inp, kid, flags)
+    layers, dev = build_layers(spec, dtype, args.layers if n_layers is None else n_layers, inp, kid, flags)
     for i in range(max(3, args.warmup)):                      # eager warm-up steps
         L = layers[i % len(layers)]
         L.step(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
@@ -748,6 +748,18 @@ def run_gpu(args, ws, rank):
         transform["note"] = ("transform path: each K tile converted to f16 in shared memory, QK as kind::f16 "
                              "on an f16 query; 4 cache stages instead of 6 (the two f16 K buffers take the room)")
 
+    # L2-warm: one layer's cache (69 MB at this shape) replayed, so it stays in
+    # the 126 MB L2; the headline keeps 8 layers and streams from HBM
+    l2_warm = None
+    if not args.no_controls and tensor:
+        ls, _, lms, _, _ = measure_variant(spec, args.dtype, args, ws, inp, n_layers=1)
+        lms = max_over_ranks(lms, ws)
+        l2_warm = {"us_per_layer": lms / args.steps * 1e3,
+                   "GBps": nb["step"] * args.steps / (lms * 1e-3) / 1e9,
+                   "note": "one layer cache replayed (L2-resident); not the headline"}
+        del ls
+        torch.cuda.empty_cache()
+
     prefill = None if args.no_prefill else measure_prefill(args, ws)
     shapes = None if args.no_shapes else measure_shapes(args)
     interval = None if args.no_interval else measure_interval(args)
@@ -781,6 +793,7 @@ def run_gpu(args, ws, rank):
             "gpu_launches": (1 if tensor else 3) * args.steps,
             "kernels_us": None if per is None else {k.replace("_ms", "_us"): v * 1e3 for k, v in per.items()},
             "clocks": clocks, "controls": controls, "transform_path": transform, "plain_launch": plain,
+            "l2_warm": l2_warm,
             "prefill": prefill,
             "shapes": shapes, "initiation_interval": interval,
         }
