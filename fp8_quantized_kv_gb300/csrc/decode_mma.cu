@@ -1151,6 +1151,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
   // (threads other than the merging ones arrived at the cluster barrier at
   // setup and never wait on it: they arrive only once)
   umma::fence_before_sync();
+  if (lane == 0) TRACE_MAX(1015);          // last warp at the final barrier
   __syncthreads();
   umma::fence_after_sync();
   if (warp == 1) umma::tmem_dealloc(tmem, 512);
@@ -1241,6 +1242,11 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
 }
 
 #ifdef FP8KV_TRACE
+// Zero the per-tile stamps (the TRACE_MAX slots keep a maximum across launches).
+extern "C" __attribute__((visibility("default"))) int fp8kv_trace_clear() {
+  static const unsigned long long zeros[1024] = {};
+  return cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros)) == cudaSuccess ? 0 : -1;
+}
 extern "C" __attribute__((visibility("default"))) int fp8kv_trace_read(unsigned long long* out, int n) {
   if (n > 1024) n = 1024;
   return cudaMemcpyFromSymbol(out, g_trace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
