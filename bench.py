@@ -63,6 +63,8 @@ def parse(argv=None):
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-shapes", action="store_true")
     ap.add_argument("--no-interval", action="store_true")
+    ap.add_argument("--shape", default=None, choices=["decode_b16_ctx512", "paged_b64_hostile"],
+                    help="time only the fused decode step on this workload (for profiling) and exit")
     return ap.parse_args(argv)
 
 
@@ -800,6 +802,46 @@ def run_gpu(args, ws, rank):
         print(json.dumps(line), flush=True)
 
 
+def run_shape(args, rank):
+    """Only the fused decode step on one of the other decode workloads: one
+    cache, `warmup` eager steps, then `steps` timed eager steps (CUDA events).
+    A small, self-contained command for profilers; not a bench line."""
+    import fp8_quantized_kv_gb300 as fk
+    spec = synth.WORKLOADS[args.shape]
+    inp = synth.decode_inputs(spec, device="cuda")
+    B, Hq, Hkv, D = spec.batch, spec.q_heads, spec.kv_heads, spec.head_dim
+    lens64 = inp.seq_lens.to(torch.int64)
+    sidx = torch.repeat_interleave(torch.arange(B), lens64).to(torch.int32).cuda()
+    pos = torch.cat([torch.arange(int(n)) for n in lens64]).to(torch.int32).cuda()
+    if spec.page_size is None:
+        cache = fk.Fp8KVCache.contiguous(B, Hkv, D, int(lens64.max()), args.dtype)
+    else:
+        cache = fk.Fp8KVCache.paged(inp.page_table, inp.num_pages, Hkv, D, spec.page_size, args.dtype)
+    fk.fp8kv_append(cache, inp.k.contiguous(), inp.v.contiguous(), sidx, pos)
+    last = (inp.cu_seqlens[1:] - 1).cuda()
+    knew, vnew = inp.k[last].contiguous(), inp.v[last].contiguous()
+    lens = inp.seq_lens.cuda()
+    q = inp.q.contiguous()
+    kid = KERNEL_IDS[args.kernel]
+    ws_t = torch.zeros(fk.fp8kv_decode_step_workspace_bytes(cache, Hq, 0, kid), dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    for _ in range(args.warmup):
+        fk.fp8kv_decode_step(q, knew, vnew, cache, lens, workspace=ws_t, out=out, kernel=kid)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fk.fp8kv_decode_step(q, knew, vnew, cache, lens, workspace=ws_t, out=out, kernel=kid)
+    e1.record()
+    torch.cuda.synchronize()
+    if fk.fp8kv_get_device_error() != 0:
+        raise RuntimeError(f"{args.shape}: device error")
+    if rank == 0:
+        print(json.dumps({"shape": args.shape, "cache": args.dtype, "kernel": args.kernel,
+                          "us_per_step": e0.elapsed_time(e1) / args.steps * 1e3, "steps": args.steps,
+                          "note": "eager launches of one cache; a profiling aid, not a bench line"}))
+
+
 def main():
     args = parse()
     ws, rank = dist_setup()
@@ -810,7 +852,10 @@ def main():
             raise SystemExit("bench.py needs a CUDA GPU (the FP8-KV kernels have no CPU path)")
         from fp8_quantized_kv_gb300._lib import get_lib
         get_lib()
-        run_gpu(args, ws, rank)
+        if args.shape:
+            run_shape(args, rank)
+        else:
+            run_gpu(args, ws, rank)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
