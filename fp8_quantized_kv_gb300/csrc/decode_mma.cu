@@ -421,7 +421,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
     } else {
       const int P = c.page_size;
       const int np = (valid + P - 1) / P;
-      const uint32_t per_page = P * 128 * (C::KB + C::VB) + P * 4 * ((int)C::K8 + (VE == ELEM_E4M3));
+      // the K and V boxes come by TMA (counted in the transaction bytes);
+      // the 64-byte-per-page scale rows come by cp.async, whose completion
+      // lanes 0 .. 128/P-1 each signal with one arrival on the stage barrier
+      // (initialised with 1 + 128/P arrivals for a paged cache): a TMA copy
+      // per scale row doubled the copies per tile, and the paged step was
+      // bound per copy
+      const uint32_t per_page = P * 128 * (C::KB + C::VB);
       int page = my_page;
       load_page(i + 1);
       if (lane == 0) tma::arrive_expect_tx(&full[s], per_page * np);
@@ -437,9 +443,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
         tma::load_2d(st + C::K_TILE + off, &tp.tmv, 0, (int)row, &full[s]);
         if (VE != ELEM_E4M3)
           tma::load_2d(st + C::K_TILE + kMmaTile * 128 + off, &tp.tmv, 64, (int)row, &full[s]);
-        if (C::K8) tma::load_1d(kss + lane * P, c.k_scale + row, P * 4, &full[s]);
-        if (VE == ELEM_E4M3) tma::load_1d(vss + lane * P, c.v_scale + row, P * 4, &full[s]);
+        for (int q = 0; q < P / 4; ++q) {
+          if (C::K8) cp_async16(kss + lane * P + 4 * q, c.k_scale + row + 4 * q);
+          if (VE == ELEM_E4M3) cp_async16(vss + lane * P + 4 * q, c.v_scale + row + 4 * q);
+        }
       }
+      if (lane < kMmaTile / P)
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(umma::smem_u32(&full[s]))
+                     : "memory");
     }
     if (lane == 0) TRACE(8 * i + 0);
   };
@@ -447,7 +458,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
   if (tid == 0) {
     // the ring's barriers first, so the first loads go out as early as possible
     for (int i = 0; i < C::NST; ++i) {
-      umma::mbar_init(&full[i], 1);
+      umma::mbar_init(&full[i], c.paged ? 1 + kMmaTile / c.page_size : 1);   // paged: + cp.async arrivals
       umma::mbar_init(&empty[i], 1 + 4);     // PV commit + the four warps of the owning group
     }
     *abort_flag = 0;
