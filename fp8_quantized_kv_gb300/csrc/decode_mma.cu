@@ -421,36 +421,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
     } else {
       const int P = c.page_size;
       const int np = (valid + P - 1) / P;
-      // the K and V boxes come by TMA (counted in the transaction bytes);
-      // the 64-byte-per-page scale rows come by cp.async, whose completion
-      // lanes 0 .. 128/P-1 each signal with one arrival on the stage barrier
-      // (initialised with 1 + 128/P arrivals for a paged cache): a TMA copy
-      // per scale row doubled the copies per tile, and the paged step was
-      // bound per copy
+      // The K and V boxes come by TMA (counted in the transaction bytes).
+      // The 64-byte-per-page scale rows come by cp.async: a TMA copy per
+      // scale row doubled the copies per tile, and the paged step was bound
+      // per copy.  Each lane's cp.async.mbarrier.arrive adds one pending
+      // arrival to the stage barrier and completes it when the lane's copies
+      // land; it runs before lane 0's arrival (the barrier's only expected
+      // one), so the phase cannot complete without the scale rows.
       const uint32_t per_page = P * 128 * (C::KB + C::VB);
       int page = my_page;
       load_page(i + 1);
+      if (lane < np && (page < 0 || page >= c.num_pages)) {
+        raise_error(p.err, FP8KV_DEVERR_BAD_PAGE);
+        page = 0;      // read a valid page; the result is flagged as wrong
+      }
+      const int64_t row = ((int64_t)page * c.kv_heads + h) * P;
+      if (lane < np && (C::K8 || VE == ELEM_E4M3)) {
+        for (int q = 0; q < P / 4; ++q) {
+          if (C::K8) cp_async16(kss + lane * P + 4 * q, c.k_scale + row + 4 * q);
+          if (VE == ELEM_E4M3) cp_async16(vss + lane * P + 4 * q, c.v_scale + row + 4 * q);
+        }
+        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" ::"r"(umma::smem_u32(&full[s]))
+                     : "memory");
+      }
+      __syncwarp();
       if (lane == 0) tma::arrive_expect_tx(&full[s], per_page * np);
       if (lane < np) {
-        if (page < 0 || page >= c.num_pages) {
-          raise_error(p.err, FP8KV_DEVERR_BAD_PAGE);
-          page = 0;      // read a valid page; the result is flagged as wrong
-        }
-        const int64_t row = ((int64_t)page * c.kv_heads + h) * P;
         const int off = lane * P * 128;
         tma::load_2d(st + off, &tp.tmk, 0, (int)row, &full[s]);
         if (!C::K8) tma::load_2d(st + kMmaTile * 128 + off, &tp.tmk, 64, (int)row, &full[s]);
         tma::load_2d(st + C::K_TILE + off, &tp.tmv, 0, (int)row, &full[s]);
         if (VE != ELEM_E4M3)
           tma::load_2d(st + C::K_TILE + kMmaTile * 128 + off, &tp.tmv, 64, (int)row, &full[s]);
-        for (int q = 0; q < P / 4; ++q) {
-          if (C::K8) cp_async16(kss + lane * P + 4 * q, c.k_scale + row + 4 * q);
-          if (VE == ELEM_E4M3) cp_async16(vss + lane * P + 4 * q, c.v_scale + row + 4 * q);
-        }
       }
-      if (lane < kMmaTile / P)
-        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(umma::smem_u32(&full[s]))
-                     : "memory");
     }
     if (lane == 0) TRACE(8 * i + 0);
   };
@@ -458,7 +461,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
   if (tid == 0) {
     // the ring's barriers first, so the first loads go out as early as possible
     for (int i = 0; i < C::NST; ++i) {
-      umma::mbar_init(&full[i], c.paged ? 1 + kMmaTile / c.page_size : 1);   // paged: + cp.async arrivals
+      umma::mbar_init(&full[i], 1);
       umma::mbar_init(&empty[i], 1 + 4);     // PV commit + the four warps of the owning group
     }
     *abort_flag = 0;
