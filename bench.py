@@ -246,6 +246,23 @@ def traffic_from_profile(kernel_key, sha):
 
 # ---------------------------------------------------------------- oracle --
 
+def host_description():
+    """The host the CPU baseline ran on: architecture, logical CPUs and the
+    CPU model where the OS reports one (the baseline itself uses one core)."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"machine": platform.machine(), "logical_cpus": os.cpu_count(), "model": model}
+
+
 def oracle_sample(inp, n_seqs, tokens):
     """Oracle work for `n_seqs` sequences over `tokens` cached tokens: e4m3
     dequantisation of their K/V and fp64 decode attention.  Returns seconds
@@ -301,7 +318,7 @@ def run_reference(args, ws, rank):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": spec.batch, "q_heads": spec.q_heads,
                    "kv_heads": spec.kv_heads, "head_dim": spec.head_dim, "ctx": T, "cache": "k8v8"},
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "host": host_description(),
                          "sample": f"per step: 1 sequence x {tokens} tokens of the workload "
                                    "(e4m3 dequantise + fp64 decode attention), single thread; "
                                    "ms_per_step scaled to the full 16 x 8192 layer"},
@@ -770,7 +787,7 @@ def run_gpu(args, ws, rank):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         host_inp = synth.decode_inputs(spec, device="cpu", seq_lens=[T] * 8)
         dt, nbytes = oracle_sample(host_inp, 8, T)
-        cpu = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "host": host_description(),
                "sample": f"8 of 16 sequences x {T} tokens (e4m3 dequantise + fp64 decode attention), "
                          f"single thread, {dt:.2f} s"}
 
