@@ -274,8 +274,8 @@ FP8KV_API fp8kv_status fp8kv_decode_step(const void *q, const void *k_new, const
  * the query/key/value projection and every layer has its own cache. */
 #define FP8KV_STEP_EARLY_CACHE_READ 1u
 
-/* Decode attention that allocates nothing (the paper has no counterpart:
- * this is a convenience of the library).  Same arguments and results as
+/* Decode attention that allocates nothing (a convenience of this library;
+ * the source pages have no such call).  Same arguments and results as
  * fp8kv_decode_attention without the workspace: the fp32 partials go to a
  * fixed array of fp8kv_decode_static_scratch_bytes() bytes (16 MiB) compiled
  * into the library, which every GPU that loads the library keeps until the
