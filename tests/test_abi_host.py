@@ -196,3 +196,30 @@ def test_workloads_match_their_description():
     # determinism
     again = synth.decode_inputs(small)
     assert torch.equal(again.k, inp.k) and torch.equal(again.page_table, inp.page_table)
+
+
+def test_python_binding_rejects_host_tensors_before_any_call(lib):
+    # the binding only marshals device tensors: host tensors and wrong dtypes
+    # are refused before the library is called
+    import fp8_quantized_kv_gb300 as fk
+    x = torch.zeros(4, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fk.fp8kv_quantize(x)
+    with pytest.raises(ValueError):
+        fk.fp8kv_quantize_mx(x)
+    with pytest.raises(ValueError):
+        fk.fp8kv_quantize_mx(torch.zeros(4, 128, dtype=torch.float32))
+    assert fk.KERNELS["tensor_cores_k_f16"] == 3 and fk.KERNELS["tensor_cores_k_f16_producer"] == 4
+    assert fk.DTYPES == {"k8v8": 0, "k16v8": 1, "k16v16": 2, "k8v16": 3, "mxk8v8": 4}
+
+
+def test_mxfp8_and_bias_workspace_match_the_plain_cache(lib):
+    # the MXFP8 dtype and a key bias change neither the split plan nor the
+    # workspace: the scale slot is the same 4 bytes per row
+    r = ctypes.byref
+    for kern in (0, 2):
+        base = lib.fp8kv_decode_workspace_bytes(r(_cache()), 16, 0, kern)
+        assert lib.fp8kv_decode_workspace_bytes(r(_cache(dtype=4)), 16, 0, kern) == base
+        assert lib.fp8kv_decode_workspace_bytes(r(_cache(k_bias=0x5000)), 16, 0, kern) == base
+        assert (lib.fp8kv_decode_step_workspace_bytes(r(_cache(dtype=4)), 16, 0, kern)
+                == lib.fp8kv_decode_step_workspace_bytes(r(_cache()), 16, 0, kern))
