@@ -30,16 +30,19 @@
 // section "Operating model": producer and consumer warps interleave the
 // stages across adjacent tiles):
 //   warp 0     TMA producer: 128-byte-swizzled tensor loads of the K and V
-//              tiles straight into the UMMA operand layout, 1-D bulk copies
-//              of the scale rows; a ring of NST stages (full/empty mbarriers).
+//              tiles straight into the UMMA operand layout; scale rows by 1-D
+//              bulk copy (contiguous cache) or cp.async (paged cache); a ring
+//              of NST stages (full/empty mbarriers).
 //   warp 1     TMEM owner and QK issuer (one thread).
 //   warp 10    PV issuer (one thread).  Issuing a few tcgen05.mma costs the
 //              issuing thread a fraction of a microsecond; one thread issuing
 //              both QK and PV set the tile interval, two run side by side.
-//   warps 2-5  softmax of tile i, then the O update of tile i-1 (thread =
-//              TMEM lane = token for S, = head dim for O).
-// S, O (TMEM) and P (shared memory) are double-buffered, so QK(i+1), PV(i)
-// and the softmax of tile i+1 overlap.  Each QK and PV is split into four
+//   warps 2-9  two softmax warpgroups on alternate tiles: the softmax of a
+//              tile, then the O update of the group's previous tile (thread =
+//              TMEM lane = token for S, = head dim for O); merged at the end
+//              like two splits.
+// S, O (TMEM) and P (shared memory) are double-buffered per group, so the
+// QKs and PVs of neighbouring tiles overlap the softmax.  Each QK and PV is split into four
 // independent MMAs (one per k-step, each with its own TMEM accumulator,
 // summed by the reading threads): dependent thin MMAs would serialise on
 // their latency.  Every wait is bounded; a wait that
