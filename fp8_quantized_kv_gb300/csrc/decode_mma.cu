@@ -7,10 +7,12 @@
 // 128-token tiles:
 //
 //   S^T[128 tokens x 16] = K_tile[128 x 128] . Q^T         tcgen05.mma -> TMEM
-//   per token (one thread each): s = S * k_scale * sm_scale, tile max, p,
-//     P' = bf16_rn(p * v_scale)                              (CUDA cores)
+//   per token (one thread each): s = S * k_scale * sm_scale (log2 units),
+//     per warp (32 tokens): anchor U = ceil(max of s + log2 v_scale),
+//     p = 2^(s - U), P' = bf16_rn(p * v_scale)               (CUDA cores)
 //   O^T[128 dims x 16]   = V_tile^T[128 x 128] . P'^T        tcgen05.mma -> TMEM
-//   per dim (one thread each): O = O * e^(m-m') + e^(m_t-m') * O_tile
+//   per dim (one thread each): O = O * 2^(m-m') + sum over the four warps w
+//     of 2^(U_w-m') * O_tile,w  (each warp's tokens are one PV k-step)
 //
 // The e4m3 cache tiles are MMA operands as they land in shared memory
 // (kind::f8f6f4; K tile K-major, V tile MN-major): no per-element K or V
@@ -18,13 +20,19 @@
 // tile preparation", sections "Measure the K8/V8 break-even" and "NVIDIA
 // Blackwell": the prepare-K and prepare-V stages of the tile interval vanish).
 // The other operand of each MMA must then be e4m3 too, so the bf16 query row
-// and the bf16-rounded P row are each written as the sum of two e4m3 numbers
-// (hi = e4m3(x), lo = e4m3(x - hi)) after an exact power-of-two scaling of
-// the row; hi and lo occupy the 16 columns of the N dimension that 8 query
-// heads leave free, and are summed after the MMA.  For every component
-// within 2^-11 of its row's largest magnitude the pair is exact; smaller
-// components carry an absolute error below 2^-19 of the row maximum.
+// and the bf16-rounded P' row are each written as the sum of two e4m3 numbers
+// (hi = e4m3(x), lo = e4m3(x - hi)); hi and lo occupy the 16 columns of the N
+// dimension that 8 query heads leave free, and are summed after the MMA.  The
+// query row is first scaled by a power of two; P' needs no per-row scaling:
+// its anchor puts the warp's largest P' in (1/2, 1], so 2^8 P' lies in
+// (128, 256].  For every component within 2^-11 of that maximum the pair is
+// exact; smaller components carry an absolute error below 2^-19 of it -- and
+// since the anchor follows p * v_scale, not p, a token whose V scale is far
+// below its neighbours' still sets the scale when its weight dominates.
 // A bf16 K (K16/V8) or V (K16/V16) side uses kind::f16 with exact operands.
+//
+// Anchors are integer-valued and depend on the tile alone: split and unsplit
+// runs round P' alike, and every fold factor is an exact power of two.
 //
 // Warp roles ("FP8 KV attention: hardware paths and tile preparation",
 // section "Operating model": producer and consumer warps interleave the
@@ -37,18 +45,21 @@
 //   warp 10    PV issuer (one thread).  Issuing a few tcgen05.mma costs the
 //              issuing thread a fraction of a microsecond; one thread issuing
 //              both QK and PV set the tile interval, two run side by side.
-//   warps 2-9  two softmax warpgroups on alternate tiles: the softmax of a
-//              tile, then the O update of the group's previous tile (thread =
-//              TMEM lane = token for S, = head dim for O); merged at the end
-//              like two splits.
+//   warps 2-9  two softmax warpgroups on alternate tiles: the O fold of the
+//              group's tile before last, then the softmax of the next tile
+//              (thread = TMEM lane = token for S, = head dim for O); merged
+//              at the end like two splits.  The four warps of a group share
+//              no barrier inside the loop: each publishes its tile anchors
+//              in shared memory before its P-ready arrival, and the O fold
+//              reads them after that phase completed.
 // S, O (TMEM) and P (shared memory) are double-buffered per group, so the
-// QKs and PVs of neighbouring tiles overlap the softmax.  Each QK and PV is split into four
-// independent MMAs (one per k-step, each with its own TMEM accumulator,
-// summed by the reading threads): dependent thin MMAs would serialise on
-// their latency.  Every wait is bounded; a wait that
-// runs out raises FP8KV_DEVERR_TIMEOUT, the CTA writes an empty partial and
-// leaves.  V rows past the sequence end are zeroed before PV (0 * NaN would
-// poison the product).
+// QKs and PVs of neighbouring tiles overlap the softmax.  Each QK and PV is
+// split into four independent MMAs (one per k-step, each with its own TMEM
+// accumulator, combined by the reading threads): dependent thin MMAs would
+// serialise on their latency.  Every wait is bounded; a wait that runs out
+// raises FP8KV_DEVERR_TIMEOUT, the CTA writes an empty partial and leaves.
+// V rows past the sequence end are zeroed before PV (0 * NaN would poison
+// the product).
 //
 // The fused decode step (append + split + merge in one launch) merges the
 // splits of a (sequence, KV head) in one of two ways.  With 2..8 splits whose
@@ -65,6 +76,8 @@
 namespace fp8kv {
 
 constexpr int kMmaTile = 128;
+// Split partials the global merge stages in the (idle) ring at a time.
+constexpr int kMergeChunk = 44;
 // warp 0 TMA producer, warp 1 QK issuer and TMEM owner, warps 2-9 softmax,
 // warp 10 PV issuer
 constexpr int kTcThreads = 352;
@@ -86,17 +99,18 @@ struct TcCfg {
   static constexpr int KB = K8 ? 1 : 2, VB = VE == ELEM_E4M3 ? 1 : 2;
   static constexpr int K_TILE = kMmaTile * D * KB;
   static constexpr int V_TILE = kMmaTile * D * VB;
-  static constexpr int STAGE = ((K_TILE + V_TILE + 2 * kMmaTile * 4) + 1023) / 1024 * 1024;
+  // K tile, V tile, then the K and V scale rows of an 8-bit side
+  static constexpr int STAGE = ((K_TILE + V_TILE + (K8 || VE == ELEM_E4M3 ? 2 * kMmaTile * 4 : 0)) + 1023) / 1024 * 1024;
   static constexpr int NST = XK != XK_NATIVE ? 4 : (K8 && VE == ELEM_E4M3) ? 6 : (K8 == (VE == ELEM_E4M3) ? 3 : 4);
   static constexpr int KCV = XK != XK_NATIVE ? 2 * kMmaTile * D * 2 : 0;   // two converted f16 K tiles
   static constexpr int QOP = QHL ? 16 * 128 : 2 * 16 * 128;
   static constexpr int POP = VE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;   // [128 tokens][16 or 32 B]
   static constexpr int XO = 8 * 128 * 4;    // group 1's O handed to group 0
-  static constexpr int MISC = 6656;         // barriers, small tables, cluster receive buffers
+  static constexpr int MISC = 7936;         // barriers, small tables, cluster receive buffers
   static constexpr int BYTES = NST * STAGE + KCV + QOP + 4 * POP + XO + MISC + 1024;
   static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
-  static_assert(NST * STAGE + KCV >= (8 * 48 * D + 2 * 8 * 48) * 4,
-                "ring too small to stage 48 partials for the merge");
+  static_assert(NST * STAGE + KCV >= (8 * kMergeChunk * D + 2 * 8 * kMergeChunk) * 4,
+                "ring too small to stage a chunk of partials for the merge");
   static_assert(XK == XK_NATIVE || KE == ELEM_E4M3, "the K transform converts e4m3 codes");
 };
 
@@ -129,7 +143,16 @@ __device__ unsigned long long g_cta_time[4096][8];   // start, end, published, l
     if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (slot) < 1024) \
       atomicMax(&g_trace[(slot)], (unsigned long long)clock64());            \
   } while (0)
+// fine stamps inside one tile's softmax (tile 8, thread 0 of its group)
+#define TRACE_SUB(tile, k)                                                   \
+  do {                                                                       \
+    if ((tile) == 8 && (t) == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) \
+      g_trace[900 + (k)] = clock64();                                        \
+  } while (0)
 #else
+#define TRACE_SUB(tile, k) \
+  do {                     \
+  } while (0)
 #define TRACE(slot) \
   do {              \
   } while (0)
@@ -205,19 +228,27 @@ __device__ __forceinline__ void cluster_exchange(const DecodeParams& p, float* r
 #pragma unroll
     for (int u = 1; u < 8; ++u) g += t >= u * m4;
     const int j = t - g * m4;
-    float M = -INFINITY;
-    for (int kk = 0; kk < S; ++kk) M = fmaxf(M, rx_ml[kk * 16 + g]);
+    // (S <= 8: unrolled, every load independent; anchors are integer-valued,
+    // so the weights are exact powers of two)
+    float mk[8];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) mk[kk] = kk < S ? rx_ml[kk * 16 + g] : -INFINITY;
+    float M = mk[0];
+#pragma unroll
+    for (int kk = 1; kk < 8; ++kk) M = fmaxf(M, mk[kk]);
     float L = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int kk = 0; kk < S; ++kk) {
-      const float mk = rx_ml[kk * 16 + g];
-      const float w = mk == -INFINITY ? 0.f : ex2(mk - M);
-      const float4 v = *reinterpret_cast<const float4*>(rx_o + 4 * ((kk * 8 + g) * m4 + j));
-      L += w * rx_ml[kk * 16 + 8 + g];
-      o.x += w * v.x; o.y += w * v.y; o.z += w * v.z; o.w += w * v.w;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      if (kk < S) {
+        const float w = pow2_diff(mk[kk] - M, 0);
+        const float4 v = *reinterpret_cast<const float4*>(rx_o + 4 * ((kk * 8 + g) * m4 + j));
+        L += w * rx_ml[kk * 16 + 8 + g];
+        o.x += w * v.x; o.y += w * v.y; o.z += w * v.z; o.w += w * v.w;
+      }
     }
     if (g < G) {
-      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
       const int64_t oi = ((int64_t)b * p.q_heads + (int64_t)h * G + g) * D + 4 * (mlo + j);
       const float r4[4] = {o.x * inv, o.y * inv, o.z * inv, o.w * inv};
       if ((reinterpret_cast<uintptr_t>(p.out) & 15) != 0) {   // caller's buffer not 16-byte aligned
@@ -303,12 +334,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
   uint64_t* kc_full = reinterpret_cast<uint64_t*>(misc + 320);   // [2] transform path: f16 K tile ready
   uint64_t* kc_empty = kc_full + 2;                              // [2] its QK completed
   float* qscale = reinterpret_cast<float*>(misc + 512);    // [8]
-  float* red = qscale + 8;                                 // [wg][2][4][9]
-  float* lred = red + 144;                                 // [wg][4][8]
+  float* lred = reinterpret_cast<float*>(misc + 1120);     // [wg][4][8]
   float* xml = lred + 64;                                  // [16]: m and l of warpgroup 1
   int* slice_tab = reinterpret_cast<int*>(misc + 1472);    // [9] first four-dim group of each rank
   float* rx_ml = reinterpret_cast<float*>(misc + 1536);    // [sender][m 8 | l 8]
   float* rx_o = reinterpret_cast<float*>(misc + 2048);     // [sender][dim of this rank's slice][8 heads]
+  float* anc0 = reinterpret_cast<float*>(misc + 544);      // [4 slots][4 warps][8 heads]: group 0's anchors
+  float* wscr = reinterpret_cast<float*>(misc + 6656);     // [softmax warp][40]: maxima, then fold factors
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -771,10 +803,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
             umma::mma_f8_ss(d + 16 * k, umma::sdesc(va + k * 4 * 1024, 1024, 1024, umma::SWIZZLE_128B),
                             umma::sdesc(pa + k * 512, 128, 128, umma::SWIZZLE_NONE), ID_PV, 0);
         } else {
+          // 16-token k-steps: accumulator j takes k-steps 2j and 2j+1, the
+          // 32 tokens of softmax warp j (each warp's tokens carry their own
+          // anchor); the second of each pair is issued after the four firsts
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            umma::mma_f16_ss(d + 16 * (k & 3), umma::sdesc(va + k * 2 * 1024, kMmaTile * 128, 1024, umma::SWIZZLE_128B),
-                             umma::sdesc(pa + k * 512, 256, 128, umma::SWIZZLE_NONE), ID_PV, k >= 4);
+          for (int kk = 0; kk < 8; ++kk) {
+            const int k = 2 * (kk & 3) + (kk >> 2);
+            umma::mma_f16_ss(d + 16 * (k >> 1), umma::sdesc(va + k * 2 * 1024, kMmaTile * 128, 1024, umma::SWIZZLE_128B),
+                             umma::sdesc(pa + k * 512, 256, 128, umma::SWIZZLE_NONE), ID_PV, kk >= 4);
+          }
         }
         umma::mma_commit(&wb[w].o_full[bb]);
         umma::mma_commit(&empty[s]);
@@ -793,17 +830,96 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
     float qs[8];
 #pragma unroll
     for (int g = 0; g < 8; ++g) qs[g] = qscale[g] * p.scale_log2;
-    float m_run[8], l_thr[8], o_run[8], a_prev[8], b_prev[8];
+    // Anchors.  The tokens one warp holds of a tile are referenced to the
+    // integer-valued U = ceil(max of s + log2(v_scale)) over them (log2
+    // units; for a bf16 V side, of s): p = 2^(s - U), and P' = bf16(p *
+    // v_scale) then lies in [0, 1] with its largest entry above 1/2, so the
+    // e4m3 P' column is exact to bf16 precision after the constant scaling
+    // by 2^8, whatever the spread of the V scales.  (log2(v_scale) is
+    // clamped at -100 so that p stays finite for a token whose V row is zero
+    // or nearly so.)  U depends on the tile alone, so split and unsplit runs
+    // round P' alike, and every fold factor is an exact power of two.
+    //   m_w: this warp's running anchor per head (reference of its threads'
+    //        partial sums l_thr), tracked by the four lanes of that head;
+    //   m_o: the group's running anchor over its four warps (reference of
+    //        O), tracked per head by the lanes that fold that head.
+    // No barrier across the group's warps inside the loop: each warp's P'
+    // columns feed their own PV k-step accumulator (tokens 32w..32w+31),
+    // and the O fold weights accumulator w with warp w's published anchor.
+    constexpr int kPShift = VE == ELEM_E4M3 ? 8 : 0;  // e4m3 P' columns hold 2^8 P'
+    float l_thr[8], o_run[8];
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      m_run[g] = -INFINITY; l_thr[g] = 0.f; o_run[g] = 0.f; a_prev[g] = 0.f; b_prev[g] = 0.f;
-    }
-    float pf_prev = 1.f;
+    for (int g = 0; g < 8; ++g) { l_thr[g] = 0.f; o_run[g] = 0.f; }
+    float m_wl = -INFINITY;                          // m_w of head (lane >> 2) & 7
+    float m_ol = -INFINITY;                          // m_o of head lane & 7
+    // published anchors, [4 slots][4 warps][8 heads]; group 1's table shares
+    // the buffer that hands its O to group 0 once its loop is over
+    float* ancA = wg == 0 ? anc0 : xo;
+    float* wsc = wscr + (warp - 2) * 40;
     bool failed = false;
     const int nl = (n_tiles - wg + 1) / 2;          // tiles of this group
-    for (int li = 0; li <= nl && !failed; ++li) {
-      float a_cur[8], b_cur[8];
-      float pf_cur = 1.f;
+    // iteration li: the O fold of the group's tile li-2 (its PV finished
+    // long ago), then the softmax of tile li
+    for (int li = 0; li < nl + 2; ++li) {
+      if (li >= 2) {
+        const int lj = li - 2, bb = lj & 1, ub = lj >> 1;
+        TRACE_SUB(2 * li + wg, 0);
+        bool ok = wait_fast(&B.o_full[bb], ub & 1, abort_flag);
+        // p_full of tile lj completed before its PV: the four warps'
+        // anchors of that tile were written before their arrivals
+        ok = ok && wait_fast(&B.p_full[bb], ub & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+        TRACE_SUB(2 * li + wg, 1);
+        umma::fence_after_sync();
+        uint32_t r[4][16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) umma::tmem_ld16_nowait(tmem + o_col + 64 * bb + 16 * k + lane_off, r[k]);
+        // fold factors, one (warp k, head g) per lane: the head's new anchor
+        // is the maximum of the four warps' anchors and its running m_o;
+        // accumulator k gets 2^(U_k - kPShift - m_o'), the old O 2^(m_o - m_o')
+        {
+          const float Aq = ancA[(lj & 3) * 32 + lane];
+          float am = fmaxf(Aq, __shfl_xor_sync(0xffffffffu, Aq, 8));
+          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 16));
+          const float mn = fmaxf(m_ol, am);
+          wsc[lane] = pow2_diff(Aq - mn, -kPShift);
+          if (lane < 8) wsc[32 + lane] = pow2_diff(m_ol - mn, 0);
+          m_ol = mn;
+        }
+        __syncwarp();
+        float fk[4][8], fa[8];
+        {
+          const float4* w4 = reinterpret_cast<const float4*>(wsc);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float4 x = w4[2 * k], y = w4[2 * k + 1];
+            fk[k][0] = x.x; fk[k][1] = x.y; fk[k][2] = x.z; fk[k][3] = x.w;
+            fk[k][4] = y.x; fk[k][5] = y.y; fk[k][6] = y.z; fk[k][7] = y.w;
+          }
+          const float4 x = w4[8], y = w4[9];
+          fa[0] = x.x; fa[1] = x.y; fa[2] = x.z; fa[3] = x.w;
+          fa[4] = y.x; fa[5] = y.y; fa[6] = y.z; fa[7] = y.w;
+        }
+        TRACE_SUB(2 * li + wg, 2);
+        umma::tmem_wait_ld();
+        TRACE_SUB(2 * li + wg, 3);
+        umma::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) umma::mbar_arrive(&B.o_empty[bb]);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          float o = o_run[g] * fa[g];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float ot = VE == ELEM_E4M3 ? __uint_as_float(r[k][g]) + __uint_as_float(r[k][g + 8])
+                                             : __uint_as_float(r[k][g]);
+            o = fmaf(ot, fk[k][g], o);
+          }
+          o_run[g] = o;
+        }
+        TRACE_SUB(2 * li + wg, 4);
+        if (t == 0) TRACE(8 * (2 * lj + wg) + 5);
+      }
       if (li < nl) {
         const int i = 2 * li + wg;
         const int s = i % C::NST, u = i / C::NST, bb = li & 1, ub = li >> 1;
@@ -811,7 +927,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
           // convert this tile's K into the group's own f16 buffer (free: the
           // group consumed the S of its previous tile, so that QK is done)
           const bool landed = wait_or_abort(&full[s], u & 1, abort_flag);
-          if (group_any(wg, !landed)) { failed = true; break; }
+          if (!__all_sync(0xffffffffu, landed)) { failed = true; break; }
           k_tile_to_f16<128>(smem + s * C::STAGE, kcv + wg * (kMmaTile * D * 2), t);
           umma::fence_proxy_async_smem();
           __syncwarp();
@@ -820,20 +936,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
         // hand-offs on the critical path: poll without a suspend-time hint
         bool ok = wait_fast(&B.s_full[bb], ub & 1, abort_flag);
         ok = ok && wait_fast(&full[s], u & 1, abort_flag);
-        if (group_any(wg, !ok)) { failed = true; break; }
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
         if (t == 0) TRACE(8 * i + 3);
+        TRACE_SUB(i, 5);
         umma::fence_after_sync();
+        uint8_t* st = smem + s * C::STAGE;
+        const float* kss = reinterpret_cast<const float*>(st + C::K_TILE + C::V_TILE);
+        const float* vss = kss + kMmaTile;
+        const int t0 = (t_begin + i) * kMmaTile;
+        const int valid = min(kMmaTile, T - t0);
+        const bool tok_ok = t < valid;
+        const float kf = KE == ELEM_E4M3 ? kss[t] : 1.f;     // (MXFP8: block scales applied below)
+        const float vsc = VE == ELEM_E4M3 ? (tok_ok ? vss[t] : 0.f) : 1.f;
         float sc[16];
         {
           uint32_t r[4][16];
 #pragma unroll
           for (int k = 0; k < 4; ++k) umma::tmem_ld16_nowait(tmem + s_col + 64 * bb + 16 * k + lane_off, r[k]);
           umma::tmem_wait_ld();
+          TRACE_SUB(i, 6);
           if constexpr (C::KMX) {
             // MXFP8 keys: accumulator k holds dims 32k..32k+31 of the dot
             // product, so the key's E8M0 block scale k applies to it here
             // (the block-scaled product, summed over the four blocks)
-            const uint32_t e8 = reinterpret_cast<const uint32_t*>(smem + s * C::STAGE + C::K_TILE + C::V_TILE)[t];
+            const uint32_t e8 = reinterpret_cast<const uint32_t*>(st + C::K_TILE + C::V_TILE)[t];
             float w[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) w[k] = pow2_exact((int)((e8 >> (8 * k)) & 0xFF) - 127);
@@ -851,28 +977,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
         umma::fence_before_sync();
         __syncwarp();
         if (lane == 0) umma::mbar_arrive(&B.s_empty[bb]);
-
-        uint8_t* st = smem + s * C::STAGE;
-        const float* kss = reinterpret_cast<const float*>(st + C::K_TILE + C::V_TILE);
-        const float* vss = kss + kMmaTile;
-        const int t0 = (t_begin + i) * kMmaTile;
-        const int valid = min(kMmaTile, T - t0);
-        const bool tok_ok = t < valid;
-        const float kf = KE == ELEM_E4M3 ? kss[t] : 1.f;     // (MXFP8: block scales applied above)
-        const float vsc = VE == ELEM_E4M3 ? (tok_ok ? vss[t] : 0.f) : 1.f;
-        float sg[8];
-        float* rb = red + (wg * 2 + (li & 1)) * 36;
+        // scores (log2 units) and s + log2(v_scale)
+        const float lvs = VE == ELEM_E4M3 ? fmaxf(lg2_approx(vsc), -100.f) : 0.f;
+        float sg[8], uu[8];
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const float raw = C::QHL ? (sc[g] + sc[g + 8]) : sc[g];
           sg[g] = tok_ok ? raw * (qs[g] * kf) : -INFINITY;
-          const float wm = warp_max_redux(sg[g]);
-          if (lane == 0) rb[sw * 9 + g] = wm;
+          uu[g] = sg[g] + lvs;
         }
-        if (VE == ELEM_E4M3) {
-          const float vm = warp_max_redux(vsc);
-          if (lane == 0) rb[sw * 9 + 8] = vm;
+        TRACE_SUB(i, 7);
+        // per head, by the four lanes that end up holding its warp maximum:
+        // the anchor U, and the factors that bring the threads' l sums to
+        // the new running anchor; broadcast through the warp's own row
+        {
+          const float U = ceilf(warp_max_transposed<8>(uu, lane));   // head (lane >> 2) & 7
+          const float mn = fmaxf(m_wl, U);
+          if ((lane & 3) == 0)
+            *reinterpret_cast<float4*>(wsc + lane) =
+                make_float4(U, pow2_diff(m_wl - mn, 0), pow2_diff(U - mn, 0), 0.f);
+          m_wl = mn;
         }
+        __syncwarp();
+        float Uh[8], f1[8], f2[8];
+        {
+          const float4* w4 = reinterpret_cast<const float4*>(wsc);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const float4 x = w4[g];
+            Uh[g] = x.x; f1[g] = x.y; f2[g] = x.z;
+          }
+        }
+        TRACE_SUB(i, 8);
         if (!tok_ok) {      // V rows past the sequence end: zero them for PV
           uint4* vrow = reinterpret_cast<uint4*>(st + C::K_TILE);
 #pragma unroll
@@ -881,121 +1017,83 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
             for (int ch = 0; ch < 8; ++ch)
               vrow[(blk * kMmaTile * 128 + t * 128 + ch * 16) / 16] = make_uint4(0, 0, 0, 0);
         }
-        group_sync(wg);
-        int pex = 0;
-        if (VE == ELEM_E4M3) {
-          const float vmax = fmaxf(fmaxf(rb[8], rb[17]), fmaxf(rb[26], rb[35]));
-          pex = e4m3_row_exp(vmax);
-          pf_cur = pow2i(pex);
-        }
-        const float pinv = pow2i(-pex);
-        uint8_t* pop = pop0 + (2 * wg + bb) * C::POP;
-        float pb[8];
+        // p (unrounded, into l) and P' = bf16(p * v_scale), head pairs
+        uint32_t pw[4];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float mt = fmaxf(fmaxf(rb[g], rb[9 + g]), fmaxf(rb[18 + g], rb[27 + g]));
-          const float mn = fmaxf(m_run[g], mt);
-          a_cur[g] = ex2(m_run[g] - mn);
-          b_cur[g] = ex2(mt - mn);
-          m_run[g] = mn;
-          const float pj = ex2(sg[g] - mt);
-          l_thr[g] = l_thr[g] * a_cur[g] + pj * b_cur[g];
-          pb[g] = bf16_round(pj * vsc);
+        for (int g = 0; g < 8; g += 2) {
+          // (a warp without valid tokens has U = -inf and all scores -inf)
+          const float p0 = ex2(sg[g] - (Uh[g] > -INFINITY ? Uh[g] : 0.f));
+          const float p1 = ex2(sg[g + 1] - (Uh[g + 1] > -INFINITY ? Uh[g + 1] : 0.f));
+          l_thr[g] = l_thr[g] * f1[g] + p0 * f2[g];
+          l_thr[g + 1] = l_thr[g + 1] * f1[g + 1] + p1 * f2[g + 1];
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0 * vsc, p1 * vsc);
+          pw[g >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
         }
+        TRACE_SUB(i, 9);
+        uint8_t* pop = pop0 + (2 * wg + bb) * C::POP;
         // P^T operand, MN-major without swizzle: token t's 16 bytes (e4m3:
         // hi of heads 0..7 then lo; bf16: heads 0..7) in one 16-byte store.
         if constexpr (VE == ELEM_E4M3) {
           uint32_t hw[4], lw[4];
 #pragma unroll
-          for (int g = 0; g < 8; g += 2) {
-            const float p0 = pb[g] * pinv, p1 = pb[g + 1] * pinv;
-            const uint32_t hi = e4m3x2_rn(p0, p1);
+          for (int j = 0; j < 4; ++j) {
+            // 2^8 P' (exact), written as hi + lo e4m3
+            const float x0 = __uint_as_float(pw[j] << 16) * 256.f;
+            const float x1 = __uint_as_float(pw[j] & 0xFFFF0000u) * 256.f;
+            const uint32_t hi = e4m3x2_rn(x0, x1);
             float hv[4];
             e4m3x4_to_f32_scaled(hi, hv);
-            hw[g >> 1] = hi;
-            lw[g >> 1] = e4m3x2_rn(p0 - hv[0] * kTwoPow120, p1 - hv[1] * kTwoPow120);
+            hw[j] = hi;
+            lw[j] = e4m3x2_rn(x0 - hv[0] * kTwoPow120, x1 - hv[1] * kTwoPow120);
           }
           *reinterpret_cast<uint4*>(pop + t * 16) =
               make_uint4(hw[0] | (hw[1] << 16), hw[2] | (hw[3] << 16), lw[0] | (lw[1] << 16), lw[2] | (lw[3] << 16));
         } else {
-          uint32_t w4[4];
-#pragma unroll
-          for (int g = 0; g < 8; g += 2) {
-            const __nv_bfloat162 v2 = __floats2bfloat162_rn(pb[g], pb[g + 1]);
-            w4[g >> 1] = *reinterpret_cast<const uint32_t*>(&v2);
-          }
-          *reinterpret_cast<uint4*>(pop + (t >> 3) * 256 + (t & 7) * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          *reinterpret_cast<uint4*>(pop + (t >> 3) * 256 + (t & 7) * 16) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
+        TRACE_SUB(i, 10);
         umma::fence_proxy_async_smem();
         __syncwarp();
+        TRACE_SUB(i, 11);
         if (lane == 0) {
+          float4* da = reinterpret_cast<float4*>(ancA + ((li & 3) * 4 + sw) * 8);
+          da[0] = make_float4(Uh[0], Uh[1], Uh[2], Uh[3]);
+          da[1] = make_float4(Uh[4], Uh[5], Uh[6], Uh[7]);
           umma::mbar_arrive(&B.p_full[bb]);
           umma::mbar_arrive(&empty[s]);
         }
         if (t == 0) TRACE(8 * i + 4);
+        TRACE_SUB(i, 12);
         if (lane == 0) TRACE_MAX(8 * i + 6);
       }
-      if (li >= 1) {
-        const int lj = li - 1, bb = lj & 1, ub = lj >> 1;
-        const bool ok = wait_fast(&B.o_full[bb], ub & 1, abort_flag);
-        if (group_any(wg, !ok)) { failed = true; break; }
-        umma::fence_after_sync();
-        float ov[16];
-        {
-          uint32_t r[4][16];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) umma::tmem_ld16_nowait(tmem + o_col + 64 * bb + 16 * k + lane_off, r[k]);
-          umma::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            ov[j] = (__uint_as_float(r[0][j]) + __uint_as_float(r[1][j])) +
-                    (__uint_as_float(r[2][j]) + __uint_as_float(r[3][j]));
-        }
-        umma::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) umma::mbar_arrive(&B.o_empty[bb]);
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float ot = VE == ELEM_E4M3 ? (ov[g] + ov[g + 8]) * pf_prev : ov[g];
-          o_run[g] = o_run[g] * a_prev[g] + ot * b_prev[g];
-        }
-        if (t == 0) TRACE(8 * (2 * lj + wg) + 5);
-      }
-      if (li < nl) {
-#pragma unroll
-        for (int g = 0; g < 8; ++g) { a_prev[g] = a_cur[g]; b_prev[g] = b_cur[g]; }
-        pf_prev = pf_cur;
-      }
     }
+    // a warp that gave up left the loop early; the group's result is empty
+    // if any of its warps did
+    failed = group_any(wg, failed);
+    float m_run[8];                                 // m_o of every head
+#pragma unroll
+    for (int g = 0; g < 8; ++g) m_run[g] = __shfl_sync(0xffffffffu, m_ol, g);
     if (failed) {
       if (t == 0) raise_error(p.err, FP8KV_DEVERR_TIMEOUT);
 #pragma unroll
-      for (int g = 0; g < 8; ++g) { m_run[g] = -INFINITY; l_thr[g] = 0.f; o_run[g] = 0.f; }
+      for (int g = 0; g < 8; ++g) { m_run[g] = -INFINITY; o_run[g] = 0.f; }
     }
-    // l: per-thread partial sums -> one total per head and group
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const float ws = warp_sum(l_thr[g]);
-      if (lane == 0) lred[(wg * 4 + sw) * 8 + g] = ws;
+    // l: each warp's sums (reference m_w) by a transposed butterfly, one
+    // head per four lanes, brought to the group's m_o: lred[wg][warp][head]
+    {
+      const float ws = warp_sum_transposed<8>(l_thr, lane);           // head (lane >> 2) & 7
+      const float mo = __shfl_sync(0xffffffffu, m_ol, (lane >> 2) & 7);
+      if ((lane & 3) == 0) lred[(wg * 4 + sw) * 8 + (lane >> 2)] = failed ? 0.f : ws * pow2_diff(m_wl - mo, 0);
     }
-    group_sync(wg);
     if (t == 0 && wg == 0) TRACE(1010);
-    float l_tot[8];
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const float* lr = lred + wg * 32;
-      l_tot[g] = (lr[g] + lr[8 + g]) + (lr[16 + g] + lr[24 + g]);
-    }
     // The two groups' running states are merged like two splits: group 1
-    // hands its (m, l, O) to group 0 through shared memory.
+    // hands its m and O to group 0 through shared memory (both groups' l
+    // sums are in lred).
     if (t == 0 && wg == 1) TRACE(1000);
     if (wg == 1) {
 #pragma unroll
       for (int g = 0; g < 8; ++g) xo[g * D + t] = o_run[g];
-      if (t == 0) {
-#pragma unroll
-        for (int g = 0; g < 8; ++g) { xml[g] = m_run[g]; xml[8 + g] = l_tot[g]; }
-      }
+      if (t < 8) xml[t] = failed ? -INFINITY : m_ol;      // lane t holds m_o of head t
     }
     asm volatile("bar.sync 3, 256;\n" ::: "memory");
     if (t == 0 && wg == 0) TRACE(1011);
@@ -1003,13 +1101,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
       float Mg[8], Lg[8], Og[8];
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
-        const float m1 = xml[g], l1 = xml[8 + g];
+        const float m1 = xml[g];
         const float M = fmaxf(m_run[g], m1);
-        const float f0 = m_run[g] == -INFINITY ? 0.f : ex2(m_run[g] - M);
-        const float f1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+        const float f0 = pow2_diff(m_run[g] - M, 0), f1 = pow2_diff(m1 - M, 0);
+        const float l0 = (lred[g] + lred[8 + g]) + (lred[16 + g] + lred[24 + g]);
+        const float l1 = (lred[32 + g] + lred[40 + g]) + (lred[48 + g] + lred[56 + g]);
         Og[g] = o_run[g] * f0 + xo[g * D + t] * f1;
         Mg[g] = M;
-        Lg[g] = l_tot[g] * f0 + l1 * f1;
+        Lg[g] = l0 * f0 + l1 * f1;
       }
       if (t == 0) TRACE(1001);
       // splits with work (only the global-memory merge needs it)
@@ -1061,21 +1160,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
             // tiles are consumed and all MMAs done) with cp.async, so all the
             // L2 reads are in flight at once, then reduce from shared memory.
             float* po_sh = reinterpret_cast<float*>(smem);              // [8 heads][nb][D]
-            float* pm_sh = po_sh + 8 * 48 * D;                          // [8][48]
-            float* pl_sh = pm_sh + 8 * 48;                              // [8][48]
-            for (int k0 = 0; k0 < n_busy; k0 += 48) {
-              const int nb = min(48, n_busy - k0);
+            float* pm_sh = po_sh + 8 * kMergeChunk * D;                          // [8][kMergeChunk]
+            float* pl_sh = pm_sh + 8 * kMergeChunk;                              // [8][kMergeChunk]
+            for (int k0 = 0; k0 < n_busy; k0 += kMergeChunk) {
+              const int nb = min(kMergeChunk, n_busy - k0);
               const int chunks = G * nb * (D / 4);                      // 16-byte chunks of O
               for (int i = t; i < chunks; i += 128) {
                 const int g = i / (nb * (D / 4)), rem = i % (nb * (D / 4)), k = rem / (D / 4), c4 = rem % (D / 4);
                 const int64_t pr = ((int64_t)b * p.q_heads + (int64_t)h * G + g) * S + k0 + k;
-                cp_async16(po_sh + (g * 48 + k) * D + c4 * 4, p.part_o + pr * D + c4 * 4);
+                cp_async16(po_sh + (g * kMergeChunk + k) * D + c4 * 4, p.part_o + pr * D + c4 * 4);
               }
               if (t < G * nb) {
                 const int g = t / nb, k = t % nb;
                 const int64_t pr = ((int64_t)b * p.q_heads + (int64_t)h * G + g) * S + k0 + k;
-                pm_sh[g * 48 + k] = __ldcg(p.part_m + pr);
-                pl_sh[g * 48 + k] = __ldcg(p.part_l + pr);
+                pm_sh[g * kMergeChunk + k] = __ldcg(p.part_m + pr);
+                pl_sh[g * kMergeChunk + k] = __ldcg(p.part_l + pr);
               }
               cp_async_commit();
               cp_async_wait<0>();
@@ -1094,16 +1193,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
 #pragma unroll
                   for (int u = 0; u < 4; ++u) {
                     const bool in = g < G && u < nb;
-                    mv[g][u] = in ? pm_sh[g * 48 + u] : -INFINITY;
-                    lv[g][u] = in ? pl_sh[g * 48 + u] : 0.f;
-                    oo[g][u] = in ? po_sh[(g * 48 + u) * D + t] : 0.f;
+                    mv[g][u] = in ? pm_sh[g * kMergeChunk + u] : -INFINITY;
+                    lv[g][u] = in ? pl_sh[g * kMergeChunk + u] : 0.f;
+                    oo[g][u] = in ? po_sh[(g * kMergeChunk + u) * D + t] : 0.f;
                   }
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
                   const float M = fmaxf(fmaxf(mv[g][0], mv[g][1]), fmaxf(mv[g][2], mv[g][3]));
                   float w[4];
 #pragma unroll
-                  for (int u = 0; u < 4; ++u) w[u] = mv[g][u] == -INFINITY ? 0.f : ex2(mv[g][u] - M);
+                  for (int u = 0; u < 4; ++u) w[u] = pow2_diff(mv[g][u] - M, 0);
                   Mg[g] = M;
                   Lg[g] = (w[0] * lv[g][0] + w[1] * lv[g][1]) + (w[2] * lv[g][2] + w[3] * lv[g][3]);
                   Og[g] = (w[0] * oo[g][0] + w[1] * oo[g][1]) + (w[2] * oo[g][2] + w[3] * oo[g][3]);
@@ -1117,20 +1216,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
                   for (int k4 = 0; k4 < nb; k4 += 4) {
                     float mk[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) mk[u] = k4 + u < nb ? pm_sh[g * 48 + k4 + u] : -INFINITY;
+                    for (int u = 0; u < 4; ++u) mk[u] = k4 + u < nb ? pm_sh[g * kMergeChunk + k4 + u] : -INFINITY;
                     M = fmaxf(M, fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])));
                   }
-                  const float resc = (k0 == 0 || Mg[g] == -INFINITY) ? 0.f : ex2(Mg[g] - M);
+                  const float resc = k0 == 0 ? 0.f : pow2_diff(Mg[g] - M, 0);
                   float L = k0 == 0 ? 0.f : Lg[g] * resc, o = k0 == 0 ? 0.f : Og[g] * resc;
                   for (int k4 = 0; k4 < nb; k4 += 4) {
                     float w[4], lv[4], ovv[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                       const bool in = k4 + u < nb;
-                      const float mk = in ? pm_sh[g * 48 + k4 + u] : -INFINITY;
-                      w[u] = mk == -INFINITY ? 0.f : ex2(mk - M);
-                      lv[u] = in ? pl_sh[g * 48 + k4 + u] : 0.f;
-                      ovv[u] = in ? po_sh[(g * 48 + k4 + u) * D + t] : 0.f;
+                      const float mk = in ? pm_sh[g * kMergeChunk + k4 + u] : -INFINITY;
+                      w[u] = pow2_diff(mk - M, 0);
+                      lv[u] = in ? pl_sh[g * kMergeChunk + k4 + u] : 0.f;
+                      ovv[u] = in ? po_sh[(g * kMergeChunk + k4 + u) * D + t] : 0.f;
                     }
                     L += (w[0] * lv[0] + w[1] * lv[1]) + (w[2] * lv[2] + w[3] * lv[3]);
                     o += (w[0] * ovv[0] + w[1] * ovv[1]) + (w[2] * ovv[2] + w[3] * ovv[3]);

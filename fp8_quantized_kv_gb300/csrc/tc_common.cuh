@@ -44,11 +44,91 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
+// log2(x) by the hardware approximation (absolute error ~2^-22); -inf for 0.
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float warp_max_redux(float x) {
   float r;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(x));
   return r;
 }
+// Maxima (or sums) of N = 8 or 16 values over the 32 lanes of a warp,
+// transposed: lane L returns the maximum (sum) over all lanes of v[idx], idx
+// = (L >> (5 - log2 N)) & (N - 1).  Each butterfly step sends half of the values still held, so the
+// whole reduction takes N shuffles (16 for 16 values) instead of one
+// reduction per value.
+template <int N, bool SUM = false>
+__device__ __forceinline__ float warp_reduce_transposed(const float (&v)[N], int lane) {
+  static_assert(N == 8 || N == 16, "8 or 16 values");
+  auto op = [](float x, float y) { return SUM ? x + y : fmaxf(x, y); };
+  float a[8];
+  if constexpr (N == 16) {
+    const bool hi = lane & 16;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float send = hi ? v[j] : v[j + 8], keep = hi ? v[j + 8] : v[j];
+      a[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = v[j];
+  }
+  constexpr int S0 = N == 16 ? 8 : 16;            // lane bit of the next step
+  float b[4];
+  {
+    const bool hi = lane & S0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float send = hi ? a[j] : a[j + 4], keep = hi ? a[j + 4] : a[j];
+      b[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, S0));
+    }
+  }
+  float c[2];
+  {
+    const bool hi = lane & (S0 >> 1);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float send = hi ? b[j] : b[j + 2], keep = hi ? b[j + 2] : b[j];
+      c[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, S0 >> 1));
+    }
+  }
+  float d;
+  {
+    const bool hi = lane & (S0 >> 2);
+    const float send = hi ? c[0] : c[1], keep = hi ? c[1] : c[0];
+    d = op(keep, __shfl_xor_sync(0xffffffffu, send, S0 >> 2));
+  }
+#pragma unroll
+  for (int o = S0 >> 3; o > 0; o >>= 1) d = op(d, __shfl_xor_sync(0xffffffffu, d, o));
+  return d;
+}
+
+template <int N>
+__device__ __forceinline__ float warp_max_transposed(const float (&v)[N], int lane) {
+  return warp_reduce_transposed<N, false>(v, lane);
+}
+template <int N>
+__device__ __forceinline__ float warp_sum_transposed(const float (&v)[N], int lane) {
+  return warp_reduce_transposed<N, true>(v, lane);
+}
+
+// 2^e for an integer e <= 127, with results below 2^-126 flushed to zero
+// (built from the bits: e + 127 <= 0 gives the pattern of +0).
+__device__ __forceinline__ float pow2_ftz(int e) { return __int_as_float(max(e + 127, 0) << 23); }
+
+// 2^(d + e) for an integer-valued d <= 0 (a difference of two anchors, or
+// -inf / NaN when an anchor is missing) and a small integer e <= 111; results
+// below 2^-126 (d = -inf, NaN included) give 0.  Floating-point and integer
+// pipes only: d + e + 127 + 2^23 puts the biased exponent in the low
+// mantissa bits, which then move to the exponent field.
+__device__ __forceinline__ float pow2_diff(float d, int e) {
+  const float x = fmaxf(d + (float)e, -127.f) + 8388735.f;    // 2^23 + 127
+  return __int_as_float((__float_as_int(x) & 0xFF) << 23);
+}
+
 // Exponent e with amax * 2^-e <= 448 (e = 0 for amax = 0).
 __device__ __forceinline__ int e4m3_row_exp(float amax) {
   int e = 0;

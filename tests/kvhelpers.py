@@ -102,3 +102,22 @@ def assert_gate(out, ref, what, rel_l2=1e-2, max_abs=2e-2):
     ok, rel, mab = oracle.attention_gate(out, ref, rel_l2, max_abs)
     assert ok, f"{what}: worst rel-L2 {rel:.3e}, worst max-abs {mab:.3e}"
     return rel, mab
+
+
+def split_last_token(inp: synth.DecodeInputs):
+    """The workload minus each sequence's last token, and those tokens."""
+    lens = inp.seq_lens.to(torch.int64)
+    last = (inp.cu_seqlens[1:] - 1).clamp(min=0)
+    keep = torch.ones(int(inp.cu_seqlens[-1]), dtype=torch.bool)
+    has = lens > 0
+    keep[last[has]] = False
+    prev = synth.DecodeInputs(inp.spec, inp.q, inp.k[keep.to(inp.k.device)], inp.v[keep.to(inp.v.device)],
+                              (inp.seq_lens - has.to(torch.int32)).to(torch.int32),
+                              torch.cat([torch.zeros(1, dtype=torch.int64), torch.cumsum(lens - has.to(torch.int64), 0)]),
+                              inp.page_table, inp.num_pages)
+    B, Hkv, D = len(lens), inp.spec.kv_heads, inp.spec.head_dim
+    knew = torch.zeros(B, Hkv, D, dtype=torch.bfloat16, device=inp.k.device)
+    vnew = torch.zeros_like(knew)
+    knew[has.to(knew.device)] = inp.k[last[has].to(inp.k.device)]
+    vnew[has.to(vnew.device)] = inp.v[last[has].to(inp.v.device)]
+    return prev, knew, vnew

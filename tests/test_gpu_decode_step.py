@@ -9,7 +9,7 @@ import torch
 import oracle
 from fp8_quantized_kv_gb300 import synth
 import fp8_quantized_kv_gb300 as fk
-from kvhelpers import assert_gate, fill_cache, oracle_decode
+from kvhelpers import assert_gate, fill_cache, oracle_decode, split_last_token as _split_last_token
 
 pytestmark = pytest.mark.gpu
 DTYPES = ["k8v8", "k16v8", "k16v16", "k8v16"]
@@ -19,25 +19,6 @@ DTYPES = ["k8v8", "k16v8", "k16v16", "k8v16"]
 def _clear_device_error():
     fk.fp8kv_get_device_error(clear=True)
     yield
-
-
-def _split_last_token(inp):
-    """The workload minus each sequence's last token, and those tokens."""
-    lens = inp.seq_lens.to(torch.int64)
-    last = (inp.cu_seqlens[1:] - 1).clamp(min=0)
-    keep = torch.ones(int(inp.cu_seqlens[-1]), dtype=torch.bool)
-    has = lens > 0
-    keep[last[has]] = False
-    prev = synth.DecodeInputs(inp.spec, inp.q, inp.k[keep.to(inp.k.device)], inp.v[keep.to(inp.v.device)],
-                              (inp.seq_lens - has.to(torch.int32)).to(torch.int32),
-                              torch.cat([torch.zeros(1, dtype=torch.int64), torch.cumsum(lens - has.to(torch.int64), 0)]),
-                              inp.page_table, inp.num_pages)
-    B, Hkv, D = len(lens), inp.spec.kv_heads, inp.spec.head_dim
-    knew = torch.zeros(B, Hkv, D, dtype=torch.bfloat16, device=inp.k.device)
-    vnew = torch.zeros_like(knew)
-    knew[has.to(knew.device)] = inp.k[last[has].to(inp.k.device)]
-    vnew[has.to(vnew.device)] = inp.v[last[has].to(inp.v.device)]
-    return prev, knew, vnew
 
 
 def _run(inp, dtype, kernel, num_splits=0, capacity=None):

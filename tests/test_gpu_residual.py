@@ -84,7 +84,7 @@ def test_residual_is_closer_to_bf16_than_plain_fp8():
 
 
 def test_fused_step_appends_residual_row():
-    from test_gpu_decode_step import _split_last_token
+    from kvhelpers import split_last_token as _split_last_token
     spec = synth.DecodeWorkload("res_step", 8, 16, 2, 128, seed=2, seq_lens=(4096,) * 8, hostile_keys=True)
     inp = synth.decode_inputs(spec, device="cuda")
     b = _bias(2, 128, 4)
