@@ -15,21 +15,26 @@
 //   per row (one thread each, whole row thread-local): s = S * k_scale *
 //     sm_scale, causal mask (diagonal tiles only), running max with lazy
 //     rescale, p = 2^(s - m), l += p, P' = p * v_scale
-//   O^T[128 x 128] += V^T . P'^T         tcgen05.mma kind::f16 -> TMEM
+//   O[128 x 128]  += P' . V                kind::f16 -> TMEM (lane = query row)
 // Two softmax warpgroups take alternate KV tiles (even, odd), each with its
 // own running (m, l) and its own O accumulator, so the softmax of two tiles
 // runs at once; the two states are combined per row in the epilogue, as two
-// flash-decoding splits are.
+// flash-decoding splits are.  The warps of a group share no barrier inside
+// the loop: each query row is one thread and one TMEM lane, so every
+// decision (the lazy rescale, a wait that gave up) is a warp vote.
 // QK runs on the e4m3 K tile as it lands in shared memory ("FP8 KV
 // attention: hardware paths and tile preparation", section "Use a native
 // narrow QK path": no K preparation), with each bf16 query row, after a
 // power-of-two scaling that puts its largest magnitude at most 448, written
 // as two e4m3 terms (hi = e4m3(x), lo = e4m3(x - hi)).  P.V is kind::f16:
-// the e4m3 V codes convert to f16 exactly (cvt.rn.f16x2.e4m3x2).  P' is rounded once, to the 16-bit operand of the
-// P.V product, as f16 (11-bit significand, 8x finer than bf16; the page's own
-// prefill keeps its probabilities in f16, section 2.4) after one power-of-two
-// scaling per CTA chosen from the largest V scale it will see.  All those
-// scalings are undone in fp32.
+// the e4m3 V codes convert to f16 exactly (cvt.rn.f16x2.e4m3x2).  P' is
+// rounded once, to the 16-bit operand of the P.V product, as f16 (11-bit
+// significand, 8x finer than bf16; the page's own prefill keeps its
+// probabilities in f16, section 2.4) after a power-of-two scaling 2^-kp of
+// the row: kp follows the largest V scale of the tiles the row has seen (it
+// is only ever raised, and O is rescaled with it), so P' stays inside f16's
+// range, and it folds into the exponential's argument.  All those scalings
+// are undone in fp32.  The per-element fp32 arithmetic runs two-wide.
 //
 // Warp roles:
 //   warp 0      TMA producer: e4m3 code tiles (64 keys x 128 B, 128-byte
@@ -39,14 +44,15 @@
 //               own operands.
 //   warps 2-5   softmax of the even tiles, warps 6-9 of the odd tiles (one
 //               query row per thread); then the output epilogue.
-//   warps 10-13 preparation: V codes -> f16 operand tiles (MN-major), per-key
-//               scales; V rows past the causal end zeroed (0 * NaN would
-//               poison P.V).
+//   warps 10-13 preparation, warp 10 + w of tiles w, w + 4, ...: V codes ->
+//               f16 operand tiles (MN-major), per-key scales and the tile's
+//               largest V scale; V rows past the causal end zeroed (0 * NaN
+//               would poison P.V).
 //   warp 15     idle.
-// TMEM: S of each group double-buffered (4 x 64 columns), one O^T per group
+// TMEM: S of each group double-buffered (4 x 64 columns), one O per group
 // (2 x 128).  O is rescaled in TMEM only when a row's maximum grows by more
-// than 2^8 (then P stays <= 2^8 relative to the stale maximum).  Every wait is
-// bounded; a timeout raises FP8KV_DEVERR_TIMEOUT.
+// than 2^8 (then P stays <= 2^8 relative to the stale maximum) or its kp
+// rises.  Every wait is bounded; a timeout raises FP8KV_DEVERR_TIMEOUT.
 #include "params.cuh"
 #include "tc_common.cuh"
 
@@ -65,7 +71,8 @@ struct PfTcCfg {
   static constexpr int NOP = 4;                                // f16 V operand buffers
   static constexpr int OPT = kPfKeys * D * 2;                 // f16 V tile [2 atoms][64][128 B]
   static constexpr int POP = kPfRows * kPfKeys * 2;           // f16 P [128 rows][128 B], one per group
-  static constexpr int COLS = 2 * kPfKeys * 4;                 // per buffer: k and v column scales
+  static constexpr int CST = 2 * kPfKeys + 4;                   // floats per buffer: k, v column scales, v max
+  static constexpr int COLS = CST * 4;
   static constexpr int MISC = 4096;
   static constexpr int BYTES = QOP + NS * STAGE + NOP * OPT + 2 * POP + NOP * COLS + MISC + 1024;
   static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
@@ -118,7 +125,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   uint8_t* vf = ring + C::NS * C::STAGE;          // [NOP] f16 V operand
   uint8_t* pop = vf + C::NOP * C::OPT;            // [group] f16 P operand
   float* cols = reinterpret_cast<float*>(pop + 2 * C::POP);   // [NOP][k 64 | v 64]
-  uint8_t* misc = reinterpret_cast<uint8_t*>(cols + C::NOP * 2 * kPfKeys);
+  uint8_t* misc = reinterpret_cast<uint8_t*>(cols + C::NOP * C::CST);
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);        // [NS] codes landed
   uint64_t* empty = full + C::NS;                             // [NS] K read by QK, V converted by the prep warps
   uint64_t* op_full = empty + C::NS;                          // [NOP] f16 V operand + scales ready
@@ -130,11 +137,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   uint64_t* drained = pv_done + 2;                            // [2] final commits of the two MMA issuers
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drained + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
-  int* kp_sh = const_cast<int*>(abort_flag) + 1;
-  float* alpha_sh = reinterpret_cast<float*>(misc + 256);     // [group][128]
   float* m_sh = reinterpret_cast<float*>(misc + 1280);        // [group][128] final reference maxima
   float* l_sh = reinterpret_cast<float*>(misc + 2304);        // [group][128] final row sums
-  float* vmax_sh = reinterpret_cast<float*>(misc + 3328);     // [4]
+  int* kp_sh = reinterpret_cast<int*>(misc + 256);           // [group][128] final P' exponents
 
   // grid (query head, sequence, query tile), the tile index slowest and
   // reversed: the CTAs with the longest causal ranges launch first
@@ -198,13 +203,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   if (tid == 0) {
     for (int i = 0; i < C::NS; ++i) {
       umma::mbar_init(&full[i], 1);
-      umma::mbar_init(&empty[i], 1 + 4);       // QK commit + the four prep warps
+      umma::mbar_init(&empty[i], 1 + 1);       // QK commit + the prep warp of the tile
     }
     *abort_flag = 0;
     umma::mbar_fence_init();
     for (int j = 0; j < n_first; ++j) produce(j);
     for (int i = 0; i < C::NOP; ++i) {
-      umma::mbar_init(&op_full[i], 4);
+      umma::mbar_init(&op_full[i], 1);
       umma::mbar_init(&op_free[i], 1);
     }
     for (int i = 0; i < 4; ++i) {
@@ -274,38 +279,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
       *reinterpret_cast<uint4*>(qop + kPfRows * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
   }
-  // prep warps: one power of two for all of this CTA's P (from the largest
-  // V scale of its keys), so P' stays inside f16's range
-  if (warp >= 10 && warp < 14) {
-    const int pt = tid - 320;
-    float vm = 0.f;
-    for (int base = 0; base < kv_end; base += 8 * 128) {   // 8 independent loads in flight
-      float v8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int key = base + 128 * u + pt;
-        const int64_t row = key < kv_end ? cache_row(c, b, hk, key, nullptr) : -1;
-        v8[u] = row >= 0 ? c.v_scale[row] : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) vm = fmaxf(vm, v8[u]);
-    }
-    vm = warp_max_redux(vm);
-    if (lane == 0) vmax_sh[warp - 10] = vm;
-    asm volatile("bar.sync 4, 128;\n" ::: "memory");
-    if (pt == 0) {
-      const float v = fmaxf(fmaxf(vmax_sh[0], vmax_sh[1]), fmaxf(vmax_sh[2], vmax_sh[3]));
-      int e = 0;
-      (void)frexpf(v * (1.0f / 128.0f), &e);        // vmax * 2^-e < 128
-      *kp_sh = max(-100, min(100, e));
-    }
-  }
   umma::fence_proxy_async_smem();
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
   const uint32_t tmem = *tslot;
-  const int kp = *kp_sh;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -353,7 +331,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   } else if (warp == 14) {
     // ------------------------------------------------------------ PV issuer
     if (lane == 0) {
-      constexpr uint32_t ID_PV = umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_MN, umma::MAJOR_K, 128, 128);
+      constexpr uint32_t ID_PV = umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_K, umma::MAJOR_MN, 128, 128);
       for (int j = 0; j < nkv; ++j) {
         const int w = j & 1, lj = j >> 1, ob = j % C::NOP, ou = j / C::NOP;
         if (!wait_fast(&p_full[w], lj & 1, abort_flag)) break;
@@ -364,8 +342,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
         const uint32_t pa = umma::smem_u32(pop + w * C::POP);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_f16_ss(tmem + 256 + 128 * w, umma::sdesc(va + kk * 2048, kPfKeys * 128, 1024, umma::SWIZZLE_128B),
-                           umma::sdesc(pa + kk * 32, 16, 1024, umma::SWIZZLE_128B), ID_PV,
+          umma::mma_f16_ss(tmem + 256 + 128 * w, umma::sdesc(pa + kk * 32, 16, 1024, umma::SWIZZLE_128B),
+                           umma::sdesc(va + kk * 2048, kPfKeys * 128, 1024, umma::SWIZZLE_128B), ID_PV,
                            (lj > 0 || kk > 0) ? 1u : 0u);
         umma::mma_commit(&pv_done[w]);
         umma::mma_commit(&op_free[ob]);
@@ -381,19 +359,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
     const int qpos_min = pos0 + i0;                 // smallest position among this CTA's queries
     const int my_tiles = (nkv - wg + 1) >> 1;       // tiles j = 2 lj + wg < nkv
     const uint32_t s_base = tmem + 64 * (2 * wg), o_base = tmem + 256 + 128 * wg;
-    float* my_alpha = alpha_sh + wg * kPfRows;
     uint8_t* my_p = pop + wg * C::POP;
     float m_used = -INFINITY, l = 0.f;
+    int kp_row = -1000;                             // this row's P' exponent (none yet)
     bool failed = false;
     for (int lj = 0; lj < my_tiles; ++lj) {
       const int j = 2 * lj + wg, bb = lj & 1, ub = lj >> 1, ob = j % C::NOP;
       bool ok = wait_fast(&s_full[2 * wg + bb], ub & 1, abort_flag);
       ok = ok && wait_fast(&op_full[ob], (j / C::NOP) & 1, abort_flag);
       ok = ok && !*abort_flag;
-      if (group_any(wg, !ok)) { failed = true; break; }
+      if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       umma::fence_after_sync();
       if (r == 0) PF_TRACE(8 * j + 4);
-      float sv[64];
+      // the row's 64 scores as pairs (packed two-wide fp32 arithmetic below)
+      float2 sv[32];
       {
         uint32_t rr[4][16];
 #pragma unroll
@@ -402,32 +381,34 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
-          for (int u = 0; u < 16; ++u) sv[16 * k + u] = __uint_as_float(rr[k][u]);
+          for (int u = 0; u < 8; ++u) sv[8 * k + u] = make_float2(__uint_as_float(rr[k][2 * u]), __uint_as_float(rr[k][2 * u + 1]));
       }
       umma::fence_before_sync();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&s_free[2 * wg + bb]);
       // t = S * k_scale * sm_scale * log2(e); the row's 2^kq comes in below
-      const float4* kc4 = reinterpret_cast<const float4*>(cols + ob * 2 * kPfKeys);
+      const float4* kc4 = reinterpret_cast<const float4*>(cols + ob * C::CST);
       const float4* vc4 = kc4 + kPfKeys / 4;
+      const float vmt = cols[ob * C::CST + 2 * kPfKeys];   // largest V scale of the tile
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 kc = kc4[c4];
-        sv[4 * c4 + 0] *= kc.x;
-        sv[4 * c4 + 1] *= kc.y;
-        sv[4 * c4 + 2] *= kc.z;
-        sv[4 * c4 + 3] *= kc.w;
+        sv[2 * c4] = __fmul2_rn(sv[2 * c4], make_float2(kc.x, kc.y));
+        sv[2 * c4 + 1] = __fmul2_rn(sv[2 * c4 + 1], make_float2(kc.z, kc.w));
       }
       const int t0 = j * kPfKeys;
       if (t0 + kPfKeys - 1 > qpos_min) {             // causal edge: keys past this row's position drop out
 #pragma unroll
-        for (int cc = 0; cc < 64; ++cc) sv[cc] = t0 + cc <= qpos ? sv[cc] : -INFINITY;
+        for (int cc = 0; cc < 32; ++cc) {
+          sv[cc].x = t0 + 2 * cc <= qpos ? sv[cc].x : -INFINITY;
+          sv[cc].y = t0 + 2 * cc + 1 <= qpos ? sv[cc].y : -INFINITY;
+        }
       }
       float m8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) m8[k] = fmaxf(fmaxf(sv[k], sv[k + 8]), fmaxf(sv[k + 16], sv[k + 24]));
-#pragma unroll
-      for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], fmaxf(fmaxf(sv[k + 32], sv[k + 40]), fmaxf(sv[k + 48], sv[k + 56])));
+      for (int k = 0; k < 8; ++k)
+        m8[k] = fmaxf(fmaxf(fmaxf(sv[k].x, sv[k].y), fmaxf(sv[k + 8].x, sv[k + 8].y)),
+                      fmaxf(fmaxf(sv[k + 16].x, sv[k + 16].y), fmaxf(sv[k + 24].x, sv[k + 24].y)));
       const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * qsr;
       // lazy rescale: move the row's reference maximum only when it grows by
       // more than 2^8 (or on the first tile with a valid key)
@@ -436,42 +417,56 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
         alpha = m_used == -INFINITY ? 0.f : ex2(m_used - mt);
         m_used = mt;
       }
-      const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-      float l4[4] = {0.f, 0.f, 0.f, 0.f};
+      // P' = p * v_scale * 2^-kp_row with p <= 2^8: kp_row (this row's, only
+      // ever raised, O rescaled with it) keeps P' below 2^15, inside f16
+      float alpha_o = alpha;                        // O's factor: the max move and the exponent move
+      if (vmt > 0.f) {
+        const int need = max(-100, min(120, ((__float_as_int(vmt) >> 23) & 0xFF) - 127 - 6));   // vmt 2^-need < 128
+        if (need > kp_row) {
+          if (kp_row > -1000) alpha_o *= pow2_diff((float)(kp_row - need), 0);
+          kp_row = need;
+        }
+      }
+      const int kpr = kp_row > -1000 ? kp_row : 0;
+      const float neg_m = (m_used == -INFINITY ? 0.f : -m_used) - (float)kpr;
+      const float2 qsr2 = make_float2(qsr, qsr), nm2 = make_float2(neg_m, neg_m);
+      float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
       uint32_t ph[32];
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 vc = vc4[c4];
-        const float p0 = ex2_ftz(fmaf(sv[4 * c4 + 0], qsr, neg_m));
-        const float p1 = ex2_ftz(fmaf(sv[4 * c4 + 1], qsr, neg_m));
-        const float p2 = ex2_ftz(fmaf(sv[4 * c4 + 2], qsr, neg_m));
-        const float p3 = ex2_ftz(fmaf(sv[4 * c4 + 3], qsr, neg_m));
-        l4[0] += p0;
-        l4[1] += p1;
-        l4[2] += p2;
-        l4[3] += p3;
-        // P' = p * v_scale * 2^-kp, rounded once to the f16 operand
-        const __half2 h01 = __floats2half2_rn(p0 * vc.x, p1 * vc.y);
-        const __half2 h23 = __floats2half2_rn(p2 * vc.z, p3 * vc.w);
+        const float2 a01 = __ffma2_rn(sv[2 * c4], qsr2, nm2), a23 = __ffma2_rn(sv[2 * c4 + 1], qsr2, nm2);
+        const float2 p01 = make_float2(ex2_ftz(a01.x), ex2_ftz(a01.y));
+        const float2 p23 = make_float2(ex2_ftz(a23.x), ex2_ftz(a23.y));
+        la = __fadd2_rn(la, p01);
+        lb = __fadd2_rn(lb, p23);
+        // (p here is p * 2^-kp_row) P' = p * v_scale * 2^-kp_row, rounded
+        // once to the f16 operand
+        const float2 q01 = __fmul2_rn(p01, make_float2(vc.x, vc.y)), q23 = __fmul2_rn(p23, make_float2(vc.z, vc.w));
+        const __half2 h01 = __floats2half2_rn(q01.x, q01.y);
+        const __half2 h23 = __floats2half2_rn(q23.x, q23.y);
         ph[2 * c4] = *reinterpret_cast<const uint32_t*>(&h01);
         ph[2 * c4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
       }
-      l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+      const float l4[4] = {la.x, la.y, lb.x, lb.y};
+      l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3])) * pow2i(kpr);
       // this group's previous P.V (tile j-2) must be done before its O is
       // rescaled and before its P buffer is overwritten
-      if (lj > 0 && !wait_fast(&pv_done[wg], (lj - 1) & 1, abort_flag)) { /* caught at the next tile */ }
-      if (group_any(wg, alpha != 1.f && lj > 0)) {
-        // O^T columns of rows whose reference moved are rescaled in TMEM
-        my_alpha[r] = alpha;
-        group_sync(wg);
+      if (lj > 0) {
+        const bool done = wait_fast(&pv_done[wg], (lj - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, done)) { failed = true; break; }
+      }
+      if (__any_sync(0xffffffffu, alpha_o != 1.f && lj > 0)) {
+        // O rows whose reference moved are rescaled in TMEM: lane = query
+        // row, so each thread scales its own row (alpha 1 elsewhere in the warp)
         umma::fence_after_sync();
 #pragma unroll 1
-        for (int k = 0; k < 8; ++k) {             // 8 chunks of 16 columns (query rows)
+        for (int k = 0; k < 8; ++k) {             // 8 chunks of 16 columns (head dims)
           uint32_t rr[16];
           umma::tmem_ld16_nowait(o_base + 16 * k + lane_off, rr);
           umma::tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < 16; ++u) rr[u] = __float_as_uint(__uint_as_float(rr[u]) * my_alpha[16 * k + u]);
+          for (int u = 0; u < 16; ++u) rr[u] = __float_as_uint(__uint_as_float(rr[u]) * alpha_o);
           asm volatile(
               "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
               "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(o_base + 16 * k + lane_off),
@@ -479,7 +474,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
               "r"(rr[8]), "r"(rr[9]), "r"(rr[10]), "r"(rr[11]), "r"(rr[12]), "r"(rr[13]), "r"(rr[14]), "r"(rr[15]));
         }
         asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-        group_sync(wg);                             // my_alpha reused next tile
       }
       uint8_t* prow = my_p + r * 128;
 #pragma unroll
@@ -493,6 +487,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
       if (r == 0) PF_TRACE(8 * j + 5);
     }
     m_sh[wg * kPfRows + r] = failed ? -INFINITY : m_used;
+    kp_sh[wg * kPfRows + r] = kp_row > -1000 ? kp_row : 0;
     l_sh[wg * kPfRows + r] = failed ? 0.f : l;
     // ------------------------------------------------------------ epilogue
     // both groups' states are visible after this barrier; a failure in
@@ -506,85 +501,121 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
       any_fail = pair_any(!ok);
     }
     if (!any_fail) {
+      // lane = query row r: combine the two groups' O rows (one flash-decoding
+      // style merge per row); group wg writes head dims 64 wg .. 64 wg + 63
       umma::fence_after_sync();
-      const int d = r;                              // O^T lane = head dim
-      const float ofac = pow2i(kp);
+      const float ma = m_sh[r], mb = m_sh[kPfRows + r];
+      const float M = fmaxf(ma, mb);
+      const float fa = (n0 == 0 || ma == -INFINITY) ? 0.f : ex2(ma - M);
+      const float fb = (n1 == 0 || mb == -INFINITY) ? 0.f : ex2(mb - M);
+      const float L = l_sh[r] * fa + l_sh[kPfRows + r] * fb;
+      const float ofac = L > 0.f ? 1.f / L : 0.f;
+      // each group's O holds P' = p * v_scale * 2^-kp of its own row exponent
+      const float fa_o = fa * pow2i(kp_sh[r]), fb_o = fb * pow2i(kp_sh[kPfRows + r]);
+      const int64_t ob0 = (((int64_t)b * p.n_q + (qi < p.n_q ? qi : 0)) * p.q_heads + hq) * D + 64 * wg;
 #pragma unroll 1
-      for (int k = 4 * wg; k < 4 * wg + 4; ++k) {   // this group writes 64 of the 128 query rows
+      for (int k = 4 * wg; k < 4 * wg + 4; ++k) {   // 16 head dims per chunk
         uint32_t r0[16], r1[16];
         if (n0 > 0) umma::tmem_ld16_nowait(tmem + 256 + 16 * k + lane_off, r0);
         if (n1 > 0) umma::tmem_ld16_nowait(tmem + 384 + 16 * k + lane_off, r1);
         umma::tmem_wait_ld();
+        float o[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const int row = 16 * k + u, qrow = i0 + row;
-          if (qrow < p.n_q) {
-            const float ma = m_sh[row], mb = m_sh[kPfRows + row];
-            const float M = fmaxf(ma, mb);
-            const float fa = ma == -INFINITY ? 0.f : ex2(ma - M);
-            const float fb = mb == -INFINITY ? 0.f : ex2(mb - M);
-            const float L = l_sh[row] * fa + l_sh[kPfRows + row] * fb;
-            float o = 0.f;
-            if (n0 > 0 && fa != 0.f) o += __uint_as_float(r0[u]) * fa;
-            if (n1 > 0 && fb != 0.f) o += __uint_as_float(r1[u]) * fb;
-            o = L > 0.f ? o * ofac / L : 0.f;
-            const int64_t oi = (((int64_t)b * p.n_q + qrow) * p.q_heads + hq) * D + d;
-            if (p.out_f32) reinterpret_cast<float*>(p.out)[oi] = o;
-            else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+          float x = 0.f;
+          if (n0 > 0 && fa != 0.f) x += __uint_as_float(r0[u]) * fa_o;
+          if (n1 > 0 && fb != 0.f) x += __uint_as_float(r1[u]) * fb_o;
+          o[u] = x * ofac;
+        }
+        const int64_t oi = ob0 + 16 * (k - 4 * wg);
+        if (qi >= p.n_q) continue;                  // (the TMEM loads above are warp-wide)
+        if ((reinterpret_cast<uintptr_t>(p.out) & 15) != 0) {   // caller's buffer not 16-byte aligned
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            if (p.out_f32) reinterpret_cast<float*>(p.out)[oi + u] = o[u];
+            else reinterpret_cast<__nv_bfloat16*>(p.out)[oi + u] = __float2bfloat16_rn(o[u]);
           }
+        } else if (p.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) dst[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+        } else {
+          uint32_t w8[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * u], o[2 * u + 1]);
+            w8[u] = *reinterpret_cast<const uint32_t*>(&v2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi);
+          dst[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+          dst[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
         }
       }
     }
     if (any_fail && r == 0 && wg == 0) raise_error(p.err, FP8KV_DEVERR_TIMEOUT);
   } else if (warp >= 10 && warp < 14) {
     // --------------------------------------------------------- preparation
-    const int pt = tid - 320;
-    const int kr = pt >> 1, hh = pt & 1;          // key row of the tile, half of the head dim
-    const float vfac = pow2i(-kp);                // keeps p * v_scale inside f16's range
+    // Warp 10 + w prepares tiles j = w, w + 4, ... (f16 operand buffer w):
+    // four tiles in flight, no barrier between the warps.
+    static_assert(C::NOP == 4, "one operand buffer per preparation warp");
+    const int pw = warp - 10;
     bool failed = false;
-    for (int j = 0; j < nkv && !failed; ++j) {
+    for (int j = pw; j < nkv && !failed; j += 4) {
       const int s = j % C::NS, u = j / C::NS, ob = j % C::NOP, ou = j / C::NOP;
       bool ok = wait_fast(&full[s], u & 1, abort_flag);
       if (ou > 0) ok = ok && wait_fast(&op_free[ob], (ou - 1) & 1, abort_flag);
-      if (group_any(3, !ok)) { failed = true; break; }
+      if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       const uint8_t* st = ring + s * C::STAGE;
+      const uint8_t* codes = st + C::CODES;
       const float* kss = reinterpret_cast<const float*>(st + 2 * C::CODES);
       const float* vss = kss + kPfKeys;
       const int t0 = j * kPfKeys;
-      const bool key_ok = t0 + kr < kv_end;
-      {
-        const uint8_t* codes = st + C::CODES + kr * 128;
-        uint8_t* dst = vf + ob * C::OPT + hh * (kPfKeys * 128) + kr * 128;
+      uint8_t* dstb = vf + ob * C::OPT;
+      // 64 key rows x 8 chunks of 16 codes: lane takes chunk ch = lane & 7 of
+      // rows 4 it + lane / 8; all of a batch's loads before its stores (the
+      // compiler cannot move a load above a store to shared memory)
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {           // 16 codes -> two 16-byte f16 chunks
-          const int ch = 4 * hh + cc;
-          uint4 w = *reinterpret_cast<const uint4*>(codes + ((ch ^ (kr & 7)) << 4));
+      for (int half = 0; half < 2; ++half) {
+        uint4 w[8];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int kr = 4 * (8 * half + it) + (lane >> 3), ch = lane & 7;
+          w[it] = *reinterpret_cast<const uint4*>(codes + kr * 128 + ((ch ^ (kr & 7)) << 4));
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int kr = 4 * (8 * half + it) + (lane >> 3), ch = lane & 7;
+          const bool key_ok = t0 + kr < kv_end;
           uint32_t h[8];
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          const uint32_t ww[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
 #pragma unroll
           for (int u4 = 0; u4 < 4; ++u4) {
-            h[2 * u4] = e4m3x2_to_f16x2((uint16_t)(ww[u4] & 0xFFFF));
-            h[2 * u4 + 1] = e4m3x2_to_f16x2((uint16_t)(ww[u4] >> 16));
+            h[2 * u4] = key_ok ? e4m3x2_to_f16x2((uint16_t)(ww[u4] & 0xFFFF)) : 0u;
+            h[2 * u4 + 1] = key_ok ? e4m3x2_to_f16x2((uint16_t)(ww[u4] >> 16)) : 0u;
           }
-          if (!key_ok) {
-#pragma unroll
-            for (int u8 = 0; u8 < 8; ++u8) h[u8] = 0u;
-          }
-          const int c0 = 2 * cc, c1 = 2 * cc + 1;   // f16 chunk indices within the 128-byte atom row
+          // dims 16 ch .. 16 ch + 15: atom ch / 4, f16 chunks 2 (ch % 4) and +1
+          uint8_t* dst = dstb + (ch >> 2) * (kPfKeys * 128) + kr * 128;
+          const int c0 = 2 * (ch & 3), c1 = c0 + 1;
           *reinterpret_cast<uint4*>(dst + ((c0 ^ (kr & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
           *reinterpret_cast<uint4*>(dst + ((c1 ^ (kr & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
         }
       }
-      if (pt < kPfKeys) {
-        float* cc2 = cols + ob * 2 * kPfKeys;
-        const bool ok2 = t0 + pt < kv_end;
-        cc2[pt] = ok2 ? kss[pt] * p.scale_log2 : 0.f;
-        cc2[kPfKeys + pt] = ok2 ? vss[pt] * vfac : 0.f;
+      {
+        const float k0 = kss[lane], k1 = kss[lane + 32], v0 = vss[lane], v1 = vss[lane + 32];
+        float* cc2 = cols + ob * C::CST;
+        const bool ok0 = t0 + lane < kv_end, ok1 = t0 + lane + 32 < kv_end;
+        const float va = ok0 ? v0 : 0.f, vb = ok1 ? v1 : 0.f;
+        cc2[lane] = ok0 ? k0 * p.scale_log2 : 0.f;
+        cc2[lane + 32] = ok1 ? k1 * p.scale_log2 : 0.f;
+        cc2[kPfKeys + lane] = va;
+        cc2[kPfKeys + lane + 32] = vb;
+        const float vm = warp_max(fmaxf(va, vb));
+        if (lane == 0) cc2[2 * kPfKeys] = vm;     // the tile's largest V scale
       }
       umma::fence_proxy_async_smem();
       __syncwarp();
-      if (pt == 0) PF_TRACE(8 * j + 3);
       if (lane == 0) {
+        PF_TRACE(8 * j + 3);
         umma::mbar_arrive(&op_full[ob]);
         umma::mbar_arrive(&empty[s]);
       }

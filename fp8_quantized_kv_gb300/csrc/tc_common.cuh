@@ -159,6 +159,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 // As wait_or_abort, but each poll resumes as soon as the phase completes
 // (no suspend-time hint): for hand-offs on the critical path of a pipeline.
 __device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (umma::mbar_test(bar, parity)) return true;         // completed: no blocking poll
   if (umma::mbar_try_wake(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {

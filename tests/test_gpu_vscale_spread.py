@@ -151,3 +151,47 @@ def test_dominance_case_is_what_it_claims():
     first = norms[:, ::G]
     others = np.delete(norms, np.arange(0, 16, G), axis=1)
     assert first.max() < 2.0 ** -10 * np.median(others)
+
+
+def _prefill_dominance(small_exp, n_q=300, pos0=20):
+    """Causal prefill with, in every 64-key tile, one key that is a multiple
+    of a query row's query (loud score for that row) and whose V row is
+    2^small_exp times its N(0,1) neighbours'.  (Outputs stay O(1), the scale
+    the absolute max-abs bar assumes.)"""
+    Hq, Hkv, D = 4, 1, 128
+    spec = synth.PrefillWorkload("pf_dominance", n_q, Hq, Hkv, D, seed=91, pos0=pos0)
+    pin = synth.prefill_inputs(spec, device="cpu")
+    k = pin.k.float().clone()
+    v = pin.v.float().clone()
+    g = torch.Generator().manual_seed(11)
+    total = pos0 + n_q
+    for t0 in range(0, total, 64):
+        j = t0 + int(torch.randint(0, min(64, total - t0), (1,), generator=g))
+        qi = max(j - pos0, 0)                  # a query row that sees key j
+        k[j, 0] = 4.0 * pin.q[min(qi, n_q - 1), 0].float()
+        v[j, 0] *= 2.0 ** small_exp
+    return pin.q, k.to(torch.bfloat16), v.to(torch.bfloat16), pos0
+
+
+@pytest.mark.gpu
+@pytest.mark.usefixtures("_clear_device_error")
+@pytest.mark.parametrize("small_exp", [-14, -20])
+@pytest.mark.parametrize("kernel", ["tensor_cores", "cuda_cores"])
+def test_prefill_dominance(small_exp, kernel):
+    import math
+    import oracle
+    q, k, v, pos0 = _prefill_dominance(small_exp)
+    n_q, Hq, D = q.shape
+    total = pos0 + n_q
+    cache = fk.Fp8KVCache.contiguous(1, 1, D, ((total + 63) // 64) * 64, "k8v8")
+    fk.fp8kv_append(cache, k.cuda().contiguous(), v.cuda().contiguous(),
+                    torch.zeros(total, dtype=torch.int32, device="cuda"),
+                    torch.arange(total, dtype=torch.int32, device="cuda"))
+    out = fk.fp8kv_prefill_attention(q[None].cuda().contiguous(), cache,
+                                     torch.tensor([pos0], dtype=torch.int32, device="cuda"),
+                                     out_dtype=torch.float32, kernel=kernel)[0].cpu().numpy()
+    kk = oracle.dequantize(*oracle.quantize(synth.bf16_bits(k).transpose(1, 0, 2)))
+    vv = oracle.dequantize(*oracle.quantize(synth.bf16_bits(v).transpose(1, 0, 2)))
+    ref = oracle.prefill_attention(oracle.bf16_to_double(synth.bf16_bits(q)), kk, vv, pos0, 1 / math.sqrt(D))
+    assert_gate(out.reshape(-1, D), ref.reshape(-1, D), f"prefill dominance 2^{small_exp} {kernel}")
+    assert fk.fp8kv_get_device_error() == 0
