@@ -289,6 +289,60 @@ def oracle_sample(inp, n_seqs, tokens):
     return dt, nbytes
 
 
+# Workloads and sequence samples of the fp8_kv_error report: the lengths of
+# the workload (paged: the two ends of its length range), seeded like the
+# workload, hostile keys where it has them.
+KV_ERROR_SAMPLES = {
+    "tiny_decode": (77, 128),
+    "decode_b16_ctx512": (512, 512),
+    "decode_b16_ctx8192": (8192, 8192),
+    "paged_b64_hostile": (1024, 16384),
+}
+KV_ERROR_DTYPES = ("k8v8", "k16v8", "k8v16", "mxk8v8", "k16v16")
+
+
+def fp8_kv_errors(samples=None, dtypes=KV_ERROR_DTYPES):
+    """fp8_kv_error ("FP8 KV cache (fp8_kv, opt-in)", bullet "Math"): the
+    relative L2 change of decode attention (all sequences and query heads of
+    the sample together) when the bf16 K/V are replaced by what each cache
+    dtype stores -- e4m3 codes with a per-row scale, or MXFP8 keys (e4m3 codes
+    with one power-of-two scale per 32 elements), on the e4m3 sides; the bf16
+    values on the bf16 sides.  Computed by the oracle in fp64 on the host."""
+    import numpy as np
+    import oracle
+    samples = KV_ERROR_SAMPLES if samples is None else samples
+    res = {}
+    for name, lens in samples.items():
+        spec = synth.WORKLOADS[name]
+        inp = synth.decode_inputs(spec, device="cpu", seq_lens=list(lens))
+        D = spec.head_dim
+        B, T = len(lens), max(lens)
+        q = oracle.bf16_to_double(synth.bf16_bits(inp.q))
+        kb = np.zeros((B, spec.kv_heads, T, D), np.uint16)
+        vb = np.zeros_like(kb)
+        for b, n in enumerate(lens):
+            s = int(inp.cu_seqlens[b])
+            kb[b, :, :n] = synth.bf16_bits(inp.k[s:s + n]).transpose(1, 0, 2)
+            vb[b, :, :n] = synth.bf16_bits(inp.v[s:s + n]).transpose(1, 0, 2)
+        seq = np.asarray(lens, np.int32)
+        sm = 1.0 / math.sqrt(D)
+        k16, v16 = oracle.bf16_to_double(kb), oracle.bf16_to_double(vb)
+        o_ref = oracle.decode_attention(q, k16, v16, seq, sm)
+        k8 = oracle.dequantize(*oracle.quantize(kb))
+        v8 = oracle.dequantize(*oracle.quantize(vb))
+        kmx = oracle.mx_dequantize(*oracle.mx_quantize(kb)) if D % 32 == 0 else None
+        sides = {"k8v8": (k8, v8), "k16v8": (k16, v8), "k8v16": (k8, v16), "mxk8v8": (kmx, v8),
+                 "k16v16": (k16, v16)}
+        res[name] = {}
+        for dt in dtypes:
+            k, v = sides[dt]
+            if k is None:
+                continue
+            o = oracle.decode_attention(q, k, v, seq, sm)
+            res[name][dt] = float(np.linalg.norm(o - o_ref) / max(np.linalg.norm(o_ref), 1e-300))
+    return res
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return
@@ -783,13 +837,16 @@ def run_gpu(args, ws, rank):
     shapes = None if args.no_shapes else measure_shapes(args)
     interval = None if args.no_interval else measure_interval(args)
 
-    cpu = None
+    cpu = kv_err = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         host_inp = synth.decode_inputs(spec, device="cpu", seq_lens=[T] * 8)
         dt, nbytes = oracle_sample(host_inp, 8, T)
         cpu = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "host": host_description(),
                "sample": f"8 of 16 sequences x {T} tokens (e4m3 dequantise + fp64 decode attention), "
                          f"single thread, {dt:.2f} s"}
+        kv_err = {"sequences": {k: list(v) for k, v in KV_ERROR_SAMPLES.items()},
+                  "note": "rel-L2 of decode attention over the stored cache against the bf16 cache (oracle, fp64)",
+                  "rel_l2": fp8_kv_errors()}
 
     if rank == 0:
         line = {
@@ -807,7 +864,7 @@ def run_gpu(args, ws, rank):
             "launch": "plain" if args.plain_launch or not tensor else
                       "programmatic dependent launch: a step streams its layer's cache while the previous step finishes (FP8KV_STEP_EARLY_CACHE_READ)",
                        "l2": f"{args.layers} distinct layer caches rotated (inputs larger than L2)"},
-            "roofline": roof, "cpu_baseline": cpu,
+            "roofline": roof, "cpu_baseline": cpu, "fp8_kv_error": kv_err,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": (1 if tensor else 3) * args.steps,
             "kernels_us": None if per is None else {k.replace("_ms", "_us"): v * 1e3 for k, v in per.items()},

@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" boundary: argument checks, launch configuration,
 // status codes.  Every entry point validates on the host, launches on the
 // caller's stream and returns; nothing here allocates device memory.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -12,35 +13,40 @@ namespace fp8kv {
 // its address as an argument.
 __device__ unsigned int g_device_error;
 
+// Per-device values looked up on first use and kept; atomics, so host
+// threads making their first call at once (each looking the value up and
+// storing the same result) do not race.
 static unsigned int* device_error_ptr() {
   constexpr int kMaxDev = 64;
-  static unsigned int* ptrs[kMaxDev];
+  static std::atomic<unsigned int*> ptrs[kMaxDev];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) { (void)cudaGetLastError(); return nullptr; }
   if (dev < 0 || dev >= kMaxDev) return nullptr;
-  if (ptrs[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) { (void)cudaGetLastError(); return nullptr; }
-    ptrs[dev] = static_cast<unsigned int*>(p);
+  unsigned int* p = ptrs[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_device_error) != cudaSuccess) { (void)cudaGetLastError(); return nullptr; }
+    p = static_cast<unsigned int*>(a);
+    ptrs[dev].store(p, std::memory_order_release);
   }
-  return ptrs[dev];
+  return p;
 }
 
 static int sm_count() {
   constexpr int kMaxDev = 64;
-  static int counts[kMaxDev];
+  static std::atomic<int> counts[kMaxDev];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) { (void)cudaGetLastError(); return 148; }
   if (dev < 0 || dev >= kMaxDev) return 148;
-  if (counts[dev] == 0) {
-    int n = 0;
+  int n = counts[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
       (void)cudaGetLastError();
       n = 148;
     }
-    counts[dev] = n;
+    counts[dev].store(n, std::memory_order_relaxed);
   }
-  return counts[dev];
+  return n;
 }
 
 static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }

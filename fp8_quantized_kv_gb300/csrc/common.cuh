@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/fp8kv.h"
 
 namespace fp8kv {
@@ -135,6 +137,13 @@ __device__ __forceinline__ int cache_capacity(const CacheView& c) {
   return c.paged ? c.max_pages_per_seq * c.page_size : c.max_tokens;
 }
 
+// Host-side caches of the launch code (kernel attributes, occupancy) are
+// shared by every host thread that calls the library: one lock guards them.
+inline std::mutex& host_cache_lock() {
+  static std::mutex m;
+  return m;
+}
+
 // Opt a kernel into `bytes` of dynamic shared memory, once per (kernel,
 // device).  A failure is read and cleared before it is returned, so that it
 // does not stay pending on the stream.
@@ -146,6 +155,7 @@ inline cudaError_t ensure_smem_optin(const void* func, int bytes) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) { (void)cudaGetLastError(); return e; }
   if (dev < 0 || dev >= kMaxDev) dev = 0;
+  std::lock_guard<std::mutex> lock(host_cache_lock());
   for (int i = 0; i < done_n[dev]; ++i)
     if (done_fn[dev][i] == func) return cudaSuccess;
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);

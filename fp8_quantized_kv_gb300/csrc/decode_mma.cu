@@ -1289,6 +1289,7 @@ static bool cluster_fits(const void* fn, dim3 grid, int smem) {
   static Key keys[16];
   static int vals[16];
   static int n = 0;
+  std::lock_guard<std::mutex> lock(host_cache_lock());
   int max_clusters = -1;
   for (int i = 0; i < n; ++i)
     if (keys[i].dev == dev && keys[i].fn == fn && keys[i].x == grid.x) max_clusters = vals[i];

@@ -15,6 +15,8 @@
 // __device__ array is only a stand-in, so the address is looked up once per
 // device (cudaGetSymbolAddress, with that device current) and passed to the
 // kernels.
+#include <atomic>
+
 #include "params.cuh"
 
 namespace fp8kv {
@@ -24,21 +26,23 @@ constexpr size_t kStaticScratchBytes = 16u << 20;   // 16 MiB per device
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 // Device address of g_decode_scratch on the current device, looked up on the
-// first use per device.  Returns nullptr if the lookup fails.
+// first use per device and kept (atomically: host threads making their first
+// call at once each look it up and store the same value).  Returns nullptr
+// if the lookup fails.
 static void* static_scratch_ptr(cudaError_t* err) {
   constexpr int kMaxDev = 64;
-  static void* ptrs[kMaxDev];
+  static std::atomic<void*> ptrs[kMaxDev];
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) { (void)cudaGetLastError(); return nullptr; }
   if (dev < 0 || dev >= kMaxDev) { *err = cudaErrorInvalidDevice; return nullptr; }
-  if (ptrs[dev] == nullptr) {
-    void* p = nullptr;
+  void* p = ptrs[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
     *err = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (*err != cudaSuccess) { (void)cudaGetLastError(); return nullptr; }
-    ptrs[dev] = p;
+    ptrs[dev].store(p, std::memory_order_release);
   }
-  return ptrs[dev];
+  return p;
 }
 
 }  // namespace fp8kv
@@ -51,7 +55,18 @@ fp8kv_status fp8kv_decode_attention_static(const void* q, const fp8kv_cache* cac
                                            fp8kv_stream_t stream) {
   // Invalid arguments give need == 0 here and are reported by the checks of
   // fp8kv_decode_attention below.
-  const size_t need = fp8kv_decode_workspace_bytes(cache, q_heads, num_splits, FP8KV_KERNEL_AUTO);
+  size_t need = fp8kv_decode_workspace_bytes(cache, q_heads, num_splits, FP8KV_KERNEL_AUTO);
+  if (need > fp8kv::kStaticScratchBytes && num_splits == 0) {
+    // The automatic split count needs more partials than the array holds:
+    // take the largest count that fits (fewer splits, fewer partials).
+    for (int s = fp8kv_decode_num_splits(cache, q_heads, 0, FP8KV_KERNEL_AUTO) - 1; s >= 1; --s) {
+      need = fp8kv_decode_workspace_bytes(cache, q_heads, s, FP8KV_KERNEL_AUTO);
+      if (need <= fp8kv::kStaticScratchBytes) {
+        num_splits = s;
+        break;
+      }
+    }
+  }
   if (need > fp8kv::kStaticScratchBytes) return FP8KV_ERR_WORKSPACE;
   cudaError_t e = cudaSuccess;
   void* scratch = fp8kv::static_scratch_ptr(&e);

@@ -32,6 +32,12 @@
  *    group size q_heads/kv_heads from 1 to 8 for decode and from 1 to 16 for
  *    prefill; page_size 16, 32 or 64; contiguous capacity max_tokens a
  *    multiple of 16.  Anything else returns FP8KV_ERR_UNSUPPORTED.
+ *  - Calls may come from several host threads.  Per-device values (the
+ *    device addresses of the library's error word and of the array of
+ *    fp8kv_decode_attention_static, kernel attributes) are looked up on the
+ *    first call on each device and kept for the life of the process:
+ *    resetting a device (cudaDeviceReset) after the library has run on it is
+ *    not supported.
  */
 #ifndef FP8KV_H
 #define FP8KV_H
@@ -285,8 +291,10 @@ FP8KV_API fp8kv_status fp8kv_decode_step(const void *q, const void *k_new, const
  * allocation on its serving path, or a plugin given only its input and
  * output tensors.  The call makes no cudaMalloc, cudaFree or allocating
  * library call.
- *  - A call whose partials would not fit (fp8kv_decode_workspace_bytes above
- *    the array size) returns FP8KV_ERR_WORKSPACE and launches nothing.
+ *  - With num_splits 0 the split count is the automatic one, lowered to the
+ *    largest count whose partials fit when they would not.  A call whose
+ *    partials cannot fit (an explicit num_splits too large, or not even one
+ *    split fitting) returns FP8KV_ERR_WORKSPACE and launches nothing.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture.

@@ -32,3 +32,19 @@ def test_shape_mode_parses():
     a = bench.parse(["--shape", "paged_b64_hostile", "--dtype", "k16v16", "--steps", "10", "--warmup", "3"])
     assert a.shape == "paged_b64_hostile" and a.dtype == "k16v16" and a.steps == 10
     assert bench.parse([]).shape is None
+
+
+def test_fp8_kv_error_report():
+    """The bench's fp8_kv_error report on the tiny workload: the bf16 cache
+    changes nothing; every 8-bit side adds error of the size an e4m3 round
+    trip (3 mantissa bits) gives, a few percent; two 8-bit sides more than one
+    of them."""
+    err = bench.fp8_kv_errors(samples={"tiny_decode": (77, 128)}, dtypes=("k8v8", "k16v8", "k8v16", "k16v16"))
+    e = err["tiny_decode"]
+    assert e["k16v16"] == 0.0
+    for dt in ("k8v8", "k16v8", "k8v16"):
+        assert 1e-3 < e[dt] < 0.1, (dt, e[dt])
+    assert e["k8v8"] > max(e["k16v8"], e["k8v16"])
+    # head_dim 64 has two MXFP8 blocks of 32: the MXFP8 key cache is reported too
+    mx = bench.fp8_kv_errors(samples={"tiny_decode": (77, 128)}, dtypes=("mxk8v8",))["tiny_decode"]["mxk8v8"]
+    assert 1e-3 < mx < 0.1
