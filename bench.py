@@ -364,18 +364,22 @@ def run_reference(args, ws, rank):
         tot_t += dt
         tot_b += nb
     gbs = tot_b / tot_t / 1e9
-    ms_per_layer = tot_t / args.steps * 1e3 * (spec.batch * T) / tokens
+    sample = (f"per step: 1 sequence x {spec.kv_heads} KV heads x {tokens} tokens of the {WORKLOAD} "
+              f"workload ({spec.q_heads} query heads, head_dim {spec.head_dim}): e4m3 dequantise + fp64 "
+              "decode attention by the oracle (C, single thread); value and ms_per_step are this "
+              "sample's own: its algorithmic KV + q/out bytes over its measured time")
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_layer,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": spec.batch, "q_heads": spec.q_heads,
-                   "kv_heads": spec.kv_heads, "head_dim": spec.head_dim, "ctx": T, "cache": "k8v8"},
+        "config": {"workload": WORKLOAD, "batch": 1, "q_heads": spec.q_heads,
+                   "kv_heads": spec.kv_heads, "head_dim": spec.head_dim, "ctx": tokens,
+                   "cache": "k8v8", "layout": "contiguous", "parallelism": "rank 0 only",
+                   "kernel": "oracle", "step": "oracle dequantise + fp64 decode attention",
+                   "launch": "host call", "l2": "host memory"},
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "host": host_description(),
-                         "sample": f"per step: 1 sequence x {tokens} tokens of the workload "
-                                   "(e4m3 dequantise + fp64 decode attention), single thread; "
-                                   "ms_per_step scaled to the full 16 x 8192 layer"},
+                         "sample": sample},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -128,14 +128,20 @@ static int resolve_kernel(const fp8kv_cache* c, int q_heads, int requested) {
   return mma_ok ? FP8KV_KERNEL_TENSOR_CORES : FP8KV_KERNEL_CUDA_CORES;
 }
 
-static SplitPlan plan_splits(const fp8kv_cache* c, int requested, int kernel) {
+// KV heads per tensor-core CTA for this cache and kernel (1 elsewhere).
+static int heads_per_cta(const fp8kv_cache* c, int q_heads, int kernel) {
+  if (kernel != FP8KV_KERNEL_TENSOR_CORES) return 1;
+  return decode_heads_per_cta(c->layout == FP8KV_LAYOUT_PAGED, c->kv_heads, q_heads / c->kv_heads, c->page_size);
+}
+
+static SplitPlan plan_splits(const fp8kv_cache* c, int requested, int kernel, int hpc) {
   const bool tc = kernel >= FP8KV_KERNEL_TENSOR_CORES;
-  const int tile = tc ? 128 : kTileTokens;
+  const int tile = tc ? 128 / hpc : kTileTokens;          // tokens per KV head in a tile
   const int max_tiles = (capacity_of(c) + tile - 1) / tile;
   if (max_tiles <= 0) return {1, 1, tile, kernel};
   int want = requested;
   if (want <= 0) {
-    const long units = (long)c->batch * c->kv_heads;
+    const long units = (long)c->batch * (c->kv_heads / hpc);
     // tensor cores: one CTA per SM, and no partial second wave; CUDA cores:
     // about four CTAs per SM
     const long target = (long)(tc ? 1 : 4) * sm_count();
@@ -218,7 +224,7 @@ int32_t fp8kv_decode_num_splits(const fp8kv_cache* cache, int32_t q_heads, int32
   if (q_heads <= 0 || q_heads % cache->kv_heads != 0 || num_splits < 0) return 0;
   const int k = resolve_kernel(cache, q_heads, kernel);
   if (k == 0) return 0;
-  return plan_splits(cache, num_splits, k).splits;
+  return plan_splits(cache, num_splits, k, heads_per_cta(cache, q_heads, k)).splits;
 }
 
 size_t fp8kv_decode_workspace_bytes(const fp8kv_cache* cache, int32_t q_heads, int32_t num_splits,
@@ -249,7 +255,8 @@ fp8kv_status prepare_decode(const void* q, const fp8kv_cache* cache, const int32
   const int k = resolve_kernel(cache, q_heads, kernel);
   if (k == 0) return FP8KV_ERR_UNSUPPORTED;
   if (need_q && cache->batch > 0 && (!q || !seq_lens)) return FP8KV_ERR_INVALID_ARG;
-  const SplitPlan plan = plan_splits(cache, num_splits, k);
+  const int hpc = heads_per_cta(cache, q_heads, k);
+  const SplitPlan plan = plan_splits(cache, num_splits, k, hpc);
   const size_t need = fp8kv_decode_workspace_bytes(cache, q_heads, num_splits, kernel);
   if (cache->batch > 0 && (workspace == nullptr || workspace_bytes < need)) return FP8KV_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 15) != 0) return FP8KV_ERR_INVALID_ARG;
@@ -275,6 +282,8 @@ fp8kv_status prepare_decode(const void* q, const fp8kv_cache* cache, const int32
   p->cluster = 0;
   p->pdl = 0;
   p->k_f16 = k == FP8KV_KERNEL_TENSOR_CORES_K_F16 ? 1 : k == FP8KV_KERNEL_TENSOR_CORES_K_F16_PRODUCER ? 2 : 0;
+  p->hpc = hpc;
+  p->hpc_shift = hpc == 8 ? 3 : hpc == 4 ? 2 : hpc == 2 ? 1 : 0;
   *resolved = k >= FP8KV_KERNEL_TENSOR_CORES ? FP8KV_KERNEL_TENSOR_CORES : k;
   return FP8KV_OK;
 }

@@ -187,7 +187,7 @@ __device__ __forceinline__ int g4_owner(int q, int S) { return ((q + 1) * S - 1)
 
 __device__ __forceinline__ void cluster_exchange(const DecodeParams& p, float* rx_ml, float* rx_o, uint64_t* rx_bar,
                                               const int* slice, float* stage, const float (&Og)[8],
-                                              const float (&Mg)[8], const float (&Lg)[8], int b, int h, int G,
+                                              const float (&Mg)[8], const float (&Lg)[8], int64_t hq0, int QH,
                                               int t, volatile int* abort) {
   constexpr int D = 128;
   const int S = p.num_splits;
@@ -247,9 +247,9 @@ __device__ __forceinline__ void cluster_exchange(const DecodeParams& p, float* r
         o.x += w * v.x; o.y += w * v.y; o.z += w * v.z; o.w += w * v.w;
       }
     }
-    if (g < G) {
+    if (g < QH) {
       const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
-      const int64_t oi = ((int64_t)b * p.q_heads + (int64_t)h * G + g) * D + 4 * (mlo + j);
+      const int64_t oi = (hq0 + g) * D + 4 * (mlo + j);
       const float r4[4] = {o.x * inv, o.y * inv, o.z * inv, o.w * inv};
       if ((reinterpret_cast<uintptr_t>(p.out) & 15) != 0) {   // caller's buffer not 16-byte aligned
 #pragma unroll
@@ -342,14 +342,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
   float* anc0 = reinterpret_cast<float*>(misc + 544);      // [4 slots][4 warps][8 heads]: group 0's anchors
   float* wscr = reinterpret_cast<float*>(misc + 6656);     // [softmax warp][40]: maxima, then fold factors
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // KV heads hkv0 .. hkv0 + HPC - 1 and their QH = HPC G query heads; a tile
+  // holds TT tokens of each (HPC > 1 only on a paged cache: rows ordered by
+  // page, then head, then token within the page)
+  const int HPC = p.hpc, hs = p.hpc_shift;
+  const int hkv0 = blockIdx.y << hs;
   if (tid == 0) {                                 // the TMA unit fetches the maps while the CTA sets up
     tma::prefetch_map(&tp.tmk);
     tma::prefetch_map(&tp.tmv);
   }
   const CacheView& c = p.c;
   const int G = p.group, S = p.num_splits;
+  const int QH = G << hs, TT = kMmaTile >> hs;
+  const int64_t hq_row0 = (int64_t)b * p.q_heads + (int64_t)hkv0 * G;   // (sequence, first query head) row
 
   int T = p.seq_lens[b];
   const int cap = cache_capacity(c);
@@ -357,10 +364,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
     if (tid == 0) raise_error(p.err, FP8KV_DEVERR_SEQ_TOO_LONG);
     T = 0;
   }
-  const int tiles = (T + kMmaTile - 1) / kMmaTile;
+  const int tiles = (T + TT - 1) / TT;
   const int t_begin = split * p.chunk_tiles;
   const int t_end = min(t_begin + p.chunk_tiles, tiles);
-  const int64_t part0 = ((int64_t)b * p.q_heads + (int64_t)h * G) * S + split;
+  const int64_t part0 = hq_row0 * S + split;
   if (t_begin >= t_end) {
     if (p.pdl) grid_dep_wait();                   // writes below
     if (p.cluster) {
@@ -379,7 +386,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
         float Og[8], Mg[8], Lg[8];
 #pragma unroll
         for (int g = 0; g < 8; ++g) { Og[g] = 0.f; Mg[g] = -INFINITY; Lg[g] = 0.f; }
-        cluster_exchange(p, rx_ml, rx_o, rx_bar, slice_tab, xo, Og, Mg, Lg, b, h, G, tid - 64, abort_flag);
+        cluster_exchange(p, rx_ml, rx_o, rx_bar, slice_tab, xo, Og, Mg, Lg, hq_row0, QH, tid - 64, abort_flag);
       }
       return;
     }
@@ -387,16 +394,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
       // No partial: splits without work take no part in the merge.  A
       // sequence with no tokens gets its zero output from split 0.
       if (tiles == 0 && split == 0)
-        for (int i = tid; i < G * D; i += blockDim.x) {
-          const int64_t o = ((int64_t)b * p.q_heads + (int64_t)h * G + i / D) * D + (i % D);
+        for (int i = tid; i < QH * D; i += blockDim.x) {
+          const int64_t o = (hq_row0 + i / D) * D + (i % D);
           if (p.out_f32) reinterpret_cast<float*>(p.out)[o] = 0.f;
           else reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(0.f);
         }
       return;
     }
-    for (int i = tid; i < G * D; i += blockDim.x)
+    for (int i = tid; i < QH * D; i += blockDim.x)
       p.part_o[(part0 + (int64_t)(i / D) * S) * D + (i % D)] = 0.f;
-    if (tid < G) {
+    if (tid < QH) {
       p.part_m[part0 + (int64_t)tid * S] = -INFINITY;
       p.part_l[part0 + (int64_t)tid * S] = 0.f;
     }
@@ -405,7 +412,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
   const int n_tiles = t_end - t_begin;
   // Fused step: the CTA whose range holds position T-1 writes the new token
   // before its producer loads that tile.
-  const int tile_new = T > 0 ? (T - 1) / kMmaTile : -1;
+  const int tile_new = T > 0 ? (T - 1) / TT : -1;
   const bool appender = p.fused && p.k_new != nullptr && tile_new >= t_begin && tile_new < t_end;
   const int i_new = appender ? tile_new - t_begin : n_tiles;
   if (tid == 0) TRACE(1020);
@@ -418,27 +425,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
   // Overlapped before the one CTA-wide barrier: thread 0 initialises the
   // barriers and issues the first tiles' loads, warp 1 allocates TMEM, warps
   // 2-5 write the query operand.
-  const int64_t cont_row0 = ((int64_t)b * c.kv_heads + h) * c.max_tokens;
+  const int64_t cont_row0 = ((int64_t)b * c.kv_heads + hkv0) * c.max_tokens;
   // Issue the TMA copies of tile i into its stage.  Called by all 32 lanes
   // of warp 0.  Contiguous layout: lane 0 issues the tile's few copies.
-  // Paged layout: lane j issues page j's copies (K and V boxes, scale rows),
+  // Paged layout: lane j issues page j's copies (K and V boxes of the HPC
+  // heads' rows, which are contiguous in the pool, and their scale rows),
   // lane 0 arms the stage's barrier (the transaction count is signed, so a
-  // copy may land first); each lane holds its page id of the next tile,
-  // loaded one tile ahead so the table lookup overlaps the wait for a stage.
-  int my_page = 0;
-  auto load_page = [&](int i) {
-    if (!c.paged || i >= n_tiles) return;
-    const int t0 = (t_begin + i) * kMmaTile;
-    const int np = (min(kMmaTile, T - t0) + c.page_size - 1) / c.page_size;
-    if (lane < np) my_page = c.page_table[(int64_t)b * c.max_pages_per_seq + (t0 >> c.page_shift) + lane];
+  // copy may land first).  Each lane keeps its page ids of the next
+  // kPageAhead tiles in registers, loaded that many tiles ahead: a table
+  // lookup issued only one tile ahead made every tile wait a full load
+  // latency in the producer, which then set the paged decode's pace.
+  constexpr int kPageAhead = 4;
+  int pg[kPageAhead];
+  auto page_of = [&](int i) -> int {
+    if (!c.paged || i >= n_tiles) return 0;
+    const int t0 = (t_begin + i) * TT;
+    const int np = (min(TT, T - t0) + c.page_size - 1) / c.page_size;
+    return lane < np ? c.page_table[(int64_t)b * c.max_pages_per_seq + (t0 >> c.page_shift) + lane] : 0;
   };
   auto produce = [&](int i) {
     const int s = i % C::NST;
     uint8_t* st = smem + s * C::STAGE;
     float* kss = reinterpret_cast<float*>(st + C::K_TILE + C::V_TILE);
     float* vss = kss + kMmaTile;
-    const int t0 = (t_begin + i) * kMmaTile;
-    const int valid = min(kMmaTile, T - t0);
+    const int t0 = (t_begin + i) * TT;
+    const int valid = min(TT, T - t0);
     if (!c.paged) {
       if (lane == 0) {
         const int nsc = min(kMmaTile, (valid + 15) & ~15);
@@ -463,18 +474,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
       // arrival to the stage barrier and completes it when the lane's copies
       // land; it runs before lane 0's arrival (the barrier's only expected
       // one), so the phase cannot complete without the scale rows.
-      const uint32_t per_page = P * 128 * (C::KB + C::VB);
-      int page = my_page;
-      load_page(i + 1);
+      const int PR = P << hs;                      // rows of one page (HPC heads x P tokens)
+      const uint32_t per_page = PR * 128 * (C::KB + C::VB);
+      int page = pg[0];
+#pragma unroll
+      for (int k = 0; k + 1 < kPageAhead; ++k) pg[k] = pg[k + 1];
+      pg[kPageAhead - 1] = page_of(i + kPageAhead);
       if (lane < np && (page < 0 || page >= c.num_pages)) {
         raise_error(p.err, FP8KV_DEVERR_BAD_PAGE);
         page = 0;      // read a valid page; the result is flagged as wrong
       }
-      const int64_t row = ((int64_t)page * c.kv_heads + h) * P;
+      const int64_t row = ((int64_t)page * c.kv_heads + hkv0) * P;
       if (lane < np && (C::K8 || VE == ELEM_E4M3)) {
-        for (int q = 0; q < P / 4; ++q) {
-          if (C::K8) cp_async16(kss + lane * P + 4 * q, c.k_scale + row + 4 * q);
-          if (VE == ELEM_E4M3) cp_async16(vss + lane * P + 4 * q, c.v_scale + row + 4 * q);
+        for (int q = 0; q < PR / 4; ++q) {
+          if (C::K8) cp_async16(kss + lane * PR + 4 * q, c.k_scale + row + 4 * q);
+          if (VE == ELEM_E4M3) cp_async16(vss + lane * PR + 4 * q, c.v_scale + row + 4 * q);
         }
         asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" ::"r"(umma::smem_u32(&full[s]))
                      : "memory");
@@ -482,7 +496,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
       __syncwarp();
       if (lane == 0) tma::arrive_expect_tx(&full[s], per_page * np);
       if (lane < np) {
-        const int off = lane * P * 128;
+        const int off = lane * PR * 128;
         tma::load_2d(st + off, &tp.tmk, 0, (int)row, &full[s]);
         if (!C::K8) tma::load_2d(st + kMmaTile * 128 + off, &tp.tmk, 64, (int)row, &full[s]);
         tma::load_2d(st + C::K_TILE + off, &tp.tmv, 0, (int)row, &full[s]);
@@ -505,7 +519,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
   }
   if (warp == 0) {
     __syncwarp();
-    load_page(0);
+#pragma unroll
+    for (int k = 0; k < kPageAhead; ++k) pg[k] = page_of(k);
     for (int i = 0; i < n_first; ++i) produce(i);
   }
   if (tid == 0) {
@@ -548,8 +563,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
   if (warp >= 2 && warp < 6) {   // query rows -> B operand of QK (e4m3 hi/lo pairs, or bf16)
     for (int g = warp - 2; g < 8; g += 4) {
       float x[4] = {0.f, 0.f, 0.f, 0.f};
-      if (g < G) {
-        const __nv_bfloat16* qr = p.q + ((int64_t)b * p.q_heads + (int64_t)h * G + g) * D + lane * 4;
+      if (g < QH) {
+        const __nv_bfloat16* qr = p.q + (hq_row0 + g) * D + lane * 4;
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[e] = __bfloat162float(qr[e]);
       }
@@ -604,45 +619,48 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
     // then publish them to the TMA loads of the producer.  The producer warp
     // does it: its first loads are in flight and no ring slot frees up for
     // a few microseconds, while the softmax warps start on the first tiles.
-    const int tpos = T - 1;
-    const int64_t row = cache_row(c, b, h, tpos, lane == 0 ? p.err : nullptr);
-    if (row >= 0) {
+    for (int hh = 0; hh < HPC; ++hh) {          // the CTA's KV heads
+      const int hk = hkv0 + hh;
+      const int tpos = T - 1;
+      const int64_t row = cache_row(c, b, hk, tpos, lane == 0 ? p.err : nullptr);
+      if (row >= 0) {
 #pragma unroll
-      for (int side = 0; side < 2; ++side) {
-        const __nv_bfloat16* src = (side == 0 ? p.k_new : p.v_new) + ((int64_t)b * c.kv_heads + h) * D + lane * 4;
-        const uint2 raw = *reinterpret_cast<const uint2*>(src);
-        const bool fp8 = side == 0 ? C::K8 : VE == ELEM_E4M3;
-        uint8_t* dst = const_cast<uint8_t*>(side == 0 ? c.k : c.v);
-        if (!fp8) {
-          *reinterpret_cast<uint2*>(dst + (row * D + lane * 4) * 2) = raw;
-        } else {
-          float x[4], t2[2];
-          bf16x2_to_f32(raw.x, t2); x[0] = t2[0]; x[1] = t2[1];
-          bf16x2_to_f32(raw.y, t2); x[2] = t2[0]; x[3] = t2[1];
-          if (side == 0 && c.k_bias != nullptr) {      // pre-bias residual key
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] -= c.k_bias[h * D + lane * 4 + e];
-          }
-          float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-          if (C::KMX && side == 0) {
-            // MXFP8 key: the arithmetic of fp8kv_quantize_mx, block = 8 lanes
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const int E = mx_block_exp(amax);
-            const float inv = pow2_exact(-E);
-            *reinterpret_cast<uint32_t*>(dst + row * D + lane * 4) =
-                e4m3x2_rn(x[0] * inv, x[1] * inv) | (e4m3x2_rn(x[2] * inv, x[3] * inv) << 16);
-            if ((lane & 7) == 0)
-              reinterpret_cast<uint8_t*>(const_cast<float*>(c.k_scale) + row)[lane >> 3] = (uint8_t)(E + 127);
+        for (int side = 0; side < 2; ++side) {
+          const __nv_bfloat16* src = (side == 0 ? p.k_new : p.v_new) + ((int64_t)b * c.kv_heads + hk) * D + lane * 4;
+          const uint2 raw = *reinterpret_cast<const uint2*>(src);
+          const bool fp8 = side == 0 ? C::K8 : VE == ELEM_E4M3;
+          uint8_t* dst = const_cast<uint8_t*>(side == 0 ? c.k : c.v);
+          if (!fp8) {
+            *reinterpret_cast<uint2*>(dst + (row * D + lane * 4) * 2) = raw;
           } else {
-            amax = warp_max(amax);
-            const float scale = __fdiv_rn(amax, 448.0f);
-            uint32_t packed = 0;
-            if (amax != 0.f)
-              packed = e4m3x2_rn(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale)) |
-                       (e4m3x2_rn(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale)) << 16);
-            *reinterpret_cast<uint32_t*>(dst + row * D + lane * 4) = packed;
-            if (lane == 0) const_cast<float*>(side == 0 ? c.k_scale : c.v_scale)[row] = scale;
+            float x[4], t2[2];
+            bf16x2_to_f32(raw.x, t2); x[0] = t2[0]; x[1] = t2[1];
+            bf16x2_to_f32(raw.y, t2); x[2] = t2[0]; x[3] = t2[1];
+            if (side == 0 && c.k_bias != nullptr) {      // pre-bias residual key
+#pragma unroll
+              for (int e = 0; e < 4; ++e) x[e] -= c.k_bias[hk * D + lane * 4 + e];
+            }
+            float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+            if (C::KMX && side == 0) {
+              // MXFP8 key: the arithmetic of fp8kv_quantize_mx, block = 8 lanes
+#pragma unroll
+              for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+              const int E = mx_block_exp(amax);
+              const float inv = pow2_exact(-E);
+              *reinterpret_cast<uint32_t*>(dst + row * D + lane * 4) =
+                  e4m3x2_rn(x[0] * inv, x[1] * inv) | (e4m3x2_rn(x[2] * inv, x[3] * inv) << 16);
+              if ((lane & 7) == 0)
+                reinterpret_cast<uint8_t*>(const_cast<float*>(c.k_scale) + row)[lane >> 3] = (uint8_t)(E + 127);
+            } else {
+              amax = warp_max(amax);
+              const float scale = __fdiv_rn(amax, 448.0f);
+              uint32_t packed = 0;
+              if (amax != 0.f)
+                packed = e4m3x2_rn(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale)) |
+                         (e4m3x2_rn(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale)) << 16);
+              *reinterpret_cast<uint32_t*>(dst + row * D + lane * 4) = packed;
+              if (lane == 0) const_cast<float*>(side == 0 ? c.k_scale : c.v_scale)[row] = scale;
+            }
           }
         }
       }
@@ -827,6 +845,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t s_col = 256 * wg, o_col = 256 * wg + 128;
     WgBars& B = wb[wg];
+    // row t of every tile: token tok of the tile's stretch of KV head hkv0 +
+    // hh, whose query heads are the score columns in cmask
+    int tok = t;
+    uint32_t cmask = 0xFFu;
+    if (HPC > 1) {
+      const int ps = c.page_shift;
+      const int hh = (t >> ps) & (HPC - 1);
+      tok = ((t >> (ps + hs)) << ps) | (t & (c.page_size - 1));
+      cmask = ((1u << G) - 1u) << (hh * G);
+    }
     float qs[8];
 #pragma unroll
     for (int g = 0; g < 8; ++g) qs[g] = qscale[g] * p.scale_log2;
@@ -943,9 +971,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
         uint8_t* st = smem + s * C::STAGE;
         const float* kss = reinterpret_cast<const float*>(st + C::K_TILE + C::V_TILE);
         const float* vss = kss + kMmaTile;
-        const int t0 = (t_begin + i) * kMmaTile;
-        const int valid = min(kMmaTile, T - t0);
-        const bool tok_ok = t < valid;
+        const int t0 = (t_begin + i) * TT;
+        const int valid = min(TT, T - t0);
+        const bool tok_ok = tok < valid;
         const float kf = KE == ELEM_E4M3 ? kss[t] : 1.f;     // (MXFP8: block scales applied below)
         const float vsc = VE == ELEM_E4M3 ? (tok_ok ? vss[t] : 0.f) : 1.f;
         float sc[16];
@@ -983,7 +1011,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const float raw = C::QHL ? (sc[g] + sc[g + 8]) : sc[g];
-          sg[g] = tok_ok ? raw * (qs[g] * kf) : -INFINITY;
+          sg[g] = tok_ok && ((cmask >> g) & 1u) ? raw * (qs[g] * kf) : -INFINITY;
           uu[g] = sg[g] + lvs;
         }
         TRACE_SUB(i, 7);
@@ -1114,22 +1142,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
       // splits with work (only the global-memory merge needs it)
       const int n_busy = p.cluster ? 0 : (tiles + p.chunk_tiles - 1) / p.chunk_tiles;
       if (p.cluster) {
-        cluster_exchange(p, rx_ml, rx_o, rx_bar, slice_tab, xo, Og, Mg, Lg, b, h, G, t, abort_flag);
+        cluster_exchange(p, rx_ml, rx_o, rx_bar, slice_tab, xo, Og, Mg, Lg, hq_row0, QH, t, abort_flag);
       } else if (p.fused && n_busy == 1) {
         // the only split of this sequence: normalise and write the output
 #pragma unroll
         for (int g = 0; g < 8; ++g)
-          if (g < G) {
+          if (g < QH) {
             const float r = Lg[g] > 0.f ? Og[g] / Lg[g] : 0.f;
-            const int64_t o = ((int64_t)b * p.q_heads + (int64_t)h * G + g) * D + t;
+            const int64_t o = (hq_row0 + g) * D + t;
             if (p.out_f32) reinterpret_cast<float*>(p.out)[o] = r;
             else reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(r);
           }
       } else {
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          if (g < G) p.part_o[(part0 + (int64_t)g * S) * D + t] = Og[g];
-          if (t == g && g < G) {
+          if (g < QH) p.part_o[(part0 + (int64_t)g * S) * D + t] = Og[g];
+          if (t == g && g < QH) {
             p.part_m[part0 + (int64_t)g * S] = Mg[g];
             p.part_l[part0 + (int64_t)g * S] = Lg[g];
           }
@@ -1144,7 +1172,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
           if (t == 0 && cta_lin < 4096) g_cta_time[cta_lin][2] = umma::globaltimer_ns();
 #endif
           if (t == 0) {
-            int* ctr = p.counters + (int64_t)b * c.kv_heads + h;
+            int* ctr = p.counters + (int64_t)b * c.kv_heads + hkv0;
             const int old = atomicAdd(ctr, 1);
             const int last = old == n_busy - 1;
             if (last) *ctr = 0;                 // ready for the next call
@@ -1164,15 +1192,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
             float* pl_sh = pm_sh + 8 * kMergeChunk;                              // [8][kMergeChunk]
             for (int k0 = 0; k0 < n_busy; k0 += kMergeChunk) {
               const int nb = min(kMergeChunk, n_busy - k0);
-              const int chunks = G * nb * (D / 4);                      // 16-byte chunks of O
+              const int chunks = QH * nb * (D / 4);                     // 16-byte chunks of O
               for (int i = t; i < chunks; i += 128) {
                 const int g = i / (nb * (D / 4)), rem = i % (nb * (D / 4)), k = rem / (D / 4), c4 = rem % (D / 4);
-                const int64_t pr = ((int64_t)b * p.q_heads + (int64_t)h * G + g) * S + k0 + k;
+                const int64_t pr = (hq_row0 + g) * S + k0 + k;
                 cp_async16(po_sh + (g * kMergeChunk + k) * D + c4 * 4, p.part_o + pr * D + c4 * 4);
               }
-              if (t < G * nb) {
-                const int g = t / nb, k = t % nb;
-                const int64_t pr = ((int64_t)b * p.q_heads + (int64_t)h * G + g) * S + k0 + k;
+              for (int i = t; i < QH * nb; i += 128) {      // (up to 8 x kMergeChunk entries)
+                const int g = i / nb, k = i % nb;
+                const int64_t pr = (hq_row0 + g) * S + k0 + k;
                 pm_sh[g * kMergeChunk + k] = __ldcg(p.part_m + pr);
                 pl_sh[g * kMergeChunk + k] = __ldcg(p.part_l + pr);
               }
@@ -1192,7 +1220,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
                 for (int g = 0; g < 8; ++g)
 #pragma unroll
                   for (int u = 0; u < 4; ++u) {
-                    const bool in = g < G && u < nb;
+                    const bool in = g < QH && u < nb;
                     mv[g][u] = in ? pm_sh[g * kMergeChunk + u] : -INFINITY;
                     lv[g][u] = in ? pl_sh[g * kMergeChunk + u] : 0.f;
                     oo[g][u] = in ? po_sh[(g * kMergeChunk + u) * D + t] : 0.f;
@@ -1210,7 +1238,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
               } else {
 #pragma unroll
               for (int g = 0; g < 8; ++g) {
-                if (g < G) {
+                if (g < QH) {
                   // up to four splits at a time, their loads independent
                   float M = k0 == 0 ? -INFINITY : Mg[g];
                   for (int k4 = 0; k4 < nb; k4 += 4) {
@@ -1249,9 +1277,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
 #endif
 #pragma unroll
             for (int g = 0; g < 8; ++g)
-              if (g < G) {
+              if (g < QH) {
                 const float r = Lg[g] > 0.f ? Og[g] / Lg[g] : 0.f;
-                const int64_t oi = ((int64_t)b * p.q_heads + (int64_t)h * G + g) * D + t;
+                const int64_t oi = (hq_row0 + g) * D + t;
                 if (p.out_f32) reinterpret_cast<float*>(p.out)[oi] = r;
                 else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(r);
               }
@@ -1323,7 +1351,7 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
   const CacheView& c = p.c;
   const int64_t rows = c.paged ? (int64_t)c.num_pages * c.kv_heads * c.page_size
                                : (int64_t)c.batch * c.kv_heads * c.max_tokens;
-  const int box_rows = c.paged ? c.page_size : kMmaTile;
+  const int box_rows = c.paged ? c.page_size * p.hpc : kMmaTile;
   if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
   if (!make_map(&tp.tmk, c.k, KE == ELEM_BF16, rows, box_rows) ||
       !make_map(&tp.tmv, c.v, VE != ELEM_E4M3, rows, box_rows))
@@ -1375,7 +1403,7 @@ extern "C" __attribute__((visibility("default"))) int fp8kv_trace_read_cta(unsig
 #endif
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int dtype, int batch, cudaStream_t st) {
-  dim3 grid(p.num_splits, p.c.kv_heads, batch);
+  dim3 grid(p.num_splits, p.c.kv_heads / p.hpc, batch);
   if (dtype == FP8KV_K8V8) {
     if (p.k_f16 == 1) return launch_tc_t<ELEM_E4M3, ELEM_E4M3, XK_CONSUMER>(p, grid, st);
     if (p.k_f16 == 2) return launch_tc_t<ELEM_E4M3, ELEM_E4M3, XK_PRODUCER>(p, grid, st);

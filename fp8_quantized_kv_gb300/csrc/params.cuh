@@ -27,7 +27,21 @@ struct DecodeParams {
   int pdl;                   // fused step launched as a programmatic dependent of the previous kernel
   int k_f16;                 // tensor-core kernel on the transform path (K converted to f16 on chip):
                              // 0 no, 1 by the softmax warpgroups, 2 by the producer warp
+  int hpc, hpc_shift;        // tensor-core kernel: KV heads per CTA (a power of two; a tile is
+                             // 128 rows = hpc heads x 128/hpc tokens)
 };
+
+// KV heads one tensor-core decode CTA takes (1, 2, 4 or 8): on a paged cache
+// with fewer than 8 query heads per KV head, neighbouring KV heads' rows of
+// a page are contiguous in the pool, so a CTA taking 8 / G of them fetches
+// each page side with one larger copy (the paged decode is bound by the
+// number of copies); everything else takes one KV head.
+inline int decode_heads_per_cta(int paged, int kv_heads, int group, int page_size) {
+  if (!paged || group < 1 || group >= 8 || 8 % group != 0) return 1;
+  int hpc = 8 / group;
+  while (hpc > 1 && (kv_heads % hpc != 0 || hpc * page_size > 128)) hpc /= 2;
+  return hpc;
+}
 
 struct PrefillParams {
   CacheView c;

@@ -119,6 +119,25 @@ def test_step_split_invariance_cluster_and_global_merge():
         assert rel <= 1e-5, (ns, rel)
 
 
+@pytest.mark.parametrize("G", [4, 8])
+def test_step_global_merge_many_partials(G):
+    """The in-kernel global merge with more (query head, split) partials than
+    the 128 merging threads, and with more splits than one staging chunk
+    (44): one KV head, 8192 tokens, up to 64 one-tile splits."""
+    spec = synth.DecodeWorkload("many_parts", 2, G, 1, 128, seed=61, seq_lens=(8192, 5000))
+    inp = synth.decode_inputs(spec, device="cuda")
+    ref = oracle_decode(inp, "k8v8", range(2))
+    outs = {}
+    for ns in (1, 17, 33, 45, 64):
+        _, out, _, _ = _run(inp, "k8v8", "tensor_cores", num_splits=ns, capacity=8192)
+        assert fk.fp8kv_get_device_error() == 0
+        assert_gate(out.cpu().numpy(), ref, f"G{G} splits {ns}")
+        outs[ns] = out.double()
+    for ns, o in outs.items():
+        rel = ((o - outs[1]).norm(dim=-1) / outs[1].norm(dim=-1)).max().item()
+        assert rel <= 1e-5, (ns, rel)
+
+
 def test_step_early_cache_read_matches_plain_launch():
     """Back-to-back steps over four layer caches with
     FP8KV_STEP_EARLY_CACHE_READ (each step streams its cache while the step
