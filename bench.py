@@ -16,6 +16,7 @@ Prints ONE JSON line (rank 0).  `--impl reference` times the oracle (plain
 fp64 C on the host cores) on the same metric instead.
 """
 import argparse
+import dataclasses
 import ctypes
 import hashlib
 import json
@@ -43,6 +44,7 @@ PAGE_NUMBER_GBS = 550.0   # the pages' figure for this workload (RTX 5070 Ti, Tr
 # previous layer's step finishes (programmatic dependent launch); the layers'
 # caches are distinct, as in a model
 STEP_EARLY_CACHE_READ = 1
+L2_BYTES = 129 * 10**6      # GB300 L2 capacity
 
 
 def parse(argv=None):
@@ -63,8 +65,10 @@ def parse(argv=None):
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-shapes", action="store_true")
     ap.add_argument("--no-interval", action="store_true")
-    ap.add_argument("--shape", default=None, choices=["decode_b16_ctx512", "paged_b64_hostile"],
+    ap.add_argument("--shape", default=None, choices=["decode_b16_ctx512", "decode_b16_ctx8192", "paged_b64_hostile"],
                     help="time only the fused decode step on this workload (for profiling) and exit")
+    ap.add_argument("--group", type=int, default=0,
+                    help="with --shape: query heads per KV head (default: the workload's own)")
     return ap.parse_args(argv)
 
 
@@ -219,13 +223,18 @@ def tensor_peak():
     return 1900.0, "fallback"
 
 
-def kernel_source_sha():
+def kernel_source_sha(kernel_file):
+    """Hash of one kernel's sources: its .cu file, every shared .cuh header
+    and the public headers (a change anywhere else leaves it alone)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_quantized_kv_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    inc = os.path.join(ROOT, "include")
+    files = [os.path.join(csrc, kernel_file)]
+    files += [os.path.join(csrc, n) for n in sorted(os.listdir(csrc)) if n.endswith(".cuh")]
+    files += [os.path.join(inc, n) for n in sorted(os.listdir(inc)) if n.endswith(".h")]
+    for path in files:
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -602,7 +611,7 @@ def measure_prefill(args, ws):
             "l2": "8 input sets rotated (~250 MB, above L2)",
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_kind": f"{kind} (dense bf16; f16 operands run at the same rate)",
-                         "traffic": traffic_from_profile("prefill_k8v8_2048", kernel_source_sha()),
+                         "traffic": traffic_from_profile("prefill_k8v8_2048", kernel_source_sha("prefill_tc.cu")),
                          "traffic_unit": "DRAM bytes per launch",
                          "algorithmic_flops_per_launch": flops}}
 
@@ -785,7 +794,7 @@ def run_gpu(args, ws, rank):
         # algorithmic bytes are the whole step's
         launch_ms = ms_per_step
         achieved = nb["step"] / (launch_ms * 1e-3) / 1e9
-        sha = kernel_source_sha()
+        sha = kernel_source_sha("decode_mma.cu")
         roof = {"bound": "hbm", "kernel": "decode_split_tc (fused decode step)",
                 "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} (HBM copy)",
@@ -894,44 +903,61 @@ def run_gpu(args, ws, rank):
 
 
 def run_shape(args, rank):
-    """Only the fused decode step on one of the other decode workloads: one
-    cache, `warmup` eager steps, then `steps` timed eager steps (CUDA events).
-    A small, self-contained command for profilers; not a bench line."""
+    """Only the fused decode step on one of the other decode workloads:
+    enough caches of it, rotated step by step, that they do not fit in L2
+    together (one for the paged workload), `warmup` eager steps, then
+    `steps` timed eager steps (CUDA events).  A small, self-contained
+    command for profilers; not a bench line."""
     import fp8_quantized_kv_gb300 as fk
     spec = synth.WORKLOADS[args.shape]
+    if args.group:
+        spec = dataclasses.replace(spec, q_heads=args.group * spec.kv_heads)
     inp = synth.decode_inputs(spec, device="cuda")
     B, Hq, Hkv, D = spec.batch, spec.q_heads, spec.kv_heads, spec.head_dim
     lens64 = inp.seq_lens.to(torch.int64)
     sidx = torch.repeat_interleave(torch.arange(B), lens64).to(torch.int32).cuda()
     pos = torch.cat([torch.arange(int(n)) for n in lens64]).to(torch.int32).cuda()
-    if spec.page_size is None:
-        cache = fk.Fp8KVCache.contiguous(B, Hkv, D, int(lens64.max()), args.dtype)
-    else:
-        cache = fk.Fp8KVCache.paged(inp.page_table, inp.num_pages, Hkv, D, spec.page_size, args.dtype)
-    fk.fp8kv_append(cache, inp.k.contiguous(), inp.v.contiguous(), sidx, pos)
+    caches = []
+    n_caches = 1
+    while len(caches) < n_caches:
+        if spec.page_size is None:
+            cache = fk.Fp8KVCache.contiguous(B, Hkv, D, int(lens64.max()), args.dtype)
+        else:
+            cache = fk.Fp8KVCache.paged(inp.page_table, inp.num_pages, Hkv, D, spec.page_size, args.dtype)
+        fk.fp8kv_append(cache, inp.k.contiguous(), inp.v.contiguous(), sidx, pos)
+        caches.append(cache)
+        if len(caches) == 1:
+            nbytes = sum(t.numel() * t.element_size() for t in (cache.k, cache.v, cache.k_scale, cache.v_scale))
+            n_caches = min(8, -(-L2_BYTES * 2 // nbytes))
     last = (inp.cu_seqlens[1:] - 1).cuda()
     knew, vnew = inp.k[last].contiguous(), inp.v[last].contiguous()
     lens = inp.seq_lens.cuda()
     q = inp.q.contiguous()
     kid = KERNEL_IDS[args.kernel]
-    ws_t = torch.zeros(fk.fp8kv_decode_step_workspace_bytes(cache, Hq, 0, kid), dtype=torch.uint8, device="cuda")
+    wss = [torch.zeros(fk.fp8kv_decode_step_workspace_bytes(c, Hq, 0, kid), dtype=torch.uint8, device="cuda")
+           for c in caches]
     out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
-    for _ in range(args.warmup):
-        fk.fp8kv_decode_step(q, knew, vnew, cache, lens, workspace=ws_t, out=out, kernel=kid)
+
+    def step(i):
+        j = i % len(caches)
+        fk.fp8kv_decode_step(q, knew, vnew, caches[j], lens, workspace=wss[j], out=out, kernel=kid)
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     spacer()
     e0.record()
-    for _ in range(args.steps):
-        fk.fp8kv_decode_step(q, knew, vnew, cache, lens, workspace=ws_t, out=out, kernel=kid)
+    for i in range(args.steps):
+        step(i)
     e1.record()
     torch.cuda.synchronize()
     if fk.fp8kv_get_device_error() != 0:
         raise RuntimeError(f"{args.shape}: device error")
     if rank == 0:
-        print(json.dumps({"shape": args.shape, "cache": args.dtype, "kernel": args.kernel,
+        print(json.dumps({"shape": args.shape, "group": spec.group, "cache": args.dtype, "kernel": args.kernel,
                           "us_per_step": e0.elapsed_time(e1) / args.steps * 1e3, "steps": args.steps,
-                          "note": "eager launches of one cache; a profiling aid, not a bench line"}))
+                          "caches_rotated": len(caches),
+                          "note": "eager launches; a profiling aid, not a bench line"}))
 
 
 def main():

@@ -72,9 +72,10 @@ struct PfTcCfg {
   static constexpr int OPT = kPfKeys * D * 2;                 // f16 V tile [2 atoms][64][128 B]
   static constexpr int POP = kPfRows * kPfKeys * 2;           // f16 P [128 rows][128 B], one per group
   static constexpr int CST = 2 * kPfKeys + 4;                   // floats per buffer: k, v column scales, v max
+  static constexpr int NCOL = 8;                                // column-scale buffers (tile j: j % 8)
   static constexpr int COLS = CST * 4;
   static constexpr int MISC = 4096;
-  static constexpr int BYTES = QOP + NS * STAGE + NOP * OPT + 2 * POP + NOP * COLS + MISC + 1024;
+  static constexpr int BYTES = QOP + NS * STAGE + NOP * OPT + 2 * POP + NCOL * COLS + MISC + 1024;
   static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
@@ -83,14 +84,32 @@ struct PfTcCfg {
 // slot 8*j + {0: TMA issue, 1: QK issue, 2: PV issue, 3: operands ready,
 // 4: softmax has S, 5: P ready}; 1010: epilogue start; 1020/1021: begin/end.
 __device__ unsigned long long g_pf_trace[1024];
+// per CTA (launch order): start, epilogue start, end (globaltimer ns), SM id
+__device__ unsigned long long g_pf_cta[2048][4];
+#define PF_CTA(k, v)                                                                              \
+  do {                                                                                            \
+    const int cl_ = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;              \
+    if (cl_ < 2048) g_pf_cta[cl_][(k)] = (v);                                                     \
+  } while (0)
 #define PF_TRACE(slot)                                                               \
   do {                                                                               \
     if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (slot) < 1024)      \
       g_pf_trace[(slot)] = clock64();                                                \
   } while (0)
+// sub-steps of the softmax of tile 10 (row 0): slots 900 + k
+#define PF_SUB(j, k)                                  \
+  do {                                                \
+    if ((j) == 10 && r == 0) PF_TRACE(900 + (k));     \
+  } while (0)
 #else
 #define PF_TRACE(slot) \
   do {                 \
+  } while (0)
+#define PF_SUB(j, k) \
+  do {               \
+  } while (0)
+#define PF_CTA(k, v) \
+  do {               \
   } while (0)
 #endif
 
@@ -124,8 +143,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   uint8_t* ring = qop + C::QOP;
   uint8_t* vf = ring + C::NS * C::STAGE;          // [NOP] f16 V operand
   uint8_t* pop = vf + C::NOP * C::OPT;            // [group] f16 P operand
-  float* cols = reinterpret_cast<float*>(pop + 2 * C::POP);   // [NOP][k 64 | v 64]
-  uint8_t* misc = reinterpret_cast<uint8_t*>(cols + C::NOP * C::CST);
+  float* cols = reinterpret_cast<float*>(pop + 2 * C::POP);   // [NCOL][k 64 | v 64 | v max]
+  uint8_t* misc = reinterpret_cast<uint8_t*>(cols + C::NCOL * C::CST);
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);        // [NS] codes landed
   uint64_t* empty = full + C::NS;                             // [NS] K read by QK, V converted by the prep warps
   uint64_t* op_full = empty + C::NS;                          // [NOP] f16 V operand + scales ready
@@ -140,6 +159,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   float* m_sh = reinterpret_cast<float*>(misc + 1280);        // [group][128] final reference maxima
   float* l_sh = reinterpret_cast<float*>(misc + 2304);        // [group][128] final row sums
   int* kp_sh = reinterpret_cast<int*>(misc + 256);           // [group][128] final P' exponents
+  uint64_t* cols_full = reinterpret_cast<uint64_t*>(misc + 3328);   // [NCOL] column scales of a tile written
 
   // grid (query head, sequence, query tile), the tile index slowest and
   // reversed: the CTAs with the longest causal ranges launch first
@@ -200,6 +220,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   // ---------------------------------------------------------------- setup
   const int n_first = min(nkv, C::NS);
   if (tid == 0) PF_TRACE(1020);
+#ifdef FP8KV_TRACE
+  if (tid == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    PF_CTA(0, umma::globaltimer_ns());
+    PF_CTA(3, smid);
+  }
+#endif
   if (tid == 0) {
     for (int i = 0; i < C::NS; ++i) {
       umma::mbar_init(&full[i], 1);
@@ -222,6 +250,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
     }
     umma::mbar_init(&drained[0], 1);
     umma::mbar_init(&drained[1], 1);
+    for (int i = 0; i < C::NCOL; ++i) umma::mbar_init(&cols_full[i], 1);
     umma::mbar_fence_init();
   }
   if (warp == 1) {
@@ -364,13 +393,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
     int kp_row = -1000;                             // this row's P' exponent (none yet)
     bool failed = false;
     for (int lj = 0; lj < my_tiles; ++lj) {
-      const int j = 2 * lj + wg, bb = lj & 1, ub = lj >> 1, ob = j % C::NOP;
+      const int j = 2 * lj + wg, bb = lj & 1, ub = lj >> 1, cb = j % C::NCOL;
+      PF_SUB(j, 0);
       bool ok = wait_fast(&s_full[2 * wg + bb], ub & 1, abort_flag);
-      ok = ok && wait_fast(&op_full[ob], (j / C::NOP) & 1, abort_flag);
+      ok = ok && wait_fast(&cols_full[cb], (j / C::NCOL) & 1, abort_flag);
       ok = ok && !*abort_flag;
       if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       umma::fence_after_sync();
       if (r == 0) PF_TRACE(8 * j + 4);
+      PF_SUB(j, 1);
       // the row's 64 scores as pairs (packed two-wide fp32 arithmetic below)
       float2 sv[32];
       {
@@ -386,10 +417,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
       umma::fence_before_sync();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&s_free[2 * wg + bb]);
+      PF_SUB(j, 2);
       // t = S * k_scale * sm_scale * log2(e); the row's 2^kq comes in below
-      const float4* kc4 = reinterpret_cast<const float4*>(cols + ob * C::CST);
+      const float4* kc4 = reinterpret_cast<const float4*>(cols + cb * C::CST);
       const float4* vc4 = kc4 + kPfKeys / 4;
-      const float vmt = cols[ob * C::CST + 2 * kPfKeys];   // largest V scale of the tile
+      const float vmt = cols[cb * C::CST + 2 * kPfKeys];   // largest V scale of the tile
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 kc = kc4[c4];
@@ -404,6 +436,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
           sv[cc].y = t0 + 2 * cc + 1 <= qpos ? sv[cc].y : -INFINITY;
         }
       }
+      PF_SUB(j, 3);
       float m8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -427,6 +460,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
           kp_row = need;
         }
       }
+      PF_SUB(j, 4);
       const int kpr = kp_row > -1000 ? kp_row : 0;
       const float neg_m = (m_used == -INFINITY ? 0.f : -m_used) - (float)kpr;
       const float2 qsr2 = make_float2(qsr, qsr), nm2 = make_float2(neg_m, neg_m);
@@ -450,12 +484,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
       }
       const float l4[4] = {la.x, la.y, lb.x, lb.y};
       l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3])) * pow2i(kpr);
+      PF_SUB(j, 5);
       // this group's previous P.V (tile j-2) must be done before its O is
       // rescaled and before its P buffer is overwritten
       if (lj > 0) {
         const bool done = wait_fast(&pv_done[wg], (lj - 1) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, done)) { failed = true; break; }
       }
+      PF_SUB(j, 6);
       if (__any_sync(0xffffffffu, alpha_o != 1.f && lj > 0)) {
         // O rows whose reference moved are rescaled in TMEM: lane = query
         // row, so each thread scales its own row (alpha 1 elsewhere in the warp)
@@ -475,6 +511,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
         }
         asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
       }
+      PF_SUB(j, 7);
       uint8_t* prow = my_p + r * 128;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8)
@@ -485,6 +522,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&p_full[wg]);
       if (r == 0) PF_TRACE(8 * j + 5);
+      PF_SUB(j, 8);
     }
     m_sh[wg * kPfRows + r] = failed ? -INFINITY : m_used;
     kp_sh[wg * kPfRows + r] = kp_row > -1000 ? kp_row : 0;
@@ -494,6 +532,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
     // either group skips the epilogue in both
     bool any_fail = pair_any(failed);
     if (r == 0 && wg == 0) PF_TRACE(1010);
+#ifdef FP8KV_TRACE
+    if (r == 0 && wg == 0) PF_CTA(1, umma::globaltimer_ns());
+#endif
     const int n0 = (nkv + 1) >> 1, n1 = nkv >> 1;   // tiles of each group
     if (!any_fail) {
       bool ok = n0 == 0 || wait_or_abort(&pv_done[0], (n0 - 1) & 1, abort_flag);
@@ -556,53 +597,37 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   } else if (warp >= 10 && warp < 14) {
     // --------------------------------------------------------- preparation
     // Warp 10 + w prepares tiles j = w, w + 4, ... (f16 operand buffer w):
-    // four tiles in flight, no barrier between the warps.
+    // four tiles in flight, no barrier between the warps.  The tile's V codes
+    // and scales are read into registers first: the column scales go out at
+    // once (the softmax waits only for them) and the ring slot is released
+    // (the next K tile's load waits only for that); the f16 operand is then
+    // written once the buffer's previous P.V has finished.  Column-scale
+    // buffer j % 8 is rewritten for tile j + 8 only after this warp saw the
+    // P.V of tile j finish (its wait for tile j + 4's buffer), so the softmax
+    // of tile j has read it by then.
     static_assert(C::NOP == 4, "one operand buffer per preparation warp");
     const int pw = warp - 10;
     bool failed = false;
     for (int j = pw; j < nkv && !failed; j += 4) {
-      const int s = j % C::NS, u = j / C::NS, ob = j % C::NOP, ou = j / C::NOP;
+      const int s = j % C::NS, u = j / C::NS, ob = j % C::NOP, ou = j / C::NOP, cb = j % C::NCOL;
       bool ok = wait_fast(&full[s], u & 1, abort_flag);
-      if (ou > 0) ok = ok && wait_fast(&op_free[ob], (ou - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       const uint8_t* st = ring + s * C::STAGE;
       const uint8_t* codes = st + C::CODES;
       const float* kss = reinterpret_cast<const float*>(st + 2 * C::CODES);
       const float* vss = kss + kPfKeys;
       const int t0 = j * kPfKeys;
-      uint8_t* dstb = vf + ob * C::OPT;
       // 64 key rows x 8 chunks of 16 codes: lane takes chunk ch = lane & 7 of
-      // rows 4 it + lane / 8; all of a batch's loads before its stores (the
-      // compiler cannot move a load above a store to shared memory)
+      // rows 4 it + lane / 8
+      uint4 w[16];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint4 w[8];
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int kr = 4 * (8 * half + it) + (lane >> 3), ch = lane & 7;
-          w[it] = *reinterpret_cast<const uint4*>(codes + kr * 128 + ((ch ^ (kr & 7)) << 4));
-        }
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int kr = 4 * (8 * half + it) + (lane >> 3), ch = lane & 7;
-          const bool key_ok = t0 + kr < kv_end;
-          uint32_t h[8];
-          const uint32_t ww[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
-#pragma unroll
-          for (int u4 = 0; u4 < 4; ++u4) {
-            h[2 * u4] = key_ok ? e4m3x2_to_f16x2((uint16_t)(ww[u4] & 0xFFFF)) : 0u;
-            h[2 * u4 + 1] = key_ok ? e4m3x2_to_f16x2((uint16_t)(ww[u4] >> 16)) : 0u;
-          }
-          // dims 16 ch .. 16 ch + 15: atom ch / 4, f16 chunks 2 (ch % 4) and +1
-          uint8_t* dst = dstb + (ch >> 2) * (kPfKeys * 128) + kr * 128;
-          const int c0 = 2 * (ch & 3), c1 = c0 + 1;
-          *reinterpret_cast<uint4*>(dst + ((c0 ^ (kr & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4*>(dst + ((c1 ^ (kr & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-        }
+      for (int it = 0; it < 16; ++it) {
+        const int kr = 4 * it + (lane >> 3), ch = lane & 7;
+        w[it] = *reinterpret_cast<const uint4*>(codes + kr * 128 + ((ch ^ (kr & 7)) << 4));
       }
       {
         const float k0 = kss[lane], k1 = kss[lane + 32], v0 = vss[lane], v1 = vss[lane + 32];
-        float* cc2 = cols + ob * C::CST;
+        float* cc2 = cols + cb * C::CST;
         const bool ok0 = t0 + lane < kv_end, ok1 = t0 + lane + 32 < kv_end;
         const float va = ok0 ? v0 : 0.f, vb = ok1 ? v1 : 0.f;
         cc2[lane] = ok0 ? k0 * p.scale_log2 : 0.f;
@@ -612,12 +637,38 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
         const float vm = warp_max(fmaxf(va, vb));
         if (lane == 0) cc2[2 * kPfKeys] = vm;     // the tile's largest V scale
       }
+      __syncwarp();
+      if (lane == 0) {
+        umma::mbar_arrive(&cols_full[cb]);
+        umma::mbar_arrive(&empty[s]);
+      }
+      if (ou > 0) {
+        ok = wait_fast(&op_free[ob], (ou - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+      }
+      uint8_t* dstb = vf + ob * C::OPT;
+#pragma unroll
+      for (int it = 0; it < 16; ++it) {
+        const int kr = 4 * it + (lane >> 3), ch = lane & 7;
+        const bool key_ok = t0 + kr < kv_end;
+        uint32_t h[8];
+        const uint32_t ww[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+          h[2 * u4] = key_ok ? e4m3x2_to_f16x2((uint16_t)(ww[u4] & 0xFFFF)) : 0u;
+          h[2 * u4 + 1] = key_ok ? e4m3x2_to_f16x2((uint16_t)(ww[u4] >> 16)) : 0u;
+        }
+        // dims 16 ch .. 16 ch + 15: atom ch / 4, f16 chunks 2 (ch % 4) and +1
+        uint8_t* dst = dstb + (ch >> 2) * (kPfKeys * 128) + kr * 128;
+        const int c0 = 2 * (ch & 3), c1 = c0 + 1;
+        *reinterpret_cast<uint4*>(dst + ((c0 ^ (kr & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(dst + ((c1 ^ (kr & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+      }
       umma::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         PF_TRACE(8 * j + 3);
         umma::mbar_arrive(&op_full[ob]);
-        umma::mbar_arrive(&empty[s]);
       }
     }
   }
@@ -626,6 +677,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc(const __grid_constan
   umma::fence_after_sync();
   if (warp == 1) umma::tmem_dealloc(tmem, 512);
   if (tid == 0) PF_TRACE(1021);
+#ifdef FP8KV_TRACE
+  if (tid == 0) PF_CTA(2, umma::globaltimer_ns());
+#endif
 }
 
 #ifdef FP8KV_TRACE
@@ -636,6 +690,10 @@ extern "C" __attribute__((visibility("default"))) int fp8kv_trace_clear_prefill(
 extern "C" __attribute__((visibility("default"))) int fp8kv_trace_read_prefill(unsigned long long* out, int n) {
   if (n > 1024) n = 1024;
   return cudaMemcpyFromSymbol(out, g_pf_trace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
+}
+extern "C" __attribute__((visibility("default"))) int fp8kv_trace_read_prefill_cta(unsigned long long* out, int n) {
+  if (n > 2048) n = 2048;
+  return cudaMemcpyFromSymbol(out, g_pf_cta, n * 4 * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
 }
 #endif
 
