@@ -170,3 +170,41 @@ def test_unsupported_dtype_rejected():
         fk.fp8kv_prefill_attention(q, cache, torch.zeros(1, dtype=torch.int32, device="cuda"),
                                    kernel="tensor_cores")
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("page_size", [None, 32])
+def test_several_items_per_cta(page_size):
+    """More (query tile, sequence, query head) work items than SMs, of
+    different lengths and sequences: three sequences with prefixes 0, 129 and
+    700, 400 queries, 16 query heads."""
+    pos0s = [0, 129, 700]
+    cache, q, ks, vs = _build(3, 400, pos0s, 16, 2, seed=73, page_size=page_size)
+    _check(cache, q, ks, vs, pos0s, "tensor_cores")
+
+
+def test_many_items_sampled():
+    """512 work items (1024 queries, 2 sequences, 32 query heads over 4 KV
+    heads): sampled query blocks against the oracle."""
+    pos0s = [0, 300]
+    cache, q, ks, vs = _build(2, 1024, pos0s, 32, 4, seed=79)
+    _check(cache, q, ks, vs, pos0s, "tensor_cores", blocks=[(0, 64), (448, 520), (960, 1024)])
+
+
+def test_invalid_sequence_skipped_others_computed():
+    """A sequence whose prefix runs past the capacity is skipped (length bit
+    raised) while the other sequence's work items stay correct: 256 items, the
+    skipped ones among valid ones."""
+    pos0s = [0, 0]
+    cache, q, ks, vs = _build(2, 256, pos0s, 64, 8, seed=83)
+    bad = [0, cache.max_tokens - 10]
+    out = fk.fp8kv_prefill_attention(q, cache, torch.tensor(bad, dtype=torch.int32, device="cuda"),
+                                     out_dtype=torch.float32, kernel="tensor_cores").cpu().numpy()
+    assert fk.fp8kv_get_device_error() & fk.DEVERR_SEQ_TOO_LONG
+    D = q.shape[-1]
+    kb = synth.bf16_bits(ks[0]).transpose(1, 0, 2)
+    vb = synth.bf16_bits(vs[0]).transpose(1, 0, 2)
+    k = oracle.dequantize(*oracle.quantize(kb))
+    v = oracle.dequantize(*oracle.quantize(vb))
+    qd = oracle.bf16_to_double(synth.bf16_bits(q[0]))
+    ref = oracle.prefill_attention(qd, k[:, :256], v[:, :256], 0, 1 / math.sqrt(D))
+    assert_gate(out[0].reshape(-1, D), ref.reshape(-1, D), "valid sequence beside a skipped one")
