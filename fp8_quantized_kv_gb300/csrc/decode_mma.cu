@@ -311,9 +311,12 @@ __device__ __forceinline__ void k_tile_to_f16(const uint8_t* src, uint8_t* dst, 
   }
 }
 
-template <int KE, int VE, int XK>
+// PG: the instantiation for paged caches whose scale rows the softmax threads
+// load themselves (the native-QK kernels); other paged launches use PG = false.
+template <int KE, int VE, int XK, bool PG>
 __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_constant__ DecodeTmaParams tp) {
   using C = TcCfg<KE, VE, XK>;
+  constexpr bool kOwnSc = PG && (C::K8 || VE == ELEM_E4M3);   // scale rows by the softmax threads
   constexpr int D = 128;
   const DecodeParams& p = tp.p;
   extern __shared__ uint8_t smem_raw[];
@@ -468,12 +471,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
       const int P = c.page_size;
       const int np = (valid + P - 1) / P;
       // The K and V boxes come by TMA (counted in the transaction bytes).
-      // The 64-byte-per-page scale rows come by cp.async: a TMA copy per
-      // scale row doubled the copies per tile, and the paged step was bound
-      // per copy.  Each lane's cp.async.mbarrier.arrive adds one pending
-      // arrival to the stage barrier and completes it when the lane's copies
-      // land; it runs before lane 0's arrival (the barrier's only expected
-      // one), so the phase cannot complete without the scale rows.
+      // The scale rows are loaded by the softmax threads themselves, two of
+      // their tiles ahead (a copy per page and side here cost the producer
+      // more than the rows' bytes), except in the tile that receives the
+      // fused step's new token: its rows come by cp.async after the append,
+      // each lane's cp.async.mbarrier.arrive adding one pending arrival to
+      // the stage barrier that completes when the lane's copies land (before
+      // lane 0's arrival, the barrier's only expected one, so the phase
+      // cannot complete without the scale rows).
       const int PR = P << hs;                      // rows of one page (HPC heads x P tokens)
       const uint32_t per_page = PR * 128 * (C::KB + C::VB);
       int page = pg[0];
@@ -485,13 +490,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
         page = 0;      // read a valid page; the result is flagged as wrong
       }
       const int64_t row = ((int64_t)page * c.kv_heads + hkv0) * P;
-      if (lane < np && (C::K8 || VE == ELEM_E4M3)) {
+      if ((!kOwnSc || i == i_new) && lane < np && (C::K8 || VE == ELEM_E4M3)) {
         for (int q = 0; q < PR / 4; ++q) {
           if (C::K8) cp_async16(kss + lane * PR + 4 * q, c.k_scale + row + 4 * q);
           if (VE == ELEM_E4M3) cp_async16(vss + lane * PR + 4 * q, c.v_scale + row + 4 * q);
         }
         asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" ::"r"(umma::smem_u32(&full[s]))
                      : "memory");
+      }
+      if (kOwnSc && i != i_new && lane < np) {
+        // the softmax threads' scale loads of this tile then hit L2
+        if (C::K8) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(c.k_scale + row));
+        if (VE == ELEM_E4M3) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(c.v_scale + row));
       }
       __syncwarp();
       if (lane == 0) tma::arrive_expect_tx(&full[s], per_page * np);
@@ -847,13 +857,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
     WgBars& B = wb[wg];
     // row t of every tile: token tok of the tile's stretch of KV head hkv0 +
     // hh, whose query heads are the score columns in cmask
-    int tok = t;
+    int tok = t, hh = 0;
     uint32_t cmask = 0xFFu;
     if (HPC > 1) {
       const int ps = c.page_shift;
-      const int hh = (t >> ps) & (HPC - 1);
+      hh = (t >> ps) & (HPC - 1);
       tok = ((t >> (ps + hs)) << ps) | (t & (c.page_size - 1));
       cmask = ((1u << G) - 1u) << (hh * G);
+    }
+    // Paged cache: this thread loads its own token's K and V scale words,
+    // two of the group's tiles ahead (its tile i + 4's page id one tile
+    // before that), so each value is used about one tile after its load was
+    // issued.  Rows past a tile's tokens read a valid row of page 0 and are
+    // masked.  The appended tile's rows come from the stage instead.
+    constexpr bool own_sc = kOwnSc;
+    auto page_raw = [&](int i) -> int {         // raw table entry (checked at use)
+      if (!own_sc || i >= n_tiles) return 0;
+      const int t0 = (t_begin + i) * TT;
+      if (tok >= T - t0) return 0;
+      return __ldg(c.page_table + (int64_t)b * c.max_pages_per_seq + ((t0 + tok) >> c.page_shift));
+    };
+    uint32_t sk_cur = 0, sv_cur = 0, sk_nxt = 0, sv_nxt = 0;
+    auto load_scales = [&](int i, int pid, uint32_t& sk, uint32_t& sv) {
+      if (!own_sc || i >= n_tiles) return;
+      if (pid < 0 || pid >= c.num_pages) pid = 0;   // (the producer flags a bad page)
+      const int t0 = (t_begin + i) * TT;
+      const int64_t row = ((int64_t)pid * c.kv_heads + hkv0 + hh) * c.page_size + ((t0 + tok) & (c.page_size - 1));
+      if (C::K8) sk = __ldg(reinterpret_cast<const uint32_t*>(c.k_scale) + row);
+      if (VE == ELEM_E4M3) sv = __ldg(reinterpret_cast<const uint32_t*>(c.v_scale) + row);
+    };
+    int pid_nx2 = 0;
+    if (own_sc) {
+      const int pa = page_raw(wg), pb = page_raw(wg + 2);
+      load_scales(wg, pa, sk_cur, sv_cur);
+      load_scales(wg + 2, pb, sk_nxt, sv_nxt);
+      pid_nx2 = page_raw(wg + 4);
     }
     float qs[8];
 #pragma unroll
@@ -974,8 +1012,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
         const int t0 = (t_begin + i) * TT;
         const int valid = min(TT, T - t0);
         const bool tok_ok = tok < valid;
-        const float kf = KE == ELEM_E4M3 ? kss[t] : 1.f;     // (MXFP8: block scales applied below)
-        const float vsc = VE == ELEM_E4M3 ? (tok_ok ? vss[t] : 0.f) : 1.f;
+        const bool own = own_sc && i != i_new;             // this thread's scale words, or the stage's
+        const float kf = KE == ELEM_E4M3 ? (own ? __uint_as_float(sk_cur) : kss[t]) : 1.f;   // (MXFP8: below)
+        const float vsc = VE == ELEM_E4M3 ? (tok_ok ? (own ? __uint_as_float(sv_cur) : vss[t]) : 0.f) : 1.f;
         float sc[16];
         {
           uint32_t r[4][16];
@@ -987,7 +1026,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
             // MXFP8 keys: accumulator k holds dims 32k..32k+31 of the dot
             // product, so the key's E8M0 block scale k applies to it here
             // (the block-scaled product, summed over the four blocks)
-            const uint32_t e8 = reinterpret_cast<const uint32_t*>(st + C::K_TILE + C::V_TILE)[t];
+            const uint32_t e8 = own ? sk_cur : reinterpret_cast<const uint32_t*>(st + C::K_TILE + C::V_TILE)[t];
             float w[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) w[k] = pow2_exact((int)((e8 >> (8 * k)) & 0xFF) - 127);
@@ -1091,6 +1130,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
           umma::mbar_arrive(&empty[s]);
         }
         if (t == 0) TRACE(8 * i + 4);
+        if (own_sc) {                       // the scale pipeline moves one group tile on
+          sk_cur = sk_nxt;
+          sv_cur = sv_nxt;
+          load_scales(i + 4, pid_nx2, sk_nxt, sv_nxt);
+          pid_nx2 = page_raw(i + 6);
+        }
         TRACE_SUB(i, 12);
         if (lane == 0) TRACE_MAX(8 * i + 6);
       }
@@ -1342,10 +1387,10 @@ static bool cluster_fits(const void* fn, dim3 grid, int smem) {
   return (long long)max_clusters >= (long long)grid.y * grid.z;
 }
 
-template <int KE, int VE, int XK = XK_NATIVE>
+template <int KE, int VE, int XK = XK_NATIVE, bool PG = false>
 static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st) {
   constexpr int smem = TcCfg<KE, VE, XK>::BYTES;
-  cudaError_t e = ensure_smem_optin((const void*)decode_split_tc<KE, VE, XK>, smem);
+  cudaError_t e = ensure_smem_optin((const void*)decode_split_tc<KE, VE, XK, PG>, smem);
   if (e != cudaSuccess) return e;
   DecodeTmaParams tp;
   const CacheView& c = p.c;
@@ -1358,7 +1403,7 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
     return cudaErrorInvalidValue;
   tp.p = p;
   tp.p.cluster = 0;
-  const void* fn = (const void*)decode_split_tc<KE, VE, XK>;
+  const void* fn = (const void*)decode_split_tc<KE, VE, XK, PG>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kTcThreads);
@@ -1381,7 +1426,7 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  const cudaError_t e2 = cudaLaunchKernelEx(&cfg, decode_split_tc<KE, VE, XK>, tp);
+  const cudaError_t e2 = cudaLaunchKernelEx(&cfg, decode_split_tc<KE, VE, XK, PG>, tp);
   if (e2 != cudaSuccess) (void)cudaGetLastError();
   return e2;
 }
@@ -1404,14 +1449,19 @@ extern "C" __attribute__((visibility("default"))) int fp8kv_trace_read_cta(unsig
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int dtype, int batch, cudaStream_t st) {
   dim3 grid(p.num_splits, p.c.kv_heads / p.hpc, batch);
+  const bool pg = p.c.paged != 0;
   if (dtype == FP8KV_K8V8) {
     if (p.k_f16 == 1) return launch_tc_t<ELEM_E4M3, ELEM_E4M3, XK_CONSUMER>(p, grid, st);
     if (p.k_f16 == 2) return launch_tc_t<ELEM_E4M3, ELEM_E4M3, XK_PRODUCER>(p, grid, st);
-    return launch_tc_t<ELEM_E4M3, ELEM_E4M3>(p, grid, st);
+    return pg ? launch_tc_t<ELEM_E4M3, ELEM_E4M3, XK_NATIVE, true>(p, grid, st)
+              : launch_tc_t<ELEM_E4M3, ELEM_E4M3>(p, grid, st);
   }
-  if (dtype == FP8KV_K16V8) return launch_tc_t<ELEM_BF16, ELEM_E4M3>(p, grid, st);
-  if (dtype == FP8KV_K8V16) return launch_tc_t<ELEM_E4M3, ELEM_BF16>(p, grid, st);
-  if (dtype == FP8KV_MXK8V8) return launch_tc_t<ELEM_MX, ELEM_E4M3>(p, grid, st);
+  if (dtype == FP8KV_K16V8)
+    return pg ? launch_tc_t<ELEM_BF16, ELEM_E4M3, XK_NATIVE, true>(p, grid, st) : launch_tc_t<ELEM_BF16, ELEM_E4M3>(p, grid, st);
+  if (dtype == FP8KV_K8V16)
+    return pg ? launch_tc_t<ELEM_E4M3, ELEM_BF16, XK_NATIVE, true>(p, grid, st) : launch_tc_t<ELEM_E4M3, ELEM_BF16>(p, grid, st);
+  if (dtype == FP8KV_MXK8V8)
+    return pg ? launch_tc_t<ELEM_MX, ELEM_E4M3, XK_NATIVE, true>(p, grid, st) : launch_tc_t<ELEM_MX, ELEM_E4M3>(p, grid, st);
   return launch_tc_t<ELEM_BF16, ELEM_BF16>(p, grid, st);
 }
 
