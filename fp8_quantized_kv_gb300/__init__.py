@@ -59,9 +59,13 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _need(t: torch.Tensor, dtype, name):
-    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
-        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor, got "
+def _need(t: torch.Tensor, dtype, name, host_ok=False):
+    """A contiguous CUDA tensor of `dtype` (or, where host_ok, a contiguous
+    page-locked host tensor, which the kernels address directly)."""
+    where_ok = t.is_cuda or (host_ok and t.is_pinned())
+    if t.dtype != dtype or not where_ok or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor"
+                         f"{' (or pinned host tensor)' if host_ok else ''}, got "
                          f"{t.dtype} on {t.device} (contiguous={t.is_contiguous()})")
 
 
@@ -261,18 +265,23 @@ def fp8kv_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     FP8KV_STEP_EARLY_CACHE_READ (the kernel issued just before on the stream
     must not write this cache or seq_lens)."""
     for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new")):
-        _need(t, torch.bfloat16, n)
-    _need(seq_lens, torch.int32, "seq_lens")
+        _need(t, torch.bfloat16, n, host_ok=True)
+    _need(seq_lens, torch.int32, "seq_lens", host_ok=True)
     B, Hq, D = q.shape
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
+    dev = cache.k.device                   # (q and the others may be pinned host tensors)
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=dev)
+    _need(out, out.dtype, "out", host_ok=True)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"out: expected bf16 or fp32, got {out.dtype}")
     odt = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     k = _kernel(kernel)
     if workspace is None:
         need = fp8kv_decode_step_workspace_bytes(cache, Hq, num_splits, k)
-        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
+    _need(workspace, torch.uint8, "workspace")
     _check(get_lib().fp8kv_decode_step(
         _ptr(q), _ptr(k_new), _ptr(v_new), cache.struct_ref, _ptr(seq_lens), Hq, float(sm_scale),
         num_splits, k, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), odt,

@@ -259,6 +259,11 @@ FP8KV_API fp8kv_status fp8kv_decode_merge(const fp8kv_cache *cache, int32_t q_he
  *                 word stays clear leaves the counters zero again; after a
  *                 timeout, zero the workspace before reusing it.
  *   flags:        0, or FP8KV_STEP_EARLY_CACHE_READ (below).
+ * q, k_new, v_new, seq_lens and out may also point to page-locked host
+ * memory (cudaHostAlloc / cudaMallocHost), which the device addresses at
+ * the same pointer under unified addressing: the kernels then read the
+ * step's inputs and write its output across the host link themselves, with
+ * no copy calls (on GB300 the link is the coherent chip-to-chip one).
  * Other arguments as in fp8kv_decode_attention. */
 FP8KV_API size_t fp8kv_decode_step_workspace_bytes(const fp8kv_cache *cache, int32_t q_heads,
                                                    int32_t num_splits, int32_t kernel);

@@ -163,3 +163,29 @@ def test_step_early_cache_read_matches_plain_launch():
         assert torch.equal(results[False][1][i].k, results[True][1][i].k)
         assert torch.equal(results[False][1][i].v_scale, results[True][1][i].v_scale)
     assert_gate(results[True][0][0].cpu().numpy(), oracle_decode(inp, "k8v8", range(16)), "early cache read")
+
+
+@pytest.mark.parametrize("kernel", ["cuda_cores", "tensor_cores"])
+def test_step_with_pinned_host_buffers(kernel):
+    """q, k_new, v_new, seq_lens and out in page-locked host memory, read and
+    written by the kernels directly: the same output and cache as with device
+    buffers."""
+    spec = synth.DecodeWorkload("host_bufs", 3, 16, 2, 128, seed=37, seq_lens=(700, 129, 1))
+    inp = synth.decode_inputs(spec, device="cuda")
+    results = []
+    for host in (False, True):
+        prev, knew, vnew = _split_last_token(inp)
+        cache = fill_cache(prev, "k8v8", capacity=768)
+        q, lens = inp.q.cuda().contiguous(), inp.seq_lens.cuda()
+        if host:
+            q, knew, vnew, lens = (t.cpu().pin_memory() for t in (q, knew, vnew, lens))
+            out = torch.empty((3, 16, 128), dtype=torch.float32).pin_memory()
+        else:
+            out = torch.empty((3, 16, 128), dtype=torch.float32, device="cuda")
+        fk.fp8kv_decode_step(q, knew, vnew, cache, lens, out=out, kernel=kernel)
+        torch.cuda.synchronize()
+        assert fk.fp8kv_get_device_error() == 0
+        results.append((out.cpu().clone(), cache.k.cpu().clone(), cache.v_scale.cpu().clone()))
+    assert torch.equal(results[0][0], results[1][0])
+    assert torch.equal(results[0][1], results[1][1]) and torch.equal(results[0][2], results[1][2])
+    assert_gate(results[1][0].numpy(), oracle_decode(inp, "k8v8", range(3)), f"host buffers {kernel}")
