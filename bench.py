@@ -940,7 +940,8 @@ def run_shape(args, rank):
         fk.fp8kv_append(cache, inp.k.contiguous(), inp.v.contiguous(), sidx, pos)
         caches.append(cache)
         if len(caches) == 1:
-            nbytes = sum(t.numel() * t.element_size() for t in (cache.k, cache.v, cache.k_scale, cache.v_scale))
+            nbytes = sum(t.numel() * t.element_size() for t in (cache.k, cache.v, cache.k_scale, cache.v_scale)
+                         if t is not None)
             n_caches = min(8, -(-L2_BYTES * 2 // nbytes))
     last = (inp.cu_seqlens[1:] - 1).cuda()
     knew, vnew = inp.k[last].contiguous(), inp.v[last].contiguous()

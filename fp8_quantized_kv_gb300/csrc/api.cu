@@ -3,6 +3,7 @@
 // caller's stream and returns; nothing here allocates device memory.
 #include <atomic>
 #include <cmath>
+#include <cstdint>
 #include <cstring>
 
 #include "params.cuh"
@@ -84,6 +85,11 @@ static fp8kv_status check_cache(const fp8kv_cache* c, CacheView* view) {
     view->page_table = c->page_table;
     view->paged = 1;
   }
+  // cache rows are addressed with 32-bit signed row coordinates
+  const int64_t rows = c->layout == FP8KV_LAYOUT_CONTIGUOUS
+                           ? (int64_t)c->batch * c->kv_heads * c->max_tokens
+                           : (int64_t)c->num_pages * c->kv_heads * c->page_size;
+  if (rows > INT32_MAX) return FP8KV_ERR_UNSUPPORTED;
   view->k = static_cast<const uint8_t*>(c->k);
   view->v = static_cast<const uint8_t*>(c->v);
   view->k_scale = c->k_scale;

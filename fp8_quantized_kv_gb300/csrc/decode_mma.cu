@@ -81,6 +81,9 @@ constexpr int kMergeChunk = 44;
 // warp 0 TMA producer, warp 1 QK issuer and TMEM owner, warps 2-9 softmax,
 // warp 10 PV issuer
 constexpr int kTcThreads = 352;
+// Paged caches: a twelfth warp is a second producer (warps 0 and 11 issue
+// the even and the odd tiles).
+constexpr int kTcThreadsPaged = 384;
 
 // XK: where K is prepared (an ablation).  XK_NATIVE: QK is the native e4m3
 // MMA on the query's e4m3 hi/lo pair.  On the transform path each landed
@@ -106,7 +109,7 @@ struct TcCfg {
   static constexpr int QOP = QHL ? 16 * 128 : 2 * 16 * 128;
   static constexpr int POP = VE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;   // [128 tokens][16 or 32 B]
   static constexpr int XO = 8 * 128 * 4;    // group 1's O handed to group 0
-  static constexpr int MISC = 7936;         // barriers, small tables, cluster receive buffers
+  static constexpr int MISC = 8192;         // barriers, small tables, cluster receive buffers, page-id ring
   static constexpr int BYTES = NST * STAGE + KCV + QOP + 4 * POP + XO + MISC + 1024;
   static_assert(BYTES <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
   static_assert(NST * STAGE + KCV >= (8 * kMergeChunk * D + 2 * 8 * kMergeChunk) * 4,
@@ -314,8 +317,16 @@ __device__ __forceinline__ void k_tile_to_f16(const uint8_t* src, uint8_t* dst, 
 // PG: the instantiation for paged caches whose scale rows the softmax threads
 // load themselves (the native-QK kernels); other paged launches use PG = false.
 template <int KE, int VE, int XK, bool PG>
-__global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_constant__ DecodeTmaParams tp) {
+__global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
+    decode_split_tc(const __grid_constant__ DecodeTmaParams tp) {
   using C = TcCfg<KE, VE, XK>;
+  // Producer warps: on a paged cache each tile takes a copy per page and
+  // side, and one warp's chain of dependent instructions per tile (page
+  // lookup, addresses, copies) was slower than the softmax's pace, so two
+  // warps issue alternate tiles.  Tile i's ring slot is i % NST with NST
+  // even, so each producer's tiles keep to their own slots.
+  constexpr int NPW = PG && XK == XK_NATIVE ? 2 : 1;
+  static_assert(NPW == 1 || C::NST % 2 == 0, "two producers need an even ring");
   constexpr bool kOwnSc = PG && (C::K8 || VE == ELEM_E4M3);   // scale rows by the softmax threads
   constexpr int D = 128;
   const DecodeParams& p = tp.p;
@@ -344,6 +355,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
   float* rx_o = reinterpret_cast<float*>(misc + 2048);     // [sender][dim of this rank's slice][8 heads]
   float* anc0 = reinterpret_cast<float*>(misc + 544);      // [4 slots][4 warps][8 heads]: group 0's anchors
   float* wscr = reinterpret_cast<float*>(misc + 6656);     // [softmax warp][40]: maxima, then fold factors
+  int* pg_ring = reinterpret_cast<int*>(misc + 7936);      // [8 tiles][8 pages]: the producer's page ids
 
   const int split = blockIdx.x, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -434,27 +446,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
   // Paged layout: lane j issues page j's copies (K and V boxes of the HPC
   // heads' rows, which are contiguous in the pool, and their scale rows),
   // lane 0 arms the stage's barrier (the transaction count is signed, so a
-  // copy may land first).  Each lane keeps its page ids of the next
-  // kPageAhead tiles in registers, loaded that many tiles ahead: a table
-  // lookup issued only one tile ahead made every tile wait a full load
-  // latency in the producer, which then set the paged decode's pace.
+  // copy may land first).  Each lane's page ids come kPageAhead tiles ahead
+  // by a 4-byte cp.async into a ring in shared memory (one commit group per
+  // tile), so no register ever holds a pending table load: page ids kept in
+  // registers and shifted down one register per tile made every tile wait
+  // for the previous tile's lookup (a register move waits for its load),
+  // and that latency set the paged decode's pace.
   constexpr int kPageAhead = 4;
-  int pg[kPageAhead];
-  auto page_of = [&](int i) -> int {
-    if (!c.paged || i >= n_tiles) return 0;
-    const int t0 = (t_begin + i) * TT;
-    const int np = (min(TT, T - t0) + c.page_size - 1) / c.page_size;
-    return lane < np ? c.page_table[(int64_t)b * c.max_pages_per_seq + (t0 >> c.page_shift) + lane] : 0;
+  // Paged layout: the producer's per-tile address arithmetic reduced to
+  // shifts and adds on per-CTA constants (pages are a power of two long and
+  // divide the tile's token stretch TT): the producer issues one tile after
+  // another, so its chain of dependent instructions per tile sets the pace.
+  const int pshift = c.page_shift;
+  const int ppt = TT >> pshift;                      // pages of a full tile
+  const int PR = 1 << (pshift + hs);                 // rows of one page (HPC heads x P tokens)
+  const uint32_t per_page = PR * 128 * (C::KB + C::VB);
+  const int pool_rpp = c.kv_heads << pshift;         // pool rows per page, all KV heads
+  const int row_h0 = hkv0 << pshift;                 // row of head hkv0 within its page
+  const int* pt_cta = c.paged ? c.page_table + (int64_t)b * c.max_pages_per_seq + ((t_begin * TT) >> pshift) : nullptr;
+  auto pages_of = [&](int i) -> int {                // pages holding tile i's tokens
+    const int rem = T - (t_begin + i) * TT;
+    return rem >= TT ? ppt : (rem + (1 << pshift) - 1) >> pshift;
+  };
+  // (each producer fetches, and waits for, its own tiles' ids: cp.async
+  // groups are per thread)
+  auto fetch_page = [&](int i) {   // tile i's page ids -> ring slot i & 7; one group
+    if (i < n_tiles && lane < pages_of(i))
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(umma::smem_u32(pg_ring + (i & 7) * 8 + lane)),
+                   "l"(pt_cta + i * ppt + lane)
+                   : "memory");
+    cp_async_commit();
   };
   auto produce = [&](int i) {
     const int s = i % C::NST;
     uint8_t* st = smem + s * C::STAGE;
     float* kss = reinterpret_cast<float*>(st + C::K_TILE + C::V_TILE);
     float* vss = kss + kMmaTile;
-    const int t0 = (t_begin + i) * TT;
-    const int valid = min(TT, T - t0);
     if (!c.paged) {
       if (lane == 0) {
+        const int t0 = (t_begin + i) * TT;
+        const int valid = min(TT, T - t0);
         const int nsc = min(kMmaTile, (valid + 15) & ~15);
         const uint32_t bytes = C::K_TILE + C::V_TILE + (C::K8 ? nsc * 4 : 0) +
                                (VE == ELEM_E4M3 ? nsc * 4 : 0);
@@ -468,8 +499,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
         if (VE == ELEM_E4M3) tma::load_1d(vss, c.v_scale + cont_row0 + t0, nsc * 4, &full[s]);
       }
     } else {
-      const int P = c.page_size;
-      const int np = (valid + P - 1) / P;
       // The K and V boxes come by TMA (counted in the transaction bytes).
       // The scale rows are loaded by the softmax threads themselves, two of
       // their tiles ahead (a copy per page and side here cost the producer
@@ -479,17 +508,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
       // the stage barrier that completes when the lane's copies land (before
       // lane 0's arrival, the barrier's only expected one, so the phase
       // cannot complete without the scale rows).
-      const int PR = P << hs;                      // rows of one page (HPC heads x P tokens)
-      const uint32_t per_page = PR * 128 * (C::KB + C::VB);
-      int page = pg[0];
-#pragma unroll
-      for (int k = 0; k + 1 < kPageAhead; ++k) pg[k] = pg[k + 1];
-      pg[kPageAhead - 1] = page_of(i + kPageAhead);
-      if (lane < np && (page < 0 || page >= c.num_pages)) {
+      const int np = pages_of(i);
+      cp_async_wait<kPageAhead / NPW - 1>();       // tile i's group has landed
+      int page = lane < np ? pg_ring[(i & 7) * 8 + lane] : 0;
+      fetch_page(i + kPageAhead);
+      if (lane < np && (unsigned)page >= (unsigned)c.num_pages) {
         raise_error(p.err, FP8KV_DEVERR_BAD_PAGE);
         page = 0;      // read a valid page; the result is flagged as wrong
       }
-      const int64_t row = ((int64_t)page * c.kv_heads + hkv0) * P;
+      const int row = page * pool_rpp + row_h0;
       if ((!kOwnSc || i == i_new) && lane < np && (C::K8 || VE == ELEM_E4M3)) {
         for (int q = 0; q < PR / 4; ++q) {
           if (C::K8) cp_async16(kss + lane * PR + 4 * q, c.k_scale + row + 4 * q);
@@ -507,11 +534,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
       if (lane == 0) tma::arrive_expect_tx(&full[s], per_page * np);
       if (lane < np) {
         const int off = lane * PR * 128;
-        tma::load_2d(st + off, &tp.tmk, 0, (int)row, &full[s]);
-        if (!C::K8) tma::load_2d(st + kMmaTile * 128 + off, &tp.tmk, 64, (int)row, &full[s]);
-        tma::load_2d(st + C::K_TILE + off, &tp.tmv, 0, (int)row, &full[s]);
+        tma::load_2d(st + off, &tp.tmk, 0, row, &full[s]);
+        if (!C::K8) tma::load_2d(st + kMmaTile * 128 + off, &tp.tmk, 64, row, &full[s]);
+        tma::load_2d(st + C::K_TILE + off, &tp.tmv, 0, row, &full[s]);
         if (VE != ELEM_E4M3)
-          tma::load_2d(st + C::K_TILE + kMmaTile * 128 + off, &tp.tmv, 64, (int)row, &full[s]);
+          tma::load_2d(st + C::K_TILE + kMmaTile * 128 + off, &tp.tmv, 64, row, &full[s]);
       }
     }
     if (lane == 0) TRACE(8 * i + 0);
@@ -527,11 +554,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
     *last_flag = 0;
     umma::mbar_fence_init();
   }
-  if (warp == 0) {
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < kPageAhead; ++k) pg[k] = page_of(k);
-    for (int i = 0; i < n_first; ++i) produce(i);
+  if (warp == 0 || (NPW == 2 && warp == 11)) {
+    const int pw = warp == 0 ? 0 : 1;
+    if (NPW == 2) {
+      // the second producer starts once the ring's barriers exist
+      if (warp == 0) {
+        __syncwarp();
+        asm volatile("bar.arrive 4, 64;\n" ::: "memory");
+      } else {
+        asm volatile("bar.sync 4, 64;\n" ::: "memory");
+      }
+    } else {
+      __syncwarp();
+    }
+    if (c.paged)
+      for (int k = pw; k < kPageAhead; k += NPW) fetch_page(k);
+    for (int i = pw; i < n_first; i += NPW) produce(i);
   }
   if (tid == 0) {
     for (int w = 0; w < 2; ++w)
@@ -680,22 +718,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
     if (lane == 0) umma::mbar_arrive(appended);
   }
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // (the whole warp: lane 0 waits for each stage and the others follow it)
+  if (warp == 0 || (NPW == 2 && warp == 11)) {
+    // ----------------------------------------------------------- producers
+    // (the whole warp: lane 0 waits for each stage and the others follow it;
+    // producer pw issues tiles pw, pw + NPW, ...)
+    const int pw = warp == 0 ? 0 : 1;
     int issued = n_first;
     if constexpr (XK != XK_PRODUCER) {
-      for (int i = n_first; i < n_tiles; ++i) {
+      int i = pw;
+      for (; i < n_tiles; i += NPW) {
+        if (i < n_first) continue;
         const int s = i % C::NST, u = i / C::NST;
         bool ok = true;
         if (lane == 0) {
-          ok = u == 0 || wait_or_abort(&empty[s], (u - 1) & 1, abort_flag);
+          if (i < 100) TRACE(500 + i);
+          ok = u == 0 || wait_fast(&empty[s], (u - 1) & 1, abort_flag);
           ok = ok && (i != i_new || wait_or_abort(appended, 0, abort_flag));
+          if (i < 100) TRACE(400 + i);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         produce(i);
-        ++issued;
       }
+      issued = max(i, n_first);   // this producer's tiles below it are issued
     } else {
       // Transform path: issue tiles as stages free up and convert each
       // landed K tile into the free f16 buffer, whichever is ready first.
@@ -750,9 +794,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
     }
     // Before leaving, let every copy this warp issued land (only an aborted
     // run has copies that nobody waited for).
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
     if (lane == 0) {
       for (int i = max(0, issued - C::NST); i < issued; ++i)
-        (void)umma::mbar_wait(&full[i % C::NST], (i / C::NST) & 1, 100000000ull);
+        if (i % NPW == pw) (void)umma::mbar_wait(&full[i % C::NST], (i / C::NST) & 1, 100000000ull);
       TRACE(1013);
     }
   } else if (warp == 1) {
@@ -1355,7 +1400,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_split_tc(const __grid_co
 // True when every cluster of grid.x CTAs (one per (sequence, KV head)) can
 // be resident at once, so the cluster launch runs in a single wave like the
 // plain launch.  Cached per device, kernel and grid shape.
-static bool cluster_fits(const void* fn, dim3 grid, int smem) {
+static bool cluster_fits(const void* fn, dim3 grid, int smem, int threads) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) { (void)cudaGetLastError(); return false; }
   struct Key { int dev; const void* fn; unsigned x; };
@@ -1369,7 +1414,7 @@ static bool cluster_fits(const void* fn, dim3 grid, int smem) {
   if (max_clusters < 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1405,13 +1450,14 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
   tp.p.cluster = 0;
   const void* fn = (const void*)decode_split_tc<KE, VE, XK, PG>;
   cudaLaunchConfig_t cfg = {};
+  constexpr int threads = PG ? kTcThreadsPaged : kTcThreads;
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   int na = 0;
-  if (p.fused && p.num_splits >= 2 && p.num_splits <= 8 && cluster_fits(fn, grid, smem)) {
+  if (p.fused && p.num_splits >= 2 && p.num_splits <= 8 && cluster_fits(fn, grid, smem, threads)) {
     tp.p.cluster = 1;
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = grid.x;

@@ -31,7 +31,9 @@
  *  - Supported shapes: head_dim 64 or 128; q_heads a multiple of kv_heads with
  *    group size q_heads/kv_heads from 1 to 8 for decode and from 1 to 16 for
  *    prefill; page_size 16, 32 or 64; contiguous capacity max_tokens a
- *    multiple of 16.  Anything else returns FP8KV_ERR_UNSUPPORTED.
+ *    multiple of 16; at most 2^31 - 1 cache rows (batch x kv_heads x
+ *    max_tokens, or num_pages x kv_heads x page_size).  Anything else
+ *    returns FP8KV_ERR_UNSUPPORTED.
  *  - Calls may come from several host threads.  Per-device values (the
  *    device addresses of the library's error word and of the array of
  *    fp8kv_decode_attention_static, kernel attributes) are looked up on the
