@@ -347,14 +347,14 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
   volatile int* last_flag = reinterpret_cast<volatile int*>(tslot + 2);
   uint64_t* kc_full = reinterpret_cast<uint64_t*>(misc + 320);   // [2] transform path: f16 K tile ready
   uint64_t* kc_empty = kc_full + 2;                              // [2] its QK completed
-  float* qscale = reinterpret_cast<float*>(misc + 512);    // [8]
+  float* qscale = reinterpret_cast<float*>(misc + 512);    // [8] query scale x softmax scale (log2 units)
+  float* wscr = reinterpret_cast<float*>(misc + 6656);     // [softmax warp][40]: fold factors
   float* lred = reinterpret_cast<float*>(misc + 1120);     // [wg][4][8]
   float* xml = lred + 64;                                  // [16]: m and l of warpgroup 1
   int* slice_tab = reinterpret_cast<int*>(misc + 1472);    // [9] first four-dim group of each rank
   float* rx_ml = reinterpret_cast<float*>(misc + 1536);    // [sender][m 8 | l 8]
   float* rx_o = reinterpret_cast<float*>(misc + 2048);     // [sender][dim of this rank's slice][8 heads]
   float* anc0 = reinterpret_cast<float*>(misc + 544);      // [4 slots][4 warps][8 heads]: group 0's anchors
-  float* wscr = reinterpret_cast<float*>(misc + 6656);     // [softmax warp][40]: maxima, then fold factors
   int* pg_ring = reinterpret_cast<int*>(misc + 7936);      // [8 tiles][8 pages]: the producer's page ids
 
   const int split = blockIdx.x, b = blockIdx.z;
@@ -624,7 +624,7 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
         int e = 0;
         (void)frexpf(amax, &e);
         const int ex = e - 15;
-        if (lane == 0) qscale[g] = ldexpf(1.0f, ex);
+        if (lane == 0) qscale[g] = ldexpf(1.0f, ex) * p.scale_log2;
 #pragma unroll
         for (int e4 = 0; e4 < 4; ++e4)
           *reinterpret_cast<__half*>(qop + sw128_off(g, (lane * 4 + e4) * 2, 16)) = __float2half_rn(ldexpf(x[e4], -ex));
@@ -632,7 +632,7 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
         float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
         amax = warp_max_redux(amax);
         const int ex = e4m3_row_exp(amax);
-        if (lane == 0) qscale[g] = ldexpf(1.0f, ex);
+        if (lane == 0) qscale[g] = ldexpf(1.0f, ex) * p.scale_log2;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float xs = ldexpf(x[e], -ex);
@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           *reinterpret_cast<__nv_bfloat16*>(qop + sw128_off(g, (lane * 4 + e) * 2, 16)) = __float2bfloat16_rn(x[e]);
-        if (lane == 0) qscale[g] = 1.f;
+        if (lane == 0) qscale[g] = p.scale_log2;
       }
     }
   }
@@ -819,32 +819,35 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
         umma::fence_after_sync();
         const uint32_t ka =
             umma::smem_u32(XK != XK_NATIVE ? kcv + (nq & 1) * (kMmaTile * D * 2) : smem + s * C::STAGE);
-        // four independent accumulators (one per 32-byte k-step) so the
-        // thin MMAs pipeline instead of waiting on each other
+        // One accumulator for the whole dot product (QK runs far enough
+        // ahead of the softmax that the chained k-steps' latency is hidden,
+        // and the softmax then reads 16 columns instead of summing four
+        // accumulators).  MXFP8 keys: one accumulator per 32-dim block, each
+        // scaled by its block's E8M0 byte in the softmax.
         const uint32_t d = tmem + 256 * w + 64 * bb;
         if constexpr (XK != XK_NATIVE) {
           constexpr uint32_t ID_F16 =
               umma::idesc(umma::FMT_F16, umma::FMT_F16, umma::MAJOR_K, umma::MAJOR_K, 128, 16);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma::mma_f16_ss(d + 16 * (k & 3),
+            umma::mma_f16_ss(d,
                              umma::sdesc(ka + (k >> 2) * (kMmaTile * 128) + (k & 3) * 32, 16, 1024,
                                          umma::SWIZZLE_128B),
                              umma::sdesc(qa + (k >> 2) * (16 * 128) + (k & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
-                             ID_F16, k >= 4);
+                             ID_F16, k > 0);
         } else if constexpr (C::K8) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma::mma_f8_ss(d + 16 * k, umma::sdesc(ka + k * 32, 16, 1024, umma::SWIZZLE_128B),
-                            umma::sdesc(qa + k * 32, 16, 1024, umma::SWIZZLE_128B), ID_QK, 0);
+            umma::mma_f8_ss(C::KMX ? d + 16 * k : d, umma::sdesc(ka + k * 32, 16, 1024, umma::SWIZZLE_128B),
+                            umma::sdesc(qa + k * 32, 16, 1024, umma::SWIZZLE_128B), ID_QK, !C::KMX && k > 0);
         } else {
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma::mma_f16_ss(d + 16 * (k & 3),
+            umma::mma_f16_ss(d,
                              umma::sdesc(ka + (k >> 2) * (kMmaTile * 128) + (k & 3) * 32, 16, 1024,
                                          umma::SWIZZLE_128B),
                              umma::sdesc(qa + (k >> 2) * (16 * 128) + (k & 3) * 32, 16, 1024, umma::SWIZZLE_128B),
-                             ID_QK, k >= 4);
+                             ID_QK, k > 0);
         }
         umma::mma_commit(&wb[w].s_full[bb]);
         if (XK == XK_PRODUCER) umma::mma_commit(&kc_empty[nq & 1]);
@@ -938,9 +941,6 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
       load_scales(wg + 2, pb, sk_nxt, sv_nxt);
       pid_nx2 = page_raw(wg + 4);
     }
-    float qs[8];
-#pragma unroll
-    for (int g = 0; g < 8; ++g) qs[g] = qscale[g] * p.scale_log2;
     // Anchors.  The tokens one warp holds of a tile are referenced to the
     // integer-valued U = ceil(max of s + log2(v_scale)) over them (log2
     // units; for a bf16 V side, of s): p = 2^(s - U), and P' = bf16(p *
@@ -951,9 +951,11 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
     // or nearly so.)  U depends on the tile alone, so split and unsplit runs
     // round P' alike, and every fold factor is an exact power of two.
     //   m_w: this warp's running anchor per head (reference of its threads'
-    //        partial sums l_thr), tracked by the four lanes of that head;
+    //        partial sums l_thr);
     //   m_o: the group's running anchor over its four warps (reference of
-    //        O), tracked per head by the lanes that fold that head.
+    //        O).
+    // Every lane keeps m_w for all eight heads (the warp maxima come from
+    // redux.sync); m_o of head g is tracked by the lanes that fold it.
     // No barrier across the group's warps inside the loop: each warp's P'
     // columns feed their own PV k-step accumulator (tokens 32w..32w+31),
     // and the O fold weights accumulator w with warp w's published anchor.
@@ -961,12 +963,14 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
     float l_thr[8], o_run[8];
 #pragma unroll
     for (int g = 0; g < 8; ++g) { l_thr[g] = 0.f; o_run[g] = 0.f; }
-    float m_wl = -INFINITY;                          // m_w of head (lane >> 2) & 7
+    float m_w[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) m_w[g] = -INFINITY;
     float m_ol = -INFINITY;                          // m_o of head lane & 7
+    float* wsc = wscr + (warp - 2) * 40;
     // published anchors, [4 slots][4 warps][8 heads]; group 1's table shares
     // the buffer that hands its O to group 0 once its loop is over
     float* ancA = wg == 0 ? anc0 : xo;
-    float* wsc = wscr + (warp - 2) * 40;
     bool failed = false;
     const int nl = (n_tiles - wg + 1) / 2;          // tiles of this group
     // iteration li: the O fold of the group's tile li-2 (its PV finished
@@ -1062,9 +1066,10 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
         const float vsc = VE == ELEM_E4M3 ? (tok_ok ? (own ? __uint_as_float(sv_cur) : vss[t]) : 0.f) : 1.f;
         float sc[16];
         {
-          uint32_t r[4][16];
+          constexpr int NACC = C::KMX ? 4 : 1;
+          uint32_t r[NACC][16];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) umma::tmem_ld16_nowait(tmem + s_col + 64 * bb + 16 * k + lane_off, r[k]);
+          for (int k = 0; k < NACC; ++k) umma::tmem_ld16_nowait(tmem + s_col + 64 * bb + 16 * k + lane_off, r[k]);
           umma::tmem_wait_ld();
           TRACE_SUB(i, 6);
           if constexpr (C::KMX) {
@@ -1081,9 +1086,7 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
                       (w[2] * __uint_as_float(r[2][j]) + w[3] * __uint_as_float(r[3][j]));
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              sc[j] = (__uint_as_float(r[0][j]) + __uint_as_float(r[1][j])) +
-                      (__uint_as_float(r[2][j]) + __uint_as_float(r[3][j]));
+            for (int j = 0; j < 16; ++j) sc[j] = __uint_as_float(r[0][j]);
           }
         }
         umma::fence_before_sync();
@@ -1091,34 +1094,31 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
         if (lane == 0) umma::mbar_arrive(&B.s_empty[bb]);
         // scores (log2 units) and s + log2(v_scale)
         const float lvs = VE == ELEM_E4M3 ? fmaxf(lg2_approx(vsc), -100.f) : 0.f;
+        float qsc[8];                      // (re-read each tile: registers are scarce)
+        {
+          const float4 x = reinterpret_cast<const float4*>(qscale)[0], y = reinterpret_cast<const float4*>(qscale)[1];
+          qsc[0] = x.x; qsc[1] = x.y; qsc[2] = x.z; qsc[3] = x.w;
+          qsc[4] = y.x; qsc[5] = y.y; qsc[6] = y.z; qsc[7] = y.w;
+        }
         float sg[8], uu[8];
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const float raw = C::QHL ? (sc[g] + sc[g + 8]) : sc[g];
-          sg[g] = tok_ok && ((cmask >> g) & 1u) ? raw * (qs[g] * kf) : -INFINITY;
+          sg[g] = tok_ok && ((cmask >> g) & 1u) ? raw * (qsc[g] * kf) : -INFINITY;
           uu[g] = sg[g] + lvs;
         }
         TRACE_SUB(i, 7);
-        // per head, by the four lanes that end up holding its warp maximum:
-        // the anchor U, and the factors that bring the threads' l sums to
-        // the new running anchor; broadcast through the warp's own row
-        {
-          const float U = ceilf(warp_max_transposed<8>(uu, lane));   // head (lane >> 2) & 7
-          const float mn = fmaxf(m_wl, U);
-          if ((lane & 3) == 0)
-            *reinterpret_cast<float4*>(wsc + lane) =
-                make_float4(U, pow2_diff(m_wl - mn, 0), pow2_diff(U - mn, 0), 0.f);
-          m_wl = mn;
-        }
-        __syncwarp();
+        // per head: the anchor U (the warp maximum, in every lane), and the
+        // factors that bring the threads' l sums to the new running anchor
         float Uh[8], f1[8], f2[8];
-        {
-          const float4* w4 = reinterpret_cast<const float4*>(wsc);
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const float4 x = w4[g];
-            Uh[g] = x.x; f1[g] = x.y; f2[g] = x.z;
-          }
+        for (int g = 0; g < 8; ++g) Uh[g] = ceilf(warp_max_f32(uu[g]));
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const float mn = fmaxf(m_w[g], Uh[g]);
+          f1[g] = pow2_diff(m_w[g] - mn, 0);
+          f2[g] = pow2_diff(Uh[g] - mn, 0);
+          m_w[g] = mn;
         }
         TRACE_SUB(i, 8);
         if (!tok_ok) {      // V rows past the sequence end: zero them for PV
@@ -1199,9 +1199,12 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
     // l: each warp's sums (reference m_w) by a transposed butterfly, one
     // head per four lanes, brought to the group's m_o: lred[wg][warp][head]
     {
+      // (each thread's sums brought to m_o first: an exact power-of-two
+      // scaling, so the order does not change the result)
+#pragma unroll
+      for (int g = 0; g < 8; ++g) l_thr[g] *= pow2_diff(m_w[g] - m_run[g], 0);
       const float ws = warp_sum_transposed<8>(l_thr, lane);           // head (lane >> 2) & 7
-      const float mo = __shfl_sync(0xffffffffu, m_ol, (lane >> 2) & 7);
-      if ((lane & 3) == 0) lred[(wg * 4 + sw) * 8 + (lane >> 2)] = failed ? 0.f : ws * pow2_diff(m_wl - mo, 0);
+      if ((lane & 3) == 0) lred[(wg * 4 + sw) * 8 + (lane >> 2)] = failed ? 0.f : ws;
     }
     if (t == 0 && wg == 0) TRACE(1010);
     // The two groups' running states are merged like two splits: group 1

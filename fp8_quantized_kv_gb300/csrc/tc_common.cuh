@@ -55,6 +55,13 @@ __device__ __forceinline__ float warp_max_redux(float x) {
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(x));
   return r;
 }
+// The same maximum as a pure function, so that several independent ones
+// can be scheduled back to back.
+__device__ __forceinline__ float warp_max_f32(float x) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(x));
+  return r;
+}
 // Maxima (or sums) of N = 8 or 16 values over the 32 lanes of a warp,
 // transposed: lane L returns the maximum (sum) over all lanes of v[idx], idx
 // = (L >> (5 - log2 N)) & (N - 1).  Each butterfly step sends half of the values still held, so the
