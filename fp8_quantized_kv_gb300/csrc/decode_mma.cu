@@ -919,18 +919,20 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
     // issued.  Rows past a tile's tokens read a valid row of page 0 and are
     // masked.  The appended tile's rows come from the stage instead.
     constexpr bool own_sc = kOwnSc;
+    // (the page of this thread's token within a tile, and its row within the
+    // page's block of the pool: tiles start on page boundaries)
+    const int tok_page = tok >> pshift;
+    const int row_thr = ((hkv0 + hh) << pshift) + (tok & ((1 << pshift) - 1));
     auto page_raw = [&](int i) -> int {         // raw table entry (checked at use)
       if (!own_sc || i >= n_tiles) return 0;
-      const int t0 = (t_begin + i) * TT;
-      if (tok >= T - t0) return 0;
-      return __ldg(c.page_table + (int64_t)b * c.max_pages_per_seq + ((t0 + tok) >> c.page_shift));
+      if (tok >= T - (t_begin + i) * TT) return 0;
+      return __ldg(pt_cta + i * ppt + tok_page);
     };
     uint32_t sk_cur = 0, sv_cur = 0, sk_nxt = 0, sv_nxt = 0;
     auto load_scales = [&](int i, int pid, uint32_t& sk, uint32_t& sv) {
       if (!own_sc || i >= n_tiles) return;
-      if (pid < 0 || pid >= c.num_pages) pid = 0;   // (the producer flags a bad page)
-      const int t0 = (t_begin + i) * TT;
-      const int64_t row = ((int64_t)pid * c.kv_heads + hkv0 + hh) * c.page_size + ((t0 + tok) & (c.page_size - 1));
+      if ((unsigned)pid >= (unsigned)c.num_pages) pid = 0;   // (the producer flags a bad page)
+      const int row = pid * pool_rpp + row_thr;
       if (C::K8) sk = __ldg(reinterpret_cast<const uint32_t*>(c.k_scale) + row);
       if (VE == ELEM_E4M3) sv = __ldg(reinterpret_cast<const uint32_t*>(c.v_scale) + row);
     };
