@@ -920,19 +920,29 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
     // masked.  The appended tile's rows come from the stage instead.
     constexpr bool own_sc = kOwnSc;
     // (the page of this thread's token within a tile, and its row within the
-    // page's block of the pool: tiles start on page boundaries)
+    // page's block of the pool: tiles start on page boundaries.  Kept as
+    // per-thread constants, except for MXFP8 keys, whose four block
+    // accumulators leave no registers for them: measured 8% slower there.)
     const int tok_page = tok >> pshift;
     const int row_thr = ((hkv0 + hh) << pshift) + (tok & ((1 << pshift) - 1));
     auto page_raw = [&](int i) -> int {         // raw table entry (checked at use)
       if (!own_sc || i >= n_tiles) return 0;
-      if (tok >= T - (t_begin + i) * TT) return 0;
-      return __ldg(pt_cta + i * ppt + tok_page);
+      const int t0 = (t_begin + i) * TT;
+      if (tok >= T - t0) return 0;
+      if constexpr (C::KMX)
+        return __ldg(c.page_table + (int64_t)b * c.max_pages_per_seq + ((t0 + tok) >> c.page_shift));
+      else
+        return __ldg(pt_cta + i * ppt + tok_page);
     };
     uint32_t sk_cur = 0, sv_cur = 0, sk_nxt = 0, sv_nxt = 0;
     auto load_scales = [&](int i, int pid, uint32_t& sk, uint32_t& sv) {
       if (!own_sc || i >= n_tiles) return;
       if ((unsigned)pid >= (unsigned)c.num_pages) pid = 0;   // (the producer flags a bad page)
-      const int row = pid * pool_rpp + row_thr;
+      int64_t row;
+      if constexpr (C::KMX)
+        row = ((int64_t)pid * c.kv_heads + hkv0 + hh) * c.page_size + (((t_begin + i) * TT + tok) & (c.page_size - 1));
+      else
+        row = pid * pool_rpp + row_thr;
       if (C::K8) sk = __ldg(reinterpret_cast<const uint32_t*>(c.k_scale) + row);
       if (VE == ELEM_E4M3) sv = __ldg(reinterpret_cast<const uint32_t*>(c.v_scale) + row);
     };
