@@ -119,11 +119,14 @@ struct SplitPlan { int splits, chunk_tiles, tile, kernel; };
 static int resolve_kernel(const fp8kv_cache* c, int q_heads, int requested) {
   const int G = q_heads / c->kv_heads;
   const bool mma_ok = c->head_dim == 128 && G >= 1 && G <= 8;
-  // MXFP8 keys: the tensor-core kernel only (its QK already keeps one
-  // accumulator per 32-dim block, where the block scales apply)
-  if (c->dtype == FP8KV_MXK8V8)
-    return (requested == FP8KV_KERNEL_AUTO || requested == FP8KV_KERNEL_TENSOR_CORES) && mma_ok
-               ? FP8KV_KERNEL_TENSOR_CORES : 0;
+  // MXFP8 keys: both kernels apply each 32-dim block's scale to its partial
+  // dot product; the transform paths (f16 K tiles) are not built for them
+  if (c->dtype == FP8KV_MXK8V8) {
+    if (requested == FP8KV_KERNEL_CUDA_CORES) return FP8KV_KERNEL_CUDA_CORES;
+    if (requested == FP8KV_KERNEL_TENSOR_CORES) return mma_ok ? FP8KV_KERNEL_TENSOR_CORES : 0;
+    if (requested == FP8KV_KERNEL_AUTO) return mma_ok ? FP8KV_KERNEL_TENSOR_CORES : FP8KV_KERNEL_CUDA_CORES;
+    return 0;
+  }
   if (requested == FP8KV_KERNEL_TENSOR_CORES) return mma_ok ? FP8KV_KERNEL_TENSOR_CORES : 0;
   if (requested == FP8KV_KERNEL_TENSOR_CORES_K_F16 || requested == FP8KV_KERNEL_TENSOR_CORES_K_F16_PRODUCER)
     return mma_ok && c->dtype == FP8KV_K8V8 ? requested : 0;
@@ -397,7 +400,6 @@ fp8kv_status fp8kv_prefill_attention(const void* q, const fp8kv_cache* cache, co
   if (!std::isfinite(sm_scale)) return FP8KV_ERR_INVALID_ARG;
   if (q_heads / cache->kv_heads > 16) return FP8KV_ERR_UNSUPPORTED;
   if (kernel < FP8KV_KERNEL_AUTO || kernel > FP8KV_KERNEL_TENSOR_CORES) return FP8KV_ERR_INVALID_ARG;
-  if (cache->dtype == FP8KV_MXK8V8) return FP8KV_ERR_UNSUPPORTED;     // decode only
   const bool tc_built = cache->dtype == FP8KV_K8V8 && cache->head_dim == 128;
   if (kernel == FP8KV_KERNEL_TENSOR_CORES && !tc_built) return FP8KV_ERR_UNSUPPORTED;
   const bool use_tc = kernel == FP8KV_KERNEL_TENSOR_CORES || (kernel == FP8KV_KERNEL_AUTO && tc_built);

@@ -9,7 +9,8 @@
 //
 // Per tile ("FP8 KV attention: hardware paths and tile preparation", section
 // "Operating model": K load -> K prep -> QK -> softmax; V load -> V prep -> PV):
-//   s_j   = (q . kcode_j) * k_scale_j * sm_scale          (K scale folded into s)
+//   s_j   = (q . kcode_j) * k_scale_j * sm_scale          (K scale folded into s;
+//           MXFP8 keys: each 32-dim block's partial dot times its E8M0 scale)
 //   m_t   = max_j s_j over the tile,   p_j = exp(s_j - m_t)
 //   p'_j  = bf16_rn(p_j * v_scale_j)                        (V scale folded into P)
 //   O     = O * e^(m - m') + e^(m_t - m') * sum_j p'_j vcode_j,   l likewise with p_j
@@ -36,7 +37,7 @@ namespace fp8kv {
 
 template <int D, int KE, int VE>
 struct FmaCfg {
-  static constexpr int KB = KE == ELEM_E4M3 ? 1 : 2;
+  static constexpr int KB = KE == ELEM_BF16 ? 2 : 1;
   static constexpr int VB = VE == ELEM_E4M3 ? 1 : 2;
   static constexpr int K_ROW = D * KB, V_ROW = D * VB;     // bytes per row
   static constexpr int K_CPR = K_ROW / 16, V_CPR = V_ROW / 16;
@@ -179,21 +180,26 @@ __global__ void __launch_bounds__(128) decode_split_fma(DecodeParams p) {
 
     // ---- QK on the CUDA cores: thread (j, hf) covers half of token j's row
     float dot[GP];
+    constexpr int HCH = C::K_CPR / 2;                    // 16-byte chunks per half row
+    constexpr int NBL = KE == ELEM_MX ? HCH / 2 : 1;     // MXFP8: 32-dim blocks per half row
+    float dotb[GP][NBL];
 #pragma unroll
-    for (int g = 0; g < GP; ++g) dot[g] = 0.f;
+    for (int g = 0; g < GP; ++g)
+#pragma unroll
+      for (int lb = 0; lb < NBL; ++lb) dotb[g][lb] = 0.f;
     {
       const uint8_t* krow = ks + j * C::K_ROW;
-      constexpr int HCH = C::K_CPR / 2;
 #pragma unroll
       for (int cc = 0; cc < HCH; ++cc) {
         const int ch = hf * HCH + cc;
         const uint4 w = *reinterpret_cast<const uint4*>(krow + swz_chunk(ch, j, C::K_CPR) * 16);
         const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-        constexpr int EPW = KE == ELEM_E4M3 ? 4 : 2;      // elements per 32-bit word
+        constexpr int EPW = KE == ELEM_BF16 ? 2 : 4;      // elements per 32-bit word
+        const int lb = KE == ELEM_MX ? cc >> 1 : 0;       // two chunks per MXFP8 block
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
           float f[4];
-          if constexpr (KE == ELEM_E4M3) {
+          if constexpr (KE != ELEM_BF16) {
             e4m3x4_to_f32_scaled(wv[wi], f);
           } else {
             float f2[2];
@@ -204,20 +210,36 @@ __global__ void __launch_bounds__(128) decode_split_fma(DecodeParams p) {
 #pragma unroll
           for (int g = 0; g < GP; ++g) {
             const float* qg = q_s + g * C::QS + q_off(d0, D);
+            float& dg = dotb[g][lb];
             if constexpr (EPW == 4) {
               const float4 qv = *reinterpret_cast<const float4*>(qg);
-              dot[g] = fmaf(qv.x, f[0], dot[g]);
-              dot[g] = fmaf(qv.y, f[1], dot[g]);
-              dot[g] = fmaf(qv.z, f[2], dot[g]);
-              dot[g] = fmaf(qv.w, f[3], dot[g]);
+              dg = fmaf(qv.x, f[0], dg);
+              dg = fmaf(qv.y, f[1], dg);
+              dg = fmaf(qv.z, f[2], dg);
+              dg = fmaf(qv.w, f[3], dg);
             } else {
               const float2 qv = *reinterpret_cast<const float2*>(qg);
-              dot[g] = fmaf(qv.x, f[0], dot[g]);
-              dot[g] = fmaf(qv.y, f[1], dot[g]);
+              dg = fmaf(qv.x, f[0], dg);
+              dg = fmaf(qv.y, f[1], dg);
             }
           }
         }
       }
+    }
+    if constexpr (KE == ELEM_MX) {
+      // the row's E8M0 bytes (block k in byte k): this half's blocks weighted
+      const uint32_t e8 = reinterpret_cast<const uint32_t*>(kss)[j];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        float d = 0.f;
+#pragma unroll
+        for (int lb = 0; lb < NBL; ++lb)
+          d = fmaf(dotb[g][lb], pow2_exact((int)((e8 >> (8 * (hf * NBL + lb))) & 0xFF) - 127), d);
+        dot[g] = d;
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < GP; ++g) dot[g] = dotb[g][0];
     }
     const bool valid = j < nvalid;
     const float kfac = (KE == ELEM_E4M3 ? kss[j] : 1.f) * p.scale_log2;
@@ -225,7 +247,7 @@ __global__ void __launch_bounds__(128) decode_split_fma(DecodeParams p) {
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
       float d2 = dot[g] + __shfl_xor_sync(0xffffffffu, dot[g], 1);
-      if (KE == ELEM_E4M3) d2 *= kTwoPow120;
+      if (KE != ELEM_BF16) d2 *= kTwoPow120;
       sc[g] = valid ? d2 * kfac : -INFINITY;
       const float wm = warp_max(sc[g]);
       if (lane == 0) red_max[warp * GP + g] = wm;
@@ -416,6 +438,8 @@ static cudaError_t launch_fma_g(const DecodeParams& p, dim3 grid, cudaStream_t s
 
 template <int D>
 static cudaError_t launch_fma_d(const DecodeParams& p, int dtype, dim3 grid, cudaStream_t st) {
+  if constexpr (D == 128)     // (MXFP8 keys are built for head_dim 128)
+    if (dtype == FP8KV_MXK8V8) return launch_fma_g<D, ELEM_MX, ELEM_E4M3>(p, grid, st);
   if (dtype == FP8KV_K8V8) return launch_fma_g<D, ELEM_E4M3, ELEM_E4M3>(p, grid, st);
   if (dtype == FP8KV_K16V8) return launch_fma_g<D, ELEM_BF16, ELEM_E4M3>(p, grid, st);
   if (dtype == FP8KV_K8V16) return launch_fma_g<D, ELEM_E4M3, ELEM_BF16>(p, grid, st);

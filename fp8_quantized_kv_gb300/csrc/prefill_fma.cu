@@ -14,7 +14,8 @@
 // 256 threads: thread t owns query row r = t/4 and a quarter (t%4) of the
 // tile's columns for QK and softmax, and the dims d = (t%4) + 4i for PV.
 // K and V codes are converted on the fly into fp32 shared-memory tiles (code
-// values, the per-token scales applied as above).
+// values, the per-token scales applied as above; MXFP8 keys with their block
+// scales applied at the conversion).
 #include "params.cuh"
 
 namespace fp8kv {
@@ -84,6 +85,13 @@ __global__ void __launch_bounds__(256) prefill_fma(PrefillParams p) {
             float f[4];
             e4m3x4_to_f32_scaled((uint32_t)c.k[row * D + d], f);
             kvv = f[0];
+          } else if constexpr (KE == ELEM_MX) {
+            // MXFP8 key: the code's value times its 32-dim block's E8M0
+            // scale (byte d / 32 of the row's scale word), exact in fp32
+            float f[4];
+            e4m3x4_to_f32_scaled((uint32_t)c.k[row * D + d], f);
+            const uint32_t e8 = reinterpret_cast<const uint32_t*>(c.k_scale)[row];
+            kvv = (f[0] * kTwoPow120) * pow2_exact((int)((e8 >> (8 * (d >> 5))) & 0xFF) - 127);
           } else {
             kvv = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(c.k)[row * D + d]);
           }
@@ -185,6 +193,8 @@ static cudaError_t launch_pf(const PrefillParams& p, dim3 grid, cudaStream_t st)
 
 template <int D>
 static cudaError_t launch_pf_d(const PrefillParams& p, int dtype, dim3 grid, cudaStream_t st) {
+  if constexpr (D == 128)     // (MXFP8 keys are built for head_dim 128)
+    if (dtype == FP8KV_MXK8V8) return launch_pf<D, ELEM_MX, ELEM_E4M3>(p, grid, st);
   if (dtype == FP8KV_K8V8) return launch_pf<D, ELEM_E4M3, ELEM_E4M3>(p, grid, st);
   if (dtype == FP8KV_K16V8) return launch_pf<D, ELEM_BF16, ELEM_E4M3>(p, grid, st);
   if (dtype == FP8KV_K8V16) return launch_pf<D, ELEM_E4M3, ELEM_BF16>(p, grid, st);

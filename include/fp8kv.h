@@ -80,9 +80,11 @@ typedef enum {
   /* K as MXFP8: e4m3 codes with one E8M0 (power-of-two) scale per 32-dim
    * block, the four block bytes of a row in its 4-byte k_scale slot (byte b
    * = dims 32b..32b+31), as fp8kv_quantize_mx writes them; V codes with an
-   * fp32 scale per row.  head_dim 128 and the tensor-core decode only
-   * ("FP8 KV attention: hardware paths and tile preparation", section
-   * "Measure block-scaled QK"). */
+   * fp32 scale per row.  head_dim 128 only.  Every kernel weights each
+   * block's partial dot product by its scale: the decode on both kernels
+   * and the CUDA-core prefill; the transform paths and the tensor-core
+   * prefill return FP8KV_ERR_UNSUPPORTED ("FP8 KV attention: hardware paths
+   * and tile preparation", section "Measure block-scaled QK"). */
   FP8KV_MXK8V8 = 4
 } fp8kv_kv_dtype;
 
@@ -326,8 +328,8 @@ FP8KV_API size_t fp8kv_decode_static_scratch_bytes(void);
  *   q_pos0: [batch] int32 device array
  *   kernel: FP8KV_KERNEL_* -- TENSOR_CORES (128-query tiles on tcgen05, K8V8
  *           with head_dim 128 only, else FP8KV_ERR_UNSUPPORTED),
- *           CUDA_CORES (64-query tiles, every dtype), AUTO (tensor cores
- *           where built)
+ *           CUDA_CORES (64-query tiles, every dtype, MXFP8 keys included),
+ *           AUTO (tensor cores where built)
  *   out:    [batch][n_q][q_heads][head_dim], bf16 or fp32 per out_dtype */
 FP8KV_API fp8kv_status fp8kv_prefill_attention(const void *q, const fp8kv_cache *cache,
                                      const int32_t *q_pos0, int32_t n_q,

@@ -105,17 +105,22 @@ def test_cache_dtype_and_scale_pointers(lib):
     assert lib.fp8kv_decode_num_splits(r(_cache(dtype=-1)), 16, 64, 2) == 0
 
 
-def test_mxfp8_cache_is_tensor_core_decode_only(lib):
+def test_mxfp8_kernel_choice(lib):
+    # MXFP8 keys: AUTO picks the tensor cores; the CUDA-core decode is built
+    # too (planned like any CUDA-core decode); the transform paths and the
+    # tensor-core prefill are not; head_dim 128 only
     r = ctypes.byref
     mx = _cache(dtype=4)
     assert lib.fp8kv_decode_num_splits(r(mx), 16, 0, 0) == lib.fp8kv_decode_num_splits(r(_cache()), 16, 0, 2)
     assert lib.fp8kv_decode_num_splits(r(mx), 16, 0, 2) > 0
-    for kid in (1, 3, 4):                        # CUDA cores, transform paths
+    assert lib.fp8kv_decode_num_splits(r(mx), 16, 0, 1) == lib.fp8kv_decode_num_splits(r(_cache()), 16, 0, 1) > 0
+    for kid in (3, 4):                           # transform paths
         assert lib.fp8kv_decode_num_splits(r(mx), 16, 0, kid) == 0
-    assert lib.fp8kv_decode_split(None, r(mx), None, 16, 0.1, 0, 1, None, 0, None) == 2
+    assert lib.fp8kv_decode_split(None, r(mx), None, 16, 0.1, 0, 3, None, 0, None) == 2
+    assert lib.fp8kv_decode_split(None, r(mx), None, 16, 0.1, 0, 1, None, 0, None) == 1   # null pointers
     assert lib.fp8kv_decode_num_splits(r(_cache(dtype=4, head_dim=64)), 16, 0, 0) == 0
     out = 0x6000
-    assert lib.fp8kv_prefill_attention(0x7000, r(mx), 0x8000, 64, 16, 0.1, 0, out, 0, None) == 2
+    assert lib.fp8kv_prefill_attention(0x7000, r(mx), 0x8000, 64, 16, 0.1, 2, out, 0, None) == 2
     # the standalone MX quantiser checks its arguments on the host
     assert lib.fp8kv_quantize_mx(None, -1, 128, None, None, None) == 1
     assert lib.fp8kv_quantize_mx(None, 10, 96, None, None, None) == 2

@@ -1,8 +1,10 @@
 """MXFP8 keys (cache dtype "mxk8v8"): e4m3 codes with one E8M0 scale per
 32-dim block of each K row, V as e4m3 with a per-row fp32 scale.  The
-quantiser and the appends are bit-exact against the oracle; the tensor-core
-decode (split, merge, fused step) is held to the attention gate against the
-oracle's fp64 attention over the block-dequantised keys."""
+quantiser and the appends are bit-exact against the oracle; the decode on
+both kernels (split, merge, fused step) and the CUDA-core prefill are held to
+the attention gate against the oracle's fp64 attention over the
+block-dequantised keys."""
+import math
 import os
 
 import numpy as np
@@ -150,14 +152,108 @@ def test_split_invariance():
         assert rel <= 1e-5, f"splits={ns}: rel {rel:.3e}"
 
 
-def test_other_kernels_rejected():
+def test_unbuilt_kernels_rejected():
+    """The transform paths (f16 K tiles) and the tensor-core prefill are not
+    built for MXFP8 keys: FP8KV_ERR_UNSUPPORTED."""
     cache = fk.Fp8KVCache.contiguous(1, 1, 128, 64, MX)
     q = torch.zeros(1, 8, 128, dtype=torch.bfloat16, device="cuda")
     lens = torch.ones(1, dtype=torch.int32, device="cuda")
-    for kernel in ("cuda_cores", "tensor_cores_k_f16"):
+    for kernel in ("tensor_cores_k_f16", "tensor_cores_k_f16_producer"):
         with pytest.raises(fk.Fp8KVError) as e:
             fk.fp8kv_decode_attention(q, cache, lens, kernel=kernel)
         assert e.value.status == 2
     with pytest.raises(fk.Fp8KVError) as e:
-        fk.fp8kv_prefill_attention(q[:, None].contiguous(), cache, torch.zeros(1, dtype=torch.int32, device="cuda"))
+        fk.fp8kv_prefill_attention(q[:, None].contiguous(), cache, torch.zeros(1, dtype=torch.int32, device="cuda"),
+                                   kernel="tensor_cores")
     assert e.value.status == 2
+
+
+# ---------------------------------------------------------------- CUDA cores
+
+def test_cuda_cores_decode_full_and_hostile():
+    """The CUDA-core split weights each 32-dim block's partial dot by its
+    E8M0 scale (each thread's half row holds two blocks)."""
+    inp = synth.decode_inputs(synth.WORKLOADS["decode_b16_ctx512"], device="cuda")
+    cache = fill_cache(inp, MX)
+    out = gpu_decode(inp, cache, kernel="cuda_cores").cpu().numpy()
+    assert_gate(out, oracle_decode(inp, MX, range(16)), "ctx512 mx cuda cores")
+    tc = gpu_decode(inp, cache, kernel="tensor_cores").cpu().numpy()
+    assert_gate(out, tc, "mx cuda cores vs tensor cores")
+    assert fk.fp8kv_get_device_error() == 0
+
+
+@pytest.mark.parametrize("G", [1, 3, 8])
+def test_cuda_cores_decode_ragged_paged(G):
+    lens = (0, 1, 31, 64, 65, 200, 513)
+    spec = synth.DecodeWorkload(f"mx_fma_G{G}", len(lens), 2 * G, 2, 128, seed=60 + G, seq_lens=lens,
+                                page_size=16, hostile_keys=True)
+    inp = synth.decode_inputs(spec, device="cuda")
+    cache = fill_cache(inp, MX)
+    ref = oracle_decode(inp, MX, range(len(lens)))
+    for ns in (0, 1, 5):
+        out = gpu_decode(inp, cache, num_splits=ns, kernel="cuda_cores").cpu().numpy()
+        assert np.all(out[0] == 0)
+        assert_gate(out[1:], ref[1:], f"mx cuda cores G{G} splits={ns}")
+    assert fk.fp8kv_get_device_error() == 0
+
+
+def test_cuda_cores_fused_step():
+    from test_gpu_decode_step import _run
+    inp = synth.decode_inputs(synth.WORKLOADS["decode_b16_ctx512"], device="cuda")
+    cache, out, knew, _ = _run(inp, MX, "cuda_cores")
+    assert fk.fp8kv_get_device_error() == 0
+    assert_gate(out.cpu().numpy(), oracle_decode(inp, MX, range(16)), "step mx cuda cores")
+    T = int(inp.seq_lens[0])
+    codes, scales = oracle.mx_quantize(synth.bf16_bits(knew))
+    assert np.array_equal(cache.k[:, :, T - 1].cpu().numpy(), codes)
+    assert np.array_equal(cache.k_scale[:, :, T - 1].cpu().numpy(), scales)
+
+
+# ------------------------------------------------------------------ prefill
+
+def _prefill_case(B, n_q, pos0s, Hq, Hkv, seed, page_size=None):
+    D = 128
+    qs, ks, vs = [], [], []
+    for b in range(B):
+        spec = synth.PrefillWorkload("pf_mx", n_q, Hq, Hkv, D, seed=seed + b, pos0=pos0s[b])
+        pin = synth.prefill_inputs(spec, device="cuda")
+        qs.append(pin.q)
+        ks.append(pin.k)
+        vs.append(pin.v)
+    totals = [p + n_q for p in pos0s]
+    if page_size is None:
+        cache = fk.Fp8KVCache.contiguous(B, Hkv, D, (max(totals) + 15) // 16 * 16, MX)
+    else:
+        per = [(t + page_size - 1) // page_size for t in totals]
+        num_pages = sum(per) + 2
+        perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(seed)).to(torch.int32)
+        table = torch.full((B, max(per)), -1, dtype=torch.int32)
+        off = 0
+        for b in range(B):
+            table[b, :per[b]] = perm[off:off + per[b]]
+            off += per[b]
+        cache = fk.Fp8KVCache.paged(table, num_pages, Hkv, D, page_size, MX)
+    seq_idx = torch.cat([torch.full((t,), b, dtype=torch.int32) for b, t in enumerate(totals)])
+    pos = torch.cat([torch.arange(t, dtype=torch.int32) for t in totals])
+    fk.fp8kv_append(cache, torch.cat(ks).contiguous(), torch.cat(vs).contiguous(), seq_idx.cuda(), pos.cuda())
+    return cache, torch.stack(qs).contiguous(), ks, vs
+
+
+@pytest.mark.parametrize("page_size", [None, 32])
+@pytest.mark.parametrize("kernel", ["auto", "cuda_cores"])
+def test_prefill_mx(kernel, page_size):
+    """Causal prefill over MXFP8 keys (the CUDA-core kernel, which applies
+    each block's scale where it converts the codes), two sequences with
+    different prefixes, against the oracle over the block-dequantised keys."""
+    pos0s = [0, 45]
+    cache, q, ks, vs = _prefill_case(2, 150, pos0s, 8, 2, seed=71, page_size=page_size)
+    out = fk.fp8kv_prefill_attention(q, cache, torch.tensor(pos0s, dtype=torch.int32, device="cuda"),
+                                     out_dtype=torch.float32, kernel=kernel).cpu().numpy()
+    assert fk.fp8kv_get_device_error() == 0
+    D = 128
+    for b in range(2):
+        k = oracle.mx_dequantize(*oracle.mx_quantize(synth.bf16_bits(ks[b]).transpose(1, 0, 2)))
+        v = oracle.dequantize(*oracle.quantize(synth.bf16_bits(vs[b]).transpose(1, 0, 2)))
+        qd = oracle.bf16_to_double(synth.bf16_bits(q[b]))
+        ref = oracle.prefill_attention(qd, k[:, :pos0s[b] + 150], v[:, :pos0s[b] + 150], pos0s[b], 1 / math.sqrt(D))
+        assert_gate(out[b].reshape(-1, D), ref.reshape(-1, D), f"prefill mx seq {b} {kernel} P{page_size}")
