@@ -38,9 +38,11 @@
 // section "Operating model": producer and consumer warps interleave the
 // stages across adjacent tiles):
 //   warp 0     TMA producer: 128-byte-swizzled tensor loads of the K and V
-//              tiles straight into the UMMA operand layout; scale rows by 1-D
-//              bulk copy (contiguous cache) or cp.async (paged cache); a ring
-//              of NST stages (full/empty mbarriers).
+//              tiles straight into the UMMA operand layout, a ring of NST
+//              stages (full/empty mbarriers).  Contiguous cache: scale rows
+//              by 1-D bulk copy.  Paged cache: warps 0 and 11 issue alternate
+//              tiles, one page per lane, page ids four tiles ahead by
+//              cp.async; the softmax threads load their tokens' scale words.
 //   warp 1     TMEM owner and QK issuer (one thread).
 //   warp 10    PV issuer (one thread).  Issuing a few tcgen05.mma costs the
 //              issuing thread a fraction of a microsecond; one thread issuing
@@ -51,12 +53,15 @@
 //              at the end like two splits.  The four warps of a group share
 //              no barrier inside the loop: each publishes its tile anchors
 //              in shared memory before its P-ready arrival, and the O fold
-//              reads them after that phase completed.
+//              reads them after that phase completed.  Warp maxima come from
+//              redux.sync, so every lane holds all heads' anchors.
 // S, O (TMEM) and P (shared memory) are double-buffered per group, so the
-// QKs and PVs of neighbouring tiles overlap the softmax.  Each QK and PV is
-// split into four independent MMAs (one per k-step, each with its own TMEM
-// accumulator, combined by the reading threads): dependent thin MMAs would
-// serialise on their latency.  Every wait is bounded; a wait that runs out
+// QKs and PVs of neighbouring tiles overlap the softmax.  A QK chains its
+// k-steps into one accumulator (it runs far enough ahead of the softmax that
+// their latency is hidden; MXFP8 keys keep one accumulator per 32-dim block
+// for the block scales).  A PV keeps one accumulator per k-step, the token
+// slice of one softmax warp with its own anchor, combined by the O fold.
+// Every wait is bounded; a wait that runs out
 // raises FP8KV_DEVERR_TIMEOUT, the CTA writes an empty partial and leaves.
 // V rows past the sequence end are zeroed before PV (0 * NaN would poison
 // the product).

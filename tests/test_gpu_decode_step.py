@@ -189,3 +189,71 @@ def test_step_with_pinned_host_buffers(kernel):
     assert torch.equal(results[0][0], results[1][0])
     assert torch.equal(results[0][1], results[1][1]) and torch.equal(results[0][2], results[1][2])
     assert_gate(results[1][0].numpy(), oracle_decode(inp, "k8v8", range(3)), f"host buffers {kernel}")
+
+
+def test_step_graph_replay_with_early_cache_read_full_size():
+    """The headline's own launch configuration at full size: four layer
+    caches of 16 sequences x 8192 tokens, the layers' fused steps captured
+    in one CUDA graph, each launched as the previous one's programmatic
+    dependent (early cache read), the graph replayed twice.  Every layer
+    matches a plain eager step bit for bit, and a sample of sequences
+    passes the gate against the oracle."""
+    inp = synth.decode_inputs(synth.WORKLOADS["decode_b16_ctx8192"], device="cuda")
+    prev, knew, vnew = _split_last_token(inp)
+    q = inp.q.cuda().contiguous()
+    lens = inp.seq_lens.cuda()
+    n_layers = 4
+    caches = [fill_cache(prev, "k8v8", capacity=8192) for _ in range(n_layers)]
+    wss = [torch.zeros(fk.fp8kv_decode_step_workspace_bytes(c, 16, 0, "tensor_cores"), dtype=torch.uint8,
+                       device="cuda") for c in caches]
+    outs = [torch.empty(16, 16, 128, dtype=torch.float32, device="cuda") for _ in range(n_layers)]
+
+    def steps(early):
+        for j in range(n_layers):
+            fk.fp8kv_decode_step(q, knew, vnew, caches[j], lens, out=outs[j], workspace=wss[j],
+                                 kernel="tensor_cores", early_cache_read=early and j > 0)
+
+    steps(False)                       # eager, plain launches: the reference outputs
+    torch.cuda.synchronize()
+    plain = [o.clone() for o in outs]
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            steps(True)
+    torch.cuda.current_stream().wait_stream(side)
+    for o in outs:
+        o.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert fk.fp8kv_get_device_error() == 0
+    for j in range(n_layers):
+        assert torch.equal(outs[j], plain[j]), j
+    sample = [0, 7, 15]
+    assert_gate(outs[3].cpu().numpy()[sample], oracle_decode(inp, "k8v8", sample), "graph replay, early read")
+
+
+@pytest.mark.parametrize("dtype", ["k8v8", "mxk8v8"])
+def test_step_paged_b64_full_sampled(dtype):
+    """The paged serving workload at full size (64 sequences of 1K-16K
+    tokens, 16-token pages, hostile keys) through the fused step, as the
+    bench runs it; the oracle checks a sample of sequences, and the appended
+    rows of those sequences are the quantiser's."""
+    inp = synth.decode_inputs(synth.WORKLOADS["paged_b64_hostile"], device="cuda")
+    prev, knew, vnew = _split_last_token(inp)
+    cache = fill_cache(prev, dtype)
+    out = fk.fp8kv_decode_step(inp.q.cuda().contiguous(), knew, vnew, cache, inp.seq_lens.cuda(),
+                               out_dtype=torch.float32)
+    assert fk.fp8kv_get_device_error() == 0
+    lens = inp.seq_lens.numpy()
+    sample = sorted({int(lens.argmin()), int(lens.argmax()), 5, 40})
+    assert_gate(out.cpu().numpy()[sample], oracle_decode(inp, dtype, sample), f"paged b64 step {dtype}")
+    pt = inp.page_table.numpy()
+    quant = oracle.mx_quantize if dtype == "mxk8v8" else oracle.quantize
+    for b in sample:
+        T = int(lens[b])
+        codes, scales = quant(synth.bf16_bits(knew[b:b + 1]))
+        got = oracle.gather_paged(cache.k.cpu().numpy(), pt, b, T)
+        assert np.array_equal(got[:, T - 1], codes[0]), b
