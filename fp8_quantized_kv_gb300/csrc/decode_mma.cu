@@ -1132,10 +1132,13 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
         for (int g = 0; g < 8; ++g) Uh[g] = ceilf(warp_max_f32(uu[g]));
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          const float mn = fmaxf(m_w[g], Uh[g]);
-          f1[g] = pow2_diff(m_w[g] - mn, 0);
-          f2[g] = pow2_diff(Uh[g] - mn, 0);
-          m_w[g] = mn;
+          // one of the two factors is 1, the other 2^-|U - m_w| (both 0 or
+          // 1 when neither anchor exists yet: l is still 0 then)
+          const bool up = Uh[g] > m_w[g];
+          const float e = pow2_diff(-fabsf(Uh[g] - m_w[g]), 0);
+          f1[g] = up ? e : 1.f;
+          f2[g] = up ? 1.f : e;
+          m_w[g] = fmaxf(m_w[g], Uh[g]);
         }
         TRACE_SUB(i, 8);
         if (!tok_ok) {      // V rows past the sequence end: zero them for PV
