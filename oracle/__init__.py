@@ -49,6 +49,10 @@ def _load():
         lib.fp8kv_oracle_dequantize.argtypes = [c_u8_p, c_f32_p, i64, i32, c_dbl_p]
         lib.fp8kv_oracle_mx_quantize.argtypes = [c_u16_p, i64, i32, c_u8_p, c_u8_p]
         lib.fp8kv_oracle_quantize_residual.argtypes = [c_u16_p, c_f32_p, i64, i32, i64, i32, c_u8_p, c_f32_p]
+        c_i32_p = ctypes.POINTER(ctypes.c_int32)
+        lib.fp8kv_oracle_rope_bias.argtypes = [c_f32_p, c_f32_p, c_f32_p, c_i32_p, i32, i64, i32, c_f32_p]
+        lib.fp8kv_oracle_quantize_residual_rope.argtypes = [c_u16_p, c_f32_p, c_f32_p, c_f32_p, c_i32_p, i32, i64,
+                                                            i32, c_u8_p, c_f32_p]
         lib.fp8kv_oracle_mx_dequantize.argtypes = [c_u8_p, c_u8_p, i64, i32, c_dbl_p]
         lib.fp8kv_oracle_gather_paged.restype = ctypes.c_int
         lib.fp8kv_oracle_gather_paged.argtypes = [
@@ -153,6 +157,54 @@ def quantize_residual(x_bits, bias):
 def residual_keys(codes, scales, bias):
     """The keys a residual cache represents: dequant(r) + bias, fp64 [Hkv, T, D]."""
     return dequantize(codes, scales) + np.asarray(bias, dtype=np.float64)[:, None, :]
+
+
+# ---------------------------------------- rotated pre-bias residual (rotary) --
+
+def rope_bias(bias, cos, sin, positions):
+    """The rotated bias R_t b of every (KV head, token): bias [Hkv, D] fp32,
+    cos and sin [P, D/2] fp32 (rotary tables, "rotate half" pairs i and
+    i + D/2), positions [T] -> fp32 [Hkv, T, D], evaluated as the appender
+    does ("Fused KV-cache quantization", section "Bias-aware symmetric FP8":
+    a bias added before the rotary embedding moves with the key's position)."""
+    lib = _load()
+    b = _c(bias, np.float32)
+    c = _c(cos, np.float32)
+    s = _c(sin, np.float32)
+    p = _c(positions, np.int32)
+    heads, d = b.shape
+    assert c.shape == s.shape and c.shape[1] == d // 2 and p.ndim == 1
+    assert p.size == 0 or (p.min() >= 0 and p.max() < c.shape[0])
+    out = np.empty((heads, p.size, d), dtype=np.float32)
+    lib.fp8kv_oracle_rope_bias(_ptr(b, ctypes.c_float), _ptr(c, ctypes.c_float), _ptr(s, ctypes.c_float),
+                               _ptr(p, ctypes.c_int32), heads, p.size, d, _ptr(out, ctypes.c_float))
+    return out
+
+
+def quantize_residual_rope(x_bits, bias, cos, sin, positions):
+    """Key rows [Hkv, T, D] (bf16 bits) at positions [T] -> codes and fp32
+    scales of the residual fp32(k) - R_t b (the per-row rule)."""
+    lib = _load()
+    x = _c(x_bits, np.uint16)
+    b = _c(bias, np.float32)
+    c = _c(cos, np.float32)
+    s = _c(sin, np.float32)
+    p = _c(positions, np.int32)
+    heads, T, d = x.shape
+    assert b.shape == (heads, d) and p.shape == (T,) and d <= 512
+    assert T == 0 or (p.min() >= 0 and p.max() < c.shape[0])
+    codes = np.empty(x.shape, dtype=np.uint8)
+    scales = np.empty(x.shape[:-1], dtype=np.float32)
+    lib.fp8kv_oracle_quantize_residual_rope(_ptr(x, ctypes.c_uint16), _ptr(b, ctypes.c_float),
+                                            _ptr(c, ctypes.c_float), _ptr(s, ctypes.c_float),
+                                            _ptr(p, ctypes.c_int32), heads, T, d,
+                                            _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_float))
+    return codes, scales
+
+
+def residual_rope_keys(codes, scales, rb):
+    """The keys a rotated-residual cache represents: dequant(r) + R_t b, fp64."""
+    return dequantize(codes, scales) + np.asarray(rb, dtype=np.float64)
 
 
 # ----------------------------------------------------------------- MXFP8 --

@@ -57,6 +57,18 @@
  *    IEEE fp32 subtraction per element).  The key the cache represents is
  *    dequant(r) + b, reconstructed here in fp64.
  *
+ *  - Rotated pre-bias residual keys (the same sections; the pages list
+ *    post-rotary residual layouts, where the cache holds rotated keys and a
+ *    bias added before the rotary embedding turns with the key's position):
+ *    the residual of the key at position t is r = fp32(k) - R_t b, with R_t
+ *    the rotary rotation in the "rotate half" layout (dims i and i + d/2 form
+ *    pair i at angle theta_{t,i}; cos and sin come from the caller's tables):
+ *      (R_t b)_i       = b_i cos - b_{i+d/2} sin
+ *      (R_t b)_{i+d/2} = b_{i+d/2} cos + b_i sin
+ *    each evaluated in fp32 as one fused multiply-add on the product with sin
+ *    rounded to fp32 first (fmaf(b_own, cos, -+ (float)(b_other * sin))).
+ *    The key the cache represents is dequant(r) + R_t b, in fp64.
+ *
  *  - Paged addressing: token t of sequence b lives in page
  *    page_table[b][t / page_size] at offset t % page_size ("FP8 KV attention:
  *    hardware paths and tile preparation", section "Collect the profiler
@@ -179,6 +191,53 @@ void fp8kv_oracle_quantize_residual(const uint16_t *x, const float *bias, int64_
       }
     }
   }
+}
+
+/* (R_t b)_e for element e of a row of width d (see the header). */
+static float rope_bias_elem(const float *b, const float *cs, const float *sn, int d, int e) {
+  const int h = d / 2;
+  if (e < h) {
+    const float p = b[e + h] * sn[e];
+    return fmaf(b[e], cs[e], -p);
+  }
+  const float p = b[e - h] * sn[e - h];
+  return fmaf(b[e], cs[e - h], p);
+}
+
+/* The rotated bias of every (head, token): bias [heads][d], cos and sin
+ * [positions][d/2], the tokens' positions pos[T] -> out [heads][T][d]. */
+void fp8kv_oracle_rope_bias(const float *bias, const float *cos_t, const float *sin_t, const int32_t *pos,
+                            int heads, int64_t T, int d, float *out) {
+  const int h2 = d / 2;
+  for (int hd = 0; hd < heads; ++hd)
+    for (int64_t t = 0; t < T; ++t)
+      for (int e = 0; e < d; ++e)
+        out[(hd * T + t) * d + e] = rope_bias_elem(bias + hd * d, cos_t + (int64_t)pos[t] * h2,
+                                                   sin_t + (int64_t)pos[t] * h2, d, e);
+}
+
+/* Key rows x [heads][T][d] (bf16 bits) at positions pos[T]: the per-row rule
+ * on the fp32 residual fp32(k) - R_t b. */
+void fp8kv_oracle_quantize_residual_rope(const uint16_t *x, const float *bias, const float *cos_t,
+                                         const float *sin_t, const int32_t *pos, int heads, int64_t T, int d,
+                                         uint8_t *codes, float *scales) {
+  const int h2 = d / 2;
+  float y[512];
+  for (int hd = 0; hd < heads; ++hd)
+    for (int64_t t = 0; t < T; ++t) {
+      const int64_t r = hd * T + t;
+      float amax = 0.0f;
+      for (int e = 0; e < d; ++e) {
+        const float rb = rope_bias_elem(bias + hd * d, cos_t + (int64_t)pos[t] * h2, sin_t + (int64_t)pos[t] * h2,
+                                        d, e);
+        y[e] = bf16_bits_to_float(x[r * d + e]) - rb;
+        if (fabsf(y[e]) > amax) amax = fabsf(y[e]);
+      }
+      const float scale = amax / 448.0f;
+      scales[r] = scale;
+      for (int e = 0; e < d; ++e)
+        codes[r * d + e] = amax == 0.0f ? 0x00 : fp8kv_oracle_e4m3_encode(y[e] / scale);
+    }
 }
 
 /* codes x scale -> fp64 values. */

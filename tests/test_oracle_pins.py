@@ -245,6 +245,91 @@ def test_constant_key_bias_cancels_in_attention():
     assert np.allclose(a, c, rtol=0, atol=1e-9)
 
 
+# --------------------------------------- rotated pre-bias residual (rotary) --
+
+def _tables(P, h, angle):
+    """cos and sin tables [P, h] fp32 for angle(p, i) (radians)."""
+    th = np.fromfunction(angle, (P, h))
+    return np.cos(th).astype(np.float32), np.sin(th).astype(np.float32)
+
+
+def test_rope_bias_at_zero_angle_is_the_constant_bias():
+    # cos 1, sin 0: R_t b = b exactly, so the rotated residual is the
+    # constant-bias residual, bit for bit
+    rng = np.random.default_rng(5)
+    b = (rng.standard_normal((2, 128)) * 20).astype(np.float32)
+    c, s = np.ones((64, 64), np.float32), np.zeros((64, 64), np.float32)
+    pos = np.arange(40, dtype=np.int32)
+    assert np.array_equal(oracle.rope_bias(b, c, s, pos), np.broadcast_to(b[:, None, :], (2, 40, 128)))
+    k = _bf16_bits(rng.standard_normal((2, 40, 128)) * 4 + b[:, None, :])
+    c1, s1 = oracle.quantize_residual_rope(k, b, c, s, pos)
+    c0, s0 = oracle.quantize_residual(k, b)
+    assert np.array_equal(c1, c0) and np.array_equal(s1.view(np.uint32), s0.view(np.uint32))
+    # and a zero bias gives the plain per-row quantiser at any angle
+    cr, sr = _tables(64, 64, lambda p, i: 0.37 * p + i)
+    cz, sz = oracle.quantize_residual_rope(k, np.zeros((2, 128), np.float32), cr, sr, pos)
+    cp, sp = oracle.quantize(k)
+    assert np.array_equal(cz, cp) and np.array_equal(sz.view(np.uint32), sp.view(np.uint32))
+
+
+def test_rope_bias_quarter_turn_is_rotate_half():
+    # cos 0, sin 1 (a quarter turn of every pair): (R b) = (-b_hi, b_lo), the
+    # "rotate half" map, exactly
+    rng = np.random.default_rng(6)
+    b = rng.standard_normal((3, 64)).astype(np.float32)
+    c, s = np.zeros((4, 32), np.float32), np.ones((4, 32), np.float32)
+    rb = oracle.rope_bias(b, c, s, np.array([0, 3], np.int32))
+    want = np.concatenate([-b[:, 32:], b[:, :32]], axis=1)
+    assert np.array_equal(rb[:, 0], want) and np.array_equal(rb[:, 1], want)
+
+
+def test_rope_bias_is_a_rotation():
+    # length kept, the inverse angle undoes it, and two rotations compose to
+    # the rotation by the summed angle (each within fp32 rounding); a sign
+    # error in either component breaks the last one
+    rng = np.random.default_rng(7)
+    b = rng.standard_normal((2, 128)).astype(np.float32)
+    P, h = 50, 64
+    th = rng.uniform(-math.pi, math.pi, (P, h))
+    c, s = np.cos(th).astype(np.float32), np.sin(th).astype(np.float32)
+    pos = np.arange(P, dtype=np.int32)
+    rb = oracle.rope_bias(b, c, s, pos).astype(np.float64)
+    assert np.allclose(np.linalg.norm(rb, axis=-1), np.linalg.norm(b, axis=-1)[:, None], rtol=1e-6)
+    for t in (0, 17, 49):
+        back = oracle.rope_bias(rb[:, t].astype(np.float32), c[t:t + 1], -s[t:t + 1], np.zeros(1, np.int32))
+        assert np.allclose(back[:, 0], b, atol=1e-5)
+        th2 = rng.uniform(-math.pi, math.pi, h)
+        c2, s2 = np.cos(th2).astype(np.float32)[None], np.sin(th2).astype(np.float32)[None]
+        two = oracle.rope_bias(rb[:, t].astype(np.float32), c2, s2, np.zeros(1, np.int32))[:, 0]
+        cs = np.cos(th[t] + th2).astype(np.float32)[None]
+        sn = np.sin(th[t] + th2).astype(np.float32)[None]
+        one = oracle.rope_bias(b, cs, sn, np.zeros(1, np.int32))[:, 0]
+        assert np.allclose(two, one, atol=1e-5)
+
+
+def test_rope_residual_reconstruction_bound():
+    # dequant(r) + R_t b stays within the residual's quantisation error of
+    # the key, and keeps the token-varying part that a plain quantiser of the
+    # biased key loses
+    rng = np.random.default_rng(8)
+    P, h = 80, 64
+    c, s = _tables(P, h, lambda p, i: p * 10000.0 ** (-i / h))
+    b = np.zeros((2, 128), np.float32)
+    b[:, :4] = 60.0
+    pos = np.arange(P, dtype=np.int32)
+    rb = oracle.rope_bias(b, c, s, pos)
+    kf = rng.standard_normal((2, P, 128)).astype(np.float32) + rb
+    k = _bf16_bits(kf)
+    codes, scales = oracle.quantize_residual_rope(k, b, c, s, pos)
+    rec = oracle.residual_rope_keys(codes, scales, rb)
+    kd = oracle.bf16_to_double(k)
+    resid = kd - rb
+    amax = np.abs(resid).max(axis=-1, keepdims=True)
+    assert np.all(np.abs(rec - kd) <= amax / 16 + 1e-12)
+    plain = oracle.dequantize(*oracle.quantize(k))
+    assert np.linalg.norm(rec - kd) < 0.5 * np.linalg.norm(plain - kd)
+
+
 # ----------------------------------------------------------------- MXFP8 --
 
 def _mx_worked_row():
