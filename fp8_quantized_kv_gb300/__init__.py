@@ -74,7 +74,8 @@ class Fp8KVCache:
     that describes them.  Layouts are those of include/fp8kv.h."""
 
     def __init__(self, *, dtype, layout, batch, kv_heads, head_dim, k, v, k_scale, v_scale,
-                 max_tokens=0, page_size=0, num_pages=0, page_table=None, k_bias=None):
+                 max_tokens=0, page_size=0, num_pages=0, page_table=None, k_bias=None, rope_cos=None,
+                 rope_sin=None):
         self.dtype = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
         self.layout = layout
         self.batch, self.kv_heads, self.head_dim = batch, kv_heads, head_dim
@@ -84,15 +85,26 @@ class Fp8KVCache:
         if k_bias is not None:
             _need(k_bias, torch.float32, "k_bias")
         self.k_bias = k_bias
+        if (rope_cos is None) != (rope_sin is None):
+            raise ValueError("rope_cos and rope_sin come together")
+        if rope_cos is not None:
+            for t, name in ((rope_cos, "rope_cos"), (rope_sin, "rope_sin")):
+                _need(t, torch.float32, name)
+                if t.dim() != 2 or t.shape[1] != head_dim // 2 or t.shape != rope_cos.shape:
+                    raise ValueError(f"{name}: want [positions, head_dim / 2] fp32, got {tuple(t.shape)}")
+        self.rope_cos, self.rope_sin = rope_cos, rope_sin
         self._struct = CacheStruct(
             dtype=self.dtype, layout=layout, batch=batch, kv_heads=kv_heads, head_dim=head_dim,
             max_tokens=max_tokens, page_size=page_size, num_pages=num_pages,
-            max_pages_per_seq=0 if page_table is None else page_table.shape[1], reserved=0,
+            max_pages_per_seq=0 if page_table is None else page_table.shape[1],
+            rope_positions=0 if rope_cos is None else rope_cos.shape[0],
             k=k.data_ptr(), v=v.data_ptr(),
             k_scale=None if k_scale is None else k_scale.data_ptr(),
             v_scale=None if v_scale is None else v_scale.data_ptr(),
             page_table=None if page_table is None else page_table.data_ptr(),
-            k_bias=None if k_bias is None else k_bias.data_ptr())
+            k_bias=None if k_bias is None else k_bias.data_ptr(),
+            rope_cos=None if rope_cos is None else rope_cos.data_ptr(),
+            rope_sin=None if rope_sin is None else rope_sin.data_ptr())
 
     @property
     def struct_ref(self):
@@ -120,21 +132,25 @@ class Fp8KVCache:
         return k, v, ks, vs
 
     @classmethod
-    def contiguous(cls, batch, kv_heads, head_dim, max_tokens, dtype="k8v8", device="cuda", k_bias=None):
+    def contiguous(cls, batch, kv_heads, head_dim, max_tokens, dtype="k8v8", device="cuda", k_bias=None,
+                   rope_cos=None, rope_sin=None):
         """k_bias: optional [kv_heads, head_dim] fp32 key bias; the cache then
-        holds pre-bias residual keys (include/fp8kv.h, fp8kv_cache.k_bias)."""
+        holds pre-bias residual keys (include/fp8kv.h, fp8kv_cache.k_bias).
+        rope_cos, rope_sin: optional [positions, head_dim / 2] fp32 rotary
+        tables; the bias then turns with the key's position (rope_cos)."""
         k, v, ks, vs = cls._alloc(dtype, (batch, kv_heads, max_tokens), head_dim, device)
         return cls(dtype=dtype, layout=LAYOUT_CONTIGUOUS, batch=batch, kv_heads=kv_heads, k_bias=k_bias,
-                   head_dim=head_dim, k=k, v=v, k_scale=ks, v_scale=vs, max_tokens=max_tokens)
+                   head_dim=head_dim, k=k, v=v, k_scale=ks, v_scale=vs, max_tokens=max_tokens,
+                   rope_cos=rope_cos, rope_sin=rope_sin)
 
     @classmethod
     def paged(cls, page_table: torch.Tensor, num_pages, kv_heads, head_dim, page_size=16,
-              dtype="k8v8", device="cuda", k_bias=None):
+              dtype="k8v8", device="cuda", k_bias=None, rope_cos=None, rope_sin=None):
         pt = page_table.to(device=device, dtype=torch.int32).contiguous()
         k, v, ks, vs = cls._alloc(dtype, (num_pages, kv_heads, page_size), head_dim, device)
         return cls(dtype=dtype, layout=LAYOUT_PAGED, batch=pt.shape[0], kv_heads=kv_heads, k_bias=k_bias,
                    head_dim=head_dim, k=k, v=v, k_scale=ks, v_scale=vs, page_size=page_size,
-                   num_pages=num_pages, page_table=pt)
+                   num_pages=num_pages, page_table=pt, rope_cos=rope_cos, rope_sin=rope_sin)
 
 
 # ------------------------------------------------------------ C-ABI calls --

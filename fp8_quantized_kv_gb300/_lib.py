@@ -41,13 +41,15 @@ class CacheStruct(ctypes.Structure):
         ("page_size", ctypes.c_int32),
         ("num_pages", ctypes.c_int32),
         ("max_pages_per_seq", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("rope_positions", ctypes.c_int32),
         ("k", ctypes.c_void_p),
         ("v", ctypes.c_void_p),
         ("k_scale", ctypes.c_void_p),
         ("v_scale", ctypes.c_void_p),
         ("page_table", ctypes.c_void_p),
         ("k_bias", ctypes.c_void_p),
+        ("rope_cos", ctypes.c_void_p),
+        ("rope_sin", ctypes.c_void_p),
     ]
 
 

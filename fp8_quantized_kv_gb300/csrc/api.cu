@@ -64,9 +64,13 @@ static fp8kv_status check_cache(const fp8kv_cache* c, CacheView* view) {
   const bool v8 = c->dtype == FP8KV_K8V8 || c->dtype == FP8KV_K16V8 || c->dtype == FP8KV_MXK8V8;
   if (k8 != (c->k_scale != nullptr) || v8 != (c->v_scale != nullptr)) return FP8KV_ERR_INVALID_ARG;
   if (c->k_bias != nullptr && c->dtype != FP8KV_K8V8 && c->dtype != FP8KV_K8V16) return FP8KV_ERR_INVALID_ARG;
+  // rotated bias: both tables, with a bias
+  if ((c->rope_cos == nullptr) != (c->rope_sin == nullptr)) return FP8KV_ERR_INVALID_ARG;
+  if (c->rope_cos != nullptr && c->k_bias == nullptr) return FP8KV_ERR_INVALID_ARG;
   // 16-byte vector copies read the cache: every base pointer must be aligned
   const uintptr_t align = (uintptr_t)c->k | (uintptr_t)c->v | (uintptr_t)c->k_scale |
-                          (uintptr_t)c->v_scale | (uintptr_t)c->page_table | (uintptr_t)c->k_bias;
+                          (uintptr_t)c->v_scale | (uintptr_t)c->page_table | (uintptr_t)c->k_bias |
+                          (uintptr_t)c->rope_cos | (uintptr_t)c->rope_sin;
   if (align & 15) return FP8KV_ERR_INVALID_ARG;
   std::memset(view, 0, sizeof(*view));
   if (c->layout == FP8KV_LAYOUT_CONTIGUOUS) {
@@ -90,11 +94,18 @@ static fp8kv_status check_cache(const fp8kv_cache* c, CacheView* view) {
                            ? (int64_t)c->batch * c->kv_heads * c->max_tokens
                            : (int64_t)c->num_pages * c->kv_heads * c->page_size;
   if (rows > INT32_MAX) return FP8KV_ERR_UNSUPPORTED;
+  if (c->rope_cos != nullptr) {               // every position the cache can hold has a table row
+    const int64_t cap = c->layout == FP8KV_LAYOUT_PAGED ? (int64_t)c->max_pages_per_seq * c->page_size
+                                                       : (int64_t)c->max_tokens;
+    if (c->rope_positions < cap) return FP8KV_ERR_INVALID_ARG;
+  }
   view->k = static_cast<const uint8_t*>(c->k);
   view->v = static_cast<const uint8_t*>(c->v);
   view->k_scale = c->k_scale;
   view->v_scale = c->v_scale;
   view->k_bias = c->k_bias;
+  view->rope_cos = c->rope_cos;
+  view->rope_sin = c->rope_sin;
   view->batch = c->batch;
   view->kv_heads = c->kv_heads;
   view->head_dim = c->head_dim;
@@ -119,6 +130,10 @@ struct SplitPlan { int splits, chunk_tiles, tile, kernel; };
 static int resolve_kernel(const fp8kv_cache* c, int q_heads, int requested) {
   const int G = q_heads / c->kv_heads;
   const bool mma_ok = c->head_dim == 128 && G >= 1 && G <= 8;
+  // rotated-bias residual keys: the CUDA-core kernel only (it adds each
+  // key's rotated bias to its score)
+  if (c->rope_cos != nullptr)
+    return requested == FP8KV_KERNEL_AUTO || requested == FP8KV_KERNEL_CUDA_CORES ? FP8KV_KERNEL_CUDA_CORES : 0;
   // MXFP8 keys: both kernels apply each 32-dim block's scale to its partial
   // dot product; the transform paths (f16 K tiles) are not built for them
   if (c->dtype == FP8KV_MXK8V8) {
@@ -400,7 +415,7 @@ fp8kv_status fp8kv_prefill_attention(const void* q, const fp8kv_cache* cache, co
   if (!std::isfinite(sm_scale)) return FP8KV_ERR_INVALID_ARG;
   if (q_heads / cache->kv_heads > 16) return FP8KV_ERR_UNSUPPORTED;
   if (kernel < FP8KV_KERNEL_AUTO || kernel > FP8KV_KERNEL_TENSOR_CORES) return FP8KV_ERR_INVALID_ARG;
-  const bool tc_built = cache->dtype == FP8KV_K8V8 && cache->head_dim == 128;
+  const bool tc_built = cache->dtype == FP8KV_K8V8 && cache->head_dim == 128 && cache->rope_cos == nullptr;
   if (kernel == FP8KV_KERNEL_TENSOR_CORES && !tc_built) return FP8KV_ERR_UNSUPPORTED;
   const bool use_tc = kernel == FP8KV_KERNEL_TENSOR_CORES || (kernel == FP8KV_KERNEL_AUTO && tc_built);
   if (cache->batch == 0 || n_q == 0) return FP8KV_OK;

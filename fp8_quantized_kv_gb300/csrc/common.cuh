@@ -30,11 +30,24 @@ struct CacheView {
   const float* v_scale;
   const int32_t* page_table;
   const float* k_bias;             // pre-bias residual keys: [kv_heads][head_dim], or null
+  const float* rope_cos;           // rotated bias: [positions][head_dim / 2], or null
+  const float* rope_sin;
   int batch, kv_heads, head_dim;
   int max_tokens;                  // contiguous capacity
   int page_size, page_shift, num_pages, max_pages_per_seq;
   int paged;
 };
+
+// Rotated key bias (R_t b)_d of KV head h at position t ("rotate half":
+// dims i and i + D/2 form pair i), in fp32 with each product with sin
+// rounded first: fma(b_d, cos, -(b_{d+D/2} sin)) or fma(b_d, cos, b_{d-D/2} sin).
+__device__ __forceinline__ float rope_bias(const CacheView& c, int h, int t, int d) {
+  const int H = c.head_dim >> 1;
+  const int p = d < H ? d : d - H;
+  const float cs = c.rope_cos[(int64_t)t * H + p], sn = c.rope_sin[(int64_t)t * H + p];
+  const float* b = c.k_bias + (int64_t)h * c.head_dim;
+  return d < H ? fmaf(b[d], cs, -__fmul_rn(b[d + H], sn)) : fmaf(b[d], cs, __fmul_rn(b[d - H], sn));
+}
 
 __device__ __forceinline__ void raise_error(unsigned int* err, unsigned int bit) {
   if (err) atomicOr(err, bit);

@@ -10,7 +10,10 @@
 // Per tile ("FP8 KV attention: hardware paths and tile preparation", section
 // "Operating model": K load -> K prep -> QK -> softmax; V load -> V prep -> PV):
 //   s_j   = (q . kcode_j) * k_scale_j * sm_scale          (K scale folded into s;
-//           MXFP8 keys: each 32-dim block's partial dot times its E8M0 scale)
+//           MXFP8 keys: each 32-dim block's partial dot times its E8M0 scale;
+//           rotated-bias residual keys: plus q . R_t b, the key's rotated
+//           bias, as sum_i A_i cos theta_{t,i} + B_i sin theta_{t,i} with
+//           A_i = q_i b_i + q_{i+D/2} b_{i+D/2}, B_i = q_{i+D/2} b_i - q_i b_{i+D/2})
 //   m_t   = max_j s_j over the tile,   p_j = exp(s_j - m_t)
 //   p'_j  = bf16_rn(p_j * v_scale_j)                        (V scale folded into P)
 //   O     = O * e^(m - m') + e^(m_t - m') * sum_j p'_j vcode_j,   l likewise with p_j
@@ -53,6 +56,9 @@ constexpr int fma_smem_bytes() {
   using C = FmaCfg<D, KE, VE>;
   return C::NSTAGE * C::STAGE + GP * C::QS * 4 + kTileTokens * GP * 4 + 2 * 4 * GP * 4;
 }
+// rotated-bias residual keys: the per-head A and B of the score term, after the rest
+template <int D, int GP>
+constexpr int fma_rope_smem_bytes() { return GP * D * 4; }
 
 __device__ __forceinline__ int q_off(int d, int D) { return d + (d >= D / 2 ? 4 : 0); }
 
@@ -64,6 +70,7 @@ __global__ void __launch_bounds__(128) decode_split_fma(DecodeParams p) {
   float* p_s = q_s + GP * C::QS;                 // [64][GP]
   float* red_max = p_s + kTileTokens * GP;        // [4][GP]
   float* red_sum = red_max + 4 * GP;              // [4][GP]
+  float* ab_s = red_sum + 4 * GP;                 // [GP][D]: A_i (i < D/2), B_i (rotated bias only)
 
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -99,6 +106,19 @@ __global__ void __launch_bounds__(128) decode_split_fma(DecodeParams p) {
     q_s[g * C::QS + q_off(d, D)] = v;
   }
 
+  const bool rope = c.rope_cos != nullptr;
+  constexpr int H = D / 2;
+  if (rope) {
+    __syncthreads();                               // q_s written
+    const float* kb = c.k_bias + (int64_t)h * D;
+    for (int i = tid; i < GP * H; i += blockDim.x) {
+      const int g = i / H, pi = i % H;
+      const float q0 = q_s[g * C::QS + q_off(pi, D)], q1 = q_s[g * C::QS + q_off(pi + H, D)];
+      const float b0 = kb[pi], b1 = kb[pi + H];
+      ab_s[g * D + pi] = fmaf(q0, b0, q1 * b1);
+      ab_s[g * D + H + pi] = fmaf(q1, b0, -(q0 * b1));
+    }
+  }
   const int64_t cont_base = ((int64_t)b * c.kv_heads + h) * c.max_tokens;   // contiguous rows
   // Issue the cp.async copies of one tile into a ring stage.  Rows up to the
   // next multiple of 16 past T are copied (still inside the cache capacity or
@@ -243,12 +263,42 @@ __global__ void __launch_bounds__(128) decode_split_fma(DecodeParams p) {
     }
     const bool valid = j < nvalid;
     const float kfac = (KE == ELEM_E4M3 ? kss[j] : 1.f) * p.scale_log2;
+    // rotated-bias residual keys: this thread's half of the pairs of q . R_t b
+    float corr[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) corr[g] = 0.f;
+    if (rope && valid) {
+      const int t = t0 + j;
+      const float4* cs4 = reinterpret_cast<const float4*>(c.rope_cos + (int64_t)t * H + hf * (H / 2));
+      const float4* sn4 = reinterpret_cast<const float4*>(c.rope_sin + (int64_t)t * H + hf * (H / 2));
+#pragma unroll 2
+      for (int u = 0; u < H / 8; ++u) {
+        const float4 cv = __ldg(cs4 + u), sv = __ldg(sn4 + u);
+        const int pi = hf * (H / 2) + 4 * u;
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          const float4 a = *reinterpret_cast<const float4*>(ab_s + g * D + pi);
+          const float4 bq = *reinterpret_cast<const float4*>(ab_s + g * D + H + pi);
+          float x = corr[g];
+          x = fmaf(a.x, cv.x, x); x = fmaf(bq.x, sv.x, x);
+          x = fmaf(a.y, cv.y, x); x = fmaf(bq.y, sv.y, x);
+          x = fmaf(a.z, cv.z, x); x = fmaf(bq.z, sv.z, x);
+          x = fmaf(a.w, cv.w, x); x = fmaf(bq.w, sv.w, x);
+          corr[g] = x;
+        }
+      }
+    }
     float sc[GP];
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
       float d2 = dot[g] + __shfl_xor_sync(0xffffffffu, dot[g], 1);
       if (KE != ELEM_BF16) d2 *= kTwoPow120;
-      sc[g] = valid ? d2 * kfac : -INFINITY;
+      if (rope) {
+        const float ct = corr[g] + __shfl_xor_sync(0xffffffffu, corr[g], 1);
+        sc[g] = valid ? fmaf(d2, KE == ELEM_E4M3 ? kss[j] : 1.f, ct) * p.scale_log2 : -INFINITY;
+      } else {
+        sc[g] = valid ? d2 * kfac : -INFINITY;
+      }
       const float wm = warp_max(sc[g]);
       if (lane == 0) red_max[warp * GP + g] = wm;
     }
@@ -421,9 +471,10 @@ __global__ void __launch_bounds__(D) decode_merge(const float* __restrict__ part
 template <int D, int GP, int KE, int VE>
 static cudaError_t launch_fma_t(const DecodeParams& p, dim3 grid, cudaStream_t st) {
   constexpr int smem = fma_smem_bytes<D, GP, KE, VE>();
-  cudaError_t e = ensure_smem_optin((const void*)decode_split_fma<D, GP, KE, VE>, smem);
+  constexpr int smem_rope = smem + fma_rope_smem_bytes<D, GP>();
+  cudaError_t e = ensure_smem_optin((const void*)decode_split_fma<D, GP, KE, VE>, smem_rope);
   if (e != cudaSuccess) return e;
-  decode_split_fma<D, GP, KE, VE><<<grid, 128, smem, st>>>(p);
+  decode_split_fma<D, GP, KE, VE><<<grid, 128, p.c.rope_cos != nullptr ? smem_rope : smem, st>>>(p);
   return cudaGetLastError();
 }
 

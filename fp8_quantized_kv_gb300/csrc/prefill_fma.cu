@@ -15,7 +15,8 @@
 // tile's columns for QK and softmax, and the dims d = (t%4) + 4i for PV.
 // K and V codes are converted on the fly into fp32 shared-memory tiles (code
 // values, the per-token scales applied as above; MXFP8 keys with their block
-// scales applied at the conversion).
+// scales applied at the conversion; rotated-bias residual keys reconstructed
+// there in full, dequant(r) + R_t b).
 #include "params.cuh"
 
 namespace fp8kv {
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(256) prefill_fma(PrefillParams p) {
   const int r = tid >> 2, qd = tid & 3;
   const int hk = hq / p.group;
   const CacheView& c = p.c;
+  const bool rope = c.rope_cos != nullptr;       // rotated-bias residual keys
   const int pos0 = p.q_pos0[b];
   const int i0 = qt * kTileTokens;
   const int last_i = min(p.n_q, i0 + kTileTokens) - 1;
@@ -85,6 +87,8 @@ __global__ void __launch_bounds__(256) prefill_fma(PrefillParams p) {
             float f[4];
             e4m3x4_to_f32_scaled((uint32_t)c.k[row * D + d], f);
             kvv = f[0];
+            if (rope)     // rotated-bias residual key: dequant(r) + R_t b, in full
+              kvv = fmaf(f[0] * kTwoPow120, c.k_scale[row], rope_bias(c, hk, t0 + rr, d));
           } else if constexpr (KE == ELEM_MX) {
             // MXFP8 key: the code's value times its 32-dim block's E8M0
             // scale (byte d / 32 of the row's scale word), exact in fp32
@@ -103,7 +107,7 @@ __global__ void __launch_bounds__(256) prefill_fma(PrefillParams p) {
             vvv = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(c.v)[row * D + d]);
           }
           if (d == 0) {
-            kss[rr] = KE == ELEM_E4M3 ? c.k_scale[row] : 1.f;
+            kss[rr] = KE == ELEM_E4M3 && !rope ? c.k_scale[row] : 1.f;
             vss[rr] = VE == ELEM_E4M3 ? c.v_scale[row] : 1.f;
           }
         }
@@ -130,7 +134,7 @@ __global__ void __launch_bounds__(256) prefill_fma(PrefillParams p) {
       const int key = t0 + col;
       const bool ok = col < nrows && key <= qpos;
       float v = s[u];
-      if (KE == ELEM_E4M3) v *= kTwoPow120;
+      if (KE == ELEM_E4M3 && !rope) v *= kTwoPow120;
       s[u] = ok ? v * (kss[col] * p.scale_log2) : -INFINITY;
       mt = fmaxf(mt, s[u]);
     }

@@ -156,9 +156,10 @@ __global__ void __launch_bounds__(256) append_kernel(CacheView c, const __nv_bfl
   }
   float v[EPL];
   load_bf16_slice<EPL>(src, lane, v);
-  if (!is_v && c.k_bias != nullptr) {            // pre-bias residual: fp32(k) - b
+  if (!is_v && c.k_bias != nullptr) {            // pre-bias residual: fp32(k) - b, or - R_t b
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) v[i] -= c.k_bias[h * D + lane * EPL + i];
+    for (int i = 0; i < EPL; ++i)
+      v[i] -= c.rope_cos != nullptr ? rope_bias(c, h, t, lane * EPL + i) : c.k_bias[h * D + lane * EPL + i];
   }
   uint8_t* codes = const_cast<uint8_t*>(is_v ? c.v : c.k) + dst * D;
   float* scale = const_cast<float*>(is_v ? c.v_scale : c.k_scale) + dst;
@@ -198,9 +199,10 @@ __global__ void __launch_bounds__(256) append_step_kernel(CacheView c, const __n
   }
   float v[EPL];
   load_bf16_slice<EPL>(src, lane, v);
-  if (!is_v && c.k_bias != nullptr) {            // pre-bias residual: fp32(k) - b
+  if (!is_v && c.k_bias != nullptr) {            // pre-bias residual: fp32(k) - b, or - R_t b
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) v[i] -= c.k_bias[h * D + lane * EPL + i];
+    for (int i = 0; i < EPL; ++i)
+      v[i] -= c.rope_cos != nullptr ? rope_bias(c, h, t, lane * EPL + i) : c.k_bias[h * D + lane * EPL + i];
   }
   uint8_t* codes = const_cast<uint8_t*>(is_v ? c.v : c.k) + dst * D;
   float* scale = const_cast<float*>(is_v ? c.v_scale : c.k_scale) + dst;

@@ -142,7 +142,7 @@ typedef struct {
   int32_t page_size;          /* paged: tokens per page (16, 32 or 64)         */
   int32_t num_pages;          /* paged: pages in the pool                      */
   int32_t max_pages_per_seq;  /* paged: columns of page_table                  */
-  int32_t reserved;
+  int32_t rope_positions;     /* rotated bias: rows of rope_cos / rope_sin    */
   void *k;                    /* e4m3 codes (uint8) or bf16, layout above      */
   void *v;
   float *k_scale;             /* fp32 per (token, KV head); NULL if K is bf16;
@@ -157,9 +157,24 @@ typedef struct {
    * FP8KV_ERR_INVALID_ARG).  Attention reads the residual codes as the keys:
    * the dropped score term q.b is the same for every key a query row sees,
    * so it cancels in the softmax.  b is one vector per KV head for all
-   * positions; a bias rotated with the key's position (a bias added before a
-   * rotary embedding, with the cache holding rotated keys) is not this. */
+   * positions, unless rope_cos and rope_sin are set (below). */
   const float *k_bias;
+  /* Rotated pre-bias residual keys (same sections; the pages' post-rotary
+   * residual layout): NULL, or both set, with k_bias.  The cache then holds
+   * rotated keys and b is a bias added before the rotary embedding, so the
+   * key at position t carries R_t b.  Appends quantise fp32(k) - R_t b, and
+   * attention reads dequant(r) + R_t b.  R_t is the "rotate half" layout:
+   * dims i and i + head_dim/2 form pair i at angle theta_{t,i}, with
+   *   (R_t b)_i           = fma(b_i, cos, -(b_{i+head_dim/2} * sin))
+   *   (R_t b)_{i+head_dim/2} = fma(b_{i+head_dim/2}, cos, b_i * sin)
+   * in fp32 (each product with sin rounded first), cos = rope_cos[t][i],
+   * sin = rope_sin[t][i]: [rope_positions][head_dim/2] fp32 device arrays,
+   * 16-byte aligned, rope_positions at least the cache's capacity (else
+   * FP8KV_ERR_INVALID_ARG).  Built on the CUDA-core kernels: the decode
+   * (AUTO picks it) and the prefill; the tensor-core kernels return
+   * FP8KV_ERR_UNSUPPORTED. */
+  const float *rope_cos;
+  const float *rope_sin;
 } fp8kv_cache;
 
 /* Quantise `rows` rows of `head_dim` bf16 values into E4M3 codes and one fp32

@@ -13,18 +13,22 @@ from fp8_quantized_kv_gb300 import synth
 import fp8_quantized_kv_gb300 as fk
 
 
-def fill_cache(inp: synth.DecodeInputs, dtype: str, device="cuda", capacity=None, k_bias=None):
+def fill_cache(inp: synth.DecodeInputs, dtype: str, device="cuda", capacity=None, k_bias=None, rope=None):
     """Append every token of a decode workload into a new cache (contiguous or
     paged per the workload) through fp8kv_append.  Returns the cache.
-    k_bias: optional [Hkv, D] fp32 device tensor (pre-bias residual keys)."""
+    k_bias: optional [Hkv, D] fp32 device tensor (pre-bias residual keys);
+    rope: optional (cos, sin) [P, D/2] fp32 device tensors (the bias turns
+    with the key's position)."""
     spec = inp.spec
     B = inp.seq_lens.numel()
+    rc, rs = rope if rope is not None else (None, None)
     if spec.page_size is None:
         cap = capacity or max(16, ((inp.max_len + 63) // 64) * 64)
-        cache = fk.Fp8KVCache.contiguous(B, spec.kv_heads, spec.head_dim, cap, dtype, device, k_bias=k_bias)
+        cache = fk.Fp8KVCache.contiguous(B, spec.kv_heads, spec.head_dim, cap, dtype, device, k_bias=k_bias,
+                                         rope_cos=rc, rope_sin=rs)
     else:
         cache = fk.Fp8KVCache.paged(inp.page_table, inp.num_pages, spec.kv_heads, spec.head_dim,
-                                    spec.page_size, dtype, device, k_bias=k_bias)
+                                    spec.page_size, dtype, device, k_bias=k_bias, rope_cos=rc, rope_sin=rs)
     lens = inp.seq_lens.to(torch.int64)
     if int(lens.sum()) == 0:
         return cache
@@ -52,14 +56,19 @@ def seq_bits(inp: synth.DecodeInputs, which: str, b: int):
     return synth.bf16_bits(t[s:e]).transpose(1, 0, 2)
 
 
-def oracle_kv(inp: synth.DecodeInputs, dtype: str, b: int, k_bias=None):
+def oracle_kv(inp: synth.DecodeInputs, dtype: str, b: int, k_bias=None, rope=None):
     """fp64 K and V of sequence b as the cache holds them: e4m3 round trip
     for an FP8 side, the bf16 value for a bf16 side, dequant(residual) + bias
-    for pre-bias residual keys.  [Hkv, T_b, D]."""
+    for pre-bias residual keys (+ R_t bias with rotary tables rope = (cos,
+    sin), numpy).  [Hkv, T_b, D]."""
     out = []
     for which, fp8 in (("k", k_fp8(dtype)), ("v", v_fp8(dtype))):
         bits = seq_bits(inp, which, b)
-        if which == "k" and k_bias is not None:
+        if which == "k" and k_bias is not None and rope is not None:
+            pos = np.arange(bits.shape[1], dtype=np.int32)
+            c, s = oracle.quantize_residual_rope(bits, k_bias, rope[0], rope[1], pos)
+            out.append(oracle.residual_rope_keys(c, s, oracle.rope_bias(k_bias, rope[0], rope[1], pos)))
+        elif which == "k" and k_bias is not None:
             c, s = oracle.quantize_residual(bits, k_bias)
             out.append(oracle.residual_keys(c, s, k_bias))
         elif which == "k" and dtype == "mxk8v8":
@@ -72,7 +81,7 @@ def oracle_kv(inp: synth.DecodeInputs, dtype: str, b: int, k_bias=None):
     return out
 
 
-def oracle_decode(inp: synth.DecodeInputs, dtype: str, batch_ids, sm_scale=None, k_bias=None):
+def oracle_decode(inp: synth.DecodeInputs, dtype: str, batch_ids, sm_scale=None, k_bias=None, rope=None):
     """Oracle decode outputs [len(batch_ids), Hq, D] for the listed sequences."""
     spec = inp.spec
     D = spec.head_dim
@@ -81,7 +90,7 @@ def oracle_decode(inp: synth.DecodeInputs, dtype: str, batch_ids, sm_scale=None,
     res = []
     for b in batch_ids:
         T = int(inp.seq_lens[b])
-        k, v = oracle_kv(inp, dtype, b, k_bias)
+        k, v = oracle_kv(inp, dtype, b, k_bias, rope)
         Tc = max(T, 1)
         kk = np.zeros((1, spec.kv_heads, Tc, D))
         vv = np.zeros((1, spec.kv_heads, Tc, D))

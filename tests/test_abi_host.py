@@ -138,6 +138,29 @@ def test_key_bias_checks(lib):
     assert lib.fp8kv_decode_num_splits(r(_cache(k_bias=0x5004)), 16, 0, 0) == 0
 
 
+def test_rotated_bias_checks(lib):
+    # rotary tables: both or neither, only with a bias, 16-byte aligned, and
+    # at least as many rows as the cache has positions; such a cache runs on
+    # the CUDA-core kernels (AUTO picks them), the tensor cores refuse it
+    r = ctypes.byref
+    ok = dict(k_bias=0x5000, rope_cos=0x6000, rope_sin=0x7000, rope_positions=8192)
+    c = _cache(**ok)
+    assert lib.fp8kv_decode_num_splits(r(c), 16, 0, 0) == lib.fp8kv_decode_num_splits(r(_cache()), 16, 0, 1) > 0
+    assert lib.fp8kv_decode_num_splits(r(c), 16, 0, 1) > 0
+    for kid in (2, 3, 4):
+        assert lib.fp8kv_decode_num_splits(r(c), 16, 0, kid) == 0
+    assert lib.fp8kv_decode_num_splits(r(_cache(**dict(ok, rope_sin=None))), 16, 0, 0) == 0
+    assert lib.fp8kv_decode_num_splits(r(_cache(**dict(ok, k_bias=None))), 16, 0, 0) == 0
+    assert lib.fp8kv_decode_num_splits(r(_cache(**dict(ok, rope_positions=8191))), 16, 0, 0) == 0
+    assert lib.fp8kv_decode_num_splits(r(_cache(**dict(ok, rope_cos=0x6004))), 16, 0, 0) == 0
+    paged = _cache(layout=1, page_size=16, num_pages=64, max_pages_per_seq=8, page_table=0x8000,
+                   **dict(ok, rope_positions=128))
+    assert lib.fp8kv_decode_num_splits(r(paged), 16, 0, 0) > 0
+    assert lib.fp8kv_decode_num_splits(r(_cache(layout=1, page_size=16, num_pages=64, max_pages_per_seq=8,
+                                                 page_table=0x8000, **dict(ok, rope_positions=127))), 16, 0, 0) == 0
+    assert lib.fp8kv_prefill_attention(0x7000, r(c), 0x8000, 64, 16, 0.1, 2, 0x9000, 0, None) == 2
+
+
 def test_transform_path_kernel_ids(lib):
     # kernels 3 and 4 (tensor cores, K converted to f16 on chip): K8V8 at
     # head_dim 128 only, planned like the tensor-core kernel; unknown ids rejected
