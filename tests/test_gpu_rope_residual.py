@@ -127,7 +127,8 @@ def test_fused_step_appends_rotated_residual_row():
         assert np.array_equal(cache.k_scale[s, :, t].cpu().numpy().view(np.uint32), rs[:, 0].view(np.uint32)), s
 
 
-def test_prefill_matches_reconstructed_keys():
+@pytest.mark.parametrize("page_size", [None, 16])
+def test_prefill_matches_reconstructed_keys(page_size):
     n_q, Hq, Hkv, D = 300, 8, 2, 128
     pin = synth.prefill_inputs(synth.PrefillWorkload("rope_pf", n_q, Hq, Hkv, D, seed=34), device="cuda")
     b = _bias(Hkv, D, 34)
@@ -135,7 +136,12 @@ def test_prefill_matches_reconstructed_keys():
     k = (pin.k.float().cpu() + torch.from_numpy(_rotated(b, cos, sin, n_q).transpose(1, 0, 2)).float())
     k = k.to(torch.bfloat16)
     bd, rope = _dev(b, cos, sin)
-    cache = fk.Fp8KVCache.contiguous(1, Hkv, D, 320, "k8v8", k_bias=bd, rope_cos=rope[0], rope_sin=rope[1])
+    if page_size is None:
+        cache = fk.Fp8KVCache.contiguous(1, Hkv, D, 320, "k8v8", k_bias=bd, rope_cos=rope[0], rope_sin=rope[1])
+    else:
+        perm = torch.randperm(20, generator=torch.Generator().manual_seed(3)).to(torch.int32)
+        cache = fk.Fp8KVCache.paged(perm[None], 20, Hkv, D, page_size, "k8v8", k_bias=bd,
+                                    rope_cos=rope[0], rope_sin=rope[1])
     fk.fp8kv_append(cache, k.cuda().contiguous(), pin.v.contiguous(), torch.zeros(n_q, dtype=torch.int32, device="cuda"),
                     torch.arange(n_q, dtype=torch.int32, device="cuda"))
     out = fk.fp8kv_prefill_attention(pin.q[None].contiguous(), cache, torch.zeros(1, dtype=torch.int32, device="cuda"),
