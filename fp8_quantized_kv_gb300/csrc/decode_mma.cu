@@ -41,8 +41,8 @@
 //              tiles straight into the UMMA operand layout, a ring of NST
 //              stages (full/empty mbarriers).  Contiguous cache: scale rows
 //              by 1-D bulk copy.  Paged cache: warps 0 and 11 issue alternate
-//              tiles, one page per lane, page ids four tiles ahead by
-//              cp.async; the softmax threads load their tokens' scale words.
+//              tiles, one page per lane (its K and V boxes and, by cp.async,
+//              its scale rows), page ids four tiles ahead by cp.async.
 //   warp 1     TMEM owner and QK issuer (one thread).
 //   warp 10    PV issuer (one thread).  Issuing a few tcgen05.mma costs the
 //              issuing thread a fraction of a microsecond; one thread issuing
@@ -332,7 +332,6 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
   // even, so each producer's tiles keep to their own slots.
   constexpr int NPW = PG && XK == XK_NATIVE ? 2 : 1;
   static_assert(NPW == 1 || C::NST % 2 == 0, "two producers need an even ring");
-  constexpr bool kOwnSc = PG && (C::K8 || VE == ELEM_E4M3);   // scale rows by the softmax threads
   constexpr int D = 128;
   const DecodeParams& p = tp.p;
   extern __shared__ uint8_t smem_raw[];
@@ -505,24 +504,21 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
       }
     } else {
       // The K and V boxes come by TMA (counted in the transaction bytes).
-      // The scale rows are loaded by the softmax threads themselves, two of
-      // their tiles ahead (a copy per page and side here cost the producer
-      // more than the rows' bytes), except in the tile that receives the
-      // fused step's new token: its rows come by cp.async after the append,
-      // each lane's cp.async.mbarrier.arrive adding one pending arrival to
-      // the stage barrier that completes when the lane's copies land (before
-      // lane 0's arrival, the barrier's only expected one, so the phase
-      // cannot complete without the scale rows).
+      // The scale rows come by cp.async, each lane's page rows, and each
+      // lane's cp.async.mbarrier.arrive adds one pending arrival to the stage
+      // barrier that completes when the lane's copies land (before lane 0's
+      // arrival, the barrier's only expected one, so the phase cannot
+      // complete without the scale rows).  The next page ids are fetched
+      // after that arrival, so the stage does not wait for them as well.
       const int np = pages_of(i);
       cp_async_wait<kPageAhead / NPW - 1>();       // tile i's group has landed
       int page = lane < np ? pg_ring[(i & 7) * 8 + lane] : 0;
-      fetch_page(i + kPageAhead);
       if (lane < np && (unsigned)page >= (unsigned)c.num_pages) {
         raise_error(p.err, FP8KV_DEVERR_BAD_PAGE);
         page = 0;      // read a valid page; the result is flagged as wrong
       }
       const int row = page * pool_rpp + row_h0;
-      if ((!kOwnSc || i == i_new) && lane < np && (C::K8 || VE == ELEM_E4M3)) {
+      if (lane < np && (C::K8 || VE == ELEM_E4M3)) {
         for (int q = 0; q < PR / 4; ++q) {
           if (C::K8) cp_async16(kss + lane * PR + 4 * q, c.k_scale + row + 4 * q);
           if (VE == ELEM_E4M3) cp_async16(vss + lane * PR + 4 * q, c.v_scale + row + 4 * q);
@@ -530,11 +526,7 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
         asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" ::"r"(umma::smem_u32(&full[s]))
                      : "memory");
       }
-      if (kOwnSc && i != i_new && lane < np) {
-        // the softmax threads' scale loads of this tile then hit L2
-        if (C::K8) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(c.k_scale + row));
-        if (VE == ELEM_E4M3) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(c.v_scale + row));
-      }
+      fetch_page(i + kPageAhead);
       __syncwarp();
       if (lane == 0) tma::arrive_expect_tx(&full[s], per_page * np);
       if (lane < np) {
@@ -918,46 +910,6 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
       tok = ((t >> (ps + hs)) << ps) | (t & (c.page_size - 1));
       cmask = ((1u << G) - 1u) << (hh * G);
     }
-    // Paged cache: this thread loads its own token's K and V scale words,
-    // two of the group's tiles ahead (its tile i + 4's page id one tile
-    // before that), so each value is used about one tile after its load was
-    // issued.  Rows past a tile's tokens read a valid row of page 0 and are
-    // masked.  The appended tile's rows come from the stage instead.
-    constexpr bool own_sc = kOwnSc;
-    // (the page of this thread's token within a tile, and its row within the
-    // page's block of the pool: tiles start on page boundaries.  Kept as
-    // per-thread constants, except for MXFP8 keys, whose four block
-    // accumulators leave no registers for them: measured 8% slower there.)
-    const int tok_page = tok >> pshift;
-    const int row_thr = ((hkv0 + hh) << pshift) + (tok & ((1 << pshift) - 1));
-    auto page_raw = [&](int i) -> int {         // raw table entry (checked at use)
-      if (!own_sc || i >= n_tiles) return 0;
-      const int t0 = (t_begin + i) * TT;
-      if (tok >= T - t0) return 0;
-      if constexpr (C::KMX)
-        return __ldg(c.page_table + (int64_t)b * c.max_pages_per_seq + ((t0 + tok) >> c.page_shift));
-      else
-        return __ldg(pt_cta + i * ppt + tok_page);
-    };
-    uint32_t sk_cur = 0, sv_cur = 0, sk_nxt = 0, sv_nxt = 0;
-    auto load_scales = [&](int i, int pid, uint32_t& sk, uint32_t& sv) {
-      if (!own_sc || i >= n_tiles) return;
-      if ((unsigned)pid >= (unsigned)c.num_pages) pid = 0;   // (the producer flags a bad page)
-      int64_t row;
-      if constexpr (C::KMX)
-        row = ((int64_t)pid * c.kv_heads + hkv0 + hh) * c.page_size + (((t_begin + i) * TT + tok) & (c.page_size - 1));
-      else
-        row = pid * pool_rpp + row_thr;
-      if (C::K8) sk = __ldg(reinterpret_cast<const uint32_t*>(c.k_scale) + row);
-      if (VE == ELEM_E4M3) sv = __ldg(reinterpret_cast<const uint32_t*>(c.v_scale) + row);
-    };
-    int pid_nx2 = 0;
-    if (own_sc) {
-      const int pa = page_raw(wg), pb = page_raw(wg + 2);
-      load_scales(wg, pa, sk_cur, sv_cur);
-      load_scales(wg + 2, pb, sk_nxt, sv_nxt);
-      pid_nx2 = page_raw(wg + 4);
-    }
     // Anchors.  The tokens one warp holds of a tile are referenced to the
     // integer-valued U = ceil(max of s + log2(v_scale)) over them (log2
     // units; for a bf16 V side, of s): p = 2^(s - U), and P' = bf16(p *
@@ -1078,9 +1030,8 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
         const int t0 = (t_begin + i) * TT;
         const int valid = min(TT, T - t0);
         const bool tok_ok = tok < valid;
-        const bool own = own_sc && i != i_new;             // this thread's scale words, or the stage's
-        const float kf = KE == ELEM_E4M3 ? (own ? __uint_as_float(sk_cur) : kss[t]) : 1.f;   // (MXFP8: below)
-        const float vsc = VE == ELEM_E4M3 ? (tok_ok ? (own ? __uint_as_float(sv_cur) : vss[t]) : 0.f) : 1.f;
+        const float kf = KE == ELEM_E4M3 ? kss[t] : 1.f;   // (MXFP8: below)
+        const float vsc = VE == ELEM_E4M3 ? (tok_ok ? vss[t] : 0.f) : 1.f;
         float sc[16];
         {
           constexpr int NACC = C::KMX ? 4 : 1;
@@ -1093,7 +1044,7 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
             // MXFP8 keys: accumulator k holds dims 32k..32k+31 of the dot
             // product, so the key's E8M0 block scale k applies to it here
             // (the block-scaled product, summed over the four blocks)
-            const uint32_t e8 = own ? sk_cur : reinterpret_cast<const uint32_t*>(st + C::K_TILE + C::V_TILE)[t];
+            const uint32_t e8 = reinterpret_cast<const uint32_t*>(st + C::K_TILE + C::V_TILE)[t];
             float w[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) w[k] = pow2_exact((int)((e8 >> (8 * k)) & 0xFF) - 127);
@@ -1195,12 +1146,6 @@ __global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
           umma::mbar_arrive(&empty[s]);
         }
         if (t == 0) TRACE(8 * i + 4);
-        if (own_sc) {                       // the scale pipeline moves one group tile on
-          sk_cur = sk_nxt;
-          sv_cur = sv_nxt;
-          load_scales(i + 4, pid_nx2, sk_nxt, sv_nxt);
-          pid_nx2 = page_raw(i + 6);
-        }
         TRACE_SUB(i, 12);
         if (lane == 0) TRACE_MAX(8 * i + 6);
       }
