@@ -39,10 +39,11 @@
 // stages across adjacent tiles):
 //   warp 0     TMA producer: 128-byte-swizzled tensor loads of the K and V
 //              tiles straight into the UMMA operand layout, a ring of NST
-//              stages (full/empty mbarriers).  Contiguous cache: scale rows
-//              by 1-D bulk copy.  Paged cache: warps 0 and 11 issue alternate
-//              tiles, one page per lane (its K and V boxes and, by cp.async,
-//              its scale rows), page ids four tiles ahead by cp.async.
+//              stages (full/empty mbarriers).  Native-QK kernels with an
+//              even ring: warps 0 and 11 issue alternate tiles.  Contiguous
+//              cache: scale rows by 1-D bulk copy.  Paged cache: one page per
+//              lane (its K and V boxes and, by cp.async, its scale rows),
+//              page ids four tiles ahead by cp.async.
 //   warp 1     TMEM owner and QK issuer (one thread).
 //   warp 10    PV issuer (one thread).  Issuing a few tcgen05.mma costs the
 //              issuing thread a fraction of a microsecond; one thread issuing
@@ -84,11 +85,9 @@ constexpr int kMmaTile = 128;
 // Split partials the global merge stages in the (idle) ring at a time.
 constexpr int kMergeChunk = 44;
 // warp 0 TMA producer, warp 1 QK issuer and TMEM owner, warps 2-9 softmax,
-// warp 10 PV issuer
+// warp 10 PV issuer; where TcCfg::NPW is 2 a twelfth warp is a second
+// producer (warps 0 and 11 issue the even and the odd tiles).
 constexpr int kTcThreads = 352;
-// Paged caches: a twelfth warp is a second producer (warps 0 and 11 issue
-// the even and the odd tiles).
-constexpr int kTcThreadsPaged = 384;
 
 // XK: where K is prepared (an ablation).  XK_NATIVE: QK is the native e4m3
 // MMA on the query's e4m3 hi/lo pair.  On the transform path each landed
@@ -110,6 +109,13 @@ struct TcCfg {
   // K tile, V tile, then the K and V scale rows of an 8-bit side
   static constexpr int STAGE = ((K_TILE + V_TILE + (K8 || VE == ELEM_E4M3 ? 2 * kMmaTile * 4 : 0)) + 1023) / 1024 * 1024;
   static constexpr int NST = XK != XK_NATIVE ? 4 : (K8 && VE == ELEM_E4M3) ? 6 : (K8 == (VE == ELEM_E4M3) ? 3 : 4);
+  // Producer warps.  One warp's chain of dependent instructions per tile
+  // (on a paged cache: a page lookup, addresses and a copy per page and
+  // side) fell behind the softmax's pace, so the native-QK kernels run two
+  // that issue alternate tiles.  Tile i's ring slot is i % NST with NST
+  // even, so each producer's tiles keep to their own slots.
+  static constexpr int NPW = XK == XK_NATIVE && NST % 2 == 0 ? 2 : 1;
+  static constexpr int THREADS = kTcThreads + (NPW - 1) * 32;
   static constexpr int KCV = XK != XK_NATIVE ? 2 * kMmaTile * D * 2 : 0;   // two converted f16 K tiles
   static constexpr int QOP = QHL ? 16 * 128 : 2 * 16 * 128;
   static constexpr int POP = VE == ELEM_E4M3 ? 16 * 128 : 2 * 16 * 128;   // [128 tokens][16 or 32 B]
@@ -322,15 +328,10 @@ __device__ __forceinline__ void k_tile_to_f16(const uint8_t* src, uint8_t* dst, 
 // PG: the instantiation for paged caches whose scale rows the softmax threads
 // load themselves (the native-QK kernels); other paged launches use PG = false.
 template <int KE, int VE, int XK, bool PG>
-__global__ void __launch_bounds__(PG ? kTcThreadsPaged : kTcThreads, 1)
+__global__ void __launch_bounds__(TcCfg<KE, VE, XK>::THREADS, 1)
     decode_split_tc(const __grid_constant__ DecodeTmaParams tp) {
   using C = TcCfg<KE, VE, XK>;
-  // Producer warps: on a paged cache each tile takes a copy per page and
-  // side, and one warp's chain of dependent instructions per tile (page
-  // lookup, addresses, copies) was slower than the softmax's pace, so two
-  // warps issue alternate tiles.  Tile i's ring slot is i % NST with NST
-  // even, so each producer's tiles keep to their own slots.
-  constexpr int NPW = PG && XK == XK_NATIVE ? 2 : 1;
+  constexpr int NPW = C::NPW;
   static_assert(NPW == 1 || C::NST % 2 == 0, "two producers need an even ring");
   constexpr int D = 128;
   const DecodeParams& p = tp.p;
@@ -1418,7 +1419,7 @@ static cudaError_t launch_tc_t(const DecodeParams& p, dim3 grid, cudaStream_t st
   tp.p.cluster = 0;
   const void* fn = (const void*)decode_split_tc<KE, VE, XK, PG>;
   cudaLaunchConfig_t cfg = {};
-  constexpr int threads = PG ? kTcThreadsPaged : kTcThreads;
+  constexpr int threads = TcCfg<KE, VE, XK>::THREADS;
   cfg.gridDim = grid;
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
