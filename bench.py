@@ -69,6 +69,8 @@ def parse(argv=None):
                     help="time only the fused decode step on this workload (for profiling) and exit")
     ap.add_argument("--group", type=int, default=0,
                     help="with --shape: query heads per KV head (default: the workload's own)")
+    ap.add_argument("--prefill-size", default=None, metavar="TOKENS,BATCH,QHEADS,KVHEADS",
+                    help="time only the tensor-core prefill at this size (head_dim 128) and exit")
     return ap.parse_args(argv)
 
 
@@ -572,38 +574,42 @@ def e2e_run(layers, host, K, W, kernel, early=False):
     return st.elapsed_time(en) * K / (reps * n), h2d, out_h.numel() * out_h.element_size()
 
 
-def measure_prefill(args, ws):
-    """Causal prefill of the 2048-token, 28 q / 4 KV head workload over a K8/V8
-    cache (tensor-core kernel).  Eight independent copies (Q, cache, output:
-    ~250 MB, above L2) are rotated; the timed region is `args.prefill_steps`
-    launches between CUDA events on the launching stream."""
+def time_prefill(spec, batch, K, warmup, ws, min_sets=1):
+    """Launches of the tensor-core causal prefill over K8/V8 caches holding
+    `batch` copies of the workload's sequence: enough independent input sets
+    (Q, cache, output) rotated launch by launch that they exceed the L2
+    twice over (at least `min_sets`, at most 8); `warmup` launches, then K
+    timed ones between CUDA events on the launching stream.  Returns
+    (max-over-ranks time per launch in us, FLOPs per launch, input sets)."""
     import fp8_quantized_kv_gb300 as fk
-    spec = synth.PREFILL_WORKLOADS["prefill_2048"]
     n, Hq, Hkv, D = spec.n_tokens, spec.q_heads, spec.kv_heads, spec.head_dim
     pin = synth.prefill_inputs(spec, device="cuda")
+    k_all = pin.k.repeat(batch, 1, 1).contiguous()
+    v_all = pin.v.repeat(batch, 1, 1).contiguous()
+    sidx = torch.repeat_interleave(torch.arange(batch, dtype=torch.int32), n).cuda()
+    pos = torch.arange(n, dtype=torch.int32).repeat(batch).cuda()
+    set_bytes = batch * n * (2 * Hq * D * 2 + Hkv * 2 * (D + 4))
+    n_sets = max(min_sets, min(8, -(-2 * L2_BYTES // set_bytes)))
     sets = []
-    for _ in range(8):
-        cache = fk.Fp8KVCache.contiguous(1, Hkv, D, n, "k8v8")
-        fk.fp8kv_append(cache, pin.k.contiguous(), pin.v.contiguous(),
-                        torch.zeros(n, dtype=torch.int32, device="cuda"),
-                        torch.arange(n, dtype=torch.int32, device="cuda"))
-        q = pin.q[None].contiguous().clone()
-        out = torch.empty(1, n, Hq, D, dtype=torch.bfloat16, device="cuda")
+    for _ in range(n_sets):
+        cache = fk.Fp8KVCache.contiguous(batch, Hkv, D, n, "k8v8")
+        fk.fp8kv_append(cache, k_all, v_all, sidx, pos)
+        q = pin.q[None].expand(batch, -1, -1, -1).clone(memory_format=torch.contiguous_format)
+        out = torch.empty(batch, n, Hq, D, dtype=torch.bfloat16, device="cuda")
         sets.append((cache, q, out))
-    p0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p0 = torch.zeros(batch, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
 
     def run(i):
         cache, q, out = sets[i % len(sets)]
         fk.fp8kv_prefill_attention(q, cache, p0, out=out, kernel="tensor_cores", stream=stream)
 
-    for i in range(max(3, args.warmup)):
+    for i in range(max(3, warmup)):
         run(i)
     torch.cuda.synchronize()
     barrier(ws)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    K = args.prefill_steps
     spacer()
     e0.record(stream)
     for i in range(K):
@@ -613,9 +619,20 @@ def measure_prefill(args, ws):
     barrier(ws)
     if fk.fp8kv_get_device_error() != 0:
         raise RuntimeError("prefill raised a device error")
-    flops = 4.0 * D * Hq * n * (n + 1) / 2
+    flops = batch * 4.0 * D * Hq * n * (n + 1) / 2
     t_max, _ = aggregate(0, K, e0.elapsed_time(e1), ws)
-    us = t_max / K * 1e3
+    return t_max / K * 1e3, flops, n_sets
+
+
+def measure_prefill(args, ws):
+    """Causal prefill of the 2048-token, 28 q / 4 KV head workload over a K8/V8
+    cache (tensor-core kernel).  Eight independent copies (Q, cache, output:
+    ~250 MB, above L2) are rotated; the timed region is `args.prefill_steps`
+    launches between CUDA events on the launching stream."""
+    spec = synth.PREFILL_WORKLOADS["prefill_2048"]
+    n, Hq, Hkv, D = spec.n_tokens, spec.q_heads, spec.kv_heads, spec.head_dim
+    K = args.prefill_steps
+    us, flops, _ = time_prefill(spec, 1, K, args.warmup, ws, min_sets=8)
     achieved = flops / (us * 1e-6) / 1e12
     peak, kind = tensor_peak()
     return {"workload": "prefill_2048", "batch": 1, "tokens": n, "q_heads": Hq, "kv_heads": Hkv,
@@ -974,6 +991,25 @@ def run_shape(args, rank):
                           "note": "eager launches; a profiling aid, not a bench line"}))
 
 
+def run_prefill_size(args, ws, rank):
+    """Only the tensor-core causal prefill at --prefill-size (tokens, batch,
+    query heads, KV heads; head_dim 128; Q, K and V ~ N(0,1) as in the
+    2048-token workload): `warmup` launches, then `prefill_steps` timed ones
+    over rotated input sets.  A measurement aid, not a bench line."""
+    n, batch, hq, hkv = (int(x) for x in args.prefill_size.split(","))
+    spec = dataclasses.replace(synth.PREFILL_WORKLOADS["prefill_2048"], name=f"prefill_{n}x{batch}",
+                               n_tokens=n, q_heads=hq, kv_heads=hkv)
+    us, flops, n_sets = time_prefill(spec, batch, args.prefill_steps, args.warmup, ws)
+    if rank == 0:
+        peak, kind = tensor_peak()
+        tf = flops / (us * 1e-6) / 1e12
+        print(json.dumps({"prefill": spec.name, "tokens": n, "batch": batch, "q_heads": hq, "kv_heads": hkv,
+                          "head_dim": spec.head_dim, "cache": "k8v8", "kernel": "prefill_tc",
+                          "us_per_launch": us, "TFLOPs": tf, "frac_of_peak": tf / peak, "peak_kind": kind,
+                          "launches": args.prefill_steps, "input_sets_rotated": n_sets,
+                          "note": "a measurement aid, not a bench line"}))
+
+
 def main():
     args = parse()
     ws, rank = dist_setup()
@@ -986,6 +1022,8 @@ def main():
         get_lib()
         if args.shape:
             run_shape(args, rank)
+        elif args.prefill_size:
+            run_prefill_size(args, ws, rank)
         else:
             run_gpu(args, ws, rank)
     if ws > 1:
