@@ -574,6 +574,13 @@ def e2e_run(layers, host, K, W, kernel, early=False):
     return st.elapsed_time(en) * K / (reps * n), h2d, out_h.numel() * out_h.element_size()
 
 
+def prefill_flops(n, batch, q_heads, head_dim):
+    """Algorithmic FLOPs of one causal prefill: query i attends keys 0..i, and
+    each (query, key) pair costs a head_dim dot product for QK and another for
+    P.V, 2 FLOPs per multiply-add: 4 D per pair, n (n + 1) / 2 pairs per head."""
+    return batch * 4.0 * head_dim * q_heads * n * (n + 1) / 2
+
+
 def time_prefill(spec, batch, K, warmup, ws, min_sets=1):
     """Launches of the tensor-core causal prefill over K8/V8 caches holding
     `batch` copies of the workload's sequence: enough independent input sets
@@ -619,7 +626,7 @@ def time_prefill(spec, batch, K, warmup, ws, min_sets=1):
     barrier(ws)
     if fk.fp8kv_get_device_error() != 0:
         raise RuntimeError("prefill raised a device error")
-    flops = batch * 4.0 * D * Hq * n * (n + 1) / 2
+    flops = prefill_flops(n, batch, Hq, D)
     t_max, _ = aggregate(0, K, e0.elapsed_time(e1), ws)
     return t_max / K * 1e3, flops, n_sets
 

@@ -34,6 +34,19 @@ def test_shape_mode_parses():
     assert bench.parse([]).shape is None
 
 
+def test_prefill_size_mode_and_flops():
+    a = bench.parse(["--prefill-size", "8192,1,28,4", "--prefill-steps", "50"])
+    assert a.prefill_size == "8192,1,28,4" and a.prefill_steps == 50
+    assert bench.parse([]).prefill_size is None
+    # 2048 tokens, 28 query heads, head_dim 128: 2,098,176 causal (query, key)
+    # pairs per head, 4 x 128 FLOPs each, 28 heads
+    assert bench.prefill_flops(2048, 1, 28, 128) == 2_098_176 * 512 * 28 == 30_079_451_136
+    # a batch of 8 is 8 independent sequences
+    assert bench.prefill_flops(2048, 8, 28, 128) == 8 * 30_079_451_136
+    # one token attends only itself
+    assert bench.prefill_flops(1, 1, 1, 128) == 512
+
+
 def test_fp8_kv_error_report():
     """The bench's fp8_kv_error report on the tiny workload: the bf16 cache
     changes nothing; every 8-bit side adds error of the size an e4m3 round
