@@ -62,7 +62,9 @@ constexpr int fma_rope_smem_bytes() { return GP * D * 4; }
 
 __device__ __forceinline__ int q_off(int d, int D) { return d + (d >= D / 2 ? 4 : 0); }
 
-template <int D, int GP, int KE, int VE>
+// RP: the instantiation for caches with rotated-bias residual keys (rotary
+// tables set); the others carry none of its code or registers.
+template <int D, int GP, int KE, int VE, bool RP>
 __global__ void __launch_bounds__(128) decode_split_fma(DecodeParams p) {
   using C = FmaCfg<D, KE, VE>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -106,9 +108,9 @@ __global__ void __launch_bounds__(128) decode_split_fma(DecodeParams p) {
     q_s[g * C::QS + q_off(d, D)] = v;
   }
 
-  const bool rope = c.rope_cos != nullptr;
+  constexpr bool rope = RP;
   constexpr int H = D / 2;
-  if (rope) {
+  if constexpr (rope) {
     __syncthreads();                               // q_s written
     const float* kb = c.k_bias + (int64_t)h * D;
     for (int i = tid; i < GP * H; i += blockDim.x) {
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(128) decode_split_fma(DecodeParams p) {
     for (int g = 0; g < GP; ++g) {
       float d2 = dot[g] + __shfl_xor_sync(0xffffffffu, dot[g], 1);
       if (KE != ELEM_BF16) d2 *= kTwoPow120;
-      if (rope) {
+      if constexpr (rope) {
         const float ct = corr[g] + __shfl_xor_sync(0xffffffffu, corr[g], 1);
         sc[g] = valid ? fmaf(d2, KE == ELEM_E4M3 ? kss[j] : 1.f, ct) * p.scale_log2 : -INFINITY;
       } else {
@@ -468,14 +470,21 @@ __global__ void __launch_bounds__(D) decode_merge(const float* __restrict__ part
 }
 
 // ------------------------------------------------------------ launchers ---
+template <int D, int GP, int KE, int VE, bool RP>
+static cudaError_t launch_fma_r(const DecodeParams& p, dim3 grid, cudaStream_t st) {
+  constexpr int smem = fma_smem_bytes<D, GP, KE, VE>() + (RP ? fma_rope_smem_bytes<D, GP>() : 0);
+  cudaError_t e = ensure_smem_optin((const void*)decode_split_fma<D, GP, KE, VE, RP>, smem);
+  if (e != cudaSuccess) return e;
+  decode_split_fma<D, GP, KE, VE, RP><<<grid, 128, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
 template <int D, int GP, int KE, int VE>
 static cudaError_t launch_fma_t(const DecodeParams& p, dim3 grid, cudaStream_t st) {
-  constexpr int smem = fma_smem_bytes<D, GP, KE, VE>();
-  constexpr int smem_rope = smem + fma_rope_smem_bytes<D, GP>();
-  cudaError_t e = ensure_smem_optin((const void*)decode_split_fma<D, GP, KE, VE>, smem_rope);
-  if (e != cudaSuccess) return e;
-  decode_split_fma<D, GP, KE, VE><<<grid, 128, p.c.rope_cos != nullptr ? smem_rope : smem, st>>>(p);
-  return cudaGetLastError();
+  if (p.c.rope_cos == nullptr) return launch_fma_r<D, GP, KE, VE, false>(p, grid, st);
+  // (rotary tables come only with a key bias, on e4m3 per-row keys)
+  if constexpr (KE == ELEM_E4M3) return launch_fma_r<D, GP, KE, VE, true>(p, grid, st);
+  return cudaErrorInvalidValue;
 }
 
 template <int D, int KE, int VE>
