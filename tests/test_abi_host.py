@@ -198,6 +198,14 @@ def test_split_plan_and_workspace(lib):
         assert ws == 16 * 16 * S * (128 + 2) * 4
     # automatic choice: group 8 at head_dim 128 runs on the tensor cores
     assert lib.fp8kv_decode_num_splits(r(c), 16, 10 ** 6, 0) == 64
+    # more (sequence, KV-head) units than SMs (the paged batch-64 serving
+    # decode: 64 sequences x 8 KV heads, group 4, so two KV heads per CTA and
+    # 64-token tiles, 16-token pages up to 16,384 tokens): splits of about 56
+    # tiles, 256 tiles -> 5 splits of 52
+    paged = _cache(layout=1, batch=64, kv_heads=8, max_tokens=16384, page_size=16,
+                   num_pages=64 * 1024, max_pages_per_seq=1024, page_table=0x7000)
+    assert lib.fp8kv_decode_num_splits(r(paged), 32, 0, 2) == 5
+    assert lib.fp8kv_decode_num_splits(r(paged), 32, 0, 0) == 5
 
 
 def test_workloads_match_their_description():
